@@ -1,0 +1,523 @@
+#!/usr/bin/env python3
+"""Benchmark of the GB300 Gated DeltaNet layer (one JSON line on rank 0).
+
+Step = one decode step of the layer for 256 sequences x 1 token (16 QK / 32 V
+heads, head_dim 128, bf16 activations, fp32 state pool of 1024 slots):
+causal_conv1d_update over the 8192-channel qkv stream -> gdn_gating ->
+gdn_decode_recurrent reading q/k/v straight out of the conv output.  value =
+decode tokens/s of the whole job; the decode kernel's state traffic is the
+roofline line (HBM bound).  Extra keys report the chunked prefill (8
+sequences, 512..8192 tokens: conv fwd -> gating -> prefill) and the MTP step
+(128 x 4 tokens with per-token snapshots and an accept copy).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+N > 1 runs under torch.distributed.run, one independent replica per GPU
+(weak scaling: sequences are independent, the path has no collective); the
+process group only carries the barrier and the max-over-ranks time.
+--impl reference times the CPU oracle (the only reference implementation
+there is) on a bounded sample of the same workload, on rank 0.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "GDN decode tokens/s + state HBM GB/s; chunked prefill tokens/s; % roofline"
+UNIT = "tokens/s"
+DECODE_WORKLOAD = ("decode step: 256 sequences x 1 token, causal_conv1d_update (8192 ch, width 4) "
+                   "+ gdn_gating + gdn_decode_recurrent, 16 QK / 32 V heads, head_dim 128, "
+                   "bf16 activations, fp32 state pool 1024 slots x 32 x 128 x 128")
+
+
+# --------------------------------------------------------------------- util --
+
+def parse_args(argv=None):
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=2000)
+    p.add_argument("--warmup", type=int, default=20)
+    p.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    p.add_argument("--no-extras", action="store_true", help="skip the prefill / MTP extras")
+    p.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle work")
+    return p.parse_args(argv)
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def init_dist(world, backend):
+    if world > 1 and not torch.distributed.is_initialized():
+        torch.distributed.init_process_group(backend=backend, init_method="env://")
+
+
+def reduce_max(x: float, device) -> float:
+    """Max of x over ranks (x itself without a process group)."""
+    if not (torch.distributed.is_available() and torch.distributed.is_initialized()):
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier():
+    if torch.distributed.is_available() and torch.distributed.is_initialized():
+        torch.distributed.barrier()
+
+
+def whole_job(units_per_rank: float, max_seconds: float, world: int) -> float:
+    """Units all ranks processed divided by the slowest rank's time."""
+    return units_per_rank * world / max_seconds
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return {"hbm_gbs": d["hbm_gbs"], "bf16_tflops": d["bf16_tflops"],
+                "bf16_tflops_sustained": d.get("bf16_tflops_sustained", d["bf16_tflops"]),
+                "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+            "source": "fallback"}
+
+
+def profile_traffic(kernel_key: str, source_files):
+    """DRAM bytes per launch recorded from an ncu capture in profiles/traffic.txt
+    (lines: key bytes sha256-of-sources), or None when the kernel's sources
+    changed since the capture or there is none."""
+    path = os.path.join(ROOT, "profiles", "traffic.txt")
+    if not os.path.exists(path):
+        return None
+    h = hashlib.sha256()
+    for f in source_files:
+        with open(os.path.join(ROOT, f), "rb") as fh:
+            h.update(fh.read())
+    digest = h.hexdigest()[:16]
+    with open(path) as f:
+        for line in f:
+            parts = line.split()
+            if len(parts) >= 3 and parts[0] == kernel_key and parts[2] == digest:
+                return float(parts[1])
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons sampled every 100 ms while running."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-i", str(self.gpu), "-lms", "100"], stdout=subprocess.PIPE,
+                stderr=subprocess.DEVNULL, text=True)
+        except (OSError, ValueError):
+            self.proc = None
+        return self
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.15)
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        rows = [[c.strip() for c in line.split(",")] for line in out.strip().splitlines()]
+        rows = [r for r in rows if len(r) >= 9]
+        if not rows:
+            return None
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({n for r in rows for n, v in zip(names, r[5:9]) if v.lower() == "active"})
+        loaded = [s for s in sm if s >= 0.5 * max(sm)] if sm else []
+        return {"sm_mhz": statistics.median(loaded) if loaded else None,
+                "sm_max_mhz": float(rows[0][2]) if rows[0][2].replace(".", "").isdigit() else None,
+                "reasons": reasons, "samples": len(rows)}
+
+
+# ------------------------------------------------------------- our kernels --
+
+def decode_kernel_bytes(n, hqk, hv, dk, dv, io_bytes):
+    """Algorithmic bytes of one decode launch (1 token per sequence): the
+    state read + written once, q/k per QK head, v, o, g, beta, slot ids."""
+    state = 2 * n * hv * dv * dk * 4
+    qk = 2 * n * hqk * dk * io_bytes
+    vo = 2 * n * hv * dv * io_bytes
+    gb = 2 * n * hv * 4
+    return state + qk + vo + gb + n * 4
+
+
+def run_ours(args):
+    import gated_deltanet_linear_10_gb300 as gdn
+    import workloads
+
+    rank, world, local = dist_env()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    init_dist(world, "nccl")
+    peaks = load_peaks()
+
+    w = workloads.decode(pool_device=dev)
+    d = w.dims
+    x, a, b = w.x.to(dev), w.a.to(dev), w.b.to(dev)
+    conv_w, A_log, dt_bias = w.conv_w.to(dev), w.A_log.to(dev), w.dt_bias.to(dev)
+    cpool, spool, slots = w.conv_pool.to(dev), w.state_pool, w.slots.to(dev)
+    N = w.n_seqs
+    y = torch.empty_like(x)
+    g = torch.empty((N, d.hv), dtype=torch.float32, device=dev)
+    beta = torch.empty_like(g)
+    o = torch.empty((N, d.hv, d.dv), dtype=x.dtype, device=dev)
+    nq = d.hqk * d.dk
+    qv = y.narrow(1, 0, nq).unflatten(1, (d.hqk, d.dk))
+    kv = y.narrow(1, nq, nq).unflatten(1, (d.hqk, d.dk))
+    vv = y.narrow(1, 2 * nq, d.hv * d.dv).unflatten(1, (d.hv, d.dv))
+    flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)   # 256 MiB > L2
+
+    stream = torch.cuda.current_stream(dev)
+
+    def step(ev=None):
+        if ev is not None:
+            ev[0].record(stream)
+        gdn.causal_conv1d_update(x, 1, conv_w, cpool, slots, y=y)
+        if ev is not None:
+            ev[1].record(stream)
+        gdn.gdn_gating(a, b, A_log, dt_bias, g=g, beta=beta)
+        if ev is not None:
+            ev[2].record(stream)
+        gdn.gdn_decode_recurrent(qv, kv, vv, g, beta, 1, spool, slots, scale=w.scale, o=o)
+        if ev is not None:
+            ev[3].record(stream)
+
+    for _ in range(max(args.warmup, 3)):
+        step()
+        flush.zero_()
+    torch.cuda.synchronize(dev)
+    assert gdn.gdn_get_device_status(clear=True) == 0
+
+    K = args.steps
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(K)]
+    sampler = ClockSampler(local).start()
+    time.sleep(0.3)
+    barrier()
+    torch.cuda.synchronize(dev)
+    t0 = time.perf_counter()
+    torch.cuda._sleep(2_000_000)                 # head start: the host enqueues ahead of the GPU
+    for i in range(K):
+        step(evs[i])
+        flush.zero_()
+    torch.cuda.synchronize(dev)
+    barrier()
+    wall = time.perf_counter() - t0
+    clocks = sampler.stop()
+    step_ms = [e[0].elapsed_time(e[3]) for e in evs]
+    conv_ms = [e[0].elapsed_time(e[1]) for e in evs]
+    gate_ms = [e[1].elapsed_time(e[2]) for e in evs]
+    dec_ms = [e[2].elapsed_time(e[3]) for e in evs]
+    ms_step = sum(step_ms) / K
+    ms_step_max = reduce_max(ms_step, dev)
+    value = whole_job(N, ms_step_max / 1e3, world)
+    dec_avg = sum(dec_ms) / K
+    dec_bytes = decode_kernel_bytes(N, d.hqk, d.hv, d.dk, d.dv, 2)
+    achieved = dec_bytes / (dec_avg / 1e3) / 1e9
+    traffic = profile_traffic("decode_kernel", ["gated_deltanet_linear_10_gb300/csrc/decode.cu",
+                                                "gated_deltanet_linear_10_gb300/csrc/common.cuh"])
+
+    # ---- end to end: host -> device inputs, the three calls, o -> host
+    x_h = w.x.pin_memory()
+    a_h, b_h = w.a.pin_memory(), w.b.pin_memory()
+    o_h = torch.empty(o.shape, dtype=o.dtype).pin_memory()
+    Ke = max(10, min(K, 500))
+    e2e_ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(Ke)]
+    torch.cuda.synchronize(dev)
+    torch.cuda._sleep(2_000_000)
+    for i in range(Ke):
+        e2e_ev[i][0].record(stream)
+        x.copy_(x_h, non_blocking=True)
+        a.copy_(a_h, non_blocking=True)
+        b.copy_(b_h, non_blocking=True)
+        step()
+        o_h.copy_(o, non_blocking=True)
+        e2e_ev[i][1].record(stream)
+        flush.zero_()
+    torch.cuda.synchronize(dev)
+    e2e_ms = reduce_max(sum(e[0].elapsed_time(e[1]) for e in e2e_ev) / Ke, dev)
+    h2d = x_h.numel() * 2 + a_h.numel() * 2 + b_h.numel() * 2
+    d2h = o_h.numel() * 2
+    assert gdn.gdn_get_device_status(clear=True) == 0
+
+    extras = {}
+    if not args.no_extras:
+        extras["mtp"] = bench_mtp(gdn, workloads, dev, flush)
+        extras["prefill"] = bench_prefill(gdn, workloads, dev, flush, peaks)
+
+    cpu = None
+    if rank == 0:
+        del flush
+        cpu = cpu_baseline(w, args.cpu_budget)
+
+    line = {
+        "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world, "steps": K,
+        "warmup": args.warmup, "ms_per_step": round(ms_step_max, 5), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": DECODE_WORKLOAD, "global_batch": N * world, "seq_len": 1,
+                   "io_dtype": "bf16", "l2": "flushed between steps (256 MiB write)",
+                   "parallelism": f"replicas x{world}"},
+        "roofline": {"bound": "hbm", "kernel": "decode_kernel", "achieved": round(achieved, 1),
+                     "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                     "frac": round(achieved / peaks["hbm_gbs"], 4), "traffic": traffic,
+                     "algorithmic_bytes": dec_bytes, "avg_launch_ms": round(dec_avg, 5),
+                     "peak_source": peaks["source"]},
+        "kernels_ms": {"causal_conv1d_update": round(sum(conv_ms) / K, 5),
+                       "gdn_gating": round(sum(gate_ms) / K, 5),
+                       "gdn_decode_recurrent": round(dec_avg, 5)},
+        "state_gbs": round(achieved, 1),
+        "e2e": {"value": round(whole_job(N, e2e_ms / 1e3, world), 1), "unit": UNIT,
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "ms_per_step": round(e2e_ms, 5)},
+        "gpu_launches": 3 * K,
+        "clocks": clocks,
+        "wall_s_timed": round(wall, 3),
+        "cpu_baseline": cpu,
+    }
+    line.update(extras)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+def bench_mtp(gdn, workloads, dev, flush, steps=50):
+    """MTP step: conv update (4 tokens, per-token conv snapshots) -> gating ->
+    decode with per-token state snapshots -> accept copy into the source slot."""
+    w = workloads.mtp(pool_device=dev)
+    d = w.dims
+    x, a, b = w.x.to(dev), w.a.to(dev), w.b.to(dev)
+    conv_w, A_log, dt_bias = w.conv_w.to(dev), w.A_log.to(dev), w.dt_bias.to(dev)
+    cpool, spool, slots, snap = w.conv_pool.to(dev), w.state_pool, w.slots.to(dev), w.snap.to(dev)
+    acc_src = w.snap[torch.arange(w.n_seqs), w.extra["accept"].long()].to(torch.int32).to(dev)
+    y = torch.empty_like(x)
+    nq = d.hqk * d.dk
+    qv = y.narrow(1, 0, nq).unflatten(1, (d.hqk, d.dk))
+    kv = y.narrow(1, nq, nq).unflatten(1, (d.hqk, d.dk))
+    vv = y.narrow(1, 2 * nq, d.hv * d.dv).unflatten(1, (d.hv, d.dv))
+    T = w.n_seqs * 4
+    g = torch.empty((T, d.hv), dtype=torch.float32, device=dev)
+    beta = torch.empty_like(g)
+    o = torch.empty((T, d.hv, d.dv), dtype=x.dtype, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(steps)]
+
+    def step(e=None):
+        if e is not None:
+            e[0].record(stream)
+        gdn.causal_conv1d_update(x, 4, conv_w, cpool, slots, snap_indices=snap, y=y)
+        gdn.gdn_gating(a, b, A_log, dt_bias, g=g, beta=beta)
+        if e is not None:
+            e[1].record(stream)
+        gdn.gdn_decode_recurrent(qv, kv, vv, g, beta, 4, spool, slots, snap_indices=snap,
+                                 scale=w.scale, o=o)
+        if e is not None:
+            e[2].record(stream)
+        gdn.gdn_state_snapshot(spool, acc_src, slots)
+        gdn.gdn_state_snapshot(cpool, acc_src, slots)
+
+    for _ in range(3):
+        step()
+        flush.zero_()
+    torch.cuda.synchronize(dev)
+    torch.cuda._sleep(1_000_000)
+    for i in range(steps):
+        step(ev[i])
+        flush.zero_()
+    torch.cuda.synchronize(dev)
+    dec = sum(e[1].elapsed_time(e[2]) for e in ev) / steps
+    # decode kernel algorithmic bytes: source state read once, 4 snapshots written
+    st = w.n_seqs * d.hv * d.dv * d.dk * 4
+    io = T * (2 * d.hqk * d.dk + 2 * d.hv * d.dv) * 2 + 2 * T * d.hv * 4
+    dec_bytes = st * 5 + io
+    peak = load_peaks()["hbm_gbs"]
+    del spool, w
+    return {"workload": "MTP: 128 sequences x 4 tokens, per-token state + conv snapshots, "
+                        "accept copy", "tokens_per_s_decode_kernel": round(T / (dec / 1e3), 1),
+            "decode_kernel_ms": round(dec, 5),
+            "decode_kernel_gbs": round(dec_bytes / (dec / 1e3) / 1e9, 1),
+            "decode_kernel_frac_hbm": round(dec_bytes / (dec / 1e3) / 1e9 / peak, 4),
+            "gpu_launches_per_step": 5}
+
+
+def prefill_flops_per_token(hv, dk, dv, chunk):
+    """Flops of the chunked form per token, full chunk x chunk tiles:
+    hv * (6 dk dv + 2 C (3 dk + 2 dv))."""
+    return hv * (6 * dk * dv + 2 * chunk * (3 * dk + 2 * dv))
+
+
+def bench_prefill(gdn, workloads, dev, flush, peaks, steps=5):
+    w = workloads.prefill()
+    d = w.dims
+    x = w.x.to(dev)
+    conv_w, A_log, dt_bias = w.conv_w.to(dev), w.A_log.to(dev), w.dt_bias.to(dev)
+    a, b = w.a.to(dev), w.b.to(dev)
+    cu, slots = w.cu_seqlens.to(dev), w.slots.to(dev)
+    has = w.has_initial_state.to(dev)
+    cpool = w.conv_pool.to(dev)
+    spool = torch.zeros((1024, d.hv, d.dv, d.dk), dtype=torch.float32, device=dev)
+    none = torch.full_like(slots, -1)
+    T = x.shape[0]
+    y = torch.empty_like(x)
+    nq = d.hqk * d.dk
+    qv = y.narrow(1, 0, nq).unflatten(1, (d.hqk, d.dk))
+    kv = y.narrow(1, nq, nq).unflatten(1, (d.hqk, d.dk))
+    vv = y.narrow(1, 2 * nq, d.hv * d.dv).unflatten(1, (d.hv, d.dv))
+    g = torch.empty((T, d.hv), dtype=torch.float32, device=dev)
+    beta = torch.empty_like(g)
+    o = torch.empty((T, d.hv, d.dv), dtype=x.dtype, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(steps)]
+
+    def step(e=None):
+        if e is not None:
+            e[0].record(stream)
+        gdn.causal_conv1d_fwd(x, conv_w, cu, cpool, slots, has, y=y)
+        if e is not None:
+            e[1].record(stream)
+        gdn.gdn_gating(a, b, A_log, dt_bias, g=g, beta=beta)
+        if e is not None:
+            e[2].record(stream)
+        gdn.gdn_prefill_chunked(qv, kv, vv, g, beta, cu, spool, none, slots, w.scale,
+                                chunk=w.chunk, o=o)
+        if e is not None:
+            e[3].record(stream)
+
+    for _ in range(2):
+        step()
+        flush.zero_()
+    torch.cuda.synchronize(dev)
+    for i in range(steps):
+        step(ev[i])
+        flush.zero_()
+    torch.cuda.synchronize(dev)
+    total = sum(e[0].elapsed_time(e[3]) for e in ev) / steps
+    conv = sum(e[0].elapsed_time(e[1]) for e in ev) / steps
+    pre = sum(e[2].elapsed_time(e[3]) for e in ev) / steps
+    flops = prefill_flops_per_token(d.hv, d.dk, d.dv, w.chunk) * T
+    tf = flops / (pre / 1e3) / 1e12
+    conv_bytes = 2 * T * d.channels * 2
+    return {"workload": f"prefill: 8 sequences, {T} tokens (lengths U[512, 8192]), conv fwd + "
+                        "gating + chunked prefill (chunk 64)",
+            "tokens_per_s": round(T / (total / 1e3), 1),
+            "layer_ms": round(total, 4), "prefill_kernel_ms": round(pre, 4),
+            "conv_kernel_ms": round(conv, 4),
+            "conv_gbs": round(conv_bytes / (conv / 1e3) / 1e9, 1),
+            "prefill_tflops": round(tf, 2),
+            "prefill_frac_bf16_peak": round(tf / peaks["bf16_tflops"], 4),
+            "flops_per_token": prefill_flops_per_token(d.hv, d.dk, d.dv, w.chunk)}
+
+
+# ------------------------------------------------------------ oracle (CPU) --
+
+def _oracle_decode_step(w, n, sub_pool):
+    """The CPU oracle on the first n sequences of a decode step: conv update,
+    gating, recurrent decode (the same three steps the GPU step runs)."""
+    import numpy as np
+
+    import oracle
+    d = w.dims
+    x = w.x[:n].double().numpy()
+    y, _ = oracle.conv1d_update(x, 1, w.conv_w.double().numpy(), None, w.conv_pool,
+                                w.slots[:n].numpy().astype(np.int64))
+    q, k, v = oracle.split_qkv(y, d.hqk, d.hv, d.dk, d.dv)
+    g, beta = oracle.gating(w.a[:n], w.b[:n], w.A_log, w.dt_bias)
+    oracle.gdn_decode(q, k, v, g, beta, 1, sub_pool, np.arange(n), scale=w.scale)
+
+
+def cpu_baseline(w, budget_s, n=None):
+    """Time the oracle as it stands on the host cores on whole decode steps
+    of the same workload, repeated until about budget_s seconds."""
+    n = w.n_seqs if n is None else n
+    sub = w.state_pool[w.slots[:n].long().to(w.state_pool.device)].cpu()
+    cores = os.cpu_count() or 1
+    t0 = time.perf_counter()
+    reps = 0
+    while True:
+        _oracle_decode_step(w, n, sub)
+        reps += 1
+        el = time.perf_counter() - t0
+        if el >= budget_s or reps >= 1000:
+            break
+    return {"value": round(reps * n / el, 2), "unit": UNIT, "cores": cores, "kind": "oracle",
+            "sample": f"{reps} x decode step of {n} sequences (conv update + gating + "
+                      f"recurrent decode, fp64 C oracle, {cores} threads), {el:.1f} s"}
+
+
+def run_reference(args):
+    rank, world, local = dist_env()
+    if rank != 0:
+        return
+    import workloads
+    w = workloads.decode()
+    n_probe = 8
+    sub = w.state_pool[w.slots[:n_probe].long()]
+    t0 = time.perf_counter()
+    _oracle_decode_step(w, n_probe, sub)
+    per_seq = (time.perf_counter() - t0) / n_probe
+    budget = 150.0
+    K, Wm = args.steps, args.warmup
+    n = int(max(1, min(w.n_seqs, budget / max(1, K + Wm) / per_seq)))
+    sub = w.state_pool[w.slots[:n].long()]
+    for _ in range(Wm):
+        _oracle_decode_step(w, n, sub)
+    t0 = time.perf_counter()
+    for _ in range(K):
+        _oracle_decode_step(w, n, sub)
+    el = time.perf_counter() - t0
+    value = K * n / el
+    cores = os.cpu_count() or 1
+    line = {"impl": "reference", "metric": METRIC, "value": round(value, 2), "unit": UNIT,
+            "n_gpus": world, "steps": K, "warmup": Wm, "ms_per_step": round(el / K * 1e3, 3),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic",
+            "config": {"workload": DECODE_WORKLOAD, "global_batch": n, "seq_len": 1,
+                       "sample": f"each step: the first {n} of the 256 sequences"},
+            "cpu_baseline": {"value": round(value, 2), "unit": UNIT, "cores": cores,
+                             "kind": "oracle",
+                             "sample": f"{K} steps x {n} sequences of the decode step"},
+            "e2e": {"value": round(value, 2), "unit": UNIT, "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

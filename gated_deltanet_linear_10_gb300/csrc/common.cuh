@@ -1,0 +1,123 @@
+// Shared device/host helpers of libgdn (internal header, not installed).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "gdn.h"
+
+namespace gdn {
+
+// ---------------------------------------------------------------- status --
+// Each translation unit owns one device status word; gdn_get_device_status
+// ORs them.  Kernels only ever set bits (atomicOr), never trap.
+#define GDN_DECLARE_STATUS_WORD(name)                                          \
+    __device__ unsigned int name = 0u;                                         \
+    __device__ __forceinline__ void flag_status(unsigned int bits) {           \
+        atomicOr(&name, bits);                                                 \
+    }
+
+// Host helpers implemented in api.cu.
+void set_last_cuda_error(cudaError_t e);
+gdn_status launch_status();  // cudaGetLastError() after a launch -> status
+
+// Per-TU readers of the status word (defined next to each word).
+gdn_status read_status_gating(uint32_t *out, int clear, cudaStream_t s);
+gdn_status read_status_conv(uint32_t *out, int clear, cudaStream_t s);
+gdn_status read_status_decode(uint32_t *out, int clear, cudaStream_t s);
+gdn_status read_status_prefill_simt(uint32_t *out, int clear, cudaStream_t s);
+gdn_status read_status_prefill_tc(uint32_t *out, int clear, cudaStream_t s);
+gdn_status read_status_api(uint32_t *out, int clear, cudaStream_t s);
+
+#define GDN_STATUS_READER(fn, word)                                             \
+    gdn_status fn(uint32_t *out, int clear, cudaStream_t s) {                  \
+        unsigned int v = 0;                                                    \
+        cudaError_t e = cudaMemcpyFromSymbolAsync(&v, word, sizeof(v), 0,      \
+                                                  cudaMemcpyDeviceToHost, s);  \
+        if (e == cudaSuccess) e = cudaStreamSynchronize(s);                    \
+        if (e == cudaSuccess && clear) {                                       \
+            unsigned int z = 0;                                                \
+            e = cudaMemcpyToSymbolAsync(word, &z, sizeof(z), 0,                \
+                                        cudaMemcpyHostToDevice, s);            \
+            if (e == cudaSuccess) e = cudaStreamSynchronize(s);                \
+        }                                                                      \
+        if (e != cudaSuccess) {                                                \
+            set_last_cuda_error(e);                                            \
+            return GDN_ERR_CUDA;                                               \
+        }                                                                      \
+        *out |= v;                                                             \
+        return GDN_OK;                                                         \
+    }
+
+// ------------------------------------------------------------ element io --
+template <typename T> struct Io;
+
+template <> struct Io<float> {
+    static __device__ __forceinline__ float load(const float *p) { return *p; }
+    static __device__ __forceinline__ void store(float *p, float v) { *p = v; }
+};
+
+template <> struct Io<__nv_bfloat16> {
+    static __device__ __forceinline__ float load(const __nv_bfloat16 *p) {
+        return __bfloat162float(*p);
+    }
+    static __device__ __forceinline__ void store(__nv_bfloat16 *p, float v) {
+        *p = __float2bfloat16_rn(v);
+    }
+};
+
+// Load 4 consecutive elements as fp32 (8-byte aligned for bf16, 16 for fp32).
+__device__ __forceinline__ float4 load4(const float *p) {
+    return *reinterpret_cast<const float4 *>(p);
+}
+__device__ __forceinline__ float4 load4(const __nv_bfloat16 *p) {
+    uint2 r = *reinterpret_cast<const uint2 *>(p);
+    __nv_bfloat162 lo = *reinterpret_cast<__nv_bfloat162 *>(&r.x);
+    __nv_bfloat162 hi = *reinterpret_cast<__nv_bfloat162 *>(&r.y);
+    float2 a = __bfloat1622float2(lo), b = __bfloat1622float2(hi);
+    return make_float4(a.x, a.y, b.x, b.y);
+}
+
+// Vector of N elements moved as 16 bytes: 8 bf16 or 4 fp32.
+template <typename T> struct Vec16;
+template <> struct Vec16<float> {
+    static constexpr int N = 4;
+    static __device__ __forceinline__ void load(const float *p, float *out) {
+        float4 v = *reinterpret_cast<const float4 *>(p);
+        out[0] = v.x; out[1] = v.y; out[2] = v.z; out[3] = v.w;
+    }
+    static __device__ __forceinline__ void store(float *p, const float *in) {
+        *reinterpret_cast<float4 *>(p) = make_float4(in[0], in[1], in[2], in[3]);
+    }
+};
+template <> struct Vec16<__nv_bfloat16> {
+    static constexpr int N = 8;
+    static __device__ __forceinline__ void load(const __nv_bfloat16 *p, float *out) {
+        uint4 r = *reinterpret_cast<const uint4 *>(p);
+        const __nv_bfloat162 *h = reinterpret_cast<const __nv_bfloat162 *>(&r);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            float2 f = __bfloat1622float2(h[i]);
+            out[2 * i] = f.x;
+            out[2 * i + 1] = f.y;
+        }
+    }
+    static __device__ __forceinline__ void store(__nv_bfloat16 *p, const float *in) {
+        uint4 r;
+        __nv_bfloat162 *h = reinterpret_cast<__nv_bfloat162 *>(&r);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) h[i] = __floats2bfloat162_rn(in[2 * i], in[2 * i + 1]);
+        *reinterpret_cast<uint4 *>(p) = r;
+    }
+};
+
+__device__ __forceinline__ float silu_f(float z) { return z / (1.0f + expf(-z)); }
+
+}  // namespace gdn
+
+// Host-side argument check helper.
+#define GDN_REQUIRE(cond, code)                                                \
+    do {                                                                       \
+        if (!(cond)) return (code);                                            \
+    } while (0)

@@ -1,0 +1,208 @@
+// Recurrent decode and MTP multi-token decode of the gated delta rule
+// ("fused recurrent GDN", "[model] support Qwen3next", Highlights; the MTP
+// linear-attention state copying of the same page's Highlights).
+//
+// One CTA per (sequence, V head).  The dv x dk fp32 state is streamed from
+// its slot into registers with 16-byte loads (lane l of a row group owns
+// columns [4l, 4l+4) of its rows), kept there across the tokens of the
+// sequence, and written once per token that has a destination slot.  Per
+// token and row the two dot products S k and S q are warp-shuffle
+// reductions over the row's lanes:
+//   u   = beta (v - alpha S k)
+//   S  <- alpha S + u k^T
+//   o   = scale (alpha S_old q + u (k . q))   (= scale S_new q)
+#include "common.cuh"
+
+namespace gdn {
+
+GDN_DECLARE_STATUS_WORD(g_status_decode)
+GDN_STATUS_READER(read_status_decode, g_status_decode)
+
+constexpr int kDecWarps = 8;
+constexpr int kDecThreads = kDecWarps * 32;
+constexpr int kMaxDv = 128;
+constexpr int kMaxTps = 16;
+constexpr float kL2Eps = 1e-6f;
+
+template <int LPR>
+__device__ __forceinline__ float row_sum(float v) {
+#pragma unroll
+    for (int o = LPR / 2; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+
+__device__ __forceinline__ float dot4(float4 a, float4 b) {
+    return fmaf(a.x, b.x, fmaf(a.y, b.y, fmaf(a.z, b.z, a.w * b.w)));
+}
+
+template <int DK, typename T>
+__global__ void __launch_bounds__(kDecThreads)
+decode_kernel(const T *__restrict__ q, int64_t qs, const T *__restrict__ k, int64_t ks,
+              const T *__restrict__ v, int64_t vs, const float *__restrict__ g,
+              const float *__restrict__ beta, int tps, int hv, int grp, int dv, float scale,
+              int l2norm, float *__restrict__ pool, int64_t n_slots,
+              const int32_t *__restrict__ idx, const int32_t *__restrict__ snap,
+              T *__restrict__ o) {
+    constexpr int LPR = DK / 4;                     // lanes per state row
+    constexpr int RPW = 32 / LPR;                   // rows per warp per pass
+    constexpr int RPP = RPW * kDecWarps;            // rows per pass
+    constexpr int NP = (kMaxDv + RPP - 1) / RPP;    // passes covering dv <= 128
+
+    __shared__ float o_s[kMaxTps][kMaxDv];
+    __shared__ float v_s[kMaxTps][kMaxDv];
+
+    const int i = blockIdx.x / hv;
+    const int h = blockIdx.x - i * hv;
+    const int hq = h / grp;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int col = (lane % LPR) * 4;
+    const int sub = lane / LPR;
+
+    const int64_t slot = idx[i];
+    const bool live = slot >= 0 && slot < n_slots;
+    if (slot >= n_slots && threadIdx.x == 0) flag_status(GDN_DEVSTAT_BAD_INDEX);
+    if (!live) {
+        for (int e = threadIdx.x; e < tps * dv; e += kDecThreads) {
+            const int t = e / dv, r = e - t * dv;
+            Io<T>::store(o + (((int64_t)i * tps + t) * hv + h) * dv + r, 0.0f);
+        }
+        return;
+    }
+
+    float *src = pool + ((slot * hv + h) * (int64_t)dv) * DK;
+    float4 st[NP];
+#pragma unroll
+    for (int p = 0; p < NP; ++p) {
+        const int r = p * RPP + warp * RPW + sub;
+        st[p] = r < dv ? __ldcs(reinterpret_cast<const float4 *>(src + (int64_t)r * DK + col))
+                       : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    for (int e = threadIdx.x; e < tps * dv; e += kDecThreads) {
+        const int t = e / dv, r = e - t * dv;
+        v_s[t][r] = Io<T>::load(v + ((int64_t)i * tps + t) * vs + (int64_t)h * dv + r);
+    }
+    __syncthreads();
+
+    for (int t = 0; t < tps; ++t) {
+        const int64_t row = (int64_t)i * tps + t;
+        float4 q4 = load4(q + row * qs + (int64_t)hq * DK + col);
+        float4 k4 = load4(k + row * ks + (int64_t)hq * DK + col);
+        if (l2norm) {
+            const float qn = rsqrtf(row_sum<LPR>(dot4(q4, q4)) + kL2Eps);
+            const float kn = rsqrtf(row_sum<LPR>(dot4(k4, k4)) + kL2Eps);
+            q4 = make_float4(q4.x * qn, q4.y * qn, q4.z * qn, q4.w * qn);
+            k4 = make_float4(k4.x * kn, k4.y * kn, k4.z * kn, k4.w * kn);
+        }
+        const float kq = row_sum<LPR>(dot4(k4, q4));
+        const float alpha = expf(g[row * hv + h]);
+        const float b = beta[row * hv + h];
+#pragma unroll
+        for (int p = 0; p < NP; ++p) {
+            const int r = p * RPP + warp * RPW + sub;
+            if (p * RPP < dv) {                      // warp-uniform: shuffles stay converged
+                const float4 s = st[p];
+                const float sk = row_sum<LPR>(dot4(s, k4));
+                const float sq = row_sum<LPR>(dot4(s, q4));
+                if (r < dv) {
+                    const float u = b * (v_s[t][r] - alpha * sk);
+                    st[p] = make_float4(fmaf(alpha, s.x, u * k4.x), fmaf(alpha, s.y, u * k4.y),
+                                        fmaf(alpha, s.z, u * k4.z), fmaf(alpha, s.w, u * k4.w));
+                    if ((lane % LPR) == 0) o_s[t][r] = scale * fmaf(alpha, sq, u * kq);
+                }
+            }
+        }
+        if (snap) {
+            const int64_t d = snap[row];
+            if (d >= n_slots) {
+                if (threadIdx.x == 0) flag_status(GDN_DEVSTAT_BAD_INDEX);
+            } else if (d >= 0) {
+                float *dst = pool + ((d * hv + h) * (int64_t)dv) * DK;
+#pragma unroll
+                for (int p = 0; p < NP; ++p) {
+                    const int r = p * RPP + warp * RPW + sub;
+                    if (r < dv) __stcs(reinterpret_cast<float4 *>(dst + (int64_t)r * DK + col), st[p]);
+                }
+            }
+        }
+    }
+    if (!snap) {
+#pragma unroll
+        for (int p = 0; p < NP; ++p) {
+            const int r = p * RPP + warp * RPW + sub;
+            if (r < dv) __stcs(reinterpret_cast<float4 *>(src + (int64_t)r * DK + col), st[p]);
+        }
+    }
+    __syncthreads();
+    for (int e = threadIdx.x; e < tps * dv; e += kDecThreads) {
+        const int t = e / dv, r = e - t * dv;
+        Io<T>::store(o + (((int64_t)i * tps + t) * hv + h) * dv + r, o_s[t][r]);
+    }
+}
+
+template <int DK, typename T>
+static void launch_decode(const void *q, int64_t qs, const void *k, int64_t ks, const void *v,
+                          int64_t vs, const float *g, const float *beta, int n_seqs, int tps,
+                          int hqk, int hv, int dv, float scale, int l2norm, float *pool,
+                          int64_t n_slots, const int32_t *idx, const int32_t *snap, void *o,
+                          cudaStream_t s) {
+    const int64_t blocks = (int64_t)n_seqs * hv;
+    decode_kernel<DK, T><<<(unsigned)blocks, kDecThreads, 0, s>>>(
+        (const T *)q, qs, (const T *)k, ks, (const T *)v, vs, g, beta, tps, hv, hv / hqk, dv,
+        scale, l2norm, pool, n_slots, idx, snap, (T *)o);
+}
+
+}  // namespace gdn
+
+using namespace gdn;
+
+extern "C" gdn_status gdn_decode_recurrent(const void *q, int64_t q_row_stride, const void *k,
+                                           int64_t k_row_stride, const void *v,
+                                           int64_t v_row_stride, const float *g,
+                                           const float *beta, int32_t n_seqs,
+                                           int32_t tokens_per_seq, int32_t hqk, int32_t hv,
+                                           int32_t dk, int32_t dv, float scale, int32_t l2norm_qk,
+                                           float *state_pool, int64_t n_slots,
+                                           const int32_t *state_indices,
+                                           const int32_t *snap_indices, void *o, int32_t dtype,
+                                           void *stream) {
+    GDN_REQUIRE(dtype == GDN_F32 || dtype == GDN_BF16, GDN_ERR_INVALID_ARG);
+    GDN_REQUIRE(n_seqs >= 0 && hqk > 0 && hv > 0 && n_slots >= 0, GDN_ERR_INVALID_ARG);
+    GDN_REQUIRE(hv % hqk == 0, GDN_ERR_INVALID_ARG);
+    GDN_REQUIRE(tokens_per_seq >= 1 && tokens_per_seq <= kMaxTps, GDN_ERR_UNSUPPORTED);
+    GDN_REQUIRE(dk == 16 || dk == 32 || dk == 64 || dk == 128, GDN_ERR_UNSUPPORTED);
+    GDN_REQUIRE(dv >= 1 && dv <= kMaxDv, GDN_ERR_UNSUPPORTED);
+    if (n_seqs == 0) return GDN_OK;
+    GDN_REQUIRE((int64_t)n_seqs * hv < (1ll << 31), GDN_ERR_UNSUPPORTED);
+    GDN_REQUIRE(q && k && v && g && beta && state_pool && state_indices && o, GDN_ERR_INVALID_ARG);
+    GDN_REQUIRE(q_row_stride >= (int64_t)hqk * dk && k_row_stride >= (int64_t)hqk * dk &&
+                    v_row_stride >= (int64_t)hv * dv,
+                GDN_ERR_INVALID_ARG);
+    const int64_t align = dtype == GDN_F32 ? 16 : 8;      // load4 of q/k rows
+    const int64_t elem = dtype == GDN_F32 ? 4 : 2;
+    GDN_REQUIRE(((uintptr_t)q % align) == 0 && ((uintptr_t)k % align) == 0, GDN_ERR_INVALID_ARG);
+    GDN_REQUIRE((q_row_stride * elem) % align == 0 && (k_row_stride * elem) % align == 0,
+                GDN_ERR_INVALID_ARG);
+    GDN_REQUIRE(((uintptr_t)state_pool % 16) == 0, GDN_ERR_INVALID_ARG);
+    cudaStream_t s = (cudaStream_t)stream;
+#define GDN_DEC(DK, T)                                                                          \
+    launch_decode<DK, T>(q, q_row_stride, k, k_row_stride, v, v_row_stride, g, beta, n_seqs,    \
+                         tokens_per_seq, hqk, hv, dv, scale, l2norm_qk, state_pool, n_slots,    \
+                         state_indices, snap_indices, o, s)
+    if (dtype == GDN_BF16) {
+        switch (dk) {
+            case 16: GDN_DEC(16, __nv_bfloat16); break;
+            case 32: GDN_DEC(32, __nv_bfloat16); break;
+            case 64: GDN_DEC(64, __nv_bfloat16); break;
+            default: GDN_DEC(128, __nv_bfloat16); break;
+        }
+    } else {
+        switch (dk) {
+            case 16: GDN_DEC(16, float); break;
+            case 32: GDN_DEC(32, float); break;
+            case 64: GDN_DEC(64, float); break;
+            default: GDN_DEC(128, float); break;
+        }
+    }
+#undef GDN_DEC
+    return launch_status();
+}

@@ -1,0 +1,65 @@
+// gdn_prefill_chunked entry point: argument checks and kernel choice.
+#include "common.cuh"
+
+namespace gdn {
+gdn_status prefill_simt(int dtype, int dk, int chunk, const void *q, int64_t qs, const void *k,
+                        int64_t ks, const void *v, int64_t vs, const float *g, const float *beta,
+                        const int32_t *cu, int n_seqs, int64_t n_tokens, int hqk, int hv,
+                        float scale, int l2norm, float *pool, int64_t n_slots, const int32_t *ii,
+                        const int32_t *fi, void *o, cudaStream_t s);
+bool prefill_tc_supported(int dtype, int dk, int dv, int chunk, const void *q, int64_t qs,
+                          const void *k, int64_t ks, const void *v, int64_t vs);
+gdn_status prefill_tc(const void *q, int64_t qs, const void *k, int64_t ks, const void *v,
+                      int64_t vs, const float *g, const float *beta, const int32_t *cu,
+                      int n_seqs, int64_t n_tokens, int hqk, int hv, float scale, int l2norm,
+                      float *pool, int64_t n_slots, const int32_t *ii, const int32_t *fi,
+                      void *o, cudaStream_t s);
+}  // namespace gdn
+
+using namespace gdn;
+
+extern "C" size_t gdn_prefill_workspace_size(int32_t n_seqs, int64_t n_tokens, int32_t hv,
+                                             int32_t dk, int32_t dv, int32_t chunk,
+                                             int32_t dtype) {
+    (void)n_seqs; (void)n_tokens; (void)hv; (void)dk; (void)dv; (void)chunk; (void)dtype;
+    return 0;
+}
+
+extern "C" gdn_status gdn_prefill_chunked(const void *q, int64_t q_row_stride, const void *k,
+                                          int64_t k_row_stride, const void *v, int64_t v_row_stride,
+                                          const float *g, const float *beta,
+                                          const int32_t *cu_seqlens, int32_t n_seqs,
+                                          int64_t n_tokens, int32_t hqk, int32_t hv, int32_t dk,
+                                          int32_t dv, float scale, int32_t l2norm_qk,
+                                          int32_t chunk, float *state_pool, int64_t n_slots,
+                                          const int32_t *initial_state_indices,
+                                          const int32_t *final_state_indices, void *o,
+                                          int32_t dtype, void *workspace, size_t workspace_bytes,
+                                          void *stream) {
+    (void)workspace; (void)workspace_bytes;
+    GDN_REQUIRE(dtype == GDN_F32 || dtype == GDN_BF16, GDN_ERR_INVALID_ARG);
+    GDN_REQUIRE(n_seqs >= 0 && n_tokens >= 0 && hqk > 0 && hv > 0 && n_slots >= 0,
+                GDN_ERR_INVALID_ARG);
+    GDN_REQUIRE(hv % hqk == 0, GDN_ERR_INVALID_ARG);
+    GDN_REQUIRE(dk == dv && (dk == 16 || dk == 32 || dk == 64 || dk == 128), GDN_ERR_UNSUPPORTED);
+    GDN_REQUIRE(chunk == 16 || chunk == 32 || chunk == 64, GDN_ERR_UNSUPPORTED);
+    if (n_seqs == 0) return n_tokens == 0 ? GDN_OK : GDN_ERR_INVALID_ARG;
+    GDN_REQUIRE((int64_t)n_seqs * hv * (dv / (dv < 32 ? dv : 32)) < (1ll << 31),
+                GDN_ERR_UNSUPPORTED);
+    GDN_REQUIRE(cu_seqlens && g && beta, GDN_ERR_INVALID_ARG);
+    GDN_REQUIRE(n_tokens == 0 || (q && k && v && o), GDN_ERR_INVALID_ARG);
+    GDN_REQUIRE(state_pool || (!initial_state_indices && !final_state_indices),
+                GDN_ERR_INVALID_ARG);
+    GDN_REQUIRE(q_row_stride >= (int64_t)hqk * dk && k_row_stride >= (int64_t)hqk * dk &&
+                    v_row_stride >= (int64_t)hv * dv,
+                GDN_ERR_INVALID_ARG);
+    cudaStream_t s = (cudaStream_t)stream;
+    if (prefill_tc_supported(dtype, dk, dv, chunk, q, q_row_stride, k, k_row_stride, v,
+                             v_row_stride))
+        return prefill_tc(q, q_row_stride, k, k_row_stride, v, v_row_stride, g, beta, cu_seqlens,
+                          n_seqs, n_tokens, hqk, hv, scale, l2norm_qk, state_pool, n_slots,
+                          initial_state_indices, final_state_indices, o, s);
+    return prefill_simt(dtype, dk, chunk, q, q_row_stride, k, k_row_stride, v, v_row_stride, g,
+                        beta, cu_seqlens, n_seqs, n_tokens, hqk, hv, scale, l2norm_qk,
+                        state_pool, n_slots, initial_state_indices, final_state_indices, o, s);
+}

@@ -1,0 +1,242 @@
+/*
+ * gdn.h — C ABI of libgdn, the GB300 (sm_103a) Gated DeltaNet layer.
+ *
+ * The layer is the linear-attention block of the Qwen3-Next hybrid model as
+ * the LightLLM pull request "[model] support Qwen3next" (Highlights: causal 1D
+ * convolutions, fused recurrent GDN, fused gating; linear-attention state
+ * copying for MTP; a cache manager for linear-attention states), the LightLLM
+ * issue "[model] Support Qwen3next" (Highlights: causal conv1d, fused GDN
+ * gating, chunked and recurrent linear-attention operations) and the lmdeploy
+ * issue "[Feature] Qwen3-Next-80B-A3B Support" (New attention kernels: 16 QK
+ * heads, 32 V heads, head_dim 128) describe it.  The pages print no formula;
+ * this library computes the standard gated delta rule:
+ *
+ *   g_t    = -exp(A_log[h]) * softplus(a_t + dt_bias[h]),  beta_t = sigmoid(b_t)
+ *   S_t    = exp(g_t) * S_{t-1} (I - beta_t k_t k_t^T) + beta_t v_t k_t^T
+ *   o_t    = scale * S_t q_t,   q, k L2-normalised per head (eps 1e-6)
+ *
+ * preceded by a causal depthwise conv1d + SiLU over the channel stream
+ * [q (hqk*dk) | k (hqk*dk) | v (hv*dv)].  V head h uses QK head
+ * h / (hv / hqk).  S is dv x dk, row-major (row = value index).
+ *
+ * Conventions shared by every entry point
+ *   - Every pointer argument is a DEVICE pointer (cudaMalloc'd or torch
+ *     storage) unless its comment says otherwise; the caller owns all memory.
+ *     The library allocates no device memory.
+ *   - `stream` is a cudaStream_t passed as void*; NULL is the legacy default
+ *     stream.  Every call is asynchronous on that stream and performs no host
+ *     synchronisation (so it may be captured in a CUDA graph), except
+ *     gdn_get_device_status, which synchronises `stream`.
+ *   - Host-side argument checks return GDN_ERR_INVALID_ARG (bad pointer or
+ *     size) or GDN_ERR_UNSUPPORTED (valid but not built, e.g. a head size);
+ *     in both cases nothing is launched.  A failed launch returns
+ *     GDN_ERR_LAUNCH.  Nothing throws across this boundary.
+ *   - Values that live on the device (slot indices, cu_seqlens) are checked
+ *     by the kernels: an index outside [0, n_slots) is skipped (as if < 0)
+ *     and sets GDN_DEVSTAT_BAD_INDEX in the device status word.
+ *   - Element counts and strides are in ELEMENTS, not bytes.
+ *   - dtype: GDN_F32 = fp32 activations, GDN_BF16 = bf16 activations.
+ *     g, beta, A_log, dt_bias and the recurrent state pool are always fp32.
+ *   - Two entries of one call naming the same slot (twice as a destination,
+ *     or as the source of one and the destination of another) give an
+ *     undefined result.
+ */
+#ifndef GDN_H
+#define GDN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum gdn_status {
+    GDN_OK = 0,
+    GDN_ERR_INVALID_ARG = 1,  /* a host-side argument check failed; nothing ran */
+    GDN_ERR_UNSUPPORTED = 2,  /* shape/dtype combination not built; nothing ran */
+    GDN_ERR_LAUNCH = 3,       /* a kernel launch failed (CUDA error recorded)   */
+    GDN_ERR_CUDA = 4          /* another CUDA runtime call failed               */
+} gdn_status;
+
+typedef enum gdn_dtype {
+    GDN_F32 = 0,
+    GDN_BF16 = 1
+} gdn_dtype;
+
+/* Bits of the device status word (gdn_get_device_status). */
+#define GDN_DEVSTAT_BAD_INDEX 0x1u  /* a slot index >= n_slots was skipped      */
+#define GDN_DEVSTAT_BAD_SEQLEN 0x2u /* cu_seqlens not non-decreasing / > n_tokens */
+#define GDN_DEVSTAT_TIMEOUT 0x4u    /* a bounded wait inside a kernel gave up     */
+
+/* Human-readable name of a status code (static string, never NULL). */
+const char *gdn_status_string(gdn_status s);
+
+/* Library version string, e.g. "gdn 0.1.0 sm_103a" (static, never NULL). */
+const char *gdn_version(void);
+
+/* Text of the last CUDA error seen by this thread's calls ("" if none). */
+const char *gdn_last_cuda_error(void);
+
+/*
+ * Fused gating ("fused gating", "[model] support Qwen3next", Highlights;
+ * "fused GDN gating", "[model] Support Qwen3next", Highlights):
+ *   g[t][h]    = -exp(A_log[h]) * softplus(a[t][h] + dt_bias[h])
+ *   beta[t][h] = sigmoid(b[t][h])
+ * a, b: [n_tokens][hv] in `in_dtype`, contiguous.  A_log, dt_bias: [hv] fp32.
+ * g, beta: [n_tokens][hv] fp32 outputs.  n_tokens may be 0 (no launch).
+ */
+gdn_status gdn_gating(const void *a, const void *b, const float *A_log,
+                      const float *dt_bias, int64_t n_tokens, int32_t hv,
+                      int32_t in_dtype, float *g, float *beta, void *stream);
+
+/*
+ * Causal depthwise conv1d + optional SiLU over packed variable-length
+ * sequences ("causal 1D convolutions", "[model] support Qwen3next",
+ * Highlights).  For token t of a sequence and channel c:
+ *   y[t][c] = act(bias[c] + sum_{w<width} weight[c][w] * e[t-(width-1)+w][c])
+ * where e is the sequence's inputs preceded by its width-1 history rows.
+ *   x: [n_tokens] rows, row r at x + r*x_row_stride, `channels` elements
+ *      each (x_row_stride >= channels).
+ *   weight: [channels][width], bias: [channels] or NULL (both in `dtype`).
+ *   cu_seqlens: [n_seqs+1] int32, cu_seqlens[0] = 0, non-decreasing,
+ *      cu_seqlens[n_seqs] = n_tokens.  Zero-length sequences are allowed.
+ *   conv_state_pool: [n_slots][width-1][channels] in `dtype`; slot s holds the
+ *      last width-1 pre-activation inputs, oldest first.
+ *   state_indices: [n_seqs] int32.  < 0: zero history, final state not
+ *      written.  Otherwise the final state is written to that slot, and the
+ *      history is read from it unless has_initial_state[i] == 0.
+ *   has_initial_state: [n_seqs] uint8, or NULL (= every slot holds history).
+ *   y: [n_tokens][channels] contiguous, `dtype`; y must not alias x.
+ * width in [2, 4]; channels a multiple of 8.
+ */
+gdn_status causal_conv1d_fwd(const void *x, int64_t x_row_stride,
+                             const void *weight, const void *bias,
+                             const int32_t *cu_seqlens, int32_t n_seqs,
+                             int64_t n_tokens, int32_t channels, int32_t width,
+                             void *conv_state_pool, int64_t n_slots,
+                             const int32_t *state_indices,
+                             const uint8_t *has_initial_state, int32_t silu,
+                             void *y, int32_t dtype, void *stream);
+
+/*
+ * Conv1d decode update for tokens_per_seq new tokens per sequence (1 =
+ * decode, mtp_step+1 = MTP; token t of sequence i is row i*tokens_per_seq+t,
+ * the layout of "Qwen3 mtp dense", LightLLM pull request 1159, review of the
+ * per-request b_seq_len slicing).  Same arithmetic as causal_conv1d_fwd with
+ * the slot's state as history.
+ *   x, y: [n_seqs*tokens_per_seq][channels] contiguous.
+ *   state_indices: [n_seqs]; < 0 = padding row: y rows zero, nothing read
+ *      or written.
+ *   snap_indices: NULL -> the slot is updated in place.  Otherwise
+ *      [n_seqs][tokens_per_seq] int32: the slot is only read and the state
+ *      after token t is written to slot snap_indices[i][t] (< 0: skipped).
+ * width in [2, 4]; channels a multiple of 8; tokens_per_seq in [1, 16].
+ */
+gdn_status causal_conv1d_update(const void *x, int32_t n_seqs,
+                                int32_t tokens_per_seq, int32_t channels,
+                                int32_t width, const void *weight,
+                                const void *bias, void *conv_state_pool,
+                                int64_t n_slots, const int32_t *state_indices,
+                                const int32_t *snap_indices, int32_t silu,
+                                void *y, int32_t dtype, void *stream);
+
+/*
+ * Chunked varlen prefill of the gated delta rule in WY/UT form ("a suite of
+ * Flash Linear Attention operations for efficient chunked ... computations",
+ * "[model] Support Qwen3next", Highlights).  Per sequence i and V head h the
+ * tokens are taken in chunks of `chunk` from the sequence start; the result
+ * equals the token-by-token recurrence up to rounding.
+ *   q: token t, QK head j at q + t*q_row_stride + j*dk (same for k);
+ *   v: token t, V head h at v + t*v_row_stride + h*dv.  (Views into the
+ *      conv output [T][channels] have row stride = channels.)
+ *   g, beta: [n_tokens][hv] fp32 (gdn_gating output).
+ *   cu_seqlens: as for causal_conv1d_fwd.
+ *   state_pool: [n_slots][hv][dv][dk] fp32.
+ *   initial_state_indices: [n_seqs]; < 0 = zero initial state.
+ *   final_state_indices: [n_seqs]; < 0 = final state not written.  It may
+ *      equal the initial index of the same sequence (in-place carry).
+ *   o: [n_tokens][hv][dv] contiguous, `dtype`.
+ *   scale: multiplies o (usually dk^-1/2).  l2norm_qk: normalise q, k.
+ *   workspace / workspace_bytes: scratch of at least
+ *      gdn_prefill_workspace_size(...) bytes (may be NULL when that is 0).
+ * Built: dk = dv in {16, 32, 64, 128}, chunk in {16, 32, 64} (any dtype);
+ * hv a multiple of hqk.
+ */
+gdn_status gdn_prefill_chunked(const void *q, int64_t q_row_stride,
+                               const void *k, int64_t k_row_stride,
+                               const void *v, int64_t v_row_stride,
+                               const float *g, const float *beta,
+                               const int32_t *cu_seqlens, int32_t n_seqs,
+                               int64_t n_tokens, int32_t hqk, int32_t hv,
+                               int32_t dk, int32_t dv, float scale,
+                               int32_t l2norm_qk, int32_t chunk,
+                               float *state_pool, int64_t n_slots,
+                               const int32_t *initial_state_indices,
+                               const int32_t *final_state_indices, void *o,
+                               int32_t dtype, void *workspace,
+                               size_t workspace_bytes, void *stream);
+
+/* Bytes of scratch gdn_prefill_chunked needs for these sizes (may be 0). */
+size_t gdn_prefill_workspace_size(int32_t n_seqs, int64_t n_tokens,
+                                  int32_t hv, int32_t dk, int32_t dv,
+                                  int32_t chunk, int32_t dtype);
+
+/*
+ * Recurrent decode ("fused recurrent GDN", "[model] support Qwen3next",
+ * Highlights) for tokens_per_seq tokens per sequence (1 = decode, 4 = MTP
+ * with mtp_step 3; row i*tokens_per_seq + t).  Each (sequence, V head) state
+ * is read once, kept on chip across the tokens and written once per token
+ * that has a destination.
+ *   q, k, v: as for gdn_prefill_chunked (rows are tokens).
+ *   g, beta: [n_seqs*tokens_per_seq][hv] fp32.
+ *   state_pool: [n_slots][hv][dv][dk] fp32.
+ *   state_indices: [n_seqs]; < 0 = padding: o rows zero, no state touched.
+ *   snap_indices: NULL -> the state after the last token is written back
+ *      to state_indices[i] (in place).  Otherwise [n_seqs][tokens_per_seq]:
+ *      state_indices[i] is only read, and the state after token t is written
+ *      to slot snap_indices[i][t] (< 0: skipped) — the per-draft-token
+ *      snapshots MTP accept/rollback needs.
+ *   o: [n_seqs*tokens_per_seq][hv][dv] contiguous, `dtype`.
+ * Built: dk in {16, 32, 64, 128}, dv <= 128 multiple of 8,
+ * tokens_per_seq in [1, 16].
+ */
+gdn_status gdn_decode_recurrent(const void *q, int64_t q_row_stride,
+                                const void *k, int64_t k_row_stride,
+                                const void *v, int64_t v_row_stride,
+                                const float *g, const float *beta,
+                                int32_t n_seqs, int32_t tokens_per_seq,
+                                int32_t hqk, int32_t hv, int32_t dk, int32_t dv,
+                                float scale, int32_t l2norm_qk,
+                                float *state_pool, int64_t n_slots,
+                                const int32_t *state_indices,
+                                const int32_t *snap_indices, void *o,
+                                int32_t dtype, void *stream);
+
+/*
+ * Whole-slot copy pool[dst[i]] <- pool[src[i]], bit for bit (the buffer copy
+ * from source to destination indices of "[model] support Qwen3next", review
+ * of the MTP buffer copy).  Used for the recurrent pool (slot_bytes =
+ * hv*dv*dk*4) and the conv pool (slot_bytes = (width-1)*channels*elem).
+ *   pool: base of [n_slots] slots of slot_bytes bytes each; 16-byte aligned,
+ *      slot_bytes a multiple of 16.
+ *   src, dst: [n] int32 device arrays; an entry < 0 on either side is
+ *      skipped.  A slot used as a destination must not be a source in the
+ *      same call.
+ */
+gdn_status gdn_state_snapshot(void *pool, int64_t n_slots, int64_t slot_bytes,
+                              const int32_t *src, const int32_t *dst,
+                              int32_t n, void *stream);
+
+/*
+ * Reads the device status word (bits GDN_DEVSTAT_*) of the current device
+ * into *out (a HOST pointer), synchronising `stream` first.  If clear != 0
+ * the word is reset to 0 afterwards.
+ */
+gdn_status gdn_get_device_status(uint32_t *out, int32_t clear, void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GDN_H */

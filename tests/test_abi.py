@@ -1,0 +1,96 @@
+"""The C ABI without a GPU: the library builds and loads, exports every entry
+point include/gdn.h declares, and rejects bad arguments on the host before
+touching the device (these calls never reach the CUDA runtime)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "gdn.h")
+
+
+def _declared():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return re.findall(r"^\s*(?:const\s+)?\w+\s*\*?\s*(\w+)\s*\(", text, flags=re.M)
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from gated_deltanet_linear_10_gb300 import build
+    path = build.build()
+    return ctypes.CDLL(path)
+
+
+def test_header_declares_the_entry_points():
+    names = set(_declared())
+    assert {"gdn_gating", "causal_conv1d_fwd", "causal_conv1d_update", "gdn_prefill_chunked",
+            "gdn_decode_recurrent", "gdn_state_snapshot", "gdn_get_device_status"} <= names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    missing = [n for n in _declared() if not hasattr(lib, n)]
+    assert not missing, missing
+
+
+def test_binding_lists_every_export(lib):
+    import gated_deltanet_linear_10_gb300 as gdn
+    assert set(gdn.EXPORTS) == set(_declared())
+
+
+def test_status_strings_and_version(lib):
+    lib.gdn_status_string.restype = ctypes.c_char_p
+    lib.gdn_version.restype = ctypes.c_char_p
+    assert lib.gdn_status_string(0) == b"GDN_OK"
+    assert lib.gdn_status_string(1) == b"GDN_ERR_INVALID_ARG"
+    assert lib.gdn_status_string(2) == b"GDN_ERR_UNSUPPORTED"
+    assert lib.gdn_status_string(99) == b"GDN_STATUS_UNKNOWN"
+    assert b"sm_103a" in lib.gdn_version()
+
+
+V, I32, I64, F32 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_float
+FAKE = V(0x1000)   # never dereferenced: every call below fails its host check first
+
+
+def test_host_argument_checks(lib):
+    # gating: null outputs / bad dtype / negative sizes
+    f = lib.gdn_gating
+    f.argtypes = [V, V, V, V, I64, I32, I32, V, V, V]
+    assert f(FAKE, FAKE, FAKE, FAKE, 4, 2, 1, None, FAKE, None) == 1
+    assert f(FAKE, FAKE, FAKE, FAKE, 4, 2, 7, FAKE, FAKE, None) == 1
+    assert f(FAKE, FAKE, FAKE, FAKE, -1, 2, 1, FAKE, FAKE, None) == 1
+    assert f(None, None, None, None, 0, 2, 1, None, None, None) == 0     # empty: no launch
+    # decode: unsupported head size, hv not a multiple of hqk, too many tokens
+    d = lib.gdn_decode_recurrent
+    d.argtypes = [V, I64, V, I64, V, I64, V, V, I32, I32, I32, I32, I32, I32, F32, I32, V, I64,
+                  V, V, V, I32, V]
+    args = lambda tps, hqk, hv, dk, dv: (FAKE, 2048, FAKE, 2048, FAKE, 4096, FAKE, FAKE, 4, tps,
+                                         hqk, hv, dk, dv, 1.0, 1, FAKE, 8, FAKE, None, FAKE, 1,
+                                         None)
+    assert d(*args(1, 16, 32, 96, 128)) == 2
+    assert d(*args(1, 16, 24, 128, 128)) == 1
+    assert d(*args(17, 16, 32, 128, 128)) == 2
+    # prefill: dk != dv, unsupported chunk
+    p = lib.gdn_prefill_chunked
+    p.argtypes = [V, I64, V, I64, V, I64, V, V, V, I32, I64, I32, I32, I32, I32, F32, I32, I32, V,
+                  I64, V, V, V, I32, V, ctypes.c_size_t, V]
+    base = [FAKE, 2048, FAKE, 2048, FAKE, 4096, FAKE, FAKE, FAKE, 2, 100, 16, 32, 128, 128, 1.0, 1,
+            64, FAKE, 8, FAKE, FAKE, FAKE, 1, None, 0, None]
+    bad = list(base); bad[14] = 64
+    assert p(*bad) == 2
+    bad = list(base); bad[17] = 48
+    assert p(*bad) == 2
+    bad = list(base); bad[1] = 100      # row stride shorter than hqk*dk
+    assert p(*bad) == 1
+    # conv: width 5 unsupported, channels not a multiple of 8
+    c = lib.causal_conv1d_update
+    c.argtypes = [V, I32, I32, I32, I32, V, V, V, I64, V, V, I32, V, I32, V]
+    assert c(FAKE, 4, 1, 8192, 5, FAKE, None, FAKE, 8, FAKE, None, 1, FAKE, 1, None) == 2
+    assert c(FAKE, 4, 1, 8190, 4, FAKE, None, FAKE, 8, FAKE, None, 1, FAKE, 1, None) == 2
+    # snapshot: slot size not a multiple of 16 bytes
+    s = lib.gdn_state_snapshot
+    s.argtypes = [V, I64, I64, V, V, I32, V]
+    assert s(FAKE, 8, 24, FAKE, FAKE, 2, None) == 1
+    assert s(FAKE, 8, 32, FAKE, FAKE, 0, None) == 0
