@@ -19,8 +19,8 @@ def _declared():
 
 @pytest.fixture(scope="module")
 def lib():
-    from gated_deltanet_linear_10_gb300 import build
-    path = build.build()
+    import __graft_entry__
+    path = __graft_entry__._build_module().build()
     return ctypes.CDLL(path)
 
 
