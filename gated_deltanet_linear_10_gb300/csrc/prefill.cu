@@ -46,8 +46,8 @@ extern "C" gdn_status gdn_prefill_chunked(const void *q, int64_t q_row_stride, c
     if (n_seqs == 0) return n_tokens == 0 ? GDN_OK : GDN_ERR_INVALID_ARG;
     GDN_REQUIRE((int64_t)n_seqs * hv * (dv / (dv < 32 ? dv : 32)) < (1ll << 31),
                 GDN_ERR_UNSUPPORTED);
-    GDN_REQUIRE(cu_seqlens && g && beta, GDN_ERR_INVALID_ARG);
-    GDN_REQUIRE(n_tokens == 0 || (q && k && v && o), GDN_ERR_INVALID_ARG);
+    GDN_REQUIRE(cu_seqlens != nullptr, GDN_ERR_INVALID_ARG);
+    GDN_REQUIRE(n_tokens == 0 || (q && k && v && o && g && beta), GDN_ERR_INVALID_ARG);
     GDN_REQUIRE(state_pool || (!initial_state_indices && !final_state_indices),
                 GDN_ERR_INVALID_ARG);
     GDN_REQUIRE(q_row_stride >= (int64_t)hqk * dk && k_row_stride >= (int64_t)hqk * dk &&
