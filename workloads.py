@@ -113,9 +113,7 @@ def pool_normal(n_slots, dims: Dims, std, seed, device="cpu"):
     g = torch.Generator(device=device)
     g.manual_seed(seed)
     out = torch.empty((n_slots, dims.hv, dims.dv, dims.dk), dtype=torch.float32, device=device)
-    # fill slot by slot to bound the temporary memory of the generator
-    for s in range(n_slots):
-        out[s].normal_(0.0, std, generator=g)
+    out.normal_(0.0, std, generator=g)
     return out
 
 
