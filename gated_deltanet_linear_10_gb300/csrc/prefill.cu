@@ -54,8 +54,8 @@ extern "C" gdn_status gdn_prefill_chunked(const void *q, int64_t q_row_stride, c
                     v_row_stride >= (int64_t)hv * dv,
                 GDN_ERR_INVALID_ARG);
     cudaStream_t s = (cudaStream_t)stream;
-    if (prefill_tc_supported(dtype, dk, dv, chunk, q, q_row_stride, k, k_row_stride, v,
-                             v_row_stride))
+    if (n_tokens > 0 && prefill_tc_supported(dtype, dk, dv, chunk, q, q_row_stride, k,
+                                             k_row_stride, v, v_row_stride))
         return prefill_tc(q, q_row_stride, k, k_row_stride, v, v_row_stride, g, beta, cu_seqlens,
                           n_seqs, n_tokens, hqk, hv, scale, l2norm_qk, state_pool, n_slots,
                           initial_state_indices, final_state_indices, o, s);
