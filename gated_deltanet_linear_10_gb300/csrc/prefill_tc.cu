@@ -3,26 +3,30 @@
 // ("Flash Linear Attention operations for efficient chunked computations",
 // "[model] Support Qwen3next", Highlights).
 //
-// One CTA per (sequence, V head) chain; 10 warps:
-//   warp 0      TMA producer: raw K|Q tiles (3 stages) and V tiles (2 stages)
-//   warp 1      TMEM owner + the single thread that issues every tcgen05.mma
-//   warps 2..5  "prep": everything that does not depend on the state, one
-//               chunk ahead of the chain (gating prefix sums, q/k norms, the
-//               UT transform T = (I + A)^-1 by a blocked fp32 solve, P)
-//   warps 6..9  "chain": the state-dependent epilogues
+// One CTA per (sequence, V head) chain; 14 warps:
+//   warp 0        TMA producer: raw K|Q tiles (3 stages) and V tiles (2 stages)
+//   warp 1        TMEM owner + the single thread that issues every tcgen05.mma
+//   warps 2..9    "prep": everything that does not depend on the state, one
+//                 chunk ahead of the chain (gating prefix sums, q/k norms,
+//                 the UT transform T = (I + A)^-1 by a blocked fp32 solve, P)
+//   warps 10..13  "chain": the state-dependent epilogues
 //
 // Per chunk (rows i, j = tokens, b = value index, a = key index; S is the
-// fp32 state [b][a]; gc = prefix sum of g, Gam = exp(gc); D = exp(gc_i-gc_j)):
-//   M1  G  = [K;Q] K^T                    (prep: A from the K rows, P from the Q rows)
-//   M2  X  = S K^T          X[b][j]       (A operand: bf16 copy of S in TMEM)
-//   M3  O  = S Q'^T         Q' = scale Gam r_q Q (rows rescaled in place)
-//   E1  R[b][j] = beta_j (V[j][b] - Gam_j r_k,j X[b][j])   -> bf16 into TMEM
-//   M4  U  = R T^T          U[b][i] = (T R)[i][b]
+// fp32 state [b][a]; gc = prefix sum of g, Gam = exp(gc); D = exp(gc_i-gc_j);
+// r_k, r_q = inverse L2 norms):
+//   M1  G  = [K;Q] K^T                  prep: A (K rows) and P (Q rows) from G
+//   MU  U  = T1 V                       T1 = T diag(beta)         (V^T read MN-major)
+//   M2  X  = S K^T       X[b][j]        A operand: bf16 copy of S in TMEM
+//   M3  O  = S Q'^T                     Q' = scale Gam r_q Q (rows rescaled in place)
+//   E1  X -> bf16 in TMEM
+//   M4  U += T2 X^T                     T2 = -T diag(beta Gam r_k), so that
+//                                       U = T diag(beta) (V - diag(Gam r_k) K S^T)
 //   E2  U -> bf16 in TMEM
-//   M5  O += U P^T          P[i][j] = scale D_ij r_q,i r_k,j (q_i . k_j), j <= i
-//   M6  S += U K''          K''_j = D[last][j] r_k,j K_j (rows rescaled in place),
-//                           S pre-scaled by Gam_last in E1
-//   E3  o <- O, S -> bf16 copy for the next chunk (final state -> pool)
+//   M5  O += U P^T       P[i][j] = scale D_ij r_q,i r_k,j (q_i . k_j), j <= i
+//   M6  S += U K''       K''_j = D[last][j] r_k,j K_j (rows rescaled in place);
+//                        S was pre-scaled by Gam_last by the previous epilogue
+//   E3  S -> bf16 copy (and pre-scaled for the next chunk), then o <- O
+//       (O is double-buffered, so the o stores leave the critical path)
 // Padded rows of a partial last chunk get beta = g = 0 and explicit zero masks.
 #include "common.cuh"
 #include "tc.cuh"
@@ -37,16 +41,20 @@ using namespace tc;
 
 constexpr int C = 64;                  // chunk
 constexpr int DH = 128;                // dk = dv
-constexpr int kThreads = 320;
+constexpr int kWarps = 14;
+constexpr int kThreads = kWarps * 32;
+constexpr int kPrepThreads = 256;
+constexpr int kChainThreads = 128;
 constexpr int kKQStages = 3;
 constexpr int kVStages = 2;
 constexpr uint32_t kKQBytes = 2 * 128 * 128;     // 2 k-blocks x (64 K rows + 64 Q rows) x 128 B
 constexpr uint32_t kKBlk = 128 * 128;            // k-block stride inside a K|Q stage
 constexpr uint32_t kVBytes = 2 * 64 * 128;       // 2 k-blocks x 64 rows x 128 B
 constexpr uint32_t kVBlk = 64 * 128;
-constexpr uint32_t kTBytes = 64 * 128;           // T[i][j], one k-block
-constexpr uint32_t kPBytes = 64 * 128;           // P[i][j]
+constexpr uint32_t kMatBytes = 64 * 128;         // one 64 x 64 bf16 operand, one k-block
+constexpr uint32_t kDBytes = 3 * kMatBytes;      // derived stage: T1, T2, P
 constexpr int kLd = 68;                          // fp32 row stride of the solve scratch
+constexpr int kWbLd = 12;                        // row stride of a warp's 16 x 8 scratch
 constexpr float kEps = 1e-6f;
 
 // TMEM columns
@@ -66,16 +74,17 @@ struct Bars {
     uint32_t tmem_base;
     int abort;
     int seq;
+    float tot0;
 };
 
 constexpr uint32_t OFF_KQ = 0;
 constexpr uint32_t OFF_V = OFF_KQ + kKQStages * kKQBytes;
-constexpr uint32_t OFF_T = OFF_V + kVStages * kVBytes;
-constexpr uint32_t OFF_P = OFF_T + 2 * kTBytes;
-constexpr uint32_t OFF_AF = OFF_P + 2 * kPBytes;
+constexpr uint32_t OFF_D = OFF_V + kVStages * kVBytes;
+constexpr uint32_t OFF_AF = OFF_D + 2 * kDBytes;
 constexpr uint32_t OFF_TF = OFF_AF + C * kLd * 4;
 constexpr uint32_t OFF_WB = OFF_TF + C * kLd * 4;
-constexpr uint32_t OFF_SCAL = OFF_WB + 4 * 16 * 20 * 4;
+constexpr uint32_t kWbFloats = 8 * 16 * kWbLd + 16 * 16;   // 8 warps' 16x8 scratch + Z30
+constexpr uint32_t OFF_SCAL = OFF_WB + kWbFloats * 4;
 constexpr uint32_t kScalBytes = (sizeof(Scal) + 127) / 128 * 128;
 constexpr uint32_t OFF_BARS = OFF_SCAL + 2 * kScalBytes;
 constexpr uint32_t SMEM_USED = OFF_BARS + (sizeof(Bars) + 127) / 128 * 128;
@@ -105,39 +114,49 @@ __device__ int seq_for_rank(const int32_t *cu, int n_seqs, int rank, int *slot) 
     return *slot < 0 ? rank : *slot;
 }
 
-// 16x16 block products for the blocked UT solve.  A warp owns one block;
-// lane (r = lane/2, hh = lane%2) holds row r, columns 8hh .. 8hh+7.
-__device__ __forceinline__ void blk_mac(float (&acc)[8], const float *X, int xr, int xc,
-                                        const float *Y, int yr, int yc, int r, int hh) {
+// Blocked UT solve helpers.  The 64 x 64 matrices are 4 x 4 blocks of 16.
+// A warp computes half a block (16 rows x 8 columns): lane (r = lane/2,
+// cg = lane%2) owns row r, columns col + 4cg .. col + 4cg + 3.
+//   acc += X[xr.., xc..] (16 x 16) * Y[yr.., col..]
+__device__ __forceinline__ void half_mac(float (&acc)[4], const float *X, int xr, int xc,
+                                         const float *Y, int yr, int col, int r, int cg) {
 #pragma unroll
     for (int kk = 0; kk < 16; ++kk) {
         const float x = X[(xr + r) * kLd + xc + kk];
-        const float4 y0 = *reinterpret_cast<const float4 *>(Y + (yr + kk) * kLd + yc + 8 * hh);
-        const float4 y1 = *reinterpret_cast<const float4 *>(Y + (yr + kk) * kLd + yc + 8 * hh + 4);
-        acc[0] = fmaf(x, y0.x, acc[0]); acc[1] = fmaf(x, y0.y, acc[1]);
-        acc[2] = fmaf(x, y0.z, acc[2]); acc[3] = fmaf(x, y0.w, acc[3]);
-        acc[4] = fmaf(x, y1.x, acc[4]); acc[5] = fmaf(x, y1.y, acc[5]);
-        acc[6] = fmaf(x, y1.z, acc[6]); acc[7] = fmaf(x, y1.w, acc[7]);
+        const float4 y = *reinterpret_cast<const float4 *>(Y + (yr + kk) * kLd + col + 4 * cg);
+        acc[0] = fmaf(x, y.x, acc[0]);
+        acc[1] = fmaf(x, y.y, acc[1]);
+        acc[2] = fmaf(x, y.z, acc[2]);
+        acc[3] = fmaf(x, y.w, acc[3]);
     }
 }
-
-// Tf[bi][bj] = -Tf[bi][bi] * W, W (in acc) staged through the warp's scratch.
-__device__ __forceinline__ void blk_finish(float (&acc)[8], float *Tf, float *wb, int bi, int bj,
-                                           int r, int hh) {
-    float *w = wb;   // 16 x 20
-#pragma unroll
-    for (int k = 0; k < 8; ++k) w[r * 20 + 8 * hh + k] = acc[k];
+// Tf[bi block rows][col..] = -Tf[bi][bi] * W, with W = acc (16 x 8) staged in wb.
+__device__ __forceinline__ void half_finish(const float (&acc)[4], float *Tf, float *wb, int bi,
+                                            int col, int r, int cg) {
+    *reinterpret_cast<float4 *>(wb + r * kWbLd + 4 * cg) = make_float4(acc[0], acc[1], acc[2], acc[3]);
     __syncwarp();
-    float out[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+    float o0 = 0.f, o1 = 0.f, o2 = 0.f, o3 = 0.f;
 #pragma unroll
     for (int kk = 0; kk < 16; ++kk) {
         const float d = Tf[(16 * bi + r) * kLd + 16 * bi + kk];
-#pragma unroll
-        for (int k = 0; k < 8; ++k) out[k] = fmaf(d, w[kk * 20 + 8 * hh + k], out[k]);
+        const float4 w = *reinterpret_cast<const float4 *>(wb + kk * kWbLd + 4 * cg);
+        o0 = fmaf(d, w.x, o0);
+        o1 = fmaf(d, w.y, o1);
+        o2 = fmaf(d, w.z, o2);
+        o3 = fmaf(d, w.w, o3);
     }
-#pragma unroll
-    for (int k = 0; k < 8; ++k) Tf[(16 * bi + r) * kLd + 16 * bj + 8 * hh + k] = -out[k];
+    *reinterpret_cast<float4 *>(Tf + (16 * bi + r) * kLd + col + 4 * cg) = make_float4(-o0, -o1, -o2, -o3);
     __syncwarp();
+}
+
+__device__ __forceinline__ uint4 scale_chunk(uint4 w, float f) {
+    uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+        const float2 v = unpack_bf16(ws[e]);
+        ws[e] = pack_bf16(v.x * f, v.y * f);
+    }
+    return make_uint4(ws[0], ws[1], ws[2], ws[3]);
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
@@ -154,6 +173,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     float *Af = reinterpret_cast<float *>(sm + OFF_AF);
     float *Tf = reinterpret_cast<float *>(sm + OFF_TF);
     float *Wb = reinterpret_cast<float *>(sm + OFF_WB);
+    float *Zs = Wb + 8 * 16 * kWbLd;          // 16 x 16 partial sum of the last block
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
     const int rank = blockIdx.x / hv;
@@ -174,11 +194,12 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     }
     const int nch = (int)((s_end - s_start + C - 1) / C);
     const size_t head_off = (size_t)h * DH * DH;
+    const size_t slot_stride = (size_t)hv * DH * DH;
     if (nch == 0) {   // empty sequence: the initial state (or zero) is the final state
         if (fslot >= 0)
             for (int e = tid; e < DH * DH; e += kThreads)
-                pool[(size_t)fslot * hv * DH * DH + head_off + e] =
-                    islot >= 0 ? pool[(size_t)islot * hv * DH * DH + head_off + e] : 0.f;
+                pool[fslot * slot_stride + head_off + e] =
+                    islot >= 0 ? pool[islot * slot_stride + head_off + e] : 0.f;
         return;
     }
 
@@ -188,15 +209,18 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     }
     if (tid == 0) {
         for (int s = 0; s < kKQStages; ++s) { mbar_init(&B.kq_full[s], 1); mbar_init(&B.kq_empty[s], 1); }
-        for (int s = 0; s < kVStages; ++s) { mbar_init(&B.v_full[s], 1); mbar_init(&B.v_empty[s], 128); }
+        for (int s = 0; s < kVStages; ++s) { mbar_init(&B.v_full[s], 1); mbar_init(&B.v_empty[s], 1); }
         mbar_init(&B.g_full, 1);
-        for (int s = 0; s < 2; ++s) { mbar_init(&B.prep_done[s], 128); mbar_init(&B.d_free[s], 128); }
+        for (int s = 0; s < 2; ++s) {
+            mbar_init(&B.prep_done[s], kPrepThreads);
+            mbar_init(&B.d_free[s], kChainThreads);
+        }
         mbar_init(&B.x_full, 1);
-        mbar_init(&B.r_full, 128);
+        mbar_init(&B.r_full, kChainThreads);
         mbar_init(&B.u_full, 1);
-        mbar_init(&B.u2_full, 128);
+        mbar_init(&B.u2_full, kChainThreads);
         mbar_init(&B.s_full, 1);
-        mbar_init(&B.s_next, 128);
+        mbar_init(&B.s_next, kChainThreads);
         mbar_init(&B.mma_done, 1);
         B.abort = 0;
         fence_mbar_init();
@@ -243,7 +267,8 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         // ------------------------------------------------------- MMA issuer
         if (lane == 0) {
             const uint32_t id64 = idesc_bf16(128, 64);
-            const uint32_t id128mn = idesc_bf16(128, 128, false, true);
+            const uint32_t id64amn = idesc_bf16(128, 64, true, false);
+            const uint32_t id128bmn = idesc_bf16(128, 128, false, true);
             auto kq_base = [&](int c) { return smem_u32(sm + OFF_KQ + (c % kKQStages) * kKQBytes); };
             auto issue_g = [&](int c) {   // M1: G = [K;Q] K^T
                 const uint32_t base = kq_base(c);
@@ -258,16 +283,24 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
             tc_fence_after();
             issue_g(0);
             for (int c = 0; c < nch; ++c) {
-                const int sd = c & 1;
+                const int sd = c & 1, sv = c % kVStages;
                 const uint32_t base = kq_base(c);
+                const uint32_t dsm = smem_u32(sm + OFF_D + sd * kDBytes);   // T1 | T2 | P
+                const uint32_t vsm = smem_u32(sm + OFF_V + sv * kVBytes);
+                const uint32_t ocol = kColO + sd * 64;
                 mbar_wait(&B.prep_done[sd], (c >> 1) & 1, abort);
                 mbar_wait(&B.s_next, c & 1, abort);
+                mbar_wait(&B.v_full[sv], (c / kVStages) & 1, abort);
                 tc_fence_after();
+                for (int s = 0; s < 4; ++s)   // MU: U = T1 V  (A = V^T, MN-major)
+                    mma_ss(tbase + kColU, sdesc_sw128(vsm + s * 16 * 128, kVBlk, 1024),
+                           sdesc_sw128(dsm + s * 32, 16, 1024), id64amn, s > 0);
+                mma_commit(&B.v_empty[sv]);
                 for (int s = 0; s < 8; ++s) {   // M2: X = S K^T ; M3: O = S Q'^T
                     const uint32_t off = (s >> 2) * kKBlk + (s & 3) * 32;
                     mma_ts(tbase + kColX, tbase + kColS16 + s * 8, sdesc_sw128(base + off, 16, 1024),
                            id64, s > 0);
-                    mma_ts(tbase + kColO, tbase + kColS16 + s * 8,
+                    mma_ts(tbase + ocol, tbase + kColS16 + s * 8,
                            sdesc_sw128(base + 64 * 128 + off, 16, 1024), id64, s > 0);
                 }
                 mma_commit(&B.x_full);
@@ -278,20 +311,18 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                 }
                 mbar_wait(&B.r_full, c & 1, abort);
                 tc_fence_after();
-                const uint32_t tsm = smem_u32(sm + OFF_T + sd * kTBytes);
-                for (int s = 0; s < 4; ++s)   // M4: U = R T^T
-                    mma_ts(tbase + kColU, tbase + kColX + s * 8, sdesc_sw128(tsm + s * 32, 16, 1024),
-                           id64, s > 0);
+                for (int s = 0; s < 4; ++s)   // M4: U += T2 X^T
+                    mma_ts(tbase + kColU, tbase + kColX + s * 8,
+                           sdesc_sw128(dsm + kMatBytes + s * 32, 16, 1024), id64, 1);
                 mma_commit(&B.u_full);
                 mbar_wait(&B.u2_full, c & 1, abort);
                 tc_fence_after();
-                const uint32_t psm = smem_u32(sm + OFF_P + sd * kPBytes);
                 for (int s = 0; s < 4; ++s) {
                     // M5: O += U P^T ; M6: S += U K''  (K'' MN-major: 2 blocks of 64 keys)
-                    mma_ts(tbase + kColO, tbase + kColU + s * 8, sdesc_sw128(psm + s * 32, 16, 1024),
-                           id64, 1);
+                    mma_ts(tbase + ocol, tbase + kColU + s * 8,
+                           sdesc_sw128(dsm + 2 * kMatBytes + s * 32, 16, 1024), id64, 1);
                     mma_ts(tbase + kColS32, tbase + kColU + s * 8,
-                           sdesc_sw128(base + s * 16 * 128, kKBlk, 1024), id128mn, 1);
+                           sdesc_sw128(base + s * 16 * 128, kKBlk, 1024), id128bmn, 1);
                 }
                 mma_commit(&B.s_full);
                 mma_commit(&B.kq_empty[c % kKQStages]);
@@ -301,287 +332,293 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
             mbar_wait(&B.mma_done, 0, &z);
         }
         __syncwarp();
-    } else if (warp < 6) {
-        // ---------------------------------------------------- prep (4 warps)
+    } else if (warp < 10) {
+        // ---------------------------------------------------- prep (8 warps)
+        const int t = tid - 64;                  // 0 .. 255
+        const int pw = warp - 2;                 // 0 .. 7
         const int q4 = warp & 3;                 // TMEM lane quadrant
         const int p = q4 * 32 + lane;            // G row: 0..63 K rows, 64..127 Q rows
-        const int pw = warp - 2;                 // 0..3 within the group
+        const int chalf = pw >> 2;               // which 32 G columns this warp reads
         for (int c = 0; c < nch; ++c) {
             const int sd = c & 1, sk = c % kKQStages;
             Scal &S = *reinterpret_cast<Scal *>(sm + OFF_SCAL + sd * kScalBytes);
             uint8_t *kq = sm + OFF_KQ + sk * kKQBytes;
+            uint8_t *dst = sm + OFF_D + sd * kDBytes;
             const int64_t c0 = s_start + (int64_t)c * C;
             const int n = (int)min((int64_t)C, s_end - c0);
+            float gv = 0.f, bv = 0.f;
+            if (t < n) {
+                gv = g[(c0 + t) * hv + h];
+                bv = beta[(c0 + t) * hv + h];
+            }
             if (c >= 2) mbar_wait(&B.d_free[sd], ((c >> 1) - 1) & 1, abort);
             mbar_wait(&B.kq_full[sk], (c / kKQStages) & 1, abort);
-            // gating values and the row norms of K (p < 64) / Q (p >= 64)
-            if (p < C) {
-                S.gam[p] = p < n ? g[(c0 + p) * hv + h] : 0.f;
-                S.beta[p] = p < n ? beta[(c0 + p) * hv + h] : 0.f;
-            }
+            // ---- inverse norms of the K rows (0..63) and Q rows (64..127)
             {
+                const uint32_t row = (uint32_t)(t >> 1), kb = (uint32_t)(t & 1);
                 float ss = 0.f;
-                const uint32_t row = (uint32_t)p;
-                for (int kb = 0; kb < 2; ++kb)
-                    for (int ch = 0; ch < 8; ++ch) {
-                        const uint4 w = *reinterpret_cast<const uint4 *>(kq + kb * kKBlk + sw128_chunk(row, ch));
-                        const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
-                        for (int e = 0; e < 4; ++e) {
-                            const float2 f = unpack_bf16(ws[e]);
-                            ss = fmaf(f.x, f.x, fmaf(f.y, f.y, ss));
-                        }
+                for (int ch = 0; ch < 8; ++ch) {
+                    const uint4 w = *reinterpret_cast<const uint4 *>(kq + kb * kKBlk + sw128_chunk(row, ch));
+                    const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const float2 f = unpack_bf16(ws[e]);
+                        ss = fmaf(f.x, f.x, fmaf(f.y, f.y, ss));
                     }
+                }
+                ss += __shfl_xor_sync(0xffffffffu, ss, 1);
                 const float r = l2norm ? rsqrtf(ss + kEps) : 1.f;
-                if (p < C) S.rk[p] = r; else S.rq[p - C] = r;
+                if (kb == 0) {
+                    if (row < C) S.rk[row] = r; else S.rq[row - C] = r;
+                }
             }
-            named_sync(1, 128);
-            if (p < C) {
-                float run = 0.f;
-                for (int j = 0; j <= p; ++j) run += S.gam[j];
-                named_sync(1, 128);      // everyone has read the raw g values
-                S.gam[p] = run;
-            } else {
-                named_sync(1, 128);
+            // ---- prefix sum of g over the chunk (warps 2, 3)
+            float x = gv;
+            if (t < C) {
+#pragma unroll
+                for (int off = 1; off < 32; off <<= 1) {
+                    const float y = __shfl_up_sync(0xffffffffu, x, off);
+                    if (lane >= off) x += y;
+                }
+                if (t == 31) B.tot0 = x;
             }
-            named_sync(1, 128);
-            const float gl = S.gam[C - 1];     // padded rows carry g = 0
-            if (p < C) {
-                const bool ok = p < n;
-                S.xs[p] = ok ? expf(S.gam[p]) * S.rk[p] : 0.f;
-                S.ks[p] = ok ? expf(gl - S.gam[p]) * S.rk[p] : 0.f;
-                if (!ok) S.beta[p] = 0.f;
-                if (p == 0) { S.gam_n = expf(gl); S.n = n; }
+            named_sync(1, kPrepThreads);
+            if (t < C) {
+                if (t >= 32) x += B.tot0;
+                S.gam[t] = x;
+                S.beta[t] = bv;
             }
-            // G row -> A (K rows) or P (Q rows)
+            named_sync(1, kPrepThreads);
+            if (t < C) {
+                const float gl = S.gam[C - 1];      // padded rows carry g = 0
+                const bool ok = t < n;
+                S.xs[t] = ok ? expf(x) * S.rk[t] : 0.f;
+                S.ks[t] = ok ? expf(gl - x) * S.rk[t] : 0.f;
+                if (t == 0) {
+                    S.gam_n = expf(gl);
+                    S.n = n;
+                }
+            }
+            named_sync(1, kPrepThreads);
+            // ---- G -> A (K rows, fp32 scratch) and P (Q rows, bf16 operand)
             mbar_wait(&B.g_full, c & 1, abort);
             tc_fence_after();
-            uint32_t graw[64];
-            {
-                uint32_t t0[32], t1[32];
-                tmem_ld32(tmem_addr(tbase, q4 * 32, kColG), t0);
-                tmem_ld32(tmem_addr(tbase, q4 * 32, kColG + 32), t1);
-#pragma unroll
-                for (int j = 0; j < 32; ++j) { graw[j] = t0[j]; graw[32 + j] = t1[j]; }
-            }
+            uint32_t gr[32];
+            tmem_ld32(tmem_addr(tbase, q4 * 32, kColG + 32 * chalf), gr);
             tc_fence_before();
-            named_sync(1, 128);          // scalars complete
             if (p < C) {
                 const int i = p;
-                const float bi = S.beta[i], gi = S.gam[i], ri = S.rk[i];
                 const bool ok = i < n;
-                float *arow = Af + i * kLd;
+                const float bi = S.beta[i] * S.rk[i], gi = S.gam[i];
+                float *arow = Af + i * kLd + 32 * chalf;
 #pragma unroll
-                for (int j = 0; j < C; ++j) {
-                    float v = 0.f;
-                    if (ok && j < i) v = bi * expf(gi - S.gam[j]) * ri * S.rk[j] * __uint_as_float(graw[j]);
-                    arow[j] = v;
+                for (int jj = 0; jj < 32; jj += 4) {
+                    float v[4];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const int j = 32 * chalf + jj + e;
+                        v[e] = (ok && j < i) ? bi * expf(gi - S.gam[j]) * S.rk[j] * __uint_as_float(gr[jj + e]) : 0.f;
+                    }
+                    *reinterpret_cast<float4 *>(arow + jj) = make_float4(v[0], v[1], v[2], v[3]);
                 }
             } else {
                 const int i = p - C;
                 const bool ok = i < n;
-                const float gi = S.gam[i], ri = scale * S.rq[i];
-                uint8_t *pt = sm + OFF_P + sd * kPBytes;
+                const float ri = scale * S.rq[i], gi = S.gam[i];
 #pragma unroll
-                for (int ch = 0; ch < 8; ++ch) {
+                for (int cc = 0; cc < 4; ++cc) {
                     uint32_t w[4];
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
-                        const int j0 = ch * 8 + 2 * e, j1 = j0 + 1;
-                        const float v0 = (ok && j0 <= i) ? expf(gi - S.gam[j0]) * ri * S.rk[j0] * __uint_as_float(graw[j0]) : 0.f;
-                        const float v1 = (ok && j1 <= i) ? expf(gi - S.gam[j1]) * ri * S.rk[j1] * __uint_as_float(graw[j1]) : 0.f;
+                        const int jl = cc * 8 + 2 * e;
+                        const int j0 = 32 * chalf + jl, j1 = j0 + 1;
+                        const float v0 = (ok && j0 <= i) ? ri * expf(gi - S.gam[j0]) * S.rk[j0] * __uint_as_float(gr[jl]) : 0.f;
+                        const float v1 = (ok && j1 <= i) ? ri * expf(gi - S.gam[j1]) * S.rk[j1] * __uint_as_float(gr[jl + 1]) : 0.f;
                         w[e] = pack_bf16(v0, v1);
                     }
-                    *reinterpret_cast<uint4 *>(pt + sw128_chunk(i, ch)) = make_uint4(w[0], w[1], w[2], w[3]);
+                    *reinterpret_cast<uint4 *>(dst + 2 * kMatBytes + sw128_chunk(i, 4 * chalf + cc)) =
+                        make_uint4(w[0], w[1], w[2], w[3]);
                 }
-                // Q' = scale Gam_i r_q,i Q_i, in place (M1 has consumed the raw rows)
-                const float f = ok ? expf(gi) * ri : 0.f;
-                for (int kb = 0; kb < 2; ++kb)
-                    for (int ch = 0; ch < 8; ++ch) {
-                        uint4 *pq = reinterpret_cast<uint4 *>(kq + kb * kKBlk + sw128_chunk(C + i, ch));
-                        uint4 w = *pq;
-                        uint32_t ws[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-                        for (int e = 0; e < 4; ++e) {
-                            const float2 v = unpack_bf16(ws[e]);
-                            ws[e] = pack_bf16(v.x * f, v.y * f);
-                        }
-                        *pq = make_uint4(ws[0], ws[1], ws[2], ws[3]);
-                    }
             }
-            named_sync(1, 128);
-            // ---- T = (I + A)^-1, blocked 4 x 16: diagonal blocks by forward
-            //      substitution (one warp each), then the block rows below.
-            {
+            named_sync(1, kPrepThreads);
+            // ---- T = (I + A)^-1: diagonal 16 x 16 blocks by forward substitution
+            //      (warps 0..3 of the group) while warps 4..7 rescale Q rows in place
+            if (pw < 4) {
                 const int r = lane >> 1, hh = lane & 1;
-                const int bb = pw;                       // diagonal block of this warp
+                const int bb = pw;
                 const int R = 16 * bb + r;
-                float t[8];
+                float tv[8];
 #pragma unroll
-                for (int k = 0; k < 8; ++k) t[k] = (8 * hh + k == r) ? 1.f : 0.f;
+                for (int k = 0; k < 8; ++k) tv[k] = (8 * hh + k == r) ? 1.f : 0.f;
+#pragma unroll
                 for (int m = 0; m < 15; ++m) {
                     const float a = Af[R * kLd + 16 * bb + m];
 #pragma unroll
                     for (int k = 0; k < 8; ++k) {
-                        const float vm = __shfl_sync(0xffffffffu, t[k], 2 * m + hh);
-                        if (r > m) t[k] = fmaf(-a, vm, t[k]);
+                        const float vm = __shfl_sync(0xffffffffu, tv[k], 2 * m + hh);
+                        if (r > m) tv[k] = fmaf(-a, vm, tv[k]);
                     }
                 }
+                *reinterpret_cast<float4 *>(Tf + R * kLd + 16 * bb + 8 * hh) = make_float4(tv[0], tv[1], tv[2], tv[3]);
+                *reinterpret_cast<float4 *>(Tf + R * kLd + 16 * bb + 8 * hh + 4) = make_float4(tv[4], tv[5], tv[6], tv[7]);
+            } else {
+                // Q' = scale Gam_i r_q,i Q_i (M1 has consumed the raw rows)
+                const int tt = t - 128;
+                const int i = tt >> 1, kb = tt & 1;
+                const float f = i < n ? scale * expf(S.gam[i]) * S.rq[i] : 0.f;
 #pragma unroll
-                for (int k = 0; k < 8; ++k) Tf[R * kLd + 16 * bb + 8 * hh + k] = t[k];
-                named_sync(1, 128);
-                float *wb = Wb + pw * 16 * 20;
-                float acc[8];
-                // level 1: T10, T21, T32
-                if (pw < 3) {
-#pragma unroll
-                    for (int k = 0; k < 8; ++k) acc[k] = 0.f;
-                    blk_mac(acc, Af, 16 * (pw + 1), 16 * pw, Tf, 16 * pw, 16 * pw, r, hh);
-                    blk_finish(acc, Tf, wb, pw + 1, pw, r, hh);
+                for (int ch = 0; ch < 8; ++ch) {
+                    uint4 *pq = reinterpret_cast<uint4 *>(kq + kb * kKBlk + sw128_chunk(C + i, ch));
+                    *pq = scale_chunk(*pq, f);
                 }
-                named_sync(1, 128);
-                // level 2: T20, T31 and the partial sum Z30 = A30 T00 + A31 T10
-                if (pw < 3) {
-#pragma unroll
-                    for (int k = 0; k < 8; ++k) acc[k] = 0.f;
-                    if (pw == 0) {
-                        blk_mac(acc, Af, 32, 0, Tf, 0, 0, r, hh);
-                        blk_mac(acc, Af, 32, 16, Tf, 16, 0, r, hh);
-                        blk_finish(acc, Tf, wb, 2, 0, r, hh);
-                    } else if (pw == 1) {
-                        blk_mac(acc, Af, 48, 16, Tf, 16, 16, r, hh);
-                        blk_mac(acc, Af, 48, 32, Tf, 32, 16, r, hh);
-                        blk_finish(acc, Tf, wb, 3, 1, r, hh);
-                    } else {
-                        blk_mac(acc, Af, 48, 0, Tf, 0, 0, r, hh);
-                        blk_mac(acc, Af, 48, 16, Tf, 16, 0, r, hh);
-#pragma unroll
-                        for (int k = 0; k < 8; ++k) Wb[3 * 16 * 20 + r * 20 + 8 * hh + k] = acc[k];
-                    }
-                }
-                named_sync(1, 128);
-                // level 3: T30 = -T33 (Z30 + A32 T20)
-                if (pw == 0) {
-#pragma unroll
-                    for (int k = 0; k < 8; ++k) acc[k] = Wb[3 * 16 * 20 + r * 20 + 8 * hh + k];
-                    blk_mac(acc, Af, 48, 32, Tf, 32, 0, r, hh);
-                    blk_finish(acc, Tf, wb, 3, 0, r, hh);
-                }
-                named_sync(1, 128);
             }
-            // T (lower triangular) -> bf16, K-major [i][j]
+            named_sync(1, kPrepThreads);
+            // ---- the blocks below the diagonal, level by level; each warp owns
+            //      one 16 x 8 half of a block (T_ij = -T_ii sum_k A_ik T_kj)
             {
-                const int i = p >> 1, half = p & 1;
-                uint8_t *tt = sm + OFF_T + sd * kTBytes;
+                const int r = lane >> 1, cg = lane & 1;
+                float *wb = Wb + pw * 16 * kWbLd;
+                float acc[4];
+                if (pw < 6) {              // level 1: T10, T21, T32
+                    const int b0 = pw >> 1, half = pw & 1;
+                    const int col = 16 * b0 + 8 * half;
+                    acc[0] = acc[1] = acc[2] = acc[3] = 0.f;
+                    half_mac(acc, Af, 16 * (b0 + 1), 16 * b0, Tf, 16 * b0, col, r, cg);
+                    half_finish(acc, Tf, wb, b0 + 1, col, r, cg);
+                }
+                named_sync(1, kPrepThreads);
+                if (pw < 6) {              // level 2: T20, T31 and Z30 = A30 T00 + A31 T10
+                    const int item = pw >> 1, half = pw & 1;
+                    acc[0] = acc[1] = acc[2] = acc[3] = 0.f;
+                    if (item == 0) {
+                        const int col = 8 * half;
+                        half_mac(acc, Af, 32, 0, Tf, 0, col, r, cg);
+                        half_mac(acc, Af, 32, 16, Tf, 16, col, r, cg);
+                        half_finish(acc, Tf, wb, 2, col, r, cg);
+                    } else if (item == 1) {
+                        const int col = 16 + 8 * half;
+                        half_mac(acc, Af, 48, 16, Tf, 16, col, r, cg);
+                        half_mac(acc, Af, 48, 32, Tf, 32, col, r, cg);
+                        half_finish(acc, Tf, wb, 3, col, r, cg);
+                    } else {
+                        const int col = 8 * half;
+                        half_mac(acc, Af, 48, 0, Tf, 0, col, r, cg);
+                        half_mac(acc, Af, 48, 16, Tf, 16, col, r, cg);
+                        *reinterpret_cast<float4 *>(Zs + r * 16 + col + 4 * cg) =
+                            make_float4(acc[0], acc[1], acc[2], acc[3]);
+                    }
+                }
+                named_sync(1, kPrepThreads);
+                if (pw < 2) {              // level 3: T30 = -T33 (Z30 + A32 T20)
+                    const int col = 8 * pw;
+                    const float4 z = *reinterpret_cast<const float4 *>(Zs + r * 16 + col + 4 * cg);
+                    acc[0] = z.x; acc[1] = z.y; acc[2] = z.z; acc[3] = z.w;
+                    half_mac(acc, Af, 48, 32, Tf, 32, col, r, cg);
+                    half_finish(acc, Tf, wb, 3, col, r, cg);
+                }
+                named_sync(1, kPrepThreads);
+            }
+            // ---- T1 = T diag(beta), T2 = -T diag(beta Gam r_k), bf16 K-major [i][j]
+            {
+                const int i = t >> 2, q2 = t & 3;
 #pragma unroll
-                for (int cc = 0; cc < 4; ++cc) {
-                    const int ch = half * 4 + cc;
-                    uint32_t w[4];
+                for (int h2 = 0; h2 < 2; ++h2) {
+                    const int ch = 2 * q2 + h2;
+                    uint32_t w1[4], w2[4];
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
-                        const int j0 = ch * 8 + 2 * e;
-                        const float v0 = j0 <= i ? Tf[i * kLd + j0] : 0.f;
-                        const float v1 = j0 + 1 <= i ? Tf[i * kLd + j0 + 1] : 0.f;
-                        w[e] = pack_bf16(v0, v1);
+                        const int j0 = ch * 8 + 2 * e, j1 = j0 + 1;
+                        const float t0 = j0 <= i ? Tf[i * kLd + j0] : 0.f;
+                        const float t1 = j1 <= i ? Tf[i * kLd + j1] : 0.f;
+                        w1[e] = pack_bf16(t0 * S.beta[j0], t1 * S.beta[j1]);
+                        w2[e] = pack_bf16(-t0 * S.beta[j0] * S.xs[j0], -t1 * S.beta[j1] * S.xs[j1]);
                     }
-                    *reinterpret_cast<uint4 *>(tt + sw128_chunk(i, ch)) = make_uint4(w[0], w[1], w[2], w[3]);
+                    *reinterpret_cast<uint4 *>(dst + sw128_chunk(i, ch)) = make_uint4(w1[0], w1[1], w1[2], w1[3]);
+                    *reinterpret_cast<uint4 *>(dst + kMatBytes + sw128_chunk(i, ch)) =
+                        make_uint4(w2[0], w2[1], w2[2], w2[3]);
                 }
             }
             fence_async_smem();
             mbar_arrive(&B.prep_done[sd]);
-            named_sync(1, 128);          // the solve scratch is free again
+            named_sync(1, kPrepThreads);   // the solve scratch is free again
         }
     } else {
         // --------------------------------------------------- chain (4 warps)
+        const int tc4 = tid - 320;                // 0 .. 127
         const int q4 = warp & 3;
         const int b = q4 * 32 + lane;            // value row of the state
         const uint32_t lrow = tmem_addr(tbase, q4 * 32, 0);
-        // E0: initial state -> fp32 accumulator + bf16 operand copy
+        // E0: initial state -> bf16 operand copy, and the fp32 accumulator
+        //     pre-scaled by the first chunk's total decay
         {
-            const float *src = islot >= 0 ? pool + (size_t)islot * hv * DH * DH + head_off + (size_t)b * DH : nullptr;
-            for (int c0 = 0; c0 < DH; c0 += 32) {
-                uint32_t r[32];
-#pragma unroll
-                for (int j = 0; j < 32; ++j) r[j] = __float_as_uint(src ? src[c0 + j] : 0.f);
-                tmem_st32(lrow + kColS32 + c0, r);
-            }
+            mbar_wait(&B.prep_done[0], 0, abort);
+            const float gn = reinterpret_cast<const Scal *>(sm + OFF_SCAL)->gam_n;
+            const float *src = islot >= 0 ? pool + islot * slot_stride + head_off + (size_t)b * DH : nullptr;
             for (int c0 = 0; c0 < DH; c0 += 64) {
-                uint32_t r[32];
+                uint32_t lo[32], hi[32], pk[32];
 #pragma unroll
-                for (int j = 0; j < 32; ++j)
-                    r[j] = pack_bf16(src ? src[c0 + 2 * j] : 0.f, src ? src[c0 + 2 * j + 1] : 0.f);
-                tmem_st32(lrow + kColS16 + c0 / 2, r);
+                for (int j = 0; j < 32; j += 4) {
+                    float4 v0 = src ? *reinterpret_cast<const float4 *>(src + c0 + j) : make_float4(0.f, 0.f, 0.f, 0.f);
+                    float4 v1 = src ? *reinterpret_cast<const float4 *>(src + c0 + 32 + j) : make_float4(0.f, 0.f, 0.f, 0.f);
+                    lo[j] = __float_as_uint(v0.x); lo[j + 1] = __float_as_uint(v0.y);
+                    lo[j + 2] = __float_as_uint(v0.z); lo[j + 3] = __float_as_uint(v0.w);
+                    hi[j] = __float_as_uint(v1.x); hi[j + 1] = __float_as_uint(v1.y);
+                    hi[j + 2] = __float_as_uint(v1.z); hi[j + 3] = __float_as_uint(v1.w);
+                }
+#pragma unroll
+                for (int jj = 0; jj < 16; ++jj) {
+                    pk[jj] = pack_bf16(__uint_as_float(lo[2 * jj]), __uint_as_float(lo[2 * jj + 1]));
+                    pk[16 + jj] = pack_bf16(__uint_as_float(hi[2 * jj]), __uint_as_float(hi[2 * jj + 1]));
+                }
+                tmem_st32(lrow + kColS16 + c0 / 2, pk);
+#pragma unroll
+                for (int j = 0; j < 32; ++j) {
+                    lo[j] = __float_as_uint(__uint_as_float(lo[j]) * gn);
+                    hi[j] = __float_as_uint(__uint_as_float(hi[j]) * gn);
+                }
+                tmem_st32(lrow + kColS32 + c0, lo);
+                tmem_st32(lrow + kColS32 + c0 + 32, hi);
             }
             tmem_wait_st();
             tc_fence_before();
             mbar_arrive(&B.s_next);
         }
         for (int c = 0; c < nch; ++c) {
-            const int sd = c & 1, sk = c % kKQStages, sv = c % kVStages;
+            const int sd = c & 1, sk = c % kKQStages;
             const Scal &S = *reinterpret_cast<const Scal *>(sm + OFF_SCAL + sd * kScalBytes);
             uint8_t *kq = sm + OFF_KQ + sk * kKQBytes;
-            const uint8_t *vt = sm + OFF_V + sv * kVBytes;
             const int64_t c0 = s_start + (int64_t)c * C;
+            const bool last = c == nch - 1;
             mbar_wait(&B.prep_done[sd], (c >> 1) & 1, abort);
             const int n = S.n;
-            // ---- E1: R = beta (V - Gam r_k X) -> bf16 in TMEM (X's columns)
+            // ---- E1: X -> bf16 in TMEM (X's columns)
             mbar_wait(&B.x_full, c & 1, abort);
             tc_fence_after();
-            mbar_wait(&B.v_full[sv], (c / kVStages) & 1, abort);
             {
-                uint32_t x0[32], x1[32];
+                uint32_t x0[32], x1[32], xx[32];
                 tmem_ld32(lrow + kColX, x0);
                 tmem_ld32(lrow + kColX + 32, x1);
-                const uint8_t *vcol = vt + (b >> 6) * kVBlk;
-                const uint32_t be = (uint32_t)(b & 63);
-                uint32_t rr[32];
 #pragma unroll
-                for (int jj = 0; jj < 32; ++jj) {
-                    float v2[2];
-#pragma unroll
-                    for (int e = 0; e < 2; ++e) {
-                        const int j = 2 * jj + e;
-                        const float x = __uint_as_float(j < 32 ? x0[j] : x1[j - 32]);
-                        const float vv = __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(vcol + sw128_off((uint32_t)j, be)));
-                        v2[e] = j < n ? S.beta[j] * (vv - S.xs[j] * x) : 0.f;
-                    }
-                    rr[jj] = pack_bf16(v2[0], v2[1]);
+                for (int jj = 0; jj < 16; ++jj) {
+                    xx[jj] = pack_bf16(__uint_as_float(x0[2 * jj]), __uint_as_float(x0[2 * jj + 1]));
+                    xx[16 + jj] = pack_bf16(__uint_as_float(x1[2 * jj]), __uint_as_float(x1[2 * jj + 1]));
                 }
-                tmem_st32(lrow + kColX, rr);
+                tmem_st32(lrow + kColX, xx);
                 tmem_wait_st();
             }
             tc_fence_before();
             mbar_arrive(&B.r_full);
-            mbar_arrive(&B.v_empty[sv]);
             // K'' = D[last][j] r_k,j K_j in place (M1, M2 have consumed the raw rows)
             {
-                const int j = tid - 192 >= 0 ? ((tid - 192) >> 1) : 0;
-                const int kb = (tid - 192) & 1;
+                const int j = tc4 >> 1, kb = tc4 & 1;
                 const float f = S.ks[j];
+#pragma unroll
                 for (int ch = 0; ch < 8; ++ch) {
                     uint4 *pk = reinterpret_cast<uint4 *>(kq + kb * kKBlk + sw128_chunk((uint32_t)j, ch));
-                    uint4 w = *pk;
-                    uint32_t ws[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const float2 v = unpack_bf16(ws[e]);
-                        ws[e] = pack_bf16(v.x * f, v.y * f);
-                    }
-                    *pk = make_uint4(ws[0], ws[1], ws[2], ws[3]);
+                    *pk = scale_chunk(*pk, f);
                 }
                 fence_async_smem();
-            }
-            // S <- Gam_last S ahead of M6
-            {
-                const float gn = S.gam_n;
-                for (int cc = 0; cc < DH; cc += 32) {
-                    uint32_t r[32];
-                    tmem_ld32(lrow + kColS32 + cc, r);
-#pragma unroll
-                    for (int j = 0; j < 32; ++j) r[j] = __float_as_uint(__uint_as_float(r[j]) * gn);
-                    tmem_st32(lrow + kColS32 + cc, r);
-                }
-                tmem_wait_st();
             }
             // ---- E2: U -> bf16 in TMEM (U's columns)
             mbar_wait(&B.u_full, c & 1, abort);
@@ -600,13 +637,55 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
             }
             tc_fence_before();
             mbar_arrive(&B.u2_full);
-            // ---- E3: o <- O ; S -> bf16 copy ; final state
+            // ---- E3a: S -> bf16 operand copy, fp32 pre-scaled for the next
+            //      chunk (or the final state -> pool)
             mbar_wait(&B.s_full, c & 1, abort);
             tc_fence_after();
+            float gnext = 1.f;
+            if (!last) {
+                mbar_wait(&B.prep_done[sd ^ 1], ((c + 1) >> 1) & 1, abort);
+                gnext = reinterpret_cast<const Scal *>(sm + OFF_SCAL + (sd ^ 1) * kScalBytes)->gam_n;
+            }
+            float *dstp = (last && fslot >= 0) ? pool + fslot * slot_stride + head_off + (size_t)b * DH : nullptr;
+            for (int cc = 0; cc < DH; cc += 64) {
+                uint32_t s0[32], s1[32];
+                tmem_ld32(lrow + kColS32 + cc, s0);
+                tmem_ld32(lrow + kColS32 + cc + 32, s1);
+                if (!last) {
+                    uint32_t pk[32];
+#pragma unroll
+                    for (int jj = 0; jj < 16; ++jj) {
+                        pk[jj] = pack_bf16(__uint_as_float(s0[2 * jj]), __uint_as_float(s0[2 * jj + 1]));
+                        pk[16 + jj] = pack_bf16(__uint_as_float(s1[2 * jj]), __uint_as_float(s1[2 * jj + 1]));
+                    }
+                    tmem_st32(lrow + kColS16 + cc / 2, pk);
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) {
+                        s0[j] = __float_as_uint(__uint_as_float(s0[j]) * gnext);
+                        s1[j] = __float_as_uint(__uint_as_float(s1[j]) * gnext);
+                    }
+                    tmem_st32(lrow + kColS32 + cc, s0);
+                    tmem_st32(lrow + kColS32 + cc + 32, s1);
+                } else if (dstp) {
+#pragma unroll
+                    for (int j = 0; j < 32; j += 4) {
+                        *reinterpret_cast<float4 *>(dstp + cc + j) = make_float4(
+                            __uint_as_float(s0[j]), __uint_as_float(s0[j + 1]),
+                            __uint_as_float(s0[j + 2]), __uint_as_float(s0[j + 3]));
+                        *reinterpret_cast<float4 *>(dstp + cc + 32 + j) = make_float4(
+                            __uint_as_float(s1[j]), __uint_as_float(s1[j + 1]),
+                            __uint_as_float(s1[j + 2]), __uint_as_float(s1[j + 3]));
+                    }
+                }
+            }
+            tmem_wait_st();
+            tc_fence_before();
+            mbar_arrive(&B.s_next);
+            // ---- E3b: o <- O (this chunk's buffer; the next chunk uses the other)
             {
                 uint32_t o0[32], o1[32];
-                tmem_ld32(lrow + kColO, o0);
-                tmem_ld32(lrow + kColO + 32, o1);
+                tmem_ld32(lrow + kColO + sd * 64, o0);
+                tmem_ld32(lrow + kColO + sd * 64 + 32, o1);
                 __nv_bfloat16 *orow = o + (c0 * hv + h) * (int64_t)DH + b;
                 const int64_t ostride = (int64_t)hv * DH;
 #pragma unroll
@@ -616,33 +695,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                 for (int i = 0; i < 32; ++i)
                     if (32 + i < n) orow[(32 + i) * ostride] = __float2bfloat16_rn(__uint_as_float(o1[i]));
             }
-            const bool last = c == nch - 1;
-            float *dst = (last && fslot >= 0) ? pool + (size_t)fslot * hv * DH * DH + head_off + (size_t)b * DH : nullptr;
-            for (int cc = 0; cc < DH; cc += 64) {
-                uint32_t s0[32], s1[32], pk[32];
-                tmem_ld32(lrow + kColS32 + cc, s0);
-                tmem_ld32(lrow + kColS32 + cc + 32, s1);
-#pragma unroll
-                for (int jj = 0; jj < 16; ++jj) {
-                    pk[jj] = pack_bf16(__uint_as_float(s0[2 * jj]), __uint_as_float(s0[2 * jj + 1]));
-                    pk[16 + jj] = pack_bf16(__uint_as_float(s1[2 * jj]), __uint_as_float(s1[2 * jj + 1]));
-                }
-                if (!last) tmem_st32(lrow + kColS16 + cc / 2, pk);
-                if (dst) {
-#pragma unroll
-                    for (int j = 0; j < 32; j += 4) {
-                        *reinterpret_cast<float4 *>(dst + cc + j) = make_float4(
-                            __uint_as_float(s0[j]), __uint_as_float(s0[j + 1]),
-                            __uint_as_float(s0[j + 2]), __uint_as_float(s0[j + 3]));
-                        *reinterpret_cast<float4 *>(dst + cc + 32 + j) = make_float4(
-                            __uint_as_float(s1[j]), __uint_as_float(s1[j + 1]),
-                            __uint_as_float(s1[j + 2]), __uint_as_float(s1[j + 3]));
-                    }
-                }
-            }
-            tmem_wait_st();
             tc_fence_before();
-            mbar_arrive(&B.s_next);
             mbar_arrive(&B.d_free[sd]);
         }
     }

@@ -5,6 +5,7 @@
 //   mode 1: B MN-major in shared memory (B given as [K][N]), TMA-loaded.
 //   mode 2: A read from tensor memory (written there with tcgen05.st),
 //           B K-major as in mode 0.
+//   mode 3: A MN-major in shared memory (A given as [K][128]), B K-major.
 // Test-only code: built by tests/test_gpu_tc_selftest.py, never by the library.
 #include <stdio.h>
 
@@ -45,7 +46,9 @@ selftest_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant_
     if (tid == 0) {
         uint32_t bytes = (mode == 2 ? 0u : 128u * K * 2u) + (uint32_t)N * K * 2u;
         mbar_arrive_expect_tx(&bar_load, bytes);
-        if (mode != 2)
+        if (mode == 3)
+            for (int mb = 0; mb < 2; ++mb) tma_load_2d(sA + mb * K * 128, &mapA, &bar_load, mb * 64, 0);
+        else if (mode != 2)
             for (int kb = 0; kb < K / 64; ++kb) tma_load_2d(sA + kb * 128 * 128, &mapA, &bar_load, kb * 64, 0);
         if (mode == 1) {
             for (int nb = 0; nb < N / 64; ++nb) tma_load_2d(sB + nb * K * 128, &mapB, &bar_load, nb * 64, 0);
@@ -70,7 +73,7 @@ selftest_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant_
     if (tid == 0) {
         tc_fence_after();
         if (!mbar_wait(&bar_load, 0, &abort_flag)) atomicOr(err, 1);
-        const uint32_t idesc = idesc_bf16(128, N, false, mode == 1);
+        const uint32_t idesc = idesc_bf16(128, N, mode == 3, mode == 1);
         for (int s = 0; s < K / 16; ++s) {
             uint64_t bdesc;
             if (mode == 1)
@@ -79,6 +82,9 @@ selftest_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant_
                 bdesc = sdesc_sw128(smem_u32(sB) + (s / 4) * N * 128 + (s % 4) * 32, 16, 1024);
             if (mode == 2) {
                 mma_ts(tbase, tbase + a_col + s * 8, bdesc, idesc, s > 0);
+            } else if (mode == 3) {
+                uint64_t adesc = sdesc_sw128(smem_u32(sA) + s * 16 * 128, K * 128, 1024);
+                mma_ss(tbase, adesc, bdesc, idesc, s > 0);
             } else {
                 uint64_t adesc = sdesc_sw128(smem_u32(sA) + (s / 4) * 128 * 128 + (s % 4) * 32, 16, 1024);
                 mma_ss(tbase, adesc, bdesc, idesc, s > 0);
@@ -100,9 +106,11 @@ selftest_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant_
 
 extern "C" int tc_selftest_gemm(const void *A, const void *B, float *D, int N, int K, int mode,
                                 int *err_dev) {
-    if ((N != 64 && N != 128) || (K != 64 && K != 128) || mode < 0 || mode > 2) return 1;
+    if ((N != 64 && N != 128) || (K != 64 && K != 128) || mode < 0 || mode > 3) return 1;
     CUtensorMap mA, mB;
-    if (!encode_tmap_2d_bf16(&mA, A, K, 128, K, 64, 128)) return 2;
+    bool okA = mode == 3 ? encode_tmap_2d_bf16(&mA, A, 128, K, 128, 64, K)
+                         : encode_tmap_2d_bf16(&mA, A, K, 128, K, 64, 128);
+    if (!okA) return 2;
     bool ok = mode == 1 ? encode_tmap_2d_bf16(&mB, B, N, K, N, 64, K)
                         : encode_tmap_2d_bf16(&mB, B, K, N, K, 64, N);
     if (!ok) return 3;

@@ -1,8 +1,8 @@
 """Self-test of the library's tcgen05 / TMA / TMEM primitives (csrc/tc.cuh):
 a one-CTA bf16 GEMM with fp32 accumulation in tensor memory, against a
 PyTorch fp32 matmul of the same bf16 values.  Covers K-major and MN-major
-shared-memory operands (128-byte swizzle, TMA-loaded) and an A operand read
-from tensor memory."""
+shared-memory operands (128-byte swizzle, TMA-loaded) for either side and an
+A operand read from tensor memory."""
 import ctypes
 import os
 import subprocess
@@ -31,14 +31,15 @@ def selftest_lib():
     return lib
 
 
-@pytest.mark.parametrize("mode", [0, 1, 2])
+@pytest.mark.parametrize("mode", [0, 1, 2, 3])
 @pytest.mark.parametrize("N,K", [(64, 64), (64, 128), (128, 64), (128, 128)])
 def test_tc_gemm(selftest_lib, mode, N, K):
     gen = torch.Generator().manual_seed(mode * 100 + N + K)
     A = torch.randn(128, K, generator=gen).to(torch.bfloat16)
     B = torch.randn(N, K, generator=gen).to(torch.bfloat16)          # D = A @ B^T
     Bdev = B.t().contiguous() if mode == 1 else B                      # mode 1 passes [K][N]
-    Ad, Bd = A.cuda(), Bdev.cuda()
+    Adev = A.t().contiguous() if mode == 3 else A                      # mode 3 passes [K][128]
+    Ad, Bd = Adev.cuda(), Bdev.cuda()
     D = torch.full((128, N), float("nan"), device="cuda")
     err = torch.zeros(1, dtype=torch.int32, device="cuda")
     rc = selftest_lib.tc_selftest_gemm(Ad.data_ptr(), Bd.data_ptr(), D.data_ptr(), N, K, mode,
