@@ -16,8 +16,9 @@
 // r_k, r_q = inverse L2 norms):
 //   M1  G  = [K;Q] K^T                  prep: A (K rows) and P (Q rows) from G
 //   MU  U  = T1 V                       T1 = T diag(beta)         (V^T read MN-major)
-//   M2  X  = S K^T       X[b][j]        A operand: bf16 copy of S in TMEM
-//   M3  O  = S Q'^T                     Q' = scale Gam r_q Q (rows rescaled in place)
+//   M23 [X | O] = S [K; Q']^T           one N = 128 MMA; X[b][j], O[b][i];
+//                                       A operand: bf16 copy of S in TMEM;
+//                                       Q' = scale Gam r_q Q (rows rescaled in place)
 //   E1  X -> bf16 in TMEM
 //   M4  U += T2 X^T                     T2 = -T diag(beta Gam r_k), so that
 //                                       U = T diag(beta) (V - diag(Gam r_k) K S^T)
@@ -25,8 +26,8 @@
 //   M5  O += U P^T       P[i][j] = scale D_ij r_q,i r_k,j (q_i . k_j), j <= i
 //   M6  S += U K''       K''_j = D[last][j] r_k,j K_j (rows rescaled in place);
 //                        S was pre-scaled by Gam_last by the previous epilogue
-//   E3  S -> bf16 copy (and pre-scaled for the next chunk), then o <- O
-//       (O is double-buffered, so the o stores leave the critical path)
+//   E3  S -> bf16 copy (and pre-scaled for the next chunk) and O -> registers,
+//       hand-off to the next chunk, then the o stores
 // Padded rows of a partial last chunk get beta = g = 0 and explicit zero masks.
 #include "common.cuh"
 #include "tc.cuh"
@@ -58,8 +59,8 @@ constexpr int kWbLd = 12;                        // row stride of a warp's 16 x 
 constexpr float kEps = 1e-6f;
 
 // TMEM columns
-constexpr uint32_t kColS32 = 0, kColS16 = 128, kColG = 192, kColX = 256, kColU = 320,
-                   kColO = 384, kTmemCols = 512;
+constexpr uint32_t kColS32 = 0, kColS16 = 128, kColG = 192, kColU = 256, kColX = 320,
+                   kColO = 384, kTmemCols = 512;   // X and O adjacent: one N = 128 MMA
 
 struct Scal {
     float beta[C], gam[C], rk[C], rq[C], xs[C], ks[C];
@@ -69,8 +70,8 @@ struct Scal {
 
 struct Bars {
     uint64_t kq_full[kKQStages], kq_empty[kKQStages], v_full[kVStages], v_empty[kVStages];
-    uint64_t g_full, prep_done[2], d_free[2], x_full, r_full, u_full, u2_full, s_full, s_next,
-        mma_done;
+    uint64_t g_full, g_free, prep_done[2], gn_ready[2], d_free[2], x_full, r_full, u_full,
+        u2_full, s_full, s_next, mma_done;
     uint32_t tmem_base;
     int abort;
     int seq;
@@ -120,32 +121,50 @@ __device__ int seq_for_rank(const int32_t *cu, int n_seqs, int rank, int *slot) 
 //   acc += X[xr.., xc..] (16 x 16) * Y[yr.., col..]
 __device__ __forceinline__ void half_mac(float (&acc)[4], const float *X, int xr, int xc,
                                          const float *Y, int yr, int col, int r, int cg) {
+    float e0 = 0.f, e1 = 0.f, e2 = 0.f, e3 = 0.f;   // second accumulator set: shorter chains
 #pragma unroll
-    for (int kk = 0; kk < 16; ++kk) {
-        const float x = X[(xr + r) * kLd + xc + kk];
-        const float4 y = *reinterpret_cast<const float4 *>(Y + (yr + kk) * kLd + col + 4 * cg);
-        acc[0] = fmaf(x, y.x, acc[0]);
-        acc[1] = fmaf(x, y.y, acc[1]);
-        acc[2] = fmaf(x, y.z, acc[2]);
-        acc[3] = fmaf(x, y.w, acc[3]);
+    for (int kk = 0; kk < 16; kk += 2) {
+        const float x0 = X[(xr + r) * kLd + xc + kk];
+        const float x1 = X[(xr + r) * kLd + xc + kk + 1];
+        const float4 y0 = *reinterpret_cast<const float4 *>(Y + (yr + kk) * kLd + col + 4 * cg);
+        const float4 y1 = *reinterpret_cast<const float4 *>(Y + (yr + kk + 1) * kLd + col + 4 * cg);
+        acc[0] = fmaf(x0, y0.x, acc[0]);
+        acc[1] = fmaf(x0, y0.y, acc[1]);
+        acc[2] = fmaf(x0, y0.z, acc[2]);
+        acc[3] = fmaf(x0, y0.w, acc[3]);
+        e0 = fmaf(x1, y1.x, e0);
+        e1 = fmaf(x1, y1.y, e1);
+        e2 = fmaf(x1, y1.z, e2);
+        e3 = fmaf(x1, y1.w, e3);
     }
+    acc[0] += e0;
+    acc[1] += e1;
+    acc[2] += e2;
+    acc[3] += e3;
 }
 // Tf[bi block rows][col..] = -Tf[bi][bi] * W, with W = acc (16 x 8) staged in wb.
 __device__ __forceinline__ void half_finish(const float (&acc)[4], float *Tf, float *wb, int bi,
                                             int col, int r, int cg) {
     *reinterpret_cast<float4 *>(wb + r * kWbLd + 4 * cg) = make_float4(acc[0], acc[1], acc[2], acc[3]);
     __syncwarp();
-    float o0 = 0.f, o1 = 0.f, o2 = 0.f, o3 = 0.f;
+    float o0 = 0.f, o1 = 0.f, o2 = 0.f, o3 = 0.f, p0 = 0.f, p1 = 0.f, p2 = 0.f, p3 = 0.f;
 #pragma unroll
-    for (int kk = 0; kk < 16; ++kk) {
-        const float d = Tf[(16 * bi + r) * kLd + 16 * bi + kk];
-        const float4 w = *reinterpret_cast<const float4 *>(wb + kk * kWbLd + 4 * cg);
-        o0 = fmaf(d, w.x, o0);
-        o1 = fmaf(d, w.y, o1);
-        o2 = fmaf(d, w.z, o2);
-        o3 = fmaf(d, w.w, o3);
+    for (int kk = 0; kk < 16; kk += 2) {
+        const float d0 = Tf[(16 * bi + r) * kLd + 16 * bi + kk];
+        const float d1 = Tf[(16 * bi + r) * kLd + 16 * bi + kk + 1];
+        const float4 w0 = *reinterpret_cast<const float4 *>(wb + kk * kWbLd + 4 * cg);
+        const float4 w1 = *reinterpret_cast<const float4 *>(wb + (kk + 1) * kWbLd + 4 * cg);
+        o0 = fmaf(d0, w0.x, o0);
+        o1 = fmaf(d0, w0.y, o1);
+        o2 = fmaf(d0, w0.z, o2);
+        o3 = fmaf(d0, w0.w, o3);
+        p0 = fmaf(d1, w1.x, p0);
+        p1 = fmaf(d1, w1.y, p1);
+        p2 = fmaf(d1, w1.z, p2);
+        p3 = fmaf(d1, w1.w, p3);
     }
-    *reinterpret_cast<float4 *>(Tf + (16 * bi + r) * kLd + col + 4 * cg) = make_float4(-o0, -o1, -o2, -o3);
+    *reinterpret_cast<float4 *>(Tf + (16 * bi + r) * kLd + col + 4 * cg) =
+        make_float4(-(o0 + p0), -(o1 + p1), -(o2 + p2), -(o3 + p3));
     __syncwarp();
 }
 
@@ -211,8 +230,10 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         for (int s = 0; s < kKQStages; ++s) { mbar_init(&B.kq_full[s], 1); mbar_init(&B.kq_empty[s], 1); }
         for (int s = 0; s < kVStages; ++s) { mbar_init(&B.v_full[s], 1); mbar_init(&B.v_empty[s], 1); }
         mbar_init(&B.g_full, 1);
+        mbar_init(&B.g_free, kPrepThreads);
         for (int s = 0; s < 2; ++s) {
             mbar_init(&B.prep_done[s], kPrepThreads);
+            mbar_init(&B.gn_ready[s], 1);
             mbar_init(&B.d_free[s], kChainThreads);
         }
         mbar_init(&B.x_full, 1);
@@ -268,6 +289,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         if (lane == 0) {
             const uint32_t id64 = idesc_bf16(128, 64);
             const uint32_t id64amn = idesc_bf16(128, 64, true, false);
+            const uint32_t id128 = idesc_bf16(128, 128);
             const uint32_t id128bmn = idesc_bf16(128, 128, false, true);
             auto kq_base = [&](int c) { return smem_u32(sm + OFF_KQ + (c % kKQStages) * kKQBytes); };
             auto issue_g = [&](int c) {   // M1: G = [K;Q] K^T
@@ -287,7 +309,13 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                 const uint32_t base = kq_base(c);
                 const uint32_t dsm = smem_u32(sm + OFF_D + sd * kDBytes);   // T1 | T2 | P
                 const uint32_t vsm = smem_u32(sm + OFF_V + sv * kVBytes);
-                const uint32_t ocol = kColO + sd * 64;
+                // the next chunk's G as soon as the prep group has read this one
+                mbar_wait(&B.g_free, c & 1, abort);
+                if (c + 1 < nch) {
+                    mbar_wait(&B.kq_full[(c + 1) % kKQStages], ((c + 1) / kKQStages) & 1, abort);
+                    tc_fence_after();
+                    issue_g(c + 1);
+                }
                 mbar_wait(&B.prep_done[sd], (c >> 1) & 1, abort);
                 mbar_wait(&B.s_next, c & 1, abort);
                 mbar_wait(&B.v_full[sv], (c / kVStages) & 1, abort);
@@ -296,19 +324,12 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                     mma_ss(tbase + kColU, sdesc_sw128(vsm + s * 16 * 128, kVBlk, 1024),
                            sdesc_sw128(dsm + s * 32, 16, 1024), id64amn, s > 0);
                 mma_commit(&B.v_empty[sv]);
-                for (int s = 0; s < 8; ++s) {   // M2: X = S K^T ; M3: O = S Q'^T
+                for (int s = 0; s < 8; ++s) {   // M23: [X | O] = S [K; Q']^T
                     const uint32_t off = (s >> 2) * kKBlk + (s & 3) * 32;
                     mma_ts(tbase + kColX, tbase + kColS16 + s * 8, sdesc_sw128(base + off, 16, 1024),
-                           id64, s > 0);
-                    mma_ts(tbase + ocol, tbase + kColS16 + s * 8,
-                           sdesc_sw128(base + 64 * 128 + off, 16, 1024), id64, s > 0);
+                           id128, s > 0);
                 }
                 mma_commit(&B.x_full);
-                if (c + 1 < nch) {
-                    mbar_wait(&B.kq_full[(c + 1) % kKQStages], ((c + 1) / kKQStages) & 1, abort);
-                    tc_fence_after();
-                    issue_g(c + 1);
-                }
                 mbar_wait(&B.r_full, c & 1, abort);
                 tc_fence_after();
                 for (int s = 0; s < 4; ++s)   // M4: U += T2 X^T
@@ -319,7 +340,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                 tc_fence_after();
                 for (int s = 0; s < 4; ++s) {
                     // M5: O += U P^T ; M6: S += U K''  (K'' MN-major: 2 blocks of 64 keys)
-                    mma_ts(tbase + ocol, tbase + kColU + s * 8,
+                    mma_ts(tbase + kColO, tbase + kColU + s * 8,
                            sdesc_sw128(dsm + 2 * kMatBytes + s * 32, 16, 1024), id64, 1);
                     mma_ts(tbase + kColS32, tbase + kColU + s * 8,
                            sdesc_sw128(base + s * 16 * 128, kKBlk, 1024), id128bmn, 1);
@@ -393,11 +414,12 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
             if (t < C) {
                 const float gl = S.gam[C - 1];      // padded rows carry g = 0
                 const bool ok = t < n;
-                S.xs[t] = ok ? expf(x) * S.rk[t] : 0.f;
-                S.ks[t] = ok ? expf(gl - x) * S.rk[t] : 0.f;
+                S.xs[t] = ok ? __expf(x) * S.rk[t] : 0.f;
+                S.ks[t] = ok ? __expf(gl - x) * S.rk[t] : 0.f;
                 if (t == 0) {
-                    S.gam_n = expf(gl);
+                    S.gam_n = __expf(gl);
                     S.n = n;
+                    mbar_arrive(&B.gn_ready[sd]);   // the chain needs only this early
                 }
             }
             named_sync(1, kPrepThreads);
@@ -407,6 +429,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
             uint32_t gr[32];
             tmem_ld32(tmem_addr(tbase, q4 * 32, kColG + 32 * chalf), gr);
             tc_fence_before();
+            mbar_arrive(&B.g_free);
             if (p < C) {
                 const int i = p;
                 const bool ok = i < n;
@@ -418,7 +441,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
                         const int j = 32 * chalf + jj + e;
-                        v[e] = (ok && j < i) ? bi * expf(gi - S.gam[j]) * S.rk[j] * __uint_as_float(gr[jj + e]) : 0.f;
+                        v[e] = (ok && j < i) ? bi * __expf(gi - S.gam[j]) * S.rk[j] * __uint_as_float(gr[jj + e]) : 0.f;
                     }
                     *reinterpret_cast<float4 *>(arow + jj) = make_float4(v[0], v[1], v[2], v[3]);
                 }
@@ -433,8 +456,8 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                     for (int e = 0; e < 4; ++e) {
                         const int jl = cc * 8 + 2 * e;
                         const int j0 = 32 * chalf + jl, j1 = j0 + 1;
-                        const float v0 = (ok && j0 <= i) ? ri * expf(gi - S.gam[j0]) * S.rk[j0] * __uint_as_float(gr[jl]) : 0.f;
-                        const float v1 = (ok && j1 <= i) ? ri * expf(gi - S.gam[j1]) * S.rk[j1] * __uint_as_float(gr[jl + 1]) : 0.f;
+                        const float v0 = (ok && j0 <= i) ? ri * __expf(gi - S.gam[j0]) * S.rk[j0] * __uint_as_float(gr[jl]) : 0.f;
+                        const float v1 = (ok && j1 <= i) ? ri * __expf(gi - S.gam[j1]) * S.rk[j1] * __uint_as_float(gr[jl + 1]) : 0.f;
                         w[e] = pack_bf16(v0, v1);
                     }
                     *reinterpret_cast<uint4 *>(dst + 2 * kMatBytes + sw128_chunk(i, 4 * chalf + cc)) =
@@ -466,7 +489,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                 // Q' = scale Gam_i r_q,i Q_i (M1 has consumed the raw rows)
                 const int tt = t - 128;
                 const int i = tt >> 1, kb = tt & 1;
-                const float f = i < n ? scale * expf(S.gam[i]) * S.rq[i] : 0.f;
+                const float f = i < n ? scale * __expf(S.gam[i]) * S.rq[i] : 0.f;
 #pragma unroll
                 for (int ch = 0; ch < 8; ++ch) {
                     uint4 *pq = reinterpret_cast<uint4 *>(kq + kb * kKBlk + sw128_chunk(C + i, ch));
@@ -552,33 +575,24 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         // E0: initial state -> bf16 operand copy, and the fp32 accumulator
         //     pre-scaled by the first chunk's total decay
         {
-            mbar_wait(&B.prep_done[0], 0, abort);
+            mbar_wait(&B.gn_ready[0], 0, abort);
             const float gn = reinterpret_cast<const Scal *>(sm + OFF_SCAL)->gam_n;
             const float *src = islot >= 0 ? pool + islot * slot_stride + head_off + (size_t)b * DH : nullptr;
-            for (int c0 = 0; c0 < DH; c0 += 64) {
-                uint32_t lo[32], hi[32], pk[32];
+            for (int c0 = 0; c0 < DH; c0 += 32) {
+                uint32_t v[32], pk[16];
 #pragma unroll
                 for (int j = 0; j < 32; j += 4) {
-                    float4 v0 = src ? *reinterpret_cast<const float4 *>(src + c0 + j) : make_float4(0.f, 0.f, 0.f, 0.f);
-                    float4 v1 = src ? *reinterpret_cast<const float4 *>(src + c0 + 32 + j) : make_float4(0.f, 0.f, 0.f, 0.f);
-                    lo[j] = __float_as_uint(v0.x); lo[j + 1] = __float_as_uint(v0.y);
-                    lo[j + 2] = __float_as_uint(v0.z); lo[j + 3] = __float_as_uint(v0.w);
-                    hi[j] = __float_as_uint(v1.x); hi[j + 1] = __float_as_uint(v1.y);
-                    hi[j + 2] = __float_as_uint(v1.z); hi[j + 3] = __float_as_uint(v1.w);
+                    const float4 f = src ? *reinterpret_cast<const float4 *>(src + c0 + j) : make_float4(0.f, 0.f, 0.f, 0.f);
+                    v[j] = __float_as_uint(f.x); v[j + 1] = __float_as_uint(f.y);
+                    v[j + 2] = __float_as_uint(f.z); v[j + 3] = __float_as_uint(f.w);
                 }
 #pragma unroll
-                for (int jj = 0; jj < 16; ++jj) {
-                    pk[jj] = pack_bf16(__uint_as_float(lo[2 * jj]), __uint_as_float(lo[2 * jj + 1]));
-                    pk[16 + jj] = pack_bf16(__uint_as_float(hi[2 * jj]), __uint_as_float(hi[2 * jj + 1]));
-                }
-                tmem_st32(lrow + kColS16 + c0 / 2, pk);
+                for (int jj = 0; jj < 16; ++jj)
+                    pk[jj] = pack_bf16(__uint_as_float(v[2 * jj]), __uint_as_float(v[2 * jj + 1]));
+                tmem_st16(lrow + kColS16 + c0 / 2, pk);
 #pragma unroll
-                for (int j = 0; j < 32; ++j) {
-                    lo[j] = __float_as_uint(__uint_as_float(lo[j]) * gn);
-                    hi[j] = __float_as_uint(__uint_as_float(hi[j]) * gn);
-                }
-                tmem_st32(lrow + kColS32 + c0, lo);
-                tmem_st32(lrow + kColS32 + c0 + 32, hi);
+                for (int j = 0; j < 32; ++j) v[j] = __float_as_uint(__uint_as_float(v[j]) * gn);
+                tmem_st32(lrow + kColS32 + c0, v);
             }
             tmem_wait_st();
             tc_fence_before();
@@ -595,18 +609,16 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
             // ---- E1: X -> bf16 in TMEM (X's columns)
             mbar_wait(&B.x_full, c & 1, abort);
             tc_fence_after();
-            {
-                uint32_t x0[32], x1[32], xx[32];
-                tmem_ld32(lrow + kColX, x0);
-                tmem_ld32(lrow + kColX + 32, x1);
 #pragma unroll
-                for (int jj = 0; jj < 16; ++jj) {
-                    xx[jj] = pack_bf16(__uint_as_float(x0[2 * jj]), __uint_as_float(x0[2 * jj + 1]));
-                    xx[16 + jj] = pack_bf16(__uint_as_float(x1[2 * jj]), __uint_as_float(x1[2 * jj + 1]));
-                }
-                tmem_st32(lrow + kColX, xx);
-                tmem_wait_st();
+            for (int h2 = 0; h2 < 2; ++h2) {
+                uint32_t x[32], xx[16];
+                tmem_ld32(lrow + kColX + 32 * h2, x);
+#pragma unroll
+                for (int jj = 0; jj < 16; ++jj)
+                    xx[jj] = pack_bf16(__uint_as_float(x[2 * jj]), __uint_as_float(x[2 * jj + 1]));
+                tmem_st16(lrow + kColX + 16 * h2, xx);
             }
+            tmem_wait_st();
             tc_fence_before();
             mbar_arrive(&B.r_full);
             // K'' = D[last][j] r_k,j K_j in place (M1, M2 have consumed the raw rows)
@@ -623,18 +635,16 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
             // ---- E2: U -> bf16 in TMEM (U's columns)
             mbar_wait(&B.u_full, c & 1, abort);
             tc_fence_after();
-            {
-                uint32_t u0[32], u1[32], uu[32];
-                tmem_ld32(lrow + kColU, u0);
-                tmem_ld32(lrow + kColU + 32, u1);
 #pragma unroll
-                for (int jj = 0; jj < 16; ++jj) {
-                    uu[jj] = pack_bf16(__uint_as_float(u0[2 * jj]), __uint_as_float(u0[2 * jj + 1]));
-                    uu[16 + jj] = pack_bf16(__uint_as_float(u1[2 * jj]), __uint_as_float(u1[2 * jj + 1]));
-                }
-                tmem_st32(lrow + kColU, uu);
-                tmem_wait_st();
+            for (int h2 = 0; h2 < 2; ++h2) {
+                uint32_t u[32], uu[16];
+                tmem_ld32(lrow + kColU + 32 * h2, u);
+#pragma unroll
+                for (int jj = 0; jj < 16; ++jj)
+                    uu[jj] = pack_bf16(__uint_as_float(u[2 * jj]), __uint_as_float(u[2 * jj + 1]));
+                tmem_st16(lrow + kColU + 16 * h2, uu);
             }
+            tmem_wait_st();
             tc_fence_before();
             mbar_arrive(&B.u2_full);
             // ---- E3a: S -> bf16 operand copy, fp32 pre-scaled for the next
@@ -643,57 +653,46 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
             tc_fence_after();
             float gnext = 1.f;
             if (!last) {
-                mbar_wait(&B.prep_done[sd ^ 1], ((c + 1) >> 1) & 1, abort);
+                mbar_wait(&B.gn_ready[sd ^ 1], ((c + 1) >> 1) & 1, abort);
                 gnext = reinterpret_cast<const Scal *>(sm + OFF_SCAL + (sd ^ 1) * kScalBytes)->gam_n;
             }
             float *dstp = (last && fslot >= 0) ? pool + fslot * slot_stride + head_off + (size_t)b * DH : nullptr;
-            for (int cc = 0; cc < DH; cc += 64) {
-                uint32_t s0[32], s1[32];
-                tmem_ld32(lrow + kColS32 + cc, s0);
-                tmem_ld32(lrow + kColS32 + cc + 32, s1);
+            for (int cc = 0; cc < DH; cc += 32) {
+                uint32_t sv[32];
+                tmem_ld32(lrow + kColS32 + cc, sv);
                 if (!last) {
-                    uint32_t pk[32];
+                    uint32_t pk[16];
 #pragma unroll
-                    for (int jj = 0; jj < 16; ++jj) {
-                        pk[jj] = pack_bf16(__uint_as_float(s0[2 * jj]), __uint_as_float(s0[2 * jj + 1]));
-                        pk[16 + jj] = pack_bf16(__uint_as_float(s1[2 * jj]), __uint_as_float(s1[2 * jj + 1]));
-                    }
-                    tmem_st32(lrow + kColS16 + cc / 2, pk);
+                    for (int jj = 0; jj < 16; ++jj)
+                        pk[jj] = pack_bf16(__uint_as_float(sv[2 * jj]), __uint_as_float(sv[2 * jj + 1]));
+                    tmem_st16(lrow + kColS16 + cc / 2, pk);
 #pragma unroll
-                    for (int j = 0; j < 32; ++j) {
-                        s0[j] = __float_as_uint(__uint_as_float(s0[j]) * gnext);
-                        s1[j] = __float_as_uint(__uint_as_float(s1[j]) * gnext);
-                    }
-                    tmem_st32(lrow + kColS32 + cc, s0);
-                    tmem_st32(lrow + kColS32 + cc + 32, s1);
+                    for (int j = 0; j < 32; ++j) sv[j] = __float_as_uint(__uint_as_float(sv[j]) * gnext);
+                    tmem_st32(lrow + kColS32 + cc, sv);
                 } else if (dstp) {
 #pragma unroll
-                    for (int j = 0; j < 32; j += 4) {
+                    for (int j = 0; j < 32; j += 4)
                         *reinterpret_cast<float4 *>(dstp + cc + j) = make_float4(
-                            __uint_as_float(s0[j]), __uint_as_float(s0[j + 1]),
-                            __uint_as_float(s0[j + 2]), __uint_as_float(s0[j + 3]));
-                        *reinterpret_cast<float4 *>(dstp + cc + 32 + j) = make_float4(
-                            __uint_as_float(s1[j]), __uint_as_float(s1[j + 1]),
-                            __uint_as_float(s1[j + 2]), __uint_as_float(s1[j + 3]));
-                    }
+                            __uint_as_float(sv[j]), __uint_as_float(sv[j + 1]),
+                            __uint_as_float(sv[j + 2]), __uint_as_float(sv[j + 3]));
                 }
             }
+            uint32_t ov0[32], ov1[32];
+            tmem_ld32(lrow + kColO, ov0);
+            tmem_ld32(lrow + kColO + 32, ov1);
             tmem_wait_st();
             tc_fence_before();
-            mbar_arrive(&B.s_next);
-            // ---- E3b: o <- O (this chunk's buffer; the next chunk uses the other)
+            mbar_arrive(&B.s_next);      // S16 ready and X | O free for the next chunk
+            // ---- E3b: o <- O (from registers)
             {
-                uint32_t o0[32], o1[32];
-                tmem_ld32(lrow + kColO + sd * 64, o0);
-                tmem_ld32(lrow + kColO + sd * 64 + 32, o1);
                 __nv_bfloat16 *orow = o + (c0 * hv + h) * (int64_t)DH + b;
                 const int64_t ostride = (int64_t)hv * DH;
 #pragma unroll
                 for (int i = 0; i < 32; ++i)
-                    if (i < n) orow[i * ostride] = __float2bfloat16_rn(__uint_as_float(o0[i]));
+                    if (i < n) orow[i * ostride] = __float2bfloat16_rn(__uint_as_float(ov0[i]));
 #pragma unroll
                 for (int i = 0; i < 32; ++i)
-                    if (32 + i < n) orow[(32 + i) * ostride] = __float2bfloat16_rn(__uint_as_float(o1[i]));
+                    if (32 + i < n) orow[(32 + i) * ostride] = __float2bfloat16_rn(__uint_as_float(ov1[i]));
             }
             tc_fence_before();
             mbar_arrive(&B.d_free[sd]);
