@@ -63,7 +63,7 @@ constexpr uint32_t kColS32 = 0, kColS16 = 128, kColG = 192, kColU = 256, kColX =
                    kColO = 384, kTmemCols = 512;   // X and O adjacent: one N = 128 MMA
 
 struct Scal {
-    float beta[C], gam[C], rk[C], rq[C], xs[C], ks[C];
+    float beta[C], gam[C], alpha[C], rk[C], rq[C], xs[C], ks[C];
     float gam_n;
     int n;
 };
@@ -233,7 +233,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         mbar_init(&B.g_free, kPrepThreads);
         for (int s = 0; s < 2; ++s) {
             mbar_init(&B.prep_done[s], kPrepThreads);
-            mbar_init(&B.gn_ready[s], 1);
+            mbar_init(&B.gn_ready[s], C);
             mbar_init(&B.d_free[s], kChainThreads);
         }
         mbar_init(&B.x_full, 1);
@@ -367,10 +367,17 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
             uint8_t *dst = sm + OFF_D + sd * kDBytes;
             const int64_t c0 = s_start + (int64_t)c * C;
             const int n = (int)min((int64_t)C, s_end - c0);
-            float gv = 0.f, bv = 0.f;
-            if (t < n) {
-                gv = g[(c0 + t) * hv + h];
-                bv = beta[(c0 + t) * hv + h];
+            // warp 0 of the group holds the chunk's gates, rows 2l and 2l+1 per lane
+            float g0 = 0.f, g1 = 0.f, b0 = 0.f, b1 = 0.f;
+            if (t < 32) {
+                if (2 * t < n) {
+                    g0 = g[(c0 + 2 * t) * hv + h];
+                    b0 = beta[(c0 + 2 * t) * hv + h];
+                }
+                if (2 * t + 1 < n) {
+                    g1 = g[(c0 + 2 * t + 1) * hv + h];
+                    b1 = beta[(c0 + 2 * t + 1) * hv + h];
+                }
             }
             if (c >= 2) mbar_wait(&B.d_free[sd], ((c >> 1) - 1) & 1, abort);
             mbar_wait(&B.kq_full[sk], (c / kKQStages) & 1, abort);
@@ -394,35 +401,34 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                     if (row < C) S.rk[row] = r; else S.rq[row - C] = r;
                 }
             }
-            // ---- prefix sum of g over the chunk (warps 2, 3)
-            float x = gv;
-            if (t < C) {
+            // ---- prefix sum of g (one warp), per-token decay alpha = exp(g)
+            if (t < 32) {
+                float x = g0 + g1;
 #pragma unroll
                 for (int off = 1; off < 32; off <<= 1) {
                     const float y = __shfl_up_sync(0xffffffffu, x, off);
                     if (lane >= off) x += y;
                 }
-                if (t == 31) B.tot0 = x;
-            }
-            named_sync(1, kPrepThreads);
-            if (t < C) {
-                if (t >= 32) x += B.tot0;
-                S.gam[t] = x;
-                S.beta[t] = bv;
+                S.gam[2 * t] = x - g1;
+                S.gam[2 * t + 1] = x;
+                S.beta[2 * t] = b0;
+                S.beta[2 * t + 1] = b1;
+                S.alpha[2 * t] = __expf(g0);
+                S.alpha[2 * t + 1] = __expf(g1);
             }
             named_sync(1, kPrepThreads);
             if (t < C) {
                 const float gl = S.gam[C - 1];      // padded rows carry g = 0
+                const float x = S.gam[t];
                 const bool ok = t < n;
                 S.xs[t] = ok ? __expf(x) * S.rk[t] : 0.f;
                 S.ks[t] = ok ? __expf(gl - x) * S.rk[t] : 0.f;
                 if (t == 0) {
                     S.gam_n = __expf(gl);
                     S.n = n;
-                    mbar_arrive(&B.gn_ready[sd]);   // the chain needs only this early
                 }
+                mbar_arrive(&B.gn_ready[sd]);   // the chain needs these early
             }
-            named_sync(1, kPrepThreads);
             // ---- G -> A (K rows, fp32 scratch) and P (Q rows, bf16 operand)
             mbar_wait(&B.g_full, c & 1, abort);
             tc_fence_after();
@@ -430,43 +436,44 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
             tmem_ld32(tmem_addr(tbase, q4 * 32, kColG + 32 * chalf), gr);
             tc_fence_before();
             mbar_arrive(&B.g_free);
-            if (p < C) {
-                const int i = p;
+            {
+                // decay factors E_ij = exp(gc_i - gc_j) for this thread's 32 columns,
+                // walked downwards as a running product of alpha (one exp per row):
+                // E_ii = 1, E_{i,j-1} = E_ij alpha_j.
+                const bool krow = p < C;
+                const int i = krow ? p : p - C;
                 const bool ok = i < n;
-                const float bi = S.beta[i] * S.rk[i], gi = S.gam[i];
-                float *arow = Af + i * kLd + 32 * chalf;
+                const int cb = 32 * chalf;
+                const float coef = krow ? S.beta[i] * S.rk[i] : scale * S.rq[i];
+                float e = (i > cb + 31) ? __expf(S.gam[i] - S.gam[cb + 31]) : 1.f;
+                float v[32];
 #pragma unroll
-                for (int jj = 0; jj < 32; jj += 4) {
-                    float v[4];
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const int j = 32 * chalf + jj + e;
-                        v[e] = (ok && j < i) ? bi * __expf(gi - S.gam[j]) * S.rk[j] * __uint_as_float(gr[jj + e]) : 0.f;
-                    }
-                    *reinterpret_cast<float4 *>(arow + jj) = make_float4(v[0], v[1], v[2], v[3]);
+                for (int jj = 31; jj >= 0; --jj) {
+                    const int j = cb + jj;
+                    const bool on = j <= i;
+                    const bool keep = ok && (krow ? j < i : on);
+                    v[jj] = keep ? coef * e * S.rk[j] * __uint_as_float(gr[jj]) : 0.f;
+                    if (on) e *= S.alpha[j];
                 }
-            } else {
-                const int i = p - C;
-                const bool ok = i < n;
-                const float ri = scale * S.rq[i], gi = S.gam[i];
+                if (krow) {      // A row (fp32, for the solve)
+                    float *arow = Af + i * kLd + cb;
 #pragma unroll
-                for (int cc = 0; cc < 4; ++cc) {
-                    uint32_t w[4];
+                    for (int jj = 0; jj < 32; jj += 4)
+                        *reinterpret_cast<float4 *>(arow + jj) = make_float4(v[jj], v[jj + 1], v[jj + 2], v[jj + 3]);
+                } else {         // P row (bf16 operand)
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const int jl = cc * 8 + 2 * e;
-                        const int j0 = 32 * chalf + jl, j1 = j0 + 1;
-                        const float v0 = (ok && j0 <= i) ? ri * __expf(gi - S.gam[j0]) * S.rk[j0] * __uint_as_float(gr[jl]) : 0.f;
-                        const float v1 = (ok && j1 <= i) ? ri * __expf(gi - S.gam[j1]) * S.rk[j1] * __uint_as_float(gr[jl + 1]) : 0.f;
-                        w[e] = pack_bf16(v0, v1);
+                    for (int cc = 0; cc < 4; ++cc) {
+                        uint32_t w[4];
+#pragma unroll
+                        for (int e2 = 0; e2 < 4; ++e2) w[e2] = pack_bf16(v[cc * 8 + 2 * e2], v[cc * 8 + 2 * e2 + 1]);
+                        *reinterpret_cast<uint4 *>(dst + 2 * kMatBytes + sw128_chunk(i, 4 * chalf + cc)) =
+                            make_uint4(w[0], w[1], w[2], w[3]);
                     }
-                    *reinterpret_cast<uint4 *>(dst + 2 * kMatBytes + sw128_chunk(i, 4 * chalf + cc)) =
-                        make_uint4(w[0], w[1], w[2], w[3]);
                 }
             }
             named_sync(1, kPrepThreads);
             // ---- T = (I + A)^-1: diagonal 16 x 16 blocks by forward substitution
-            //      (warps 0..3 of the group) while warps 4..7 rescale Q rows in place
+            //      (warps 0..3 of the group)
             if (pw < 4) {
                 const int r = lane >> 1, hh = lane & 1;
                 const int bb = pw;
@@ -485,16 +492,6 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                 }
                 *reinterpret_cast<float4 *>(Tf + R * kLd + 16 * bb + 8 * hh) = make_float4(tv[0], tv[1], tv[2], tv[3]);
                 *reinterpret_cast<float4 *>(Tf + R * kLd + 16 * bb + 8 * hh + 4) = make_float4(tv[4], tv[5], tv[6], tv[7]);
-            } else {
-                // Q' = scale Gam_i r_q,i Q_i (M1 has consumed the raw rows)
-                const int tt = t - 128;
-                const int i = tt >> 1, kb = tt & 1;
-                const float f = i < n ? scale * __expf(S.gam[i]) * S.rq[i] : 0.f;
-#pragma unroll
-                for (int ch = 0; ch < 8; ++ch) {
-                    uint4 *pq = reinterpret_cast<uint4 *>(kq + kb * kKBlk + sw128_chunk(C + i, ch));
-                    *pq = scale_chunk(*pq, f);
-                }
             }
             named_sync(1, kPrepThreads);
             // ---- the blocks below the diagonal, level by level; each warp owns
@@ -533,21 +530,9 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                     }
                 }
                 named_sync(1, kPrepThreads);
-                if (pw < 2) {              // level 3: T30 = -T33 (Z30 + A32 T20)
-                    const int col = 8 * pw;
-                    const float4 z = *reinterpret_cast<const float4 *>(Zs + r * 16 + col + 4 * cg);
-                    acc[0] = z.x; acc[1] = z.y; acc[2] = z.z; acc[3] = z.w;
-                    half_mac(acc, Af, 48, 32, Tf, 32, col, r, cg);
-                    half_finish(acc, Tf, wb, 3, col, r, cg);
-                }
-                named_sync(1, kPrepThreads);
-            }
-            // ---- T1 = T diag(beta), T2 = -T diag(beta Gam r_k), bf16 K-major [i][j]
-            {
-                const int i = t >> 2, q2 = t & 3;
-#pragma unroll
-                for (int h2 = 0; h2 < 2; ++h2) {
-                    const int ch = 2 * q2 + h2;
+                // T1 = T diag(beta), T2 = -T diag(beta Gam r_k), bf16 K-major [i][j];
+                // block rows 0..2 are final now, block row 3 after level 3
+                auto write_t12 = [&](int i, int ch) {
                     uint32_t w1[4], w2[4];
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
@@ -560,7 +545,20 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                     *reinterpret_cast<uint4 *>(dst + sw128_chunk(i, ch)) = make_uint4(w1[0], w1[1], w1[2], w1[3]);
                     *reinterpret_cast<uint4 *>(dst + kMatBytes + sw128_chunk(i, ch)) =
                         make_uint4(w2[0], w2[1], w2[2], w2[3]);
+                };
+                if (pw < 2) {              // level 3: T30 = -T33 (Z30 + A32 T20)
+                    const int col = 8 * pw;
+                    const float4 z = *reinterpret_cast<const float4 *>(Zs + r * 16 + col + 4 * cg);
+                    acc[0] = z.x; acc[1] = z.y; acc[2] = z.z; acc[3] = z.w;
+                    half_mac(acc, Af, 48, 32, Tf, 32, col, r, cg);
+                    half_finish(acc, Tf, wb, 3, col, r, cg);
+                } else {                   // meanwhile rows 0..47: 384 chunks over 192 threads
+                    const int u = t - 64;
+                    write_t12(u >> 2, 2 * (u & 3));
+                    write_t12(u >> 2, 2 * (u & 3) + 1);
                 }
+                named_sync(1, kPrepThreads);
+                if (t < 128) write_t12(48 + (t >> 3), t & 7);
             }
             fence_async_smem();
             mbar_arrive(&B.prep_done[sd]);
@@ -572,6 +570,23 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         const int q4 = warp & 3;
         const int b = q4 * 32 + lane;            // value row of the state
         const uint32_t lrow = tmem_addr(tbase, q4 * 32, 0);
+        // Q' = scale Gam_i r_q,i Q_i in place for chunk cq, once its scalars are
+        // out and M1 has read the raw rows (g_free); before M23 of that chunk.
+        auto rescale_q = [&](int cq) {
+            const int sq = cq & 1;
+            mbar_wait(&B.gn_ready[sq], (cq >> 1) & 1, abort);
+            mbar_wait(&B.g_free, cq & 1, abort);
+            const Scal &Sq = *reinterpret_cast<const Scal *>(sm + OFF_SCAL + sq * kScalBytes);
+            uint8_t *kqq = sm + OFF_KQ + (cq % kKQStages) * kKQBytes;
+            const int i = tc4 >> 1, kb = tc4 & 1;
+            const float f = i < Sq.n ? scale * __expf(Sq.gam[i]) * Sq.rq[i] : 0.f;
+#pragma unroll
+            for (int ch = 0; ch < 8; ++ch) {
+                uint4 *pq = reinterpret_cast<uint4 *>(kqq + kb * kKBlk + sw128_chunk(C + i, ch));
+                *pq = scale_chunk(*pq, f);
+            }
+            fence_async_smem();
+        };
         // E0: initial state -> bf16 operand copy, and the fp32 accumulator
         //     pre-scaled by the first chunk's total decay
         {
@@ -595,6 +610,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                 tmem_st32(lrow + kColS32 + c0, v);
             }
             tmem_wait_st();
+            rescale_q(0);
             tc_fence_before();
             mbar_arrive(&B.s_next);
         }
@@ -647,6 +663,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
             tmem_wait_st();
             tc_fence_before();
             mbar_arrive(&B.u2_full);
+            if (!last) rescale_q(c + 1);   // overlaps M5 / M6
             // ---- E3a: S -> bf16 operand copy, fp32 pre-scaled for the next
             //      chunk (or the final state -> pool)
             mbar_wait(&B.s_full, c & 1, abort);
