@@ -35,7 +35,9 @@ __device__ __forceinline__ float dot4(float4 a, float4 b) {
     return fmaf(a.x, b.x, fmaf(a.y, b.y, fmaf(a.z, b.z, a.w * b.w)));
 }
 
-template <int DK, typename T>
+// SPLIT CTAs share one (sequence, V head): CTA `part` owns the state rows
+// [part*rows, (part+1)*rows).  Fewer registers per thread, more resident CTAs.
+template <int DK, int SPLIT, typename T>
 __global__ void __launch_bounds__(kDecThreads)
 decode_kernel(const T *__restrict__ q, int64_t qs, const T *__restrict__ k, int64_t ks,
               const T *__restrict__ v, int64_t vs, const float *__restrict__ g,
@@ -46,40 +48,46 @@ decode_kernel(const T *__restrict__ q, int64_t qs, const T *__restrict__ k, int6
     constexpr int LPR = DK / 4;                     // lanes per state row
     constexpr int RPW = 32 / LPR;                   // rows per warp per pass
     constexpr int RPP = RPW * kDecWarps;            // rows per pass
-    constexpr int NP = (kMaxDv + RPP - 1) / RPP;    // passes covering dv <= 128
+    constexpr int kMaxRows = kMaxDv / SPLIT;
+    constexpr int NP = (kMaxRows + RPP - 1) / RPP;  // passes covering this CTA's rows
 
-    __shared__ float o_s[kMaxTps][kMaxDv];
-    __shared__ float v_s[kMaxTps][kMaxDv];
+    __shared__ float o_s[kMaxTps][kMaxRows];
+    __shared__ float v_s[kMaxTps][kMaxRows];
 
-    const int i = blockIdx.x / hv;
-    const int h = blockIdx.x - i * hv;
+    const int part = blockIdx.x % SPLIT;
+    const int ih = blockIdx.x / SPLIT;
+    const int i = ih / hv;
+    const int h = ih - i * hv;
     const int hq = h / grp;
+    const int rows = (dv + SPLIT - 1) / SPLIT;
+    const int r0 = part * rows;
+    const int nr = max(0, min(dv, r0 + rows) - r0);   // rows of this CTA
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int col = (lane % LPR) * 4;
     const int sub = lane / LPR;
 
     const int64_t slot = idx[i];
     const bool live = slot >= 0 && slot < n_slots;
-    if (slot >= n_slots && threadIdx.x == 0) flag_status(GDN_DEVSTAT_BAD_INDEX);
+    if (slot >= n_slots && threadIdx.x == 0 && part == 0) flag_status(GDN_DEVSTAT_BAD_INDEX);
     if (!live) {
-        for (int e = threadIdx.x; e < tps * dv; e += kDecThreads) {
-            const int t = e / dv, r = e - t * dv;
-            Io<T>::store(o + (((int64_t)i * tps + t) * hv + h) * dv + r, 0.0f);
+        for (int e = threadIdx.x; e < tps * nr; e += kDecThreads) {
+            const int t = e / nr, r = e - t * nr;
+            Io<T>::store(o + (((int64_t)i * tps + t) * hv + h) * dv + r0 + r, 0.0f);
         }
         return;
     }
 
-    float *src = pool + ((slot * hv + h) * (int64_t)dv) * DK;
+    float *src = pool + ((slot * hv + h) * (int64_t)dv + r0) * DK;
     float4 st[NP];
 #pragma unroll
     for (int p = 0; p < NP; ++p) {
         const int r = p * RPP + warp * RPW + sub;
-        st[p] = r < dv ? __ldcs(reinterpret_cast<const float4 *>(src + (int64_t)r * DK + col))
+        st[p] = r < nr ? __ldcs(reinterpret_cast<const float4 *>(src + (int64_t)r * DK + col))
                        : make_float4(0.f, 0.f, 0.f, 0.f);
     }
-    for (int e = threadIdx.x; e < tps * dv; e += kDecThreads) {
-        const int t = e / dv, r = e - t * dv;
-        v_s[t][r] = Io<T>::load(v + ((int64_t)i * tps + t) * vs + (int64_t)h * dv + r);
+    for (int e = threadIdx.x; e < tps * nr; e += kDecThreads) {
+        const int t = e / nr, r = e - t * nr;
+        v_s[t][r] = Io<T>::load(v + ((int64_t)i * tps + t) * vs + (int64_t)h * dv + r0 + r);
     }
     __syncthreads();
 
@@ -99,11 +107,11 @@ decode_kernel(const T *__restrict__ q, int64_t qs, const T *__restrict__ k, int6
 #pragma unroll
         for (int p = 0; p < NP; ++p) {
             const int r = p * RPP + warp * RPW + sub;
-            if (p * RPP < dv) {                      // warp-uniform: shuffles stay converged
+            if (p * RPP < nr) {                      // warp-uniform: shuffles stay converged
                 const float4 s = st[p];
                 const float sk = row_sum<LPR>(dot4(s, k4));
                 const float sq = row_sum<LPR>(dot4(s, q4));
-                if (r < dv) {
+                if (r < nr) {
                     const float u = b * (v_s[t][r] - alpha * sk);
                     st[p] = make_float4(fmaf(alpha, s.x, u * k4.x), fmaf(alpha, s.y, u * k4.y),
                                         fmaf(alpha, s.z, u * k4.z), fmaf(alpha, s.w, u * k4.w));
@@ -114,13 +122,13 @@ decode_kernel(const T *__restrict__ q, int64_t qs, const T *__restrict__ k, int6
         if (snap) {
             const int64_t d = snap[row];
             if (d >= n_slots) {
-                if (threadIdx.x == 0) flag_status(GDN_DEVSTAT_BAD_INDEX);
+                if (threadIdx.x == 0 && part == 0) flag_status(GDN_DEVSTAT_BAD_INDEX);
             } else if (d >= 0) {
-                float *dst = pool + ((d * hv + h) * (int64_t)dv) * DK;
+                float *dst = pool + ((d * hv + h) * (int64_t)dv + r0) * DK;
 #pragma unroll
                 for (int p = 0; p < NP; ++p) {
                     const int r = p * RPP + warp * RPW + sub;
-                    if (r < dv) __stcs(reinterpret_cast<float4 *>(dst + (int64_t)r * DK + col), st[p]);
+                    if (r < nr) __stcs(reinterpret_cast<float4 *>(dst + (int64_t)r * DK + col), st[p]);
                 }
             }
         }
@@ -129,13 +137,13 @@ decode_kernel(const T *__restrict__ q, int64_t qs, const T *__restrict__ k, int6
 #pragma unroll
         for (int p = 0; p < NP; ++p) {
             const int r = p * RPP + warp * RPW + sub;
-            if (r < dv) __stcs(reinterpret_cast<float4 *>(src + (int64_t)r * DK + col), st[p]);
+            if (r < nr) __stcs(reinterpret_cast<float4 *>(src + (int64_t)r * DK + col), st[p]);
         }
     }
     __syncthreads();
-    for (int e = threadIdx.x; e < tps * dv; e += kDecThreads) {
-        const int t = e / dv, r = e - t * dv;
-        Io<T>::store(o + (((int64_t)i * tps + t) * hv + h) * dv + r, o_s[t][r]);
+    for (int e = threadIdx.x; e < tps * nr; e += kDecThreads) {
+        const int t = e / nr, r = e - t * nr;
+        Io<T>::store(o + (((int64_t)i * tps + t) * hv + h) * dv + r0 + r, o_s[t][r]);
     }
 }
 
@@ -145,10 +153,16 @@ static void launch_decode(const void *q, int64_t qs, const void *k, int64_t ks, 
                           int hqk, int hv, int dv, float scale, int l2norm, float *pool,
                           int64_t n_slots, const int32_t *idx, const int32_t *snap, void *o,
                           cudaStream_t s) {
-    const int64_t blocks = (int64_t)n_seqs * hv;
-    decode_kernel<DK, T><<<(unsigned)blocks, kDecThreads, 0, s>>>(
-        (const T *)q, qs, (const T *)k, ks, (const T *)v, vs, g, beta, tps, hv, hv / hqk, dv,
-        scale, l2norm, pool, n_slots, idx, snap, (T *)o);
+    const int64_t heads = (int64_t)n_seqs * hv;
+    if (dv > 64) {     // two CTAs per state: half the registers, twice the CTAs in flight
+        decode_kernel<DK, 2, T><<<(unsigned)(heads * 2), kDecThreads, 0, s>>>(
+            (const T *)q, qs, (const T *)k, ks, (const T *)v, vs, g, beta, tps, hv, hv / hqk, dv,
+            scale, l2norm, pool, n_slots, idx, snap, (T *)o);
+    } else {
+        decode_kernel<DK, 1, T><<<(unsigned)heads, kDecThreads, 0, s>>>(
+            (const T *)q, qs, (const T *)k, ks, (const T *)v, vs, g, beta, tps, hv, hv / hqk, dv,
+            scale, l2norm, pool, n_slots, idx, snap, (T *)o);
+    }
 }
 
 }  // namespace gdn
@@ -172,7 +186,7 @@ extern "C" gdn_status gdn_decode_recurrent(const void *q, int64_t q_row_stride, 
     GDN_REQUIRE(dk == 16 || dk == 32 || dk == 64 || dk == 128, GDN_ERR_UNSUPPORTED);
     GDN_REQUIRE(dv >= 1 && dv <= kMaxDv, GDN_ERR_UNSUPPORTED);
     if (n_seqs == 0) return GDN_OK;
-    GDN_REQUIRE((int64_t)n_seqs * hv < (1ll << 31), GDN_ERR_UNSUPPORTED);
+    GDN_REQUIRE((int64_t)n_seqs * hv * 2 < (1ll << 31), GDN_ERR_UNSUPPORTED);
     GDN_REQUIRE(q && k && v && g && beta && state_pool && state_indices && o, GDN_ERR_INVALID_ARG);
     GDN_REQUIRE(q_row_stride >= (int64_t)hqk * dk && k_row_stride >= (int64_t)hqk * dk &&
                     v_row_stride >= (int64_t)hv * dv,
