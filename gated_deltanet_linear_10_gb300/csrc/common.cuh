@@ -90,9 +90,22 @@ template <> struct Vec16<float> {
     static __device__ __forceinline__ void store(float *p, const float *in) {
         *reinterpret_cast<float4 *>(p) = make_float4(in[0], in[1], in[2], in[3]);
     }
+    static __device__ __forceinline__ void unpack(const uint4 &r, float *out) {
+        out[0] = __uint_as_float(r.x); out[1] = __uint_as_float(r.y);
+        out[2] = __uint_as_float(r.z); out[3] = __uint_as_float(r.w);
+    }
 };
 template <> struct Vec16<__nv_bfloat16> {
     static constexpr int N = 8;
+    static __device__ __forceinline__ void unpack(const uint4 &r, float *out) {
+        const __nv_bfloat162 *h = reinterpret_cast<const __nv_bfloat162 *>(&r);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            float2 f = __bfloat1622float2(h[i]);
+            out[2 * i] = f.x;
+            out[2 * i + 1] = f.y;
+        }
+    }
     static __device__ __forceinline__ void load(const __nv_bfloat16 *p, float *out) {
         uint4 r = *reinterpret_cast<const uint4 *>(p);
         const __nv_bfloat162 *h = reinterpret_cast<const __nv_bfloat162 *>(&r);
@@ -112,7 +125,9 @@ template <> struct Vec16<__nv_bfloat16> {
     }
 };
 
-__device__ __forceinline__ float silu_f(float z) { return z / (1.0f + expf(-z)); }
+// SiLU(z) = z * sigmoid(z), with the fast exponential and a correctly rounded
+// reciprocal (relative error ~1e-6; for z << 0 the reciprocal goes to 0).
+__device__ __forceinline__ float silu_f(float z) { return z * __frcp_rn(1.0f + __expf(-z)); }
 
 }  // namespace gdn
 

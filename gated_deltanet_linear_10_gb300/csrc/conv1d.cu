@@ -13,19 +13,29 @@ GDN_DECLARE_STATUS_WORD(g_status_conv)
 GDN_STATUS_READER(read_status_conv, g_status_conv)
 
 constexpr int kConvThreads = 128;
-constexpr int kConvTokensPerThread = 16;
+constexpr int kConvTokensPerThread = 8;
 
 template <typename T, int W>
 struct ConvTaps {
     static constexpr int V = Vec16<T>::N;
     float w[W][V];
     float bias[V];
+    // The V x W taps of channels c0 .. c0+V-1 are 16 W contiguous bytes: W
+    // 16-byte loads (weight and bias 16-byte aligned, checked on the host).
     __device__ __forceinline__ void load(const T *weight, const T *b, int c0) {
+        float e[V * W];
+        const uint4 *src = reinterpret_cast<const uint4 *>(weight + (int64_t)c0 * W);
 #pragma unroll
-        for (int v = 0; v < V; ++v) {
+        for (int u = 0; u < W; ++u) Vec16<T>::unpack(__ldg(src + u), e + u * V);
 #pragma unroll
-            for (int j = 0; j < W; ++j) w[j][v] = Io<T>::load(weight + (int64_t)(c0 + v) * W + j);
-            bias[v] = b ? Io<T>::load(b + c0 + v) : 0.0f;
+        for (int v = 0; v < V; ++v)
+#pragma unroll
+            for (int j = 0; j < W; ++j) w[j][v] = e[v * W + j];
+        if (b) {
+            Vec16<T>::load(b + c0, bias);
+        } else {
+#pragma unroll
+            for (int v = 0; v < V; ++v) bias[v] = 0.0f;
         }
     }
     // out = act(bias + sum_j w[j] * e[t-(W-1)+j]); win holds e[t-(W-1) .. t-1].
@@ -91,6 +101,41 @@ conv_fwd_kernel(const T *__restrict__ x, int64_t x_stride, const T *__restrict__
     }
     int i = lo;
     float win[W - 1][V];
+    // fast path: the whole run lies in one sequence, so every load is issued
+    // before the first use (8 token rows + the history rows in flight)
+    if (i < n_seqs) {
+        const int64_t ss = cu[i], se = cu[i + 1];
+        if (ss >= 0 && ss <= t0 && t1 <= se && se <= n_tokens) {
+            uint4 raw[kConvTokensPerThread];
+#pragma unroll
+            for (int tt = 0; tt < kConvTokensPerThread; ++tt)
+                if (t0 + tt < t1) raw[tt] = *reinterpret_cast<const uint4 *>(x + (t0 + tt) * x_stride + c0);
+            const int64_t hs = (t0 - ss < W - 1) ? history_slot(idx, has_init, i, n_slots) : -1;
+#pragma unroll
+            for (int r = 0; r < W - 1; ++r) {
+                const int64_t n = t0 - (W - 1) + r;
+                if (n >= ss) {
+                    Vec16<T>::load(x + n * x_stride + c0, win[r]);
+                } else if (hs >= 0) {
+                    Vec16<T>::load(pool + (hs * (W - 1) + (W - 1) + (n - ss)) * C + c0, win[r]);
+                } else {
+#pragma unroll
+                    for (int v = 0; v < V; ++v) win[r][v] = 0.0f;
+                }
+            }
+#pragma unroll
+            for (int tt = 0; tt < kConvTokensPerThread; ++tt) {
+                if (t0 + tt < t1) {
+                    float cur[V], out[V];
+                    Vec16<T>::unpack(raw[tt], cur);
+                    taps.apply(win, cur, silu, out);
+                    Vec16<T>::store(y + (t0 + tt) * C + c0, out);
+                    shift_in<W, V>(win, cur);
+                }
+            }
+            return;
+        }
+    }
     int64_t s_end = -1;
     for (int64_t t = t0; t < t1; ++t) {
         if (t >= s_end) {
@@ -273,6 +318,7 @@ extern "C" gdn_status causal_conv1d_fwd(const void *x, int64_t x_row_stride, con
     const int elem = dtype == GDN_F32 ? 4 : 2;
     GDN_REQUIRE((x_row_stride * elem) % 16 == 0, GDN_ERR_INVALID_ARG);
     GDN_REQUIRE(aligned16(x) && aligned16(y) && aligned16(conv_state_pool), GDN_ERR_INVALID_ARG);
+    GDN_REQUIRE(aligned16(weight) && aligned16(bias), GDN_ERR_INVALID_ARG);
     cudaStream_t s = (cudaStream_t)stream;
 #define GDN_CONV_FWD(T, W)                                                                     \
     launch_fwd<T, W>(x, x_row_stride, weight, bias, cu_seqlens, n_seqs, n_tokens, channels,    \
@@ -304,6 +350,7 @@ extern "C" gdn_status causal_conv1d_update(const void *x, int32_t n_seqs, int32_
     if (n_seqs == 0) return GDN_OK;
     GDN_REQUIRE(x && y && weight && conv_state_pool && state_indices, GDN_ERR_INVALID_ARG);
     GDN_REQUIRE(aligned16(x) && aligned16(y) && aligned16(conv_state_pool), GDN_ERR_INVALID_ARG);
+    GDN_REQUIRE(aligned16(weight) && aligned16(bias), GDN_ERR_INVALID_ARG);
     cudaStream_t s = (cudaStream_t)stream;
 #define GDN_CONV_UPD(T, W)                                                                     \
     launch_update<T, W>(x, n_seqs, tokens_per_seq, channels, weight, bias, conv_state_pool,    \

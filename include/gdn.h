@@ -98,7 +98,8 @@ gdn_status gdn_gating(const void *a, const void *b, const float *A_log,
  * where e is the sequence's inputs preceded by its width-1 history rows.
  *   x: [n_tokens] rows, row r at x + r*x_row_stride, `channels` elements
  *      each (x_row_stride >= channels).
- *   weight: [channels][width], bias: [channels] or NULL (both in `dtype`).
+ *   weight: [channels][width], bias: [channels] or NULL (both in `dtype`,
+ *      16-byte aligned).
  *   cu_seqlens: [n_seqs+1] int32, cu_seqlens[0] = 0, non-decreasing,
  *      cu_seqlens[n_seqs] = n_tokens.  Zero-length sequences are allowed.
  *   conv_state_pool: [n_slots][width-1][channels] in `dtype`; slot s holds the
@@ -131,6 +132,7 @@ gdn_status causal_conv1d_fwd(const void *x, int64_t x_row_stride,
  *   snap_indices: NULL -> the slot is updated in place.  Otherwise
  *      [n_seqs][tokens_per_seq] int32: the slot is only read and the state
  *      after token t is written to slot snap_indices[i][t] (< 0: skipped).
+ * weight / bias as for causal_conv1d_fwd (16-byte aligned).
  * width in [2, 4]; channels a multiple of 8; tokens_per_seq in [1, 16].
  */
 gdn_status causal_conv1d_update(const void *x, int32_t n_seqs,
