@@ -50,6 +50,8 @@ def parse_args(argv=None):
     p.add_argument("--warmup", type=int, default=20)
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--no-extras", action="store_true", help="skip the prefill / MTP extras")
+    p.add_argument("--only", choices=["mtp", "prefill"], default=None,
+                   help="profiling aid: run just this extra (its own JSON line, no decode step)")
     p.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle work")
     return p.parse_args(argv)
 
@@ -172,10 +174,27 @@ def decode_kernel_bytes(n, hqk, hv, dk, dv, io_bytes):
     return state + qk + vo + gb + n * 4
 
 
+def run_only(args):
+    """One extra workload alone (for profiler captures of its kernels)."""
+    import gated_deltanet_linear_10_gb300 as gdn
+    import workloads
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
+    if args.only == "mtp":
+        res = bench_mtp(gdn, workloads, dev, flush, steps=max(1, args.steps))
+    else:
+        res = bench_prefill(gdn, workloads, dev, flush, load_peaks(), steps=max(1, args.steps))
+    assert gdn.gdn_get_device_status(clear=True) == 0
+    print(json.dumps({"only": args.only, **res}), flush=True)
+
+
 def run_ours(args):
     import gated_deltanet_linear_10_gb300 as gdn
     import workloads
 
+    if args.only:
+        return run_only(args)
     rank, world, local = dist_env()
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
