@@ -90,6 +90,12 @@ conv_fwd_kernel(const T *__restrict__ x, int64_t x_stride, const T *__restrict__
     if (t0 >= n_tokens) return;
     const int64_t t1 = min(t0 + (int64_t)kConvTokensPerThread, n_tokens);
 
+    // The token rows and taps do not depend on the sequence lookup: issue
+    // their loads first, so the binary search below overlaps them.
+    uint4 raw[kConvTokensPerThread];
+#pragma unroll
+    for (int tt = 0; tt < kConvTokensPerThread; ++tt)
+        if (t0 + tt < t1) raw[tt] = *reinterpret_cast<const uint4 *>(x + (t0 + tt) * x_stride + c0);
     ConvTaps<T, W> taps;
     taps.load(weight, bias, c0);
 
@@ -106,10 +112,6 @@ conv_fwd_kernel(const T *__restrict__ x, int64_t x_stride, const T *__restrict__
     if (i < n_seqs) {
         const int64_t ss = cu[i], se = cu[i + 1];
         if (ss >= 0 && ss <= t0 && t1 <= se && se <= n_tokens) {
-            uint4 raw[kConvTokensPerThread];
-#pragma unroll
-            for (int tt = 0; tt < kConvTokensPerThread; ++tt)
-                if (t0 + tt < t1) raw[tt] = *reinterpret_cast<const uint4 *>(x + (t0 + tt) * x_stride + c0);
             const int64_t hs = (t0 - ss < W - 1) ? history_slot(idx, has_init, i, n_slots) : -1;
 #pragma unroll
             for (int r = 0; r < W - 1; ++r) {
