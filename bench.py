@@ -417,8 +417,10 @@ def bench_prefill(gdn, workloads, dev, flush, peaks, steps=5):
     o = torch.empty((T, d.hv, d.dv), dtype=x.dtype, device=dev)
     stream = torch.cuda.current_stream(dev)
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(steps)]
+    need = gdn.gdn_prefill_workspace_size(cu.numel() - 1, T, d.hv, d.dk, d.dv, w.chunk)
+    ws = torch.empty(need, dtype=torch.uint8, device=dev) if need else False
 
-    def step(e=None):
+    def step(e=None, workspace=ws):
         if e is not None:
             e[0].record(stream)
         gdn.causal_conv1d_fwd(x, conv_w, cu, cpool, slots, has, y=y)
@@ -428,9 +430,20 @@ def bench_prefill(gdn, workloads, dev, flush, peaks, steps=5):
         if e is not None:
             e[2].record(stream)
         gdn.gdn_prefill_chunked(qv, kv, vv, g, beta, cu, spool, none, slots, w.scale,
-                                chunk=w.chunk, o=o)
+                                chunk=w.chunk, o=o, workspace=workspace)
         if e is not None:
             e[3].record(stream)
+
+    # the single fused kernel (no workspace), for comparison
+    for _ in range(2):
+        step(workspace=False)
+        flush.zero_()
+    torch.cuda.synchronize(dev)
+    for i in range(steps):
+        step(ev[i], workspace=False)
+        flush.zero_()
+    torch.cuda.synchronize(dev)
+    pre_fused = sum(e[2].elapsed_time(e[3]) for e in ev) / steps
 
     for _ in range(2):
         step()
@@ -450,6 +463,8 @@ def bench_prefill(gdn, workloads, dev, flush, peaks, steps=5):
                         "gating + chunked prefill (chunk 64)",
             "tokens_per_s": round(T / (total / 1e3), 1),
             "layer_ms": round(total, 4), "prefill_kernel_ms": round(pre, 4),
+            "prefill_path": "prep kernel + chain kernel (workspace %.1f MiB)" % (need / 2**20),
+            "prefill_fused_kernel_ms": round(pre_fused, 4),
             "conv_kernel_ms": round(conv, 4),
             "conv_gbs": round(conv_bytes / (conv / 1e3) / 1e9, 1),
             "prefill_tflops": round(tf, 2),

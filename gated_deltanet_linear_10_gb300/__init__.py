@@ -196,7 +196,12 @@ def gdn_prefill_chunked(q, k, v, g, beta, cu_seqlens, state_pool, initial_state_
                         workspace=None):
     """Chunked varlen prefill.  q, k [T, hqk, dk]; v [T, hv, dv] (views with a
     free row stride); g, beta [T, hv] fp32; state_pool [slots, hv, dv, dk]
-    fp32.  Returns o [T, hv, dv]."""
+    fp32.  Returns o [T, hv, dv].
+
+    workspace: None allocates the scratch gdn_prefill_workspace_size asks for
+    (the bf16 dk = dv = 128 path then runs as a chunk-parallel prep kernel and
+    a chain kernel); a uint8 CUDA tensor is used as given; False passes none,
+    which selects the single fused kernel."""
     _cuda(q, k, v, g, beta, cu_seqlens, state_pool, initial_state_indices, final_state_indices)
     T, hqk, dk = q.shape
     hv, dv = v.shape[1], v.shape[2]
@@ -218,9 +223,14 @@ def gdn_prefill_chunked(q, k, v, g, beta, cu_seqlens, state_pool, initial_state_
     o = torch.empty((T, hv, dv), dtype=q.dtype, device=q.device) if o is None else o
     _need(o.is_contiguous() and o.shape == (T, hv, dv), "o: [T, hv, dv] contiguous")
     dt = _dtype_code(q)
-    need = gdn_prefill_workspace_size(n, T, hv, dk, dv, chunk, dt)
-    if need and workspace is None:
-        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    if workspace is False:
+        workspace = None
+    elif workspace is None:
+        need = gdn_prefill_workspace_size(n, T, hv, dk, dv, chunk, dt)
+        if need:
+            workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    else:
+        _cuda(workspace)
     wbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     _check(_lib.gdn_prefill_chunked(_ptr(q), qs, _ptr(k), ks, _ptr(v), vs, _ptr(g), _ptr(beta),
                                     _ptr(cu_seqlens), n, T, hqk, hv, dk, dv, float(scale),

@@ -14,15 +14,24 @@ gdn_status prefill_tc(const void *q, int64_t qs, const void *k, int64_t ks, cons
                       int n_seqs, int64_t n_tokens, int hqk, int hv, float scale, int l2norm,
                       float *pool, int64_t n_slots, const int32_t *ii, const int32_t *fi,
                       void *o, cudaStream_t s);
+size_t prefill_split_workspace(int n_seqs, int64_t n_tokens, int hv);
+gdn_status prefill_split(const void *q, int64_t qs, const void *k, int64_t ks, const void *v,
+                         int64_t vs, const float *g, const float *beta, const int32_t *cu,
+                         int n_seqs, int64_t n_tokens, int hqk, int hv, float scale, int l2norm,
+                         float *pool, int64_t n_slots, const int32_t *ii, const int32_t *fi,
+                         void *o, void *ws, cudaStream_t s);
 }  // namespace gdn
 
 using namespace gdn;
 
+// Only the tensor-core path (bf16, dk = dv = 128, chunk 64) uses scratch: the
+// chunk-parallel prep kernel writes each (chunk, head) item's operands there.
 extern "C" size_t gdn_prefill_workspace_size(int32_t n_seqs, int64_t n_tokens, int32_t hv,
                                              int32_t dk, int32_t dv, int32_t chunk,
                                              int32_t dtype) {
-    (void)n_seqs; (void)n_tokens; (void)hv; (void)dk; (void)dv; (void)chunk; (void)dtype;
-    return 0;
+    if (n_seqs <= 0 || n_tokens <= 0 || hv <= 0) return 0;
+    if (dtype != GDN_BF16 || dk != 128 || dv != 128 || chunk != 64) return 0;
+    return prefill_split_workspace(n_seqs, n_tokens, hv);
 }
 
 extern "C" gdn_status gdn_prefill_chunked(const void *q, int64_t q_row_stride, const void *k,
@@ -36,7 +45,6 @@ extern "C" gdn_status gdn_prefill_chunked(const void *q, int64_t q_row_stride, c
                                           const int32_t *final_state_indices, void *o,
                                           int32_t dtype, void *workspace, size_t workspace_bytes,
                                           void *stream) {
-    (void)workspace; (void)workspace_bytes;
     GDN_REQUIRE(dtype == GDN_F32 || dtype == GDN_BF16, GDN_ERR_INVALID_ARG);
     GDN_REQUIRE(n_seqs >= 0 && n_tokens >= 0 && hqk > 0 && hv > 0 && n_slots >= 0,
                 GDN_ERR_INVALID_ARG);
@@ -55,10 +63,17 @@ extern "C" gdn_status gdn_prefill_chunked(const void *q, int64_t q_row_stride, c
                 GDN_ERR_INVALID_ARG);
     cudaStream_t s = (cudaStream_t)stream;
     if (n_tokens > 0 && prefill_tc_supported(dtype, dk, dv, chunk, q, q_row_stride, k,
-                                             k_row_stride, v, v_row_stride))
+                                             k_row_stride, v, v_row_stride)) {
+        if (workspace && ((uintptr_t)workspace & 15u) == 0 &&
+            workspace_bytes >= prefill_split_workspace(n_seqs, n_tokens, hv))
+            return prefill_split(q, q_row_stride, k, k_row_stride, v, v_row_stride, g, beta,
+                                 cu_seqlens, n_seqs, n_tokens, hqk, hv, scale, l2norm_qk,
+                                 state_pool, n_slots, initial_state_indices,
+                                 final_state_indices, o, workspace, s);
         return prefill_tc(q, q_row_stride, k, k_row_stride, v, v_row_stride, g, beta, cu_seqlens,
                           n_seqs, n_tokens, hqk, hv, scale, l2norm_qk, state_pool, n_slots,
                           initial_state_indices, final_state_indices, o, s);
+    }
     return prefill_simt(dtype, dk, chunk, q, q_row_stride, k, k_row_stride, v, v_row_stride, g,
                         beta, cu_seqlens, n_seqs, n_tokens, hqk, hv, scale, l2norm_qk,
                         state_pool, n_slots, initial_state_indices, final_state_indices, o, s);

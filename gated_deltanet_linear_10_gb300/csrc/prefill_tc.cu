@@ -29,8 +29,7 @@
 //   E3  S -> bf16 copy (and pre-scaled for the next chunk) and O -> registers,
 //       hand-off to the next chunk, then the o stores
 // Padded rows of a partial last chunk get beta = g = 0 and explicit zero masks.
-#include "common.cuh"
-#include "tc.cuh"
+#include "prefill_common.cuh"
 
 namespace gdn {
 
@@ -40,23 +39,13 @@ GDN_STATUS_READER(read_status_prefill_tc, g_status_prefill_tc)
 namespace ptc {
 using namespace tc;
 
-constexpr int C = 64;                  // chunk
-constexpr int DH = 128;                // dk = dv
 constexpr int kWarps = 14;
 constexpr int kThreads = kWarps * 32;
 constexpr int kPrepThreads = 256;
 constexpr int kChainThreads = 128;
 constexpr int kKQStages = 3;
 constexpr int kVStages = 2;
-constexpr uint32_t kKQBytes = 2 * 128 * 128;     // 2 k-blocks x (64 K rows + 64 Q rows) x 128 B
-constexpr uint32_t kKBlk = 128 * 128;            // k-block stride inside a K|Q stage
-constexpr uint32_t kVBytes = 2 * 64 * 128;       // 2 k-blocks x 64 rows x 128 B
-constexpr uint32_t kVBlk = 64 * 128;
-constexpr uint32_t kMatBytes = 64 * 128;         // one 64 x 64 bf16 operand, one k-block
 constexpr uint32_t kDBytes = 3 * kMatBytes;      // derived stage: T1, T2, P
-constexpr int kLd = 68;                          // fp32 row stride of the solve scratch
-constexpr int kWbLd = 12;                        // row stride of a warp's 16 x 8 scratch
-constexpr float kEps = 1e-6f;
 
 // TMEM columns
 constexpr uint32_t kColS32 = 0, kColS16 = 128, kColG = 192, kColU = 256, kColX = 320,
@@ -92,92 +81,6 @@ constexpr uint32_t SMEM_USED = OFF_BARS + (sizeof(Bars) + 127) / 128 * 128;
 constexpr uint32_t SMEM_BYTES = SMEM_USED + 1024;    // slack to align the base to 1024
 static_assert(SMEM_BYTES <= 232448, "shared memory budget");
 
-__device__ __forceinline__ void named_sync(int id, int n) {
-    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
-}
-
-// Rank -> sequence in decreasing-length order (ties by index), so that the
-// longest chains start first.  Every thread tests a share of the candidates.
-__device__ int seq_for_rank(const int32_t *cu, int n_seqs, int rank, int *slot) {
-    if (n_seqs > 1024) return rank;
-    if (threadIdx.x == 0) *slot = -1;
-    __syncthreads();
-    for (int i = threadIdx.x; i < n_seqs; i += blockDim.x) {
-        const int li = cu[i + 1] - cu[i];
-        int r = 0;
-        for (int j = 0; j < n_seqs; ++j) {
-            const int lj = cu[j + 1] - cu[j];
-            r += (lj > li) || (lj == li && j < i);
-        }
-        if (r == rank) *slot = i;
-    }
-    __syncthreads();
-    return *slot < 0 ? rank : *slot;
-}
-
-// Blocked UT solve helpers.  The 64 x 64 matrices are 4 x 4 blocks of 16.
-// A warp computes half a block (16 rows x 8 columns): lane (r = lane/2,
-// cg = lane%2) owns row r, columns col + 4cg .. col + 4cg + 3.
-//   acc += X[xr.., xc..] (16 x 16) * Y[yr.., col..]
-__device__ __forceinline__ void half_mac(float (&acc)[4], const float *X, int xr, int xc,
-                                         const float *Y, int yr, int col, int r, int cg) {
-    float e0 = 0.f, e1 = 0.f, e2 = 0.f, e3 = 0.f;   // second accumulator set: shorter chains
-#pragma unroll
-    for (int kk = 0; kk < 16; kk += 2) {
-        const float x0 = X[(xr + r) * kLd + xc + kk];
-        const float x1 = X[(xr + r) * kLd + xc + kk + 1];
-        const float4 y0 = *reinterpret_cast<const float4 *>(Y + (yr + kk) * kLd + col + 4 * cg);
-        const float4 y1 = *reinterpret_cast<const float4 *>(Y + (yr + kk + 1) * kLd + col + 4 * cg);
-        acc[0] = fmaf(x0, y0.x, acc[0]);
-        acc[1] = fmaf(x0, y0.y, acc[1]);
-        acc[2] = fmaf(x0, y0.z, acc[2]);
-        acc[3] = fmaf(x0, y0.w, acc[3]);
-        e0 = fmaf(x1, y1.x, e0);
-        e1 = fmaf(x1, y1.y, e1);
-        e2 = fmaf(x1, y1.z, e2);
-        e3 = fmaf(x1, y1.w, e3);
-    }
-    acc[0] += e0;
-    acc[1] += e1;
-    acc[2] += e2;
-    acc[3] += e3;
-}
-// Tf[bi block rows][col..] = -Tf[bi][bi] * W, with W = acc (16 x 8) staged in wb.
-__device__ __forceinline__ void half_finish(const float (&acc)[4], float *Tf, float *wb, int bi,
-                                            int col, int r, int cg) {
-    *reinterpret_cast<float4 *>(wb + r * kWbLd + 4 * cg) = make_float4(acc[0], acc[1], acc[2], acc[3]);
-    __syncwarp();
-    float o0 = 0.f, o1 = 0.f, o2 = 0.f, o3 = 0.f, p0 = 0.f, p1 = 0.f, p2 = 0.f, p3 = 0.f;
-#pragma unroll
-    for (int kk = 0; kk < 16; kk += 2) {
-        const float d0 = Tf[(16 * bi + r) * kLd + 16 * bi + kk];
-        const float d1 = Tf[(16 * bi + r) * kLd + 16 * bi + kk + 1];
-        const float4 w0 = *reinterpret_cast<const float4 *>(wb + kk * kWbLd + 4 * cg);
-        const float4 w1 = *reinterpret_cast<const float4 *>(wb + (kk + 1) * kWbLd + 4 * cg);
-        o0 = fmaf(d0, w0.x, o0);
-        o1 = fmaf(d0, w0.y, o1);
-        o2 = fmaf(d0, w0.z, o2);
-        o3 = fmaf(d0, w0.w, o3);
-        p0 = fmaf(d1, w1.x, p0);
-        p1 = fmaf(d1, w1.y, p1);
-        p2 = fmaf(d1, w1.z, p2);
-        p3 = fmaf(d1, w1.w, p3);
-    }
-    *reinterpret_cast<float4 *>(Tf + (16 * bi + r) * kLd + col + 4 * cg) =
-        make_float4(-(o0 + p0), -(o1 + p1), -(o2 + p2), -(o3 + p3));
-    __syncwarp();
-}
-
-__device__ __forceinline__ uint4 scale_chunk(uint4 w, float f) {
-    uint32_t ws[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-        const float2 v = unpack_bf16(ws[e]);
-        ws[e] = pack_bf16(v.x * f, v.y * f);
-    }
-    return make_uint4(ws[0], ws[1], ws[2], ws[3]);
-}
-
 __global__ void __launch_bounds__(kThreads, 1)
 prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, const float *__restrict__ g,
@@ -192,7 +95,6 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     float *Af = reinterpret_cast<float *>(sm + OFF_AF);
     float *Tf = reinterpret_cast<float *>(sm + OFF_TF);
     float *Wb = reinterpret_cast<float *>(sm + OFF_WB);
-    float *Zs = Wb + 8 * 16 * kWbLd;          // 16 x 16 partial sum of the last block
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
     const int rank = blockIdx.x / hv;
@@ -383,21 +285,9 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
             mbar_wait(&B.kq_full[sk], (c / kKQStages) & 1, abort);
             // ---- inverse norms of the K rows (0..63) and Q rows (64..127)
             {
-                const uint32_t row = (uint32_t)(t >> 1), kb = (uint32_t)(t & 1);
-                float ss = 0.f;
-#pragma unroll
-                for (int ch = 0; ch < 8; ++ch) {
-                    const uint4 w = *reinterpret_cast<const uint4 *>(kq + kb * kKBlk + sw128_chunk(row, ch));
-                    const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const float2 f = unpack_bf16(ws[e]);
-                        ss = fmaf(f.x, f.x, fmaf(f.y, f.y, ss));
-                    }
-                }
-                ss += __shfl_xor_sync(0xffffffffu, ss, 1);
-                const float r = l2norm ? rsqrtf(ss + kEps) : 1.f;
-                if (kb == 0) {
+                const float r = kq_row_inv_norm(kq, t, l2norm);
+                const int row = t >> 1;
+                if ((t & 1) == 0) {
                     if (row < C) S.rk[row] = r; else S.rq[row - C] = r;
                 }
             }
@@ -436,130 +326,10 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
             tmem_ld32(tmem_addr(tbase, q4 * 32, kColG + 32 * chalf), gr);
             tc_fence_before();
             mbar_arrive(&B.g_free);
-            {
-                // decay factors E_ij = exp(gc_i - gc_j) for this thread's 32 columns,
-                // walked downwards as a running product of alpha (one exp per row):
-                // E_ii = 1, E_{i,j-1} = E_ij alpha_j.
-                const bool krow = p < C;
-                const int i = krow ? p : p - C;
-                const bool ok = i < n;
-                const int cb = 32 * chalf;
-                const float coef = krow ? S.beta[i] * S.rk[i] : scale * S.rq[i];
-                float e = (i > cb + 31) ? __expf(S.gam[i] - S.gam[cb + 31]) : 1.f;
-                float v[32];
-#pragma unroll
-                for (int jj = 31; jj >= 0; --jj) {
-                    const int j = cb + jj;
-                    const bool on = j <= i;
-                    const bool keep = ok && (krow ? j < i : on);
-                    v[jj] = keep ? coef * e * S.rk[j] * __uint_as_float(gr[jj]) : 0.f;
-                    if (on) e *= S.alpha[j];
-                }
-                if (krow) {      // A row (fp32, for the solve)
-                    float *arow = Af + i * kLd + cb;
-#pragma unroll
-                    for (int jj = 0; jj < 32; jj += 4)
-                        *reinterpret_cast<float4 *>(arow + jj) = make_float4(v[jj], v[jj + 1], v[jj + 2], v[jj + 3]);
-                } else {         // P row (bf16 operand)
-#pragma unroll
-                    for (int cc = 0; cc < 4; ++cc) {
-                        uint32_t w[4];
-#pragma unroll
-                        for (int e2 = 0; e2 < 4; ++e2) w[e2] = pack_bf16(v[cc * 8 + 2 * e2], v[cc * 8 + 2 * e2 + 1]);
-                        *reinterpret_cast<uint4 *>(dst + 2 * kMatBytes + sw128_chunk(i, 4 * chalf + cc)) =
-                            make_uint4(w[0], w[1], w[2], w[3]);
-                    }
-                }
-            }
+            g_to_a_p(gr, p, chalf, n, S.beta, S.gam, S.alpha, S.rk, S.rq, scale, Af, dst + 2 * kMatBytes);
             named_sync(1, kPrepThreads);
-            // ---- T = (I + A)^-1: diagonal 16 x 16 blocks by forward substitution
-            //      (warps 0..3 of the group)
-            if (pw < 4) {
-                const int r = lane >> 1, hh = lane & 1;
-                const int bb = pw;
-                const int R = 16 * bb + r;
-                float tv[8];
-#pragma unroll
-                for (int k = 0; k < 8; ++k) tv[k] = (8 * hh + k == r) ? 1.f : 0.f;
-#pragma unroll
-                for (int m = 0; m < 15; ++m) {
-                    const float a = Af[R * kLd + 16 * bb + m];
-#pragma unroll
-                    for (int k = 0; k < 8; ++k) {
-                        const float vm = __shfl_sync(0xffffffffu, tv[k], 2 * m + hh);
-                        if (r > m) tv[k] = fmaf(-a, vm, tv[k]);
-                    }
-                }
-                *reinterpret_cast<float4 *>(Tf + R * kLd + 16 * bb + 8 * hh) = make_float4(tv[0], tv[1], tv[2], tv[3]);
-                *reinterpret_cast<float4 *>(Tf + R * kLd + 16 * bb + 8 * hh + 4) = make_float4(tv[4], tv[5], tv[6], tv[7]);
-            }
-            named_sync(1, kPrepThreads);
-            // ---- the blocks below the diagonal, level by level; each warp owns
-            //      one 16 x 8 half of a block (T_ij = -T_ii sum_k A_ik T_kj)
-            {
-                const int r = lane >> 1, cg = lane & 1;
-                float *wb = Wb + pw * 16 * kWbLd;
-                float acc[4];
-                if (pw < 6) {              // level 1: T10, T21, T32
-                    const int b0 = pw >> 1, half = pw & 1;
-                    const int col = 16 * b0 + 8 * half;
-                    acc[0] = acc[1] = acc[2] = acc[3] = 0.f;
-                    half_mac(acc, Af, 16 * (b0 + 1), 16 * b0, Tf, 16 * b0, col, r, cg);
-                    half_finish(acc, Tf, wb, b0 + 1, col, r, cg);
-                }
-                named_sync(1, kPrepThreads);
-                if (pw < 6) {              // level 2: T20, T31 and Z30 = A30 T00 + A31 T10
-                    const int item = pw >> 1, half = pw & 1;
-                    acc[0] = acc[1] = acc[2] = acc[3] = 0.f;
-                    if (item == 0) {
-                        const int col = 8 * half;
-                        half_mac(acc, Af, 32, 0, Tf, 0, col, r, cg);
-                        half_mac(acc, Af, 32, 16, Tf, 16, col, r, cg);
-                        half_finish(acc, Tf, wb, 2, col, r, cg);
-                    } else if (item == 1) {
-                        const int col = 16 + 8 * half;
-                        half_mac(acc, Af, 48, 16, Tf, 16, col, r, cg);
-                        half_mac(acc, Af, 48, 32, Tf, 32, col, r, cg);
-                        half_finish(acc, Tf, wb, 3, col, r, cg);
-                    } else {
-                        const int col = 8 * half;
-                        half_mac(acc, Af, 48, 0, Tf, 0, col, r, cg);
-                        half_mac(acc, Af, 48, 16, Tf, 16, col, r, cg);
-                        *reinterpret_cast<float4 *>(Zs + r * 16 + col + 4 * cg) =
-                            make_float4(acc[0], acc[1], acc[2], acc[3]);
-                    }
-                }
-                named_sync(1, kPrepThreads);
-                // T1 = T diag(beta), T2 = -T diag(beta Gam r_k), bf16 K-major [i][j];
-                // block rows 0..2 are final now, block row 3 after level 3
-                auto write_t12 = [&](int i, int ch) {
-                    uint32_t w1[4], w2[4];
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const int j0 = ch * 8 + 2 * e, j1 = j0 + 1;
-                        const float t0 = j0 <= i ? Tf[i * kLd + j0] : 0.f;
-                        const float t1 = j1 <= i ? Tf[i * kLd + j1] : 0.f;
-                        w1[e] = pack_bf16(t0 * S.beta[j0], t1 * S.beta[j1]);
-                        w2[e] = pack_bf16(-t0 * S.beta[j0] * S.xs[j0], -t1 * S.beta[j1] * S.xs[j1]);
-                    }
-                    *reinterpret_cast<uint4 *>(dst + sw128_chunk(i, ch)) = make_uint4(w1[0], w1[1], w1[2], w1[3]);
-                    *reinterpret_cast<uint4 *>(dst + kMatBytes + sw128_chunk(i, ch)) =
-                        make_uint4(w2[0], w2[1], w2[2], w2[3]);
-                };
-                if (pw < 2) {              // level 3: T30 = -T33 (Z30 + A32 T20)
-                    const int col = 8 * pw;
-                    const float4 z = *reinterpret_cast<const float4 *>(Zs + r * 16 + col + 4 * cg);
-                    acc[0] = z.x; acc[1] = z.y; acc[2] = z.z; acc[3] = z.w;
-                    half_mac(acc, Af, 48, 32, Tf, 32, col, r, cg);
-                    half_finish(acc, Tf, wb, 3, col, r, cg);
-                } else {                   // meanwhile rows 0..47: 384 chunks over 192 threads
-                    const int u = t - 64;
-                    write_t12(u >> 2, 2 * (u & 3));
-                    write_t12(u >> 2, 2 * (u & 3) + 1);
-                }
-                named_sync(1, kPrepThreads);
-                if (t < 128) write_t12(48 + (t >> 3), t & 7);
-            }
+            // ---- T = (I + A)^-1 and the T1 / T2 operands
+            ut_solve(Af, Tf, Wb, t, pw, lane, S.beta, S.xs, dst);
             fence_async_smem();
             mbar_arrive(&B.prep_done[sd]);
             named_sync(1, kPrepThreads);   // the solve scratch is free again

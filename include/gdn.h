@@ -160,8 +160,14 @@ gdn_status causal_conv1d_update(const void *x, int32_t n_seqs,
  *      equal the initial index of the same sequence (in-place carry).
  *   o: [n_tokens][hv][dv] contiguous, `dtype`.
  *   scale: multiplies o (usually dk^-1/2).  l2norm_qk: normalise q, k.
- *   workspace / workspace_bytes: scratch of at least
- *      gdn_prefill_workspace_size(...) bytes (may be NULL when that is 0).
+ *   workspace / workspace_bytes: device scratch, 16-byte aligned, owned by
+ *      the caller and not kept after the call's work on `stream` ends.
+ *      gdn_prefill_workspace_size(...) gives the size the two-kernel
+ *      tensor-core path needs (bf16, dk = dv = 128, chunk 64): a chunk-
+ *      parallel prep kernel writes every (chunk, V head) item's operands
+ *      there and a chain kernel streams them back.  With less (or NULL) that
+ *      path runs as one fused kernel instead; other shapes need none.
+ *      Calls sharing one workspace on different streams race.
  * Built: dk = dv in {16, 32, 64, 128}, chunk in {16, 32, 64} (any dtype);
  * hv a multiple of hqk.
  */
@@ -179,7 +185,9 @@ gdn_status gdn_prefill_chunked(const void *q, int64_t q_row_stride,
                                int32_t dtype, void *workspace,
                                size_t workspace_bytes, void *stream);
 
-/* Bytes of scratch gdn_prefill_chunked needs for these sizes (may be 0). */
+/* Bytes of scratch gdn_prefill_chunked uses for these sizes (0: none):
+ * 1 KiB-rounded header of n_seqs + 1 chunk offsets, then
+ * (ceil(n_tokens / 64) + n_seqs) * hv blocks of 25 KiB. */
 size_t gdn_prefill_workspace_size(int32_t n_seqs, int64_t n_tokens,
                                   int32_t hv, int32_t dk, int32_t dv,
                                   int32_t chunk, int32_t dtype);

@@ -94,3 +94,24 @@ def test_host_argument_checks(lib):
     s.argtypes = [V, I64, I64, V, V, I32, V]
     assert s(FAKE, 8, 24, FAKE, FAKE, 2, None) == 1
     assert s(FAKE, 8, 32, FAKE, FAKE, 0, None) == 0
+
+
+def test_prefill_workspace_size(lib):
+    """Only the bf16 dk = dv = 128, chunk-64 path uses scratch: a small header
+    plus one operand block per (chunk bound, V head) item, where the chunk
+    bound is ceil(n_tokens / 64) + n_seqs."""
+    f = lib.gdn_prefill_workspace_size
+    f.argtypes = [I32, I64, I32, I32, I32, I32, I32]
+    f.restype = ctypes.c_size_t
+    F32_, BF16_ = 0, 1
+    assert f(4, 1000, 32, 64, 64, 64, BF16_) == 0
+    assert f(4, 1000, 32, 128, 128, 64, F32_) == 0
+    assert f(4, 1000, 32, 128, 128, 32, BF16_) == 0
+    assert f(4, 0, 32, 128, 128, 64, BF16_) == 0
+    a = f(4, 1000, 32, 128, 128, 64, BF16_)          # bound 16 + 4
+    b = f(4, 1024, 32, 128, 128, 64, BF16_)          # same bound
+    c = f(4, 1025, 32, 128, 128, 64, BF16_)          # bound 17 + 4
+    assert a > 0 and a == b
+    item = (c - a) // 32
+    assert c - a == 32 * item and item >= 3 * 64 * 128   # at least T1, T2, P in bf16
+    assert a - 20 * 32 * item in (1024, 2048)          # header: n_seqs + 1 offsets, 1 KiB pages

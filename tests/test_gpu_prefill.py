@@ -91,6 +91,38 @@ def test_prefill_sweep(dtype, dk, chunk, low_decay):
                 assert bits_equal(got[s, h], pool[s, h]), f"untouched {s},{h}"
 
 
+@pytest.mark.parametrize("workspace", [None, False], ids=["split", "fused"])
+@pytest.mark.parametrize("low_decay", [False, True])
+def test_prefill_tc_paths(workspace, low_decay):
+    """bf16, dk = dv = 128, chunk 64: the two-kernel path (prep kernel +
+    chain kernel, workspace given) and the single fused kernel (no
+    workspace).  Ragged lengths up to 10 chunks so that every stage ring
+    wraps, nonzero initial states, GQA 2 -> 4 heads."""
+    lens = [65, 0, 1, 63, 64, 199, 9 * 64 + 13, 2]
+    hqk, hv, dk = 2, 4, 128
+    cu, q, k, v, a, b, A_log, dt_bias, pool = _direct_batch(4242 + low_decay, lens, hqk, hv, dk,
+                                                            torch.bfloat16, low_decay, n_slots=10)
+    init = torch.tensor([0, 1, -1, 3, 4, 5, 8, 9], dtype=torch.int32)
+    final = torch.tensor([6, 7, 2, 3, -1, 5, 8, -1], dtype=torch.int32)
+    pd = cuda(pool)
+    g, beta = gdn().gdn_gating(cuda(a), cuda(b), cuda(A_log), cuda(dt_bias))
+    o = gdn().gdn_prefill_chunked(cuda(q), cuda(k), cuda(v), g, beta, cuda(cu), pd, cuda(init),
+                                  cuda(final), 0.125, chunk=64, workspace=workspace)
+    torch.cuda.synchronize()
+    status_clean()
+    g_ref, b_ref = oracle_gating(a, b, A_log, dt_bias)
+    o_ref, upd, _ = oracle.gdn_prefill(to_np(q), to_np(k), to_np(v), g_ref, b_ref, to_np(cu),
+                                       to_np(pool), to_np(init), to_np(final), 0.125)
+    assert_close(o, o_ref, TOL[torch.bfloat16], "o")
+    got = pd.cpu()
+    for s in range(pool.shape[0]):
+        for h in range(hv):
+            if (s, h) in upd:
+                assert_close(got[s, h], upd[(s, h)], TOL[torch.bfloat16], f"state {s},{h}")
+            else:
+                assert bits_equal(got[s, h], pool[s, h]), f"untouched {s},{h}"
+
+
 def test_prefill_empty_batch_and_all_empty_sequences():
     hv, dk = 4, 16
     pool = torch.randn(3, hv, dk, dk)
@@ -126,9 +158,11 @@ def _oracle_chain_from_x(w, seq, h):
                                   beta[:, 0], scale=w.scale)
 
 
-def test_prefill_full_layer_sampled_chains():
-    """8 sequences, lengths U{512..8192}: conv -> gating -> prefill on the GPU;
-    the oracle recomputes 5 (sequence, head) chains end to end from x."""
+@pytest.mark.parametrize("workspace", [None, False], ids=["split", "fused"])
+def test_prefill_full_layer_sampled_chains(workspace):
+    """8 sequences, lengths U{512..8192}: conv -> gating -> prefill on the GPU
+    (two-kernel and fused paths); the oracle recomputes 5 (sequence, head)
+    chains end to end from x."""
     w = workloads.prefill()
     d = w.dims
     cpool = cuda(w.conv_pool)
@@ -140,7 +174,7 @@ def test_prefill_full_layer_sampled_chains():
     q, k, v = qkv_views(y, d)
     g, beta = gdn().gdn_gating(cuda(w.a), cuda(w.b), cuda(w.A_log), cuda(w.dt_bias))
     o = gdn().gdn_prefill_chunked(q, k, v, g, beta, cuda(w.cu_seqlens), spool, cuda(none),
-                                  cuda(slots), w.scale, chunk=w.chunk)
+                                  cuda(slots), w.scale, chunk=w.chunk, workspace=workspace)
     torch.cuda.synchronize()
     status_clean()
     lens = w.extra["lengths"]
@@ -188,3 +222,28 @@ def test_long_context_sampled_heads_and_split():
     for h in picks:
         assert_close(o[:, h], o_ref[:, h], TOL[torch.bfloat16], f"long o head {h}")
         assert_close(pool[1, h], finals[(0, h)], TOL[torch.bfloat16], f"long S head {h}")
+
+
+def test_prefill_split_matches_fused_every_head():
+    """The two tensor-core paths run the same arithmetic: on the full
+    8-sequence batch every output row and final state agrees within the bf16
+    tolerance (they are expected to agree far more closely)."""
+    w = workloads.prefill()
+    d = w.dims
+    gen = torch.Generator().manual_seed(77)
+    T = int(w.cu_seqlens[-1])
+    q = cuda(torch.randn(T, d.hqk, d.dk, generator=gen).bfloat16())
+    k = cuda(torch.randn(T, d.hqk, d.dk, generator=gen).bfloat16())
+    v = cuda(torch.randn(T, d.hv, d.dv, generator=gen).bfloat16())
+    g, beta = gdn().gdn_gating(cuda(w.a), cuda(w.b), cuda(w.A_log), cuda(w.dt_bias))
+    n = w.cu_seqlens.numel() - 1
+    slots = cuda(torch.arange(n, dtype=torch.int32))
+    p1 = torch.zeros((n, d.hv, d.dv, d.dk), device=DEV)
+    p2 = torch.zeros_like(p1)
+    o1 = gdn().gdn_prefill_chunked(q, k, v, g, beta, cuda(w.cu_seqlens), p1, None, slots, w.scale)
+    o2 = gdn().gdn_prefill_chunked(q, k, v, g, beta, cuda(w.cu_seqlens), p2, None, slots, w.scale,
+                                   workspace=False)
+    torch.cuda.synchronize()
+    status_clean()
+    assert_close(o1, o2, 1e-3, "o split vs fused")
+    assert_close(p1, p2, 1e-3, "S split vs fused")
