@@ -17,7 +17,9 @@ import torch
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libgdn.so")
 
-GDN_OK, GDN_ERR_INVALID_ARG, GDN_ERR_UNSUPPORTED, GDN_ERR_LAUNCH, GDN_ERR_CUDA = range(5)
+(GDN_OK, GDN_ERR_INVALID_ARG, GDN_ERR_UNSUPPORTED, GDN_ERR_LAUNCH, GDN_ERR_CUDA,
+ GDN_ERR_TOO_LARGE) = range(6)
+PREFILL_STATIC_SCRATCH_BYTES = 16 << 20
 GDN_F32, GDN_BF16 = 0, 1
 DEVSTAT_BAD_INDEX, DEVSTAT_BAD_SEQLEN, DEVSTAT_TIMEOUT = 0x1, 0x2, 0x4
 
@@ -26,7 +28,7 @@ EXPORTS = (
     "gdn_status_string", "gdn_version", "gdn_last_cuda_error", "gdn_gating",
     "causal_conv1d_fwd", "causal_conv1d_update", "gdn_prefill_chunked",
     "gdn_prefill_workspace_size", "gdn_decode_recurrent", "gdn_state_snapshot",
-    "gdn_get_device_status",
+    "gdn_get_device_status", "gdn_prefill_chunked_static",
 )
 
 if not os.path.exists(LIB_PATH):
@@ -55,6 +57,8 @@ _SIGS = {
                              _i32, _i32, _f32, _i32, _vp, _i64, _vp, _vp, _vp, _i32, _vp],
     "gdn_state_snapshot": [_vp, _i64, _i64, _vp, _vp, _i32, _vp],
     "gdn_get_device_status": [ctypes.POINTER(ctypes.c_uint32), _i32, _vp],
+    "gdn_prefill_chunked_static": [_vp, _i64, _vp, _i64, _vp, _i64, _vp, _vp, _vp, _i32, _i64,
+                                   _i32, _i32, _f32, _i32, _vp, _i64, _vp, _vp, _vp, _vp],
 }
 for _name, _args in _SIGS.items():
     _fn = getattr(_lib, _name)
@@ -238,6 +242,43 @@ def gdn_prefill_chunked(q, k, v, g, beta, cu_seqlens, state_pool, initial_state_
                                     _ptr(initial_state_indices), _ptr(final_state_indices),
                                     _ptr(o), dt, _ptr(workspace), wbytes, _stream(q.device)),
            "gdn_prefill_chunked")
+    return o
+
+
+def gdn_prefill_chunked_static(q, k, v, g, beta, cu_seqlens, state_pool, initial_state_indices,
+                               final_state_indices, scale, l2norm_qk=True, o=None):
+    """gdn_prefill_chunked for bf16, dk = dv = 128, chunk 64, with the
+    library's fixed device scratch instead of a workspace: no allocation in
+    the library (o is allocated here unless given).  Raises GdnError
+    (GDN_ERR_TOO_LARGE) past PREFILL_STATIC_SCRATCH_BYTES of scratch."""
+    _cuda(q, k, v, g, beta, cu_seqlens, state_pool, initial_state_indices, final_state_indices)
+    T, hqk, dk = q.shape
+    hv, dv = v.shape[1], v.shape[2]
+    _need(q.dtype == k.dtype == v.dtype == torch.bfloat16 and dk == dv == 128,
+          "q, k, v: bf16, head dim 128")
+    qs = _heads_view(q, hqk, dk, "q")
+    ks = _heads_view(k, hqk, dk, "k")
+    vs = _heads_view(v, hv, dv, "v")
+    _need(g.dtype == torch.float32 and beta.dtype == torch.float32 and g.is_contiguous()
+          and beta.is_contiguous() and g.shape == (T, hv) and beta.shape == (T, hv), "g, beta")
+    _need(state_pool.dtype == torch.float32 and state_pool.is_contiguous()
+          and state_pool.shape[1:] == (hv, dv, dk), "state_pool: [slots, hv, dv, dk] fp32")
+    _i32_vec(cu_seqlens, "cu_seqlens")
+    n = cu_seqlens.numel() - 1
+    for name, t in (("initial_state_indices", initial_state_indices),
+                    ("final_state_indices", final_state_indices)):
+        if t is not None:
+            _i32_vec(t, name)
+            _need(t.numel() == n, f"{name}: [n_seqs]")
+    o = torch.empty((T, hv, dv), dtype=q.dtype, device=q.device) if o is None else o
+    _need(o.is_contiguous() and o.shape == (T, hv, dv), "o: [T, hv, dv] contiguous")
+    _check(_lib.gdn_prefill_chunked_static(_ptr(q), qs, _ptr(k), ks, _ptr(v), vs, _ptr(g),
+                                           _ptr(beta), _ptr(cu_seqlens), n, T, hqk, hv,
+                                           float(scale), int(l2norm_qk), _ptr(state_pool),
+                                           state_pool.shape[0], _ptr(initial_state_indices),
+                                           _ptr(final_state_indices), _ptr(o),
+                                           _stream(q.device)),
+           "gdn_prefill_chunked_static")
     return o
 
 

@@ -67,6 +67,7 @@ const char *gdn_status_string(gdn_status s) {
         case GDN_ERR_UNSUPPORTED: return "GDN_ERR_UNSUPPORTED";
         case GDN_ERR_LAUNCH: return "GDN_ERR_LAUNCH";
         case GDN_ERR_CUDA: return "GDN_ERR_CUDA";
+        case GDN_ERR_TOO_LARGE: return "GDN_ERR_TOO_LARGE";
     }
     return "GDN_STATUS_UNKNOWN";
 }

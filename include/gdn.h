@@ -56,7 +56,8 @@ typedef enum gdn_status {
     GDN_ERR_INVALID_ARG = 1,  /* a host-side argument check failed; nothing ran */
     GDN_ERR_UNSUPPORTED = 2,  /* shape/dtype combination not built; nothing ran */
     GDN_ERR_LAUNCH = 3,       /* a kernel launch failed (CUDA error recorded)   */
-    GDN_ERR_CUDA = 4          /* another CUDA runtime call failed               */
+    GDN_ERR_CUDA = 4,         /* another CUDA runtime call failed               */
+    GDN_ERR_TOO_LARGE = 5     /* beyond a fixed built-in capacity; nothing ran  */
 } gdn_status;
 
 typedef enum gdn_dtype {
@@ -191,6 +192,43 @@ gdn_status gdn_prefill_chunked(const void *q, int64_t q_row_stride,
 size_t gdn_prefill_workspace_size(int32_t n_seqs, int64_t n_tokens,
                                   int32_t hv, int32_t dk, int32_t dv,
                                   int32_t chunk, int32_t dtype);
+
+/*
+ * The prefill above on its bf16, dk = dv = 128, chunk-64 two-kernel path,
+ * with the scratch in a fixed device array built into the library instead of
+ * a caller workspace.  The pages describe no such variant: it exists for
+ * callers that cannot allocate device memory per call -- a C or C++ runtime
+ * with no device allocator of its own in its step loop, where a cudaMalloc /
+ * cudaFree pair per call would add synchronising calls mid-step.  It
+ * allocates nothing.
+ *
+ * Arguments are those of gdn_prefill_chunked with dk = dv = 128, chunk = 64,
+ * dtype = GDN_BF16 fixed (and no workspace); q, k, v must be 16-byte aligned
+ * with row strides that are multiples of 8 elements.
+ * Capacity: gdn_prefill_workspace_size(n_seqs, n_tokens, hv, 128, 128, 64,
+ * GDN_BF16) <= GDN_PREFILL_STATIC_SCRATCH_BYTES (16 MiB: about 655
+ * (chunk, V head) items, i.e. ceil(n_tokens / 64) + n_seqs <= 20 at hv = 32),
+ * else GDN_ERR_TOO_LARGE and nothing runs.  n_tokens = 0 returns
+ * GDN_ERR_UNSUPPORTED (use gdn_prefill_chunked).
+ * The array's address is looked up once per device (cudaGetSymbolAddress
+ * with the current device, the one `stream` must belong to); make the first
+ * call on each device before any stream capture.  Nothing in the array needs
+ * clearing: each call writes every byte it reads before reading it.  There
+ * is one array per device, so calls that overlap in time on one device (on
+ * different streams or host threads) race and give wrong results.
+ */
+#define GDN_PREFILL_STATIC_SCRATCH_BYTES (16u << 20)
+gdn_status gdn_prefill_chunked_static(const void *q, int64_t q_row_stride,
+                                      const void *k, int64_t k_row_stride,
+                                      const void *v, int64_t v_row_stride,
+                                      const float *g, const float *beta,
+                                      const int32_t *cu_seqlens, int32_t n_seqs,
+                                      int64_t n_tokens, int32_t hqk, int32_t hv,
+                                      float scale, int32_t l2norm_qk,
+                                      float *state_pool, int64_t n_slots,
+                                      const int32_t *initial_state_indices,
+                                      const int32_t *final_state_indices,
+                                      void *o, void *stream);
 
 /*
  * Recurrent decode ("fused recurrent GDN", "[model] support Qwen3next",
