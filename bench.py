@@ -404,7 +404,8 @@ def bench_prefill(gdn, workloads, dev, flush, peaks, steps=5):
     cu, slots = w.cu_seqlens.to(dev), w.slots.to(dev)
     has = w.has_initial_state.to(dev)
     cpool = w.conv_pool.to(dev)
-    spool = torch.zeros((1024, d.hv, d.dv, d.dk), dtype=torch.float32, device=dev)
+    spool = torch.zeros((64, d.hv, d.dv, d.dk), dtype=torch.float32, device=dev)
+    sslots = (slots % 64).to(torch.int32)      # final-state slots in the 64-slot pool
     none = torch.full_like(slots, -1)
     T = x.shape[0]
     y = torch.empty_like(x)
@@ -429,7 +430,7 @@ def bench_prefill(gdn, workloads, dev, flush, peaks, steps=5):
         gdn.gdn_gating(a, b, A_log, dt_bias, g=g, beta=beta)
         if e is not None:
             e[2].record(stream)
-        gdn.gdn_prefill_chunked(qv, kv, vv, g, beta, cu, spool, none, slots, w.scale,
+        gdn.gdn_prefill_chunked(qv, kv, vv, g, beta, cu, spool, none, sslots, w.scale,
                                 chunk=w.chunk, o=o, workspace=workspace)
         if e is not None:
             e[3].record(stream)

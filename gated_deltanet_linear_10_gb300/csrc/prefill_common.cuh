@@ -16,7 +16,7 @@ constexpr uint32_t kVBytes = 2 * 64 * 128;       // 2 k-blocks x 64 rows x 128 B
 constexpr uint32_t kVBlk = 64 * 128;
 constexpr uint32_t kMatBytes = 64 * 128;         // one 64 x 64 bf16 operand, one k-block
 constexpr int kLd = 68;                          // fp32 row stride of the solve scratch
-constexpr int kWbLd = 12;                        // row stride of a warp's 16 x 8 scratch
+constexpr int kWbLd = 8;                         // row stride of a warp's 16 x 8 scratch
 constexpr float kEps = 1e-6f;
 
 __device__ __forceinline__ void named_sync(int id, int n) {
@@ -170,12 +170,14 @@ __device__ __forceinline__ void g_to_a_p(const uint32_t (&gr)[32], int p, int ch
 }
 
 // T = (I + A)^-1 for the strictly lower triangular A in Af (fp32, row stride
-// kLd), then T1 = T diag(beta) and T2 = -T diag(beta xs) as bf16 K-major
-// operands at dst and dst + kMatBytes (xs = Gam r_k, zero on padded rows).
+// kLd), then T1 = T diag(beta) and (kT2) T2 = -T diag(beta xs) as bf16
+// K-major operands at dst and dst + kMatBytes (xs = Gam r_k, zero on padded
+// rows).
 // The diagonal 16 x 16 blocks by forward substitution, then the blocks below
 // the diagonal level by level (T_ij = -T_ii sum_k A_ik T_kj); Wb holds each
 // warp's 16 x 8 scratch followed by a 16 x 16 partial sum.  Ends with the
 // T1 / T2 writes issued (no barrier after the last of them).
+template <bool kT2>
 __device__ __forceinline__ void ut_solve(const float *Af, float *Tf, float *Wb, int t, int pw,
                                          int lane, const float *beta, const float *xs,
                                          uint8_t *dst) {
@@ -242,11 +244,12 @@ __device__ __forceinline__ void ut_solve(const float *Af, float *Tf, float *Wb, 
             const float t0 = j0 <= i ? Tf[i * kLd + j0] : 0.f;
             const float t1 = j1 <= i ? Tf[i * kLd + j1] : 0.f;
             w1[e] = pack_bf16(t0 * beta[j0], t1 * beta[j1]);
-            w2[e] = pack_bf16(-t0 * beta[j0] * xs[j0], -t1 * beta[j1] * xs[j1]);
+            if (kT2) w2[e] = pack_bf16(-t0 * beta[j0] * xs[j0], -t1 * beta[j1] * xs[j1]);
         }
         *reinterpret_cast<uint4 *>(dst + sw128_chunk(i, ch)) = make_uint4(w1[0], w1[1], w1[2], w1[3]);
-        *reinterpret_cast<uint4 *>(dst + kMatBytes + sw128_chunk(i, ch)) =
-            make_uint4(w2[0], w2[1], w2[2], w2[3]);
+        if (kT2)
+            *reinterpret_cast<uint4 *>(dst + kMatBytes + sw128_chunk(i, ch)) =
+                make_uint4(w2[0], w2[1], w2[2], w2[3]);
     };
     if (pw < 2) {              // level 3: T30 = -T33 (Z30 + A32 T20)
         const int col = 8 * pw;

@@ -1,17 +1,25 @@
 // Chunked prefill in two kernels, for callers that pass a workspace
 // ("Flash Linear Attention operations for efficient chunked computations",
-// "[model] Support Qwen3next", Highlights).  Same arithmetic as the fused
+// "[model] Support Qwen3next", Highlights).  Same recurrence as the fused
 // tensor-core kernel (prefill_tc.cu), split where the dependency structure
 // allows it:
 //
 //   1. prep_kernel: everything that does not depend on the state, for every
 //      (chunk, V head) item at once -- chunk-parallel, several CTAs per SM:
 //      G = [K;Q] K^T on the tensor cores, gates, norms, A and P, the UT solve
-//      T = (I + A)^-1, and T1 = T diag(beta), T2 = -T diag(beta Gam r_k).
-//      Each item's T1 | T2 | P | scalars block (25 KiB) is written to the
+//      T = (I + A)^-1, T1 = T diag(beta), and on the tensor cores again
+//      W = T diag(beta Gam r_k) K (the WY form's key term, kept negated).
+//      Each item's T1 | P | W^T | row factors block is written to the
 //      workspace in exactly the shared-memory layout the MMAs read.
-//   2. chain_kernel: per (sequence, V head) only the state chain, with the
-//      item blocks streamed in by 1-D bulk copies next to the K|Q and V tiles.
+//   2. chain_kernel: per (sequence, V head) only the state chain,
+//        MU  U  = T1 V                  (issued a chunk ahead: no state needed)
+//        M2  U += S W'^T                W' = -W, so U = T1 V - W S^T
+//        O   O  = S Q'^T                Q' = scale Gam r_q Q
+//        E2  U -> bf16;  M6  S += U K'';  M5  O += U P^T
+//        E3  S -> bf16 copy for the next chunk, S pre-scaled by its decay
+//      with the item blocks streamed in by 1-D bulk copies next to the K|Q
+//      and V tiles.  Against the fused kernel this drops the X = S K^T
+//      round trip (and its epilogue) from the chain's critical path.
 //
 // Workspace: [chunk offsets, int32 x (n_seqs + 1), padded to 1 KiB]
 //            [items: (ceil(n_tokens / 64) + n_seqs) x hv blocks of kItemBytes]
@@ -25,15 +33,19 @@ GDN_STATUS_READER(read_status_prefill_split, g_status_prefill_split)
 namespace psp {
 using namespace ptc;
 
-// item block: T1 | T2 | P (bf16, 128-byte swizzle, K-major) | scalars
-constexpr uint32_t kItemScal = 3 * kMatBytes;
+// item block: T1 [i][j] | P [i][j] (64 x 64 bf16, K-major) | W'^T [a][i]
+// (128 x 64 bf16, 128 rows of 128 B) | row factors.  All 128-byte swizzled.
+constexpr uint32_t kItemT1 = 0, kItemP = kMatBytes, kItemW = 2 * kMatBytes;
+constexpr uint32_t kItemWBytes = 128 * 128;
+constexpr uint32_t kItemOps = kItemW + kItemWBytes;            // 32 KiB of operands
 struct ItemScal {
     float ks[C];      // D[last][j] r_k,j      (K'' row factors)
     float sq[C];      // scale Gam_i r_q,i     (Q' row factors)
     float gam_n;      // total decay of the chunk
     int n;            // valid rows
 };
-constexpr uint32_t kItemBytes = (kItemScal + sizeof(ItemScal) + 1023) / 1024 * 1024;
+constexpr uint32_t kItemScalCopy = (sizeof(ItemScal) + 15) / 16 * 16;
+constexpr uint32_t kItemBytes = (kItemOps + kItemScalCopy + 1023) / 1024 * 1024;
 
 __host__ __device__ inline size_t header_bytes(int n_seqs) {
     return ((size_t)4 * (n_seqs + 1) + 1023) / 1024 * 1024;
@@ -42,7 +54,6 @@ __host__ __device__ inline int64_t chunk_bound(int64_t n_tokens, int n_seqs) {
     return (n_tokens + C - 1) / C + n_seqs;
 }
 
-// chunk_base[s] = sum over sequences before s of ceil(len / 64); one CTA.
 // A sequence whose bounds are invalid gets no chunks (the chain kernel
 // reports it).
 __device__ __forceinline__ int seq_chunks(const int32_t *cu, int s, int64_t n_tokens) {
@@ -50,6 +61,7 @@ __device__ __forceinline__ int seq_chunks(const int32_t *cu, int s, int64_t n_to
     return (a < 0 || e < a || e > n_tokens) ? 0 : (e - a + C - 1) / C;
 }
 
+// chunk_base[s] = sum over sequences before s of ceil(len / 64); one CTA.
 __global__ void __launch_bounds__(1024) chunk_base_kernel(const int32_t *__restrict__ cu,
                                                           int n_seqs, int64_t n_tokens,
                                                           int32_t *__restrict__ base) {
@@ -94,29 +106,31 @@ struct PrepScal {
     float beta[C], gam[C], alpha[C], rk[C], rq[C], xs[C];
 };
 struct PrepBars {
-    uint64_t kq_full, g_full;
+    uint64_t kq_full, g_full, w_go, w_full;
     uint32_t tmem_base;
     int abort;
 };
-// The raw K|Q tile is dead once G is in TMEM and the norms are taken: its
-// first kItemCopy bytes then stage the item block, the rest the solve scratch.
-constexpr uint32_t kItemCopy = (kItemScal + sizeof(ItemScal) + 15) / 16 * 16;
+// Shared memory.  The raw K|Q tile keeps its K rows (scaled in place to
+// K~ = -xs K for the W MMA); its Q halves become the P and T1 staging once
+// G is in TMEM.  After the solve, Af stages W'^T and Wb the row factors.
 constexpr uint32_t P_OFF_KQ = 0;
-constexpr uint32_t P_OFF_WB = P_OFF_KQ + 25600;
-constexpr uint32_t kPWbFloats = 8 * 16 * kWbLd + 16 * 16;
+constexpr uint32_t P_OFF_P = P_OFF_KQ + 64 * 128;              // Q rows of k-block 0
+constexpr uint32_t P_OFF_T1 = P_OFF_KQ + kKBlk + 64 * 128;     // Q rows of k-block 1
 constexpr uint32_t P_OFF_AF = P_OFF_KQ + kKQBytes;
 constexpr uint32_t P_OFF_TF = P_OFF_AF + C * kLd * 4;
-constexpr uint32_t P_OFF_SCAL = P_OFF_TF + C * kLd * 4;
+constexpr uint32_t P_OFF_WB = P_OFF_TF + C * kLd * 4;
+constexpr uint32_t kPWbBytes = (8 * 16 * kWbLd + 16 * 16) * 4;
+constexpr uint32_t P_OFF_SCAL = P_OFF_WB + kPWbBytes;
 constexpr uint32_t P_OFF_BARS = P_OFF_SCAL + (sizeof(PrepScal) + 127) / 128 * 128;
 constexpr uint32_t P_SMEM_BYTES = P_OFF_BARS + 128 + 1024;   // + slack to align to 1024
-constexpr uint32_t kPrepTmemCols = 64;
-static_assert(kItemCopy <= P_OFF_WB && P_OFF_WB + kPWbFloats * 4 <= kKQBytes, "staging layout");
+constexpr uint32_t kPrepTmemCols = 64;                       // G, then W'^T
+static_assert(kItemWBytes <= C * kLd * 4 && sizeof(ItemScal) <= kPWbBytes, "staging");
 static_assert(sizeof(PrepBars) <= 128, "barrier block");
 static_assert(3 * (P_SMEM_BYTES + 1024) <= 233472, "three prep CTAs per SM");
 
 // One CTA per (chunk, V head) item.  Warp 0: TMEM, TMA of the raw K|Q tile,
-// M1 G = [K;Q] K^T; warps 1..8: the prep arithmetic (as in the fused kernel),
-// then one bulk store of the item block.
+// M1 G = [K;Q] K^T, then MW W'^T = K~^T T1^T; warps 1..8: the prep
+// arithmetic (as in the fused kernel), then bulk stores of the item block.
 __global__ void __launch_bounds__(kPrepKernelThreads, 3)
 prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
             const float *__restrict__ g, const float *__restrict__ beta,
@@ -147,6 +161,8 @@ prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
     if (tid == 0) {
         mbar_init(&B.kq_full, 1);
         mbar_init(&B.g_full, 1);
+        mbar_init(&B.w_go, kPrepThreads);
+        mbar_init(&B.w_full, 1);
         B.abort = 0;
         fence_mbar_init();
     }
@@ -163,6 +179,7 @@ prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
                 tma_load_2d(kq + kb * kKBlk, &tm_k, &B.kq_full, hq * DH + kb * 64, (int)c0);
                 tma_load_2d(kq + kb * kKBlk + 64 * 128, &tm_q, &B.kq_full, hq * DH + kb * 64, (int)c0);
             }
+            uint64_t *last = nullptr;   // the last commit: TMEM is freed once it completes
             if (mbar_wait(&B.kq_full, 0, abort)) {
                 tc_fence_after();
                 const uint32_t id64 = idesc_bf16(128, 64);
@@ -173,12 +190,23 @@ prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
                            id64, s > 0);
                 }
                 mma_commit(&B.g_full);
-                int z = 0;       // TMEM is freed at the end: the MMAs must be done
-                mbar_wait(&B.g_full, 0, &z);
+                last = &B.g_full;
+                if (mbar_wait(&B.w_go, 0, abort)) {
+                    // MW: W'^T[a][i] = sum_j K~[j][a] T1[i][j]  (A = K~^T, MN-major)
+                    tc_fence_after();
+                    const uint32_t id64amn = idesc_bf16(128, 64, true, false);
+                    const uint32_t t1 = smem_u32(sm + P_OFF_T1);
+                    for (int s = 0; s < 4; ++s)
+                        mma_ss(tbase, sdesc_sw128(kb0 + s * 16 * 128, kKBlk, 1024),
+                               sdesc_sw128(t1 + s * 32, 16, 1024), id64amn, s > 0);
+                    mma_commit(&B.w_full);
+                    last = &B.w_full;
+                }
             } else {
                 int z = 0;       // never leave with the copy in flight
                 mbar_wait(&B.kq_full, 0, &z);
             }
+            if (last) { int z = 0; mbar_wait(last, 0, &z); }
         }
         __syncwarp();
     } else {
@@ -186,12 +214,11 @@ prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
         const int pw = warp - 1;                // 0 .. 7
         const int q4 = warp & 3;                // TMEM lane quadrant
         const int p = q4 * 32 + lane;           // G row: 0..63 K rows, 64..127 Q rows
-        const int chalf = pw >> 2;              // which 32 G columns this warp reads
+        const int chalf = pw >> 2;              // which 32 TMEM columns this warp reads
         PrepScal &S = *reinterpret_cast<PrepScal *>(sm + P_OFF_SCAL);
         float *Af = reinterpret_cast<float *>(sm + P_OFF_AF);
         float *Tf = reinterpret_cast<float *>(sm + P_OFF_TF);
         float *Wb = reinterpret_cast<float *>(sm + P_OFF_WB);
-        ItemScal &I = *reinterpret_cast<ItemScal *>(kq + kItemScal);
         float g0 = 0.f, g1 = 0.f, b0 = 0.f, b1 = 0.f;
         if (t < 32) {
             if (2 * t < n) {
@@ -238,10 +265,28 @@ prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
         }
         mbar_wait(&B.g_full, 0, abort);
         tc_fence_after();
-        uint32_t gr[32];
-        tmem_ld32(tmem_addr(tbase, q4 * 32, 32 * chalf), gr);
-        // the raw tile is dead from here on: it becomes the item staging area
-        g_to_a_p(gr, p, chalf, n, S.beta, S.gam, S.alpha, S.rk, S.rq, scale, Af, kq + 2 * kMatBytes);
+        {
+            uint32_t gr[32];
+            tmem_ld32(tmem_addr(tbase, q4 * 32, 32 * chalf), gr);
+            // the Q rows are dead from here on: P goes to k-block 0's
+            g_to_a_p(gr, p, chalf, n, S.beta, S.gam, S.alpha, S.rk, S.rq, scale, Af, sm + P_OFF_P);
+        }
+        named_sync(1, kPrepThreads);
+        {   // K~_j = -xs_j K_j in place (4 of the 1024 16-byte chunks per thread)
+            const int j = t >> 2, kb = (t >> 1) & 1, ch0 = (t & 1) * 4;
+            const float f = -S.xs[j];
+#pragma unroll
+            for (int ch = ch0; ch < ch0 + 4; ++ch) {
+                uint4 *pk = reinterpret_cast<uint4 *>(kq + kb * kKBlk + sw128_chunk((uint32_t)j, ch));
+                *pk = scale_chunk(*pk, f);
+            }
+        }
+        ut_solve<false>(Af, Tf, Wb, t, pw, lane, S.beta, S.xs, sm + P_OFF_T1);
+        fence_async_smem();
+        tc_fence_before();
+        mbar_arrive(&B.w_go);                  // T1 and K~ are in place: MW may run
+        // the solve scratch is dead: the row factors go to Wb, W'^T to Af
+        ItemScal &I = *reinterpret_cast<ItemScal *>(Wb);
         if (t < C) {
             I.ks[t] = ksv;
             I.sq[t] = sqv;
@@ -250,12 +295,30 @@ prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
                 I.n = n;
             }
         }
-        named_sync(1, kPrepThreads);
-        ut_solve(Af, Tf, Wb, t, pw, lane, S.beta, S.xs, kq);
+        mbar_wait(&B.w_full, 0, abort);
+        tc_fence_after();
+        {
+            uint32_t wr[32];
+            tmem_ld32(tmem_addr(tbase, q4 * 32, 32 * chalf), wr);
+            uint8_t *wt = sm + P_OFF_AF;
+#pragma unroll
+            for (int cc = 0; cc < 4; ++cc) {
+                uint32_t w[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e)
+                    w[e] = pack_bf16(__uint_as_float(wr[8 * cc + 2 * e]), __uint_as_float(wr[8 * cc + 2 * e + 1]));
+                *reinterpret_cast<uint4 *>(wt + sw128_chunk((uint32_t)p, 4 * chalf + cc)) =
+                    make_uint4(w[0], w[1], w[2], w[3]);
+            }
+        }
         fence_async_smem();
         named_sync(1, kPrepThreads);
         if (t == 0 && !*abort) {
-            bulk_store(items + ((size_t)it * hv + h) * kItemBytes, kq, kItemCopy);
+            uint8_t *item = items + ((size_t)it * hv + h) * kItemBytes;
+            bulk_store(item + kItemT1, sm + P_OFF_T1, kMatBytes);
+            bulk_store(item + kItemP, sm + P_OFF_P, kMatBytes);
+            bulk_store(item + kItemW, sm + P_OFF_AF, kItemWBytes);
+            bulk_store(item + kItemOps, Wb, kItemScalCopy);
             bulk_commit();
             bulk_wait_all();
         }
@@ -270,21 +333,31 @@ prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
 }
 
 // ------------------------------------------------------------ chain kernel --
-// One CTA per (sequence, V head): only the state chain of the fused kernel
-// (MU, M23, E1, M4, E2, M5, M6, E3), its per-chunk operands read from the
-// item blocks.  Warp 0: TMA / bulk producer; warp 1: TMEM + MMA issue;
-// warps 2..5: the epilogues.
-constexpr int kChainWarps = 6;
+// One CTA per (sequence, V head).  Per chunk c (S pre-scaled by the chunk's
+// decay, S16 its bf16 copy; K, Q, V raw tiles; T1, P, W' from the item):
+//   MU  U   = T1 V                    (a chunk ahead: needs no state)
+//   M2  U  += S16 W'^T                W' = T2 K, so U = T1 V + T2 (S K^T)^T
+//   E2  U16 = bf16(U), U16k = bf16(U diag(ks))      ks = D[last][j] r_k,j
+//   M6  S  += U16k K                  (= U K'')
+//   O1  O1  = S16 Q^T    O2  O2 = U16 P^T     o = diag(sq) O1 + O2 (epilogue)
+//   E3  S16 = bf16(S) for the next chunk, S *= its decay, o stores
+// The critical path  s_next -> M2 -> E2 -> M6 -> E3a -> s_next  has its own
+// MMA issuer (warp 1); a second issuer (warp 10) puts O1, O2 and MU(c + 1)
+// into the slots where the tensor pipe is otherwise idle.  Warp 0: TMA /
+// bulk producer; warps 2..9: the epilogues as two warpgroups that each take
+// half of the TMEM columns of S, U and O.
+constexpr int kChainWarps = 11;
 constexpr int kChainKernelThreads = kChainWarps * 32;
-constexpr int kChainThreads = 128;
-constexpr int kKQStages = 3, kVStages = 2, kDStages = 3;
-constexpr uint32_t kColS32 = 0, kColS16 = 128, kColU = 192, kColX = 256, kColO = 320,
-                   kTmemCols = 512;   // X and O adjacent: one N = 128 MMA
+constexpr int kEpiThreads = 256;
+constexpr int kKQStages = 3, kVStages = 2, kDStages = 2, kCStages = 4;
+constexpr uint32_t kColS32 = 0, kColS16 = 128, kColU = 192, kColO1 = 256, kColO2 = 320,
+                   kColU16 = 384, kColU16k = 416, kTmemCols = 512;
+constexpr uint32_t kCStageBytes = 1024;
 
 struct ChainBars {
     uint64_t kq_full[kKQStages], kq_empty[kKQStages], v_full[kVStages], v_empty[kVStages],
-        d_full[kDStages], d_empty[kDStages];
-    uint64_t x_full, r_full, u_full, u2_full, s_full, s_next, mma_done;
+        d_full[kDStages], d_empty[kDStages], c_full[kCStages], c_empty[kCStages];
+    uint64_t mu_full, u_full, u2_full, s_full, o1_done, o_full, s_next, o_free, done_a, done_b;
     uint32_t tmem_base;
     int abort;
     int seq;
@@ -292,10 +365,10 @@ struct ChainBars {
 constexpr uint32_t C_OFF_KQ = 0;
 constexpr uint32_t C_OFF_V = C_OFF_KQ + kKQStages * kKQBytes;
 constexpr uint32_t C_OFF_D = C_OFF_V + kVStages * kVBytes;
-constexpr uint32_t C_OFF_BARS = C_OFF_D + kDStages * kItemBytes;
+constexpr uint32_t C_OFF_C = C_OFF_D + kDStages * kItemOps;
+constexpr uint32_t C_OFF_BARS = C_OFF_C + kCStages * kCStageBytes;
 constexpr uint32_t C_SMEM_BYTES = C_OFF_BARS + (sizeof(ChainBars) + 127) / 128 * 128 + 1024;
-static_assert(kItemBytes % 1024 == 0, "item stages stay 1024-aligned");
-static_assert(kDStages == kKQStages, "one stage index for K|Q and items");
+static_assert(kItemOps % 1024 == 0 && kItemScalCopy <= kCStageBytes, "stage layout");
 static_assert(C_SMEM_BYTES <= 232448, "shared memory budget");
 
 __global__ void __launch_bounds__(kChainKernelThreads, 1)
@@ -346,17 +419,18 @@ chain_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
     if (tid == 0) {
         for (int s = 0; s < kKQStages; ++s) { mbar_init(&B.kq_full[s], 1); mbar_init(&B.kq_empty[s], 1); }
         for (int s = 0; s < kVStages; ++s) { mbar_init(&B.v_full[s], 1); mbar_init(&B.v_empty[s], 1); }
-        for (int s = 0; s < kDStages; ++s) {
-            mbar_init(&B.d_full[s], 1);
-            mbar_init(&B.d_empty[s], 1 + kChainThreads);   // the MMAs and the epilogues
-        }
-        mbar_init(&B.x_full, 1);
-        mbar_init(&B.r_full, kChainThreads);
+        for (int s = 0; s < kDStages; ++s) { mbar_init(&B.d_full[s], 1); mbar_init(&B.d_empty[s], 1); }
+        for (int s = 0; s < kCStages; ++s) { mbar_init(&B.c_full[s], 1); mbar_init(&B.c_empty[s], kEpiThreads); }
+        mbar_init(&B.mu_full, 1);
         mbar_init(&B.u_full, 1);
-        mbar_init(&B.u2_full, kChainThreads);
+        mbar_init(&B.u2_full, kEpiThreads);
         mbar_init(&B.s_full, 1);
-        mbar_init(&B.s_next, kChainThreads);
-        mbar_init(&B.mma_done, 1);
+        mbar_init(&B.o1_done, 1);
+        mbar_init(&B.o_full, 1);
+        mbar_init(&B.s_next, kEpiThreads);
+        mbar_init(&B.o_free, kEpiThreads);
+        mbar_init(&B.done_a, 1);
+        mbar_init(&B.done_b, 1);
         B.abort = 0;
         fence_mbar_init();
     }
@@ -372,11 +446,12 @@ chain_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
             prefetch_tensormap(&tm_q);
             prefetch_tensormap(&tm_k);
             prefetch_tensormap(&tm_v);
-            int kq_issued[kKQStages] = {0, 0, 0}, d_issued[kDStages] = {0, 0, 0},
-                v_issued[kVStages] = {0, 0};
+            int kq_n[kKQStages] = {0, 0, 0}, v_n[kVStages] = {0, 0}, d_n[kDStages] = {0, 0},
+                c_n[kCStages] = {0, 0, 0, 0};
             for (int c = 0; c < nch && !*abort; ++c) {
                 const int y = (int)(s_start + (int64_t)c * C);
-                const int sk = c % kKQStages, sv = c % kVStages;
+                const uint8_t *item = items + ((item0 + c) * hv + h) * kItemBytes;
+                const int sk = c % kKQStages, sv = c % kVStages, sd = c % kDStages, sc = c % kCStages;
                 if (c >= kKQStages) mbar_wait(&B.kq_empty[sk], ((c / kKQStages) - 1) & 1, abort);
                 uint8_t *kq = sm + C_OFF_KQ + sk * kKQBytes;
                 mbar_arrive_expect_tx(&B.kq_full[sk], kKQBytes);
@@ -384,110 +459,130 @@ chain_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
                     tma_load_2d(kq + kb * kKBlk, &tm_k, &B.kq_full[sk], hq * DH + kb * 64, y);
                     tma_load_2d(kq + kb * kKBlk + 64 * 128, &tm_q, &B.kq_full[sk], hq * DH + kb * 64, y);
                 }
-                kq_issued[sk] = c / kKQStages + 1;
-                if (c >= kDStages) mbar_wait(&B.d_empty[sk], ((c / kDStages) - 1) & 1, abort);
-                mbar_arrive_expect_tx(&B.d_full[sk], kItemCopy);
-                bulk_load(sm + C_OFF_D + sk * kItemBytes, items + ((item0 + c) * hv + h) * kItemBytes,
-                          kItemCopy, &B.d_full[sk]);
-                d_issued[sk] = c / kDStages + 1;
+                kq_n[sk] = c / kKQStages + 1;
+                if (c >= kCStages) mbar_wait(&B.c_empty[sc], ((c / kCStages) - 1) & 1, abort);
+                mbar_arrive_expect_tx(&B.c_full[sc], kItemScalCopy);
+                bulk_load(sm + C_OFF_C + sc * kCStageBytes, item + kItemOps, kItemScalCopy, &B.c_full[sc]);
+                c_n[sc] = c / kCStages + 1;
+                if (c >= kDStages) mbar_wait(&B.d_empty[sd], ((c / kDStages) - 1) & 1, abort);
+                mbar_arrive_expect_tx(&B.d_full[sd], kItemOps);
+                bulk_load(sm + C_OFF_D + sd * kItemOps, item, kItemOps, &B.d_full[sd]);
+                d_n[sd] = c / kDStages + 1;
                 if (c >= kVStages) mbar_wait(&B.v_empty[sv], ((c / kVStages) - 1) & 1, abort);
                 uint8_t *vt = sm + C_OFF_V + sv * kVBytes;
                 mbar_arrive_expect_tx(&B.v_full[sv], kVBytes);
                 for (int kb = 0; kb < 2; ++kb)
                     tma_load_2d(vt + kb * kVBlk, &tm_v, &B.v_full[sv], h * DH + kb * 64, y);
-                v_issued[sv] = c / kVStages + 1;
+                v_n[sv] = c / kVStages + 1;
             }
             // never leave with copies in flight: wait for the last load of every stage
             for (int s = 0; s < kKQStages; ++s)
-                if (kq_issued[s]) { int z = 0; mbar_wait(&B.kq_full[s], (kq_issued[s] - 1) & 1, &z); }
+                if (kq_n[s]) { int z = 0; mbar_wait(&B.kq_full[s], (kq_n[s] - 1) & 1, &z); }
+            for (int s = 0; s < kCStages; ++s)
+                if (c_n[s]) { int z = 0; mbar_wait(&B.c_full[s], (c_n[s] - 1) & 1, &z); }
             for (int s = 0; s < kDStages; ++s)
-                if (d_issued[s]) { int z = 0; mbar_wait(&B.d_full[s], (d_issued[s] - 1) & 1, &z); }
+                if (d_n[s]) { int z = 0; mbar_wait(&B.d_full[s], (d_n[s] - 1) & 1, &z); }
             for (int s = 0; s < kVStages; ++s)
-                if (v_issued[s]) { int z = 0; mbar_wait(&B.v_full[s], (v_issued[s] - 1) & 1, &z); }
+                if (v_n[s]) { int z = 0; mbar_wait(&B.v_full[s], (v_n[s] - 1) & 1, &z); }
         }
         __syncwarp();
     } else if (warp == 1) {
-        // ------------------------------------------------------- MMA issuer
+        // ------------------------------------ MMA issuer A: the critical path
+        if (lane == 0) {
+            const uint32_t id64bmn = idesc_bf16(128, 64, false, true);
+            const uint32_t id128bmn = idesc_bf16(128, 128, false, true);
+            for (int c = 0; c < nch; ++c) {
+                const int sk = c % kKQStages, sd = c % kDStages;
+                const uint32_t kqb = smem_u32(sm + C_OFF_KQ + sk * kKQBytes);
+                const uint32_t dsm = smem_u32(sm + C_OFF_D + sd * kItemOps);
+                mbar_wait(&B.kq_full[sk], (c / kKQStages) & 1, abort);
+                mbar_wait(&B.d_full[sd], (c / kDStages) & 1, abort);
+                mbar_wait(&B.mu_full, c & 1, abort);     // U = T1 V of this chunk
+                mbar_wait(&B.s_next, c & 1, abort);      // S16 of this chunk
+                tc_fence_after();
+                for (int s = 0; s < 8; ++s)   // M2: U += S16 W'^T  (W'^T: 128 rows a of 64 i)
+                    mma_ts(tbase + kColU, tbase + kColS16 + s * 8,
+                           sdesc_sw128(dsm + kItemW + s * 16 * 128, 8192, 1024), id64bmn, 1);
+                mma_commit(&B.u_full);
+                mbar_wait(&B.u2_full, c & 1, abort);     // U16k in TMEM
+                tc_fence_after();
+                for (int s = 0; s < 4; ++s)   // M6: S += U16k K  (K MN-major: 2 blocks of 64 keys)
+                    mma_ts(tbase + kColS32, tbase + kColU16k + s * 8,
+                           sdesc_sw128(kqb + s * 16 * 128, kKBlk, 1024), id128bmn, 1);
+                mma_commit(&B.s_full);
+            }
+            mma_commit(&B.done_a);
+            int z = 0;
+            mbar_wait(&B.done_a, 0, &z);
+        }
+        __syncwarp();
+    } else if (warp == 10) {
+        // ------------------------------- MMA issuer B: MU and the O products
         if (lane == 0) {
             const uint32_t id64 = idesc_bf16(128, 64);
             const uint32_t id64amn = idesc_bf16(128, 64, true, false);
-            const uint32_t id128 = idesc_bf16(128, 128);
-            const uint32_t id128bmn = idesc_bf16(128, 128, false, true);
-            for (int c = 0; c < nch; ++c) {
-                const int sk = c % kKQStages, sv = c % kVStages;
-                const uint32_t kqb = smem_u32(sm + C_OFF_KQ + sk * kKQBytes);
-                const uint32_t dsm = smem_u32(sm + C_OFF_D + sk * kItemBytes);   // T1 | T2 | P
-                const uint32_t vsm = smem_u32(sm + C_OFF_V + sv * kVBytes);
-                mbar_wait(&B.d_full[sk], (c / kDStages) & 1, abort);
-                mbar_wait(&B.kq_full[sk], (c / kKQStages) & 1, abort);
-                mbar_wait(&B.s_next, c & 1, abort);      // S16 and Q' of this chunk ready
+            auto issue_mu = [&](int c) {   // MU: U = T1 V  (A = V^T, MN-major)
+                const int sd = c % kDStages, sv = c % kVStages;
+                mbar_wait(&B.d_full[sd], (c / kDStages) & 1, abort);
                 mbar_wait(&B.v_full[sv], (c / kVStages) & 1, abort);
                 tc_fence_after();
-                for (int s = 0; s < 4; ++s)   // MU: U = T1 V  (A = V^T, MN-major)
+                const uint32_t dsm = smem_u32(sm + C_OFF_D + sd * kItemOps);
+                const uint32_t vsm = smem_u32(sm + C_OFF_V + sv * kVBytes);
+                for (int s = 0; s < 4; ++s)
                     mma_ss(tbase + kColU, sdesc_sw128(vsm + s * 16 * 128, kVBlk, 1024),
-                           sdesc_sw128(dsm + s * 32, 16, 1024), id64amn, s > 0);
+                           sdesc_sw128(dsm + kItemT1 + s * 32, 16, 1024), id64amn, s > 0);
                 mma_commit(&B.v_empty[sv]);
-                for (int s = 0; s < 8; ++s) {   // M23: [X | O] = S [K; Q']^T
-                    const uint32_t off = (s >> 2) * kKBlk + (s & 3) * 32;
-                    mma_ts(tbase + kColX, tbase + kColS16 + s * 8, sdesc_sw128(kqb + off, 16, 1024),
-                           id128, s > 0);
-                }
-                mma_commit(&B.x_full);
-                mbar_wait(&B.r_full, c & 1, abort);
+                mma_commit(&B.mu_full);
+            };
+            issue_mu(0);
+            for (int c = 0; c < nch; ++c) {
+                const int sk = c % kKQStages, sd = c % kDStages;
+                const uint32_t kqb = smem_u32(sm + C_OFF_KQ + sk * kKQBytes);
+                const uint32_t dsm = smem_u32(sm + C_OFF_D + sd * kItemOps);
+                mbar_wait(&B.s_next, c & 1, abort);      // S16 of this chunk
+                mbar_wait(&B.u_full, c & 1, abort);      // M2 done: E2 runs, the pipe is free
+                mbar_wait(&B.o_free, c & 1, abort);      // the last chunk's O read out
+                mbar_wait(&B.kq_full[sk], (c / kKQStages) & 1, abort);
                 tc_fence_after();
-                for (int s = 0; s < 4; ++s)   // M4: U += T2 X^T
-                    mma_ts(tbase + kColU, tbase + kColX + s * 8,
-                           sdesc_sw128(dsm + kMatBytes + s * 32, 16, 1024), id64, 1);
-                mma_commit(&B.u_full);
-                mbar_wait(&B.u2_full, c & 1, abort);
-                tc_fence_after();
-                for (int s = 0; s < 4; ++s) {
-                    // M5: O += U P^T ; M6: S += U K''  (K'' MN-major: 2 blocks of 64 keys)
-                    mma_ts(tbase + kColO, tbase + kColU + s * 8,
-                           sdesc_sw128(dsm + 2 * kMatBytes + s * 32, 16, 1024), id64, 1);
-                    mma_ts(tbase + kColS32, tbase + kColU + s * 8,
-                           sdesc_sw128(kqb + s * 16 * 128, kKBlk, 1024), id128bmn, 1);
+                for (int s = 0; s < 8; ++s) {   // O1 = S16 Q^T  (S16 still holds this chunk's S)
+                    const uint32_t off = (s >> 2) * kKBlk + 64 * 128 + (s & 3) * 32;
+                    mma_ts(tbase + kColO1, tbase + kColS16 + s * 8, sdesc_sw128(kqb + off, 16, 1024),
+                           id64, s > 0);
                 }
-                mma_commit(&B.s_full);
-                mma_commit(&B.kq_empty[sk]);
-                mma_commit(&B.d_empty[sk]);
+                mma_commit(&B.o1_done);
+                mbar_wait(&B.s_full, c & 1, abort);      // M6 done (U16 ready long since)
+                tc_fence_after();
+                for (int s = 0; s < 4; ++s)   // O2 = U16 P^T
+                    mma_ts(tbase + kColO2, tbase + kColU16 + s * 8,
+                           sdesc_sw128(dsm + kItemP + s * 32, 16, 1024), id64, s > 0);
+                mma_commit(&B.o_full);
+                mma_commit(&B.kq_empty[sk]);             // every MMA on these stages is done
+                mma_commit(&B.d_empty[sd]);
+                if (c + 1 < nch) issue_mu(c + 1);
             }
-            mma_commit(&B.mma_done);
+            mma_commit(&B.done_b);
             int z = 0;
-            mbar_wait(&B.mma_done, 0, &z);
+            mbar_wait(&B.done_b, 0, &z);
         }
         __syncwarp();
     } else {
-        // --------------------------------------------------- chain (4 warps)
-        const int tc4 = tid - 64;                 // 0 .. 127
+        // ------------------------------------------- epilogues (2 warpgroups)
+        const int hf = (warp - 2) >> 2;           // column half of S, U and O
         const int q4 = warp & 3;
         const int b = q4 * 32 + lane;            // value row of the state
         const uint32_t lrow = tmem_addr(tbase, q4 * 32, 0);
-        auto item_scal = [&](int c) -> const ItemScal & {
-            return *reinterpret_cast<const ItemScal *>(sm + C_OFF_D + (c % kDStages) * kItemBytes +
-                                                       kItemScal);
+        const uint32_t s32 = lrow + kColS32 + hf * 64, s16 = lrow + kColS16 + hf * 32;
+        auto scal = [&](int c) -> const ItemScal & {
+            return *reinterpret_cast<const ItemScal *>(sm + C_OFF_C + (c % kCStages) * kCStageBytes);
         };
-        // Q' = scale Gam_i r_q,i Q_i in place for chunk cq, before M23 of that chunk
-        auto rescale_q = [&](int cq) {
-            mbar_wait(&B.d_full[cq % kDStages], (cq / kDStages) & 1, abort);
-            mbar_wait(&B.kq_full[cq % kKQStages], (cq / kKQStages) & 1, abort);
-            uint8_t *kqq = sm + C_OFF_KQ + (cq % kKQStages) * kKQBytes;
-            const int i = tc4 >> 1, kb = tc4 & 1;
-            const float f = item_scal(cq).sq[i];
-#pragma unroll
-            for (int ch = 0; ch < 8; ++ch) {
-                uint4 *pq = reinterpret_cast<uint4 *>(kqq + kb * kKBlk + sw128_chunk(C + i, ch));
-                *pq = scale_chunk(*pq, f);
-            }
-            fence_async_smem();
-        };
-        // E0: initial state -> bf16 operand copy, and the fp32 accumulator
-        //     pre-scaled by the first chunk's total decay
+        // E0: this half of the initial state -> bf16 operand copy, and the
+        //     fp32 accumulator pre-scaled by the first chunk's total decay
         {
-            mbar_wait(&B.d_full[0], 0, abort);
-            const float gn = item_scal(0).gam_n;
-            const float *src = islot >= 0 ? pool + islot * slot_stride + head_off + (size_t)b * DH : nullptr;
-            for (int c0 = 0; c0 < DH; c0 += 32) {
+            mbar_wait(&B.c_full[0], 0, abort);
+            const float gn = scal(0).gam_n;
+            const float *src = islot >= 0 ? pool + islot * slot_stride + head_off + (size_t)b * DH + hf * 64
+                                          : nullptr;
+            for (int c0 = 0; c0 < 64; c0 += 32) {
                 uint32_t v[32], pk[16];
 #pragma unroll
                 for (int j = 0; j < 32; j += 4) {
@@ -498,112 +593,109 @@ chain_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
 #pragma unroll
                 for (int jj = 0; jj < 16; ++jj)
                     pk[jj] = pack_bf16(__uint_as_float(v[2 * jj]), __uint_as_float(v[2 * jj + 1]));
-                tmem_st16(lrow + kColS16 + c0 / 2, pk);
+                tmem_st16(s16 + c0 / 2, pk);
 #pragma unroll
                 for (int j = 0; j < 32; ++j) v[j] = __float_as_uint(__uint_as_float(v[j]) * gn);
-                tmem_st32(lrow + kColS32 + c0, v);
+                tmem_st32(s32 + c0, v);
             }
             tmem_wait_st();
-            rescale_q(0);
             tc_fence_before();
             mbar_arrive(&B.s_next);
+            mbar_arrive(&B.o_free);
         }
         for (int c = 0; c < nch; ++c) {
-            const int sd = c % kDStages;
-            const ItemScal &I = item_scal(c);     // d_full(c) was waited by rescale_q(c)
-            uint8_t *kq = sm + C_OFF_KQ + (c % kKQStages) * kKQBytes;
+            const ItemScal &I = scal(c);             // c_full(c) was waited one chunk earlier
             const int64_t c0 = s_start + (int64_t)c * C;
             const bool last = c == nch - 1;
             const int n = I.n;
-            // ---- E1: X -> bf16 in TMEM (X's columns)
-            mbar_wait(&B.x_full, c & 1, abort);
-            tc_fence_after();
-#pragma unroll
-            for (int h2 = 0; h2 < 2; ++h2) {
-                uint32_t x[32], xx[16];
-                tmem_ld32(lrow + kColX + 32 * h2, x);
-#pragma unroll
-                for (int jj = 0; jj < 16; ++jj)
-                    xx[jj] = pack_bf16(__uint_as_float(x[2 * jj]), __uint_as_float(x[2 * jj + 1]));
-                tmem_st16(lrow + kColX + 16 * h2, xx);
-            }
-            tmem_wait_st();
-            tc_fence_before();
-            mbar_arrive(&B.r_full);
-            // K'' = D[last][j] r_k,j K_j in place (M23 has consumed the raw rows)
-            {
-                const int j = tc4 >> 1, kb = tc4 & 1;
-                const float f = I.ks[j];
-#pragma unroll
-                for (int ch = 0; ch < 8; ++ch) {
-                    uint4 *pk = reinterpret_cast<uint4 *>(kq + kb * kKBlk + sw128_chunk((uint32_t)j, ch));
-                    *pk = scale_chunk(*pk, f);
-                }
-                fence_async_smem();
-            }
-            // ---- E2: U -> bf16 in TMEM (U's columns)
+            // ---- E2: this half of U -> U16 = bf16(U) and U16k = bf16(U diag(ks))
             mbar_wait(&B.u_full, c & 1, abort);
             tc_fence_after();
+            {
+                uint32_t u[32], uu[16], uk[16];
+                tmem_ld32(lrow + kColU + 32 * hf, u);
+                const float4 *ks4 = reinterpret_cast<const float4 *>(I.ks + 32 * hf);
 #pragma unroll
-            for (int h2 = 0; h2 < 2; ++h2) {
-                uint32_t u[32], uu[16];
-                tmem_ld32(lrow + kColU + 32 * h2, u);
-#pragma unroll
-                for (int jj = 0; jj < 16; ++jj)
-                    uu[jj] = pack_bf16(__uint_as_float(u[2 * jj]), __uint_as_float(u[2 * jj + 1]));
-                tmem_st16(lrow + kColU + 16 * h2, uu);
+                for (int q = 0; q < 8; ++q) {
+                    const float4 f = ks4[q];
+                    const float u0 = __uint_as_float(u[4 * q]), u1 = __uint_as_float(u[4 * q + 1]);
+                    const float u2 = __uint_as_float(u[4 * q + 2]), u3 = __uint_as_float(u[4 * q + 3]);
+                    uu[2 * q] = pack_bf16(u0, u1);
+                    uu[2 * q + 1] = pack_bf16(u2, u3);
+                    uk[2 * q] = pack_bf16(u0 * f.x, u1 * f.y);
+                    uk[2 * q + 1] = pack_bf16(u2 * f.z, u3 * f.w);
+                }
+                tmem_st16(lrow + kColU16k + 16 * hf, uk);
+                tmem_st16(lrow + kColU16 + 16 * hf, uu);
             }
             tmem_wait_st();
             tc_fence_before();
             mbar_arrive(&B.u2_full);
-            if (!last) rescale_q(c + 1);   // overlaps M5 / M6
-            // ---- E3a: S -> bf16 operand copy, fp32 pre-scaled for the next
-            //      chunk (or the final state -> pool)
+            // ---- E3a: S -> bf16 operand copy first (the next chunk's M2 waits
+            //      on it), then the fp32 state pre-scaled by the next decay
             mbar_wait(&B.s_full, c & 1, abort);
+            mbar_wait(&B.o1_done, c & 1, abort);     // O1 has read the old S16
             tc_fence_after();
-            const float gnext = last ? 1.f : item_scal(c + 1).gam_n;
-            float *dstp = (last && fslot >= 0) ? pool + fslot * slot_stride + head_off + (size_t)b * DH : nullptr;
-            for (int cc = 0; cc < DH; cc += 32) {
-                uint32_t sv[32];
-                tmem_ld32(lrow + kColS32 + cc, sv);
-                if (!last) {
+            uint32_t sv[64];
+            tmem_ld32(s32, *reinterpret_cast<uint32_t(*)[32]>(sv));
+            tmem_ld32(s32 + 32, *reinterpret_cast<uint32_t(*)[32]>(sv + 32));
+            if (!last) {
+#pragma unroll
+                for (int cc = 0; cc < 64; cc += 32) {
                     uint32_t pk[16];
 #pragma unroll
                     for (int jj = 0; jj < 16; ++jj)
-                        pk[jj] = pack_bf16(__uint_as_float(sv[2 * jj]), __uint_as_float(sv[2 * jj + 1]));
-                    tmem_st16(lrow + kColS16 + cc / 2, pk);
-#pragma unroll
-                    for (int j = 0; j < 32; ++j) sv[j] = __float_as_uint(__uint_as_float(sv[j]) * gnext);
-                    tmem_st32(lrow + kColS32 + cc, sv);
-                } else if (dstp) {
-#pragma unroll
-                    for (int j = 0; j < 32; j += 4)
-                        *reinterpret_cast<float4 *>(dstp + cc + j) = make_float4(
-                            __uint_as_float(sv[j]), __uint_as_float(sv[j + 1]),
-                            __uint_as_float(sv[j + 2]), __uint_as_float(sv[j + 3]));
+                        pk[jj] = pack_bf16(__uint_as_float(sv[cc + 2 * jj]), __uint_as_float(sv[cc + 2 * jj + 1]));
+                    tmem_st16(s16 + cc / 2, pk);
                 }
+                tmem_wait_st();
+                tc_fence_before();
+                mbar_arrive(&B.s_next);
+                mbar_wait(&B.c_full[(c + 1) % kCStages], ((c + 1) / kCStages) & 1, abort);
+                const float gnext = scal(c + 1).gam_n;
+#pragma unroll
+                for (int cc = 0; cc < 64; cc += 32) {
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) sv[cc + j] = __float_as_uint(__uint_as_float(sv[cc + j]) * gnext);
+                    tmem_st32(s32 + cc, *reinterpret_cast<uint32_t(*)[32]>(sv + cc));
+                }
+            } else if (fslot >= 0) {
+                float *dstp = pool + fslot * slot_stride + head_off + (size_t)b * DH + hf * 64;
+#pragma unroll
+                for (int j = 0; j < 64; j += 4)
+                    *reinterpret_cast<float4 *>(dstp + j) = make_float4(
+                        __uint_as_float(sv[j]), __uint_as_float(sv[j + 1]),
+                        __uint_as_float(sv[j + 2]), __uint_as_float(sv[j + 3]));
             }
-            uint32_t ov0[32], ov1[32];
-            tmem_ld32(lrow + kColO, ov0);
-            tmem_ld32(lrow + kColO + 32, ov1);
+            // ---- o = diag(sq) O1 + O2 for rows 32 hf .. 32 hf + 31
+            mbar_wait(&B.o_full, c & 1, abort);
+            tc_fence_after();
+            uint32_t o1[32], o2[32];
+            tmem_ld32(lrow + kColO1 + 32 * hf, o1);
+            tmem_ld32(lrow + kColO2 + 32 * hf, o2);
             tmem_wait_st();
             tc_fence_before();
-            mbar_arrive(&B.s_next);      // S16 ready and X | O free for the next chunk
-            // ---- E3b: o <- O (from registers)
+            mbar_arrive(&B.o_free);
             {
-                __nv_bfloat16 *orow = o + (c0 * hv + h) * (int64_t)DH + b;
                 const int64_t ostride = (int64_t)hv * DH;
+                __nv_bfloat16 *orow = o + ((c0 + 32 * hf) * hv + h) * (int64_t)DH + b;
+                const float4 *sq4 = reinterpret_cast<const float4 *>(I.sq + 32 * hf);
 #pragma unroll
-                for (int i = 0; i < 32; ++i)
-                    if (i < n) orow[i * ostride] = __float2bfloat16_rn(__uint_as_float(ov0[i]));
+                for (int q = 0; q < 8; ++q) {
+                    const float4 f = sq4[q];
+                    const float fs[4] = {f.x, f.y, f.z, f.w};
 #pragma unroll
-                for (int i = 0; i < 32; ++i)
-                    if (32 + i < n) orow[(32 + i) * ostride] = __float2bfloat16_rn(__uint_as_float(ov1[i]));
+                    for (int e = 0; e < 4; ++e) {
+                        const int i = 4 * q + e;
+                        if (32 * hf + i < n)
+                            orow[i * ostride] = __float2bfloat16_rn(
+                                fmaf(fs[e], __uint_as_float(o1[i]), __uint_as_float(o2[i])));
+                    }
+                }
             }
-            mbar_arrive(&B.d_empty[sd]);
+            mbar_arrive(&B.c_empty[c % kCStages]);
         }
     }
-
     tc_fence_before();
     __syncthreads();
     if (warp == 1) {

@@ -329,7 +329,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
             g_to_a_p(gr, p, chalf, n, S.beta, S.gam, S.alpha, S.rk, S.rq, scale, Af, dst + 2 * kMatBytes);
             named_sync(1, kPrepThreads);
             // ---- T = (I + A)^-1 and the T1 / T2 operands
-            ut_solve(Af, Tf, Wb, t, pw, lane, S.beta, S.xs, dst);
+            ut_solve<true>(Af, Tf, Wb, t, pw, lane, S.beta, S.xs, dst);
             fence_async_smem();
             mbar_arrive(&B.prep_done[sd]);
             named_sync(1, kPrepThreads);   // the solve scratch is free again

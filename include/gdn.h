@@ -188,7 +188,7 @@ gdn_status gdn_prefill_chunked(const void *q, int64_t q_row_stride,
 
 /* Bytes of scratch gdn_prefill_chunked uses for these sizes (0: none):
  * 1 KiB-rounded header of n_seqs + 1 chunk offsets, then
- * (ceil(n_tokens / 64) + n_seqs) * hv blocks of 25 KiB. */
+ * (ceil(n_tokens / 64) + n_seqs) * hv blocks of 33 KiB. */
 size_t gdn_prefill_workspace_size(int32_t n_seqs, int64_t n_tokens,
                                   int32_t hv, int32_t dk, int32_t dv,
                                   int32_t chunk, int32_t dtype);
@@ -206,8 +206,8 @@ size_t gdn_prefill_workspace_size(int32_t n_seqs, int64_t n_tokens,
  * dtype = GDN_BF16 fixed (and no workspace); q, k, v must be 16-byte aligned
  * with row strides that are multiples of 8 elements.
  * Capacity: gdn_prefill_workspace_size(n_seqs, n_tokens, hv, 128, 128, 64,
- * GDN_BF16) <= GDN_PREFILL_STATIC_SCRATCH_BYTES (16 MiB: about 655
- * (chunk, V head) items, i.e. ceil(n_tokens / 64) + n_seqs <= 20 at hv = 32),
+ * GDN_BF16) <= GDN_PREFILL_STATIC_SCRATCH_BYTES (16 MiB: 496 (chunk, V head)
+ * items, i.e. ceil(n_tokens / 64) + n_seqs <= 15 at hv = 32),
  * else GDN_ERR_TOO_LARGE and nothing runs.  n_tokens = 0 returns
  * GDN_ERR_UNSUPPORTED (use gdn_prefill_chunked).
  * The array's address is looked up once per device (cudaGetSymbolAddress

@@ -225,9 +225,11 @@ def test_long_context_sampled_heads_and_split():
 
 
 def test_prefill_split_matches_fused_every_head():
-    """The two tensor-core paths run the same arithmetic: on the full
-    8-sequence batch every output row and final state agrees within the bf16
-    tolerance (they are expected to agree far more closely)."""
+    """The two tensor-core paths compute the same recurrence but round
+    different intermediates to bf16 (the fused kernel X = S K^T, the split
+    path W = T diag(beta Gam r_k) K), so on the full 8-sequence batch they
+    agree within a few bf16 ulps of max|o| (each is within the 2e-2 bf16
+    tolerance of the oracle; here 1e-2 between them)."""
     w = workloads.prefill()
     d = w.dims
     gen = torch.Generator().manual_seed(77)
@@ -245,5 +247,5 @@ def test_prefill_split_matches_fused_every_head():
                                    workspace=False)
     torch.cuda.synchronize()
     status_clean()
-    assert_close(o1, o2, 1e-3, "o split vs fused")
-    assert_close(p1, p2, 1e-3, "S split vs fused")
+    assert_close(o1, o2, 1e-2, "o split vs fused")
+    assert_close(p1, p2, 1e-2, "S split vs fused")
