@@ -64,7 +64,7 @@ extern "C" gdn_status gdn_prefill_chunked(const void *q, int64_t q_row_stride, c
     cudaStream_t s = (cudaStream_t)stream;
     if (n_tokens > 0 && prefill_tc_supported(dtype, dk, dv, chunk, q, q_row_stride, k,
                                              k_row_stride, v, v_row_stride)) {
-        if (workspace && ((uintptr_t)workspace & 15u) == 0 &&
+        if (workspace && ((uintptr_t)workspace & 15u) == 0 && ((uintptr_t)o & 15u) == 0 &&
             workspace_bytes >= prefill_split_workspace(n_seqs, n_tokens, hv))
             return prefill_split(q, q_row_stride, k, k_row_stride, v, v_row_stride, g, beta,
                                  cu_seqlens, n_seqs, n_tokens, hqk, hv, scale, l2norm_qk,

@@ -335,29 +335,33 @@ prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
 // ------------------------------------------------------------ chain kernel --
 // One CTA per (sequence, V head).  Per chunk c (S pre-scaled by the chunk's
 // decay, S16 its bf16 copy; K, Q, V raw tiles; T1, P, W' from the item):
-//   MU  U   = T1 V                    (a chunk ahead: needs no state)
-//   M2  U  += S16 W'^T                W' = T2 K, so U = T1 V + T2 (S K^T)^T
-//   E2  U16 = bf16(U), U16k = bf16(U diag(ks))      ks = D[last][j] r_k,j
-//   M6  S  += U16k K                  (= U K'')
-//   O1  O1  = S16 Q^T    O2  O2 = U16 P^T     o = diag(sq) O1 + O2 (epilogue)
+//   MU  U1  = T1 V                    (a chunk ahead: needs no state)
+//   M2  U1 += S16[:, a < 64] W'^T,  U2 = S16[:, a >= 64] W'^T    (W' = T2 K)
+//   E2  U = U1 + U2;  U16 = bf16(U), U16k = bf16(U diag(ks))     (ks: K'' rows)
+//   M6  S += U16k K                   (= U K'')
+//   O   O1 = S16 Q^T,  O2 = U16 P^T,  o = diag(sq) O1 + O2       (sq: Q' rows)
 //   E3  S16 = bf16(S) for the next chunk, S *= its decay, o stores
-// The critical path  s_next -> M2 -> E2 -> M6 -> E3a -> s_next  has its own
-// MMA issuer (warp 1); a second issuer (warp 10) puts O1, O2 and MU(c + 1)
-// into the slots where the tensor pipe is otherwise idle.  Warp 0: TMA /
-// bulk producer; warps 2..9: the epilogues as two warpgroups that each take
-// half of the TMEM columns of S, U and O.
+// A tcgen05.mma costs its issuing thread about 60 cycles whatever N is, and
+// an N = 64 product occupies the tensor pipe for about half that, so M2 is
+// split by K over two issuing threads (warps 1 and 10) into separate
+// accumulators that E2 adds.  The critical path is
+//   s_next -> M2 -> E2 -> M6 -> E3a -> s_next;
+// O1, O2, MU(c + 1) and the o stores fill the gaps.  Warp 0: TMA / bulk
+// producer; warps 2..9: the epilogues as two warpgroups that each take half
+// of the TMEM columns of S, U and O, and store o a 32 x 32 tile per warp
+// through shared memory with TMA.
 constexpr int kChainWarps = 11;
 constexpr int kChainKernelThreads = kChainWarps * 32;
 constexpr int kEpiThreads = 256;
 constexpr int kKQStages = 3, kVStages = 2, kDStages = 2, kCStages = 4;
-constexpr uint32_t kColS32 = 0, kColS16 = 128, kColU = 192, kColO1 = 256, kColO2 = 320,
-                   kColU16 = 384, kColU16k = 416, kTmemCols = 512;
+constexpr uint32_t kColS32 = 0, kColS16 = 128, kColU1 = 192, kColU2 = 256, kColO1 = 320,
+                   kColO2 = 384, kColU16 = 448, kColU16k = 480, kTmemCols = 512;
 constexpr uint32_t kCStageBytes = 1024;
 
 struct ChainBars {
     uint64_t kq_full[kKQStages], kq_empty[kKQStages], v_full[kVStages], v_empty[kVStages],
         d_full[kDStages], d_empty[kDStages], c_full[kCStages], c_empty[kCStages];
-    uint64_t mu_full, u_full, u2_full, s_full, o1_done, o_full, s_next, o_free, done_a, done_b;
+    uint64_t mu_full, u_full, u2_full, s_full, o1_full, o2_full, s_next, o_free, done_a, done_b;
     uint32_t tmem_base;
     int abort;
     int seq;
@@ -366,14 +370,17 @@ constexpr uint32_t C_OFF_KQ = 0;
 constexpr uint32_t C_OFF_V = C_OFF_KQ + kKQStages * kKQBytes;
 constexpr uint32_t C_OFF_D = C_OFF_V + kVStages * kVBytes;
 constexpr uint32_t C_OFF_C = C_OFF_D + kDStages * kItemOps;
-constexpr uint32_t C_OFF_BARS = C_OFF_C + kCStages * kCStageBytes;
+constexpr uint32_t kOTileBytes = 32 * 32 * 2;               // one warp's o tile [i][b]
+constexpr uint32_t C_OFF_OT = C_OFF_C + kCStages * kCStageBytes;
+constexpr uint32_t C_OFF_BARS = C_OFF_OT + 8 * kOTileBytes;
 constexpr uint32_t C_SMEM_BYTES = C_OFF_BARS + (sizeof(ChainBars) + 127) / 128 * 128 + 1024;
 static_assert(kItemOps % 1024 == 0 && kItemScalCopy <= kCStageBytes, "stage layout");
 static_assert(C_SMEM_BYTES <= 232448, "shared memory budget");
 
 __global__ void __launch_bounds__(kChainKernelThreads, 1)
 chain_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-             const __grid_constant__ CUtensorMap tm_v, const int32_t *__restrict__ cu,
+             const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
+             const int32_t *__restrict__ cu,
              const int32_t *__restrict__ base, int n_seqs, int64_t n_tokens, int hv, int grp,
              const uint8_t *__restrict__ items, float *__restrict__ pool, int64_t n_slots,
              const int32_t *__restrict__ init_idx, const int32_t *__restrict__ final_idx,
@@ -422,11 +429,11 @@ chain_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
         for (int s = 0; s < kDStages; ++s) { mbar_init(&B.d_full[s], 1); mbar_init(&B.d_empty[s], 1); }
         for (int s = 0; s < kCStages; ++s) { mbar_init(&B.c_full[s], 1); mbar_init(&B.c_empty[s], kEpiThreads); }
         mbar_init(&B.mu_full, 1);
-        mbar_init(&B.u_full, 1);
+        mbar_init(&B.u_full, 2);                       // one commit from each issuer
         mbar_init(&B.u2_full, kEpiThreads);
         mbar_init(&B.s_full, 1);
-        mbar_init(&B.o1_done, 1);
-        mbar_init(&B.o_full, 1);
+        mbar_init(&B.o1_full, 1);
+        mbar_init(&B.o2_full, 1);
         mbar_init(&B.s_next, kEpiThreads);
         mbar_init(&B.o_free, kEpiThreads);
         mbar_init(&B.done_a, 1);
@@ -486,42 +493,21 @@ chain_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
                 if (v_n[s]) { int z = 0; mbar_wait(&B.v_full[s], (v_n[s] - 1) & 1, &z); }
         }
         __syncwarp();
-    } else if (warp == 1) {
-        // ------------------------------------ MMA issuer A: the critical path
+    } else if (warp == 1 || warp == 10) {
+        // ------------------------------------------------ the two MMA issuers
+        // Issuer A (warp 1): M2 over a < 64, M6, O2.
+        // Issuer B (warp 10): M2 over a >= 64, O1, and MU(c + 1) once M6 has
+        // left the tensor pipe (issued earlier, it slows M6 down more than it
+        // gains).
         if (lane == 0) {
-            const uint32_t id64bmn = idesc_bf16(128, 64, false, true);
-            const uint32_t id128bmn = idesc_bf16(128, 128, false, true);
-            for (int c = 0; c < nch; ++c) {
-                const int sk = c % kKQStages, sd = c % kDStages;
-                const uint32_t kqb = smem_u32(sm + C_OFF_KQ + sk * kKQBytes);
-                const uint32_t dsm = smem_u32(sm + C_OFF_D + sd * kItemOps);
-                mbar_wait(&B.kq_full[sk], (c / kKQStages) & 1, abort);
-                mbar_wait(&B.d_full[sd], (c / kDStages) & 1, abort);
-                mbar_wait(&B.mu_full, c & 1, abort);     // U = T1 V of this chunk
-                mbar_wait(&B.s_next, c & 1, abort);      // S16 of this chunk
-                tc_fence_after();
-                for (int s = 0; s < 8; ++s)   // M2: U += S16 W'^T  (W'^T: 128 rows a of 64 i)
-                    mma_ts(tbase + kColU, tbase + kColS16 + s * 8,
-                           sdesc_sw128(dsm + kItemW + s * 16 * 128, 8192, 1024), id64bmn, 1);
-                mma_commit(&B.u_full);
-                mbar_wait(&B.u2_full, c & 1, abort);     // U16k in TMEM
-                tc_fence_after();
-                for (int s = 0; s < 4; ++s)   // M6: S += U16k K  (K MN-major: 2 blocks of 64 keys)
-                    mma_ts(tbase + kColS32, tbase + kColU16k + s * 8,
-                           sdesc_sw128(kqb + s * 16 * 128, kKBlk, 1024), id128bmn, 1);
-                mma_commit(&B.s_full);
-            }
-            mma_commit(&B.done_a);
-            int z = 0;
-            mbar_wait(&B.done_a, 0, &z);
-        }
-        __syncwarp();
-    } else if (warp == 10) {
-        // ------------------------------- MMA issuer B: MU and the O products
-        if (lane == 0) {
+            const bool isA = warp == 1;
             const uint32_t id64 = idesc_bf16(128, 64);
             const uint32_t id64amn = idesc_bf16(128, 64, true, false);
-            auto issue_mu = [&](int c) {   // MU: U = T1 V  (A = V^T, MN-major)
+            const uint32_t id64bmn = idesc_bf16(128, 64, false, true);
+            const uint32_t id128bmn = idesc_bf16(128, 128, false, true);
+            const int s0 = isA ? 0 : 4;                  // this issuer's k-steps over a
+            const uint32_t ucol = isA ? kColU1 : kColU2;
+            auto issue_mu = [&](int c) {   // MU: U1 = T1 V  (A = V^T, MN-major)
                 const int sd = c % kDStages, sv = c % kVStages;
                 mbar_wait(&B.d_full[sd], (c / kDStages) & 1, abort);
                 mbar_wait(&B.v_full[sv], (c / kVStages) & 1, abort);
@@ -529,45 +515,65 @@ chain_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
                 const uint32_t dsm = smem_u32(sm + C_OFF_D + sd * kItemOps);
                 const uint32_t vsm = smem_u32(sm + C_OFF_V + sv * kVBytes);
                 for (int s = 0; s < 4; ++s)
-                    mma_ss(tbase + kColU, sdesc_sw128(vsm + s * 16 * 128, kVBlk, 1024),
+                    mma_ss(tbase + kColU1, sdesc_sw128(vsm + s * 16 * 128, kVBlk, 1024),
                            sdesc_sw128(dsm + kItemT1 + s * 32, 16, 1024), id64amn, s > 0);
                 mma_commit(&B.v_empty[sv]);
                 mma_commit(&B.mu_full);
             };
-            issue_mu(0);
+            if (!isA) issue_mu(0);
             for (int c = 0; c < nch; ++c) {
                 const int sk = c % kKQStages, sd = c % kDStages;
                 const uint32_t kqb = smem_u32(sm + C_OFF_KQ + sk * kKQBytes);
                 const uint32_t dsm = smem_u32(sm + C_OFF_D + sd * kItemOps);
-                mbar_wait(&B.s_next, c & 1, abort);      // S16 of this chunk
-                mbar_wait(&B.u_full, c & 1, abort);      // M2 done: E2 runs, the pipe is free
-                mbar_wait(&B.o_free, c & 1, abort);      // the last chunk's O read out
                 mbar_wait(&B.kq_full[sk], (c / kKQStages) & 1, abort);
+                mbar_wait(&B.d_full[sd], (c / kDStages) & 1, abort);
+                if (isA) mbar_wait(&B.mu_full, c & 1, abort);   // M2 accumulates onto MU
+                mbar_wait(&B.s_next, c & 1, abort);      // S16 of this chunk
                 tc_fence_after();
-                for (int s = 0; s < 8; ++s) {   // O1 = S16 Q^T  (S16 still holds this chunk's S)
-                    const uint32_t off = (s >> 2) * kKBlk + 64 * 128 + (s & 3) * 32;
-                    mma_ts(tbase + kColO1, tbase + kColS16 + s * 8, sdesc_sw128(kqb + off, 16, 1024),
-                           id64, s > 0);
+                for (int s = s0; s < s0 + 4; ++s)   // M2: U(1|2) (+)= S16 W'^T over this a half
+                    mma_ts(tbase + ucol, tbase + kColS16 + s * 8,
+                           sdesc_sw128(dsm + kItemW + s * 16 * 128, 8192, 1024), id64bmn,
+                           isA || s > s0);
+                mma_commit(&B.u_full);
+                if (isA) {
+                    mbar_wait(&B.u2_full, c & 1, abort);     // U16, U16k in TMEM
+                    tc_fence_after();
+                    for (int s = 0; s < 4; ++s)   // M6: S += U16k K  (K MN-major: 2 blocks of 64 keys)
+                        mma_ts(tbase + kColS32, tbase + kColU16k + s * 8,
+                               sdesc_sw128(kqb + s * 16 * 128, kKBlk, 1024), id128bmn, 1);
+                    mma_commit(&B.s_full);
+                    mbar_wait(&B.o_free, c & 1, abort);      // the last chunk's O read out
+                    tc_fence_after();
+                    for (int s = 0; s < 4; ++s)   // O2 = U16 P^T
+                        mma_ts(tbase + kColO2, tbase + kColU16 + s * 8,
+                               sdesc_sw128(dsm + kItemP + s * 32, 16, 1024), id64, s > 0);
+                    mma_commit(&B.o2_full);
+                    mbar_wait(&B.o1_full, c & 1, abort);     // B's reads of these stages are done
+                    mma_commit(&B.kq_empty[sk]);
+                    mma_commit(&B.d_empty[sd]);
+                } else {
+                    mbar_wait(&B.u_full, c & 1, abort);      // M2 done: E2 runs, the pipe is free
+                    mbar_wait(&B.o_free, c & 1, abort);      // the last chunk's O read out
+                    tc_fence_after();
+                    for (int s = 0; s < 8; ++s) {   // O1 = S16 Q^T  (S16 still holds this chunk's S)
+                        const uint32_t off = (s >> 2) * kKBlk + 64 * 128 + (s & 3) * 32;
+                        mma_ts(tbase + kColO1, tbase + kColS16 + s * 8, sdesc_sw128(kqb + off, 16, 1024),
+                               id64, s > 0);
+                    }
+                    mma_commit(&B.o1_full);
+                    mbar_wait(&B.s_full, c & 1, abort);      // M6 done (and E2 has read U1)
+                    if (c + 1 < nch) issue_mu(c + 1);
                 }
-                mma_commit(&B.o1_done);
-                mbar_wait(&B.s_full, c & 1, abort);      // M6 done (U16 ready long since)
-                tc_fence_after();
-                for (int s = 0; s < 4; ++s)   // O2 = U16 P^T
-                    mma_ts(tbase + kColO2, tbase + kColU16 + s * 8,
-                           sdesc_sw128(dsm + kItemP + s * 32, 16, 1024), id64, s > 0);
-                mma_commit(&B.o_full);
-                mma_commit(&B.kq_empty[sk]);             // every MMA on these stages is done
-                mma_commit(&B.d_empty[sd]);
-                if (c + 1 < nch) issue_mu(c + 1);
             }
-            mma_commit(&B.done_b);
+            mma_commit(isA ? &B.done_a : &B.done_b);
             int z = 0;
-            mbar_wait(&B.done_b, 0, &z);
+            mbar_wait(isA ? &B.done_a : &B.done_b, 0, &z);
         }
         __syncwarp();
     } else {
         // ------------------------------------------- epilogues (2 warpgroups)
-        const int hf = (warp - 2) >> 2;           // column half of S, U and O
+        const int et = tid - 64;                  // 0 .. 255
+        const int hf = et >> 7;                   // column half of S, U and O
         const int q4 = warp & 3;
         const int b = q4 * 32 + lane;            // value row of the state
         const uint32_t lrow = tmem_addr(tbase, q4 * 32, 0);
@@ -608,22 +614,24 @@ chain_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
             const int64_t c0 = s_start + (int64_t)c * C;
             const bool last = c == nch - 1;
             const int n = I.n;
-            // ---- E2: this half of U -> U16 = bf16(U) and U16k = bf16(U diag(ks))
+            // ---- E2: U = U1 + U2 (this half) -> U16 = bf16(U), U16k = bf16(U diag(ks))
             mbar_wait(&B.u_full, c & 1, abort);
             tc_fence_after();
             {
-                uint32_t u[32], uu[16], uk[16];
-                tmem_ld32(lrow + kColU + 32 * hf, u);
+                uint32_t u1[32], u2[32], uu[16], uk[16];
+                tmem_ld32x2(lrow + kColU1 + 32 * hf, lrow + kColU2 + 32 * hf, u1, u2);
                 const float4 *ks4 = reinterpret_cast<const float4 *>(I.ks + 32 * hf);
 #pragma unroll
                 for (int q = 0; q < 8; ++q) {
                     const float4 f = ks4[q];
-                    const float u0 = __uint_as_float(u[4 * q]), u1 = __uint_as_float(u[4 * q + 1]);
-                    const float u2 = __uint_as_float(u[4 * q + 2]), u3 = __uint_as_float(u[4 * q + 3]);
-                    uu[2 * q] = pack_bf16(u0, u1);
-                    uu[2 * q + 1] = pack_bf16(u2, u3);
-                    uk[2 * q] = pack_bf16(u0 * f.x, u1 * f.y);
-                    uk[2 * q + 1] = pack_bf16(u2 * f.z, u3 * f.w);
+                    const float x0 = __uint_as_float(u1[4 * q]) + __uint_as_float(u2[4 * q]);
+                    const float x1 = __uint_as_float(u1[4 * q + 1]) + __uint_as_float(u2[4 * q + 1]);
+                    const float x2 = __uint_as_float(u1[4 * q + 2]) + __uint_as_float(u2[4 * q + 2]);
+                    const float x3 = __uint_as_float(u1[4 * q + 3]) + __uint_as_float(u2[4 * q + 3]);
+                    uu[2 * q] = pack_bf16(x0, x1);
+                    uu[2 * q + 1] = pack_bf16(x2, x3);
+                    uk[2 * q] = pack_bf16(x0 * f.x, x1 * f.y);
+                    uk[2 * q + 1] = pack_bf16(x2 * f.z, x3 * f.w);
                 }
                 tmem_st16(lrow + kColU16k + 16 * hf, uk);
                 tmem_st16(lrow + kColU16 + 16 * hf, uu);
@@ -634,11 +642,11 @@ chain_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
             // ---- E3a: S -> bf16 operand copy first (the next chunk's M2 waits
             //      on it), then the fp32 state pre-scaled by the next decay
             mbar_wait(&B.s_full, c & 1, abort);
-            mbar_wait(&B.o1_done, c & 1, abort);     // O1 has read the old S16
+            mbar_wait(&B.o1_full, c & 1, abort);     // O1 has read the old S16
             tc_fence_after();
             uint32_t sv[64];
-            tmem_ld32(s32, *reinterpret_cast<uint32_t(*)[32]>(sv));
-            tmem_ld32(s32 + 32, *reinterpret_cast<uint32_t(*)[32]>(sv + 32));
+            tmem_ld32x2(s32, s32 + 32, *reinterpret_cast<uint32_t(*)[32]>(sv),
+                        *reinterpret_cast<uint32_t(*)[32]>(sv + 32));
             if (!last) {
 #pragma unroll
                 for (int cc = 0; cc < 64; cc += 32) {
@@ -668,33 +676,59 @@ chain_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
                         __uint_as_float(sv[j + 2]), __uint_as_float(sv[j + 3]));
             }
             // ---- o = diag(sq) O1 + O2 for rows 32 hf .. 32 hf + 31
-            mbar_wait(&B.o_full, c & 1, abort);
+            mbar_wait(&B.o2_full, c & 1, abort);
             tc_fence_after();
             uint32_t o1[32], o2[32];
-            tmem_ld32(lrow + kColO1 + 32 * hf, o1);
-            tmem_ld32(lrow + kColO2 + 32 * hf, o2);
+            tmem_ld32x2(lrow + kColO1 + 32 * hf, lrow + kColO2 + 32 * hf, o1, o2);
             tmem_wait_st();
             tc_fence_before();
             mbar_arrive(&B.o_free);
             {
-                const int64_t ostride = (int64_t)hv * DH;
-                __nv_bfloat16 *orow = o + ((c0 + 32 * hf) * hv + h) * (int64_t)DH + b;
+                // o rows 32 hf + i of column b; a full tile leaves through TMA,
+                // a partial last one through plain stores
                 const float4 *sq4 = reinterpret_cast<const float4 *>(I.sq + 32 * hf);
+                if (32 * hf + 32 <= n) {
+                    __nv_bfloat16 *ot = reinterpret_cast<__nv_bfloat16 *>(sm + C_OFF_OT + (warp - 2) * kOTileBytes);
+                    if (lane == 0) bulk_wait_read_all();     // the last tile has left
+                    __syncwarp();
 #pragma unroll
-                for (int q = 0; q < 8; ++q) {
-                    const float4 f = sq4[q];
-                    const float fs[4] = {f.x, f.y, f.z, f.w};
+                    for (int q = 0; q < 8; ++q) {
+                        const float4 f = sq4[q];
+                        const float fs[4] = {f.x, f.y, f.z, f.w};
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const int i = 4 * q + e;
-                        if (32 * hf + i < n)
-                            orow[i * ostride] = __float2bfloat16_rn(
+                        for (int e = 0; e < 4; ++e) {
+                            const int i = 4 * q + e;
+                            ot[i * 32 + lane] = __float2bfloat16_rn(
                                 fmaf(fs[e], __uint_as_float(o1[i]), __uint_as_float(o2[i])));
+                        }
+                    }
+                    fence_async_smem();
+                    __syncwarp();
+                    if (lane == 0) {
+                        tma_store_2d(&tm_o, ot, h * DH + q4 * 32, (int)(c0 + 32 * hf));
+                        bulk_commit();
+                    }
+                } else {
+                    const int64_t ostride = (int64_t)hv * DH;
+                    __nv_bfloat16 *orow = o + ((c0 + 32 * hf) * hv + h) * (int64_t)DH + b;
+#pragma unroll
+                    for (int q = 0; q < 8; ++q) {
+                        const float4 f = sq4[q];
+                        const float fs[4] = {f.x, f.y, f.z, f.w};
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const int i = 4 * q + e;
+                            if (32 * hf + i < n)
+                                orow[i * ostride] = __float2bfloat16_rn(
+                                    fmaf(fs[e], __uint_as_float(o1[i]), __uint_as_float(o2[i])));
+                        }
                     }
                 }
             }
             mbar_arrive(&B.c_empty[c % kCStages]);
         }
+        if (lane == 0) bulk_wait_all();              // o tiles written before the exit
+        __syncwarp();
     }
     tc_fence_before();
     __syncthreads();
@@ -719,11 +753,12 @@ gdn_status prefill_split(const void *q, int64_t qs, const void *k, int64_t ks, c
                          void *o, void *ws, cudaStream_t s) {
     const int64_t items = psp::chunk_bound(n_tokens, n_seqs) * hv;
     if (items >= (1ll << 31)) return GDN_ERR_UNSUPPORTED;
-    CUtensorMap tq, tk, tv;
+    CUtensorMap tq, tk, tv, to;
     const uint64_t rows = (uint64_t)n_tokens;
     if (!encode_tmap_2d_bf16(&tq, q, (uint64_t)hqk * 128, rows, qs, 64, 64) ||
         !encode_tmap_2d_bf16(&tk, k, (uint64_t)hqk * 128, rows, ks, 64, 64) ||
-        !encode_tmap_2d_bf16(&tv, v, (uint64_t)hv * 128, rows, vs, 64, 64))
+        !encode_tmap_2d_bf16(&tv, v, (uint64_t)hv * 128, rows, vs, 64, 64) ||
+        !encode_tmap_2d_bf16(&to, o, (uint64_t)hv * 128, rows, (uint64_t)hv * 128, 32, 32, false))
         return GDN_ERR_LAUNCH;
     cudaError_t e = cudaFuncSetAttribute(psp::prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)psp::P_SMEM_BYTES);
@@ -744,7 +779,7 @@ gdn_status prefill_split(const void *q, int64_t qs, const void *k, int64_t ks, c
     st = launch_status();
     if (st != GDN_OK) return st;
     psp::chain_kernel<<<(unsigned)((int64_t)n_seqs * hv), psp::kChainKernelThreads,
-                        psp::C_SMEM_BYTES, s>>>(tq, tk, tv, cu, base, n_seqs, n_tokens, hv,
+                        psp::C_SMEM_BYTES, s>>>(tq, tk, tv, to, cu, base, n_seqs, n_tokens, hv,
                                                 hv / hqk, item_blocks, pool, n_slots, ii, fi,
                                                 (__nv_bfloat16 *)o);
     return launch_status();

@@ -72,7 +72,8 @@ extern "C" gdn_status gdn_prefill_chunked_static(
                 GDN_ERR_INVALID_ARG);
     GDN_REQUIRE(n_tokens > 0, GDN_ERR_UNSUPPORTED);
     GDN_REQUIRE(prefill_tc_supported(GDN_BF16, 128, 128, 64, q, q_row_stride, k, k_row_stride, v,
-                                     v_row_stride),
+                                     v_row_stride) &&
+                    ((uintptr_t)o & 15u) == 0,
                 GDN_ERR_UNSUPPORTED);
     GDN_REQUIRE(prefill_split_workspace(n_seqs, n_tokens, hv) <= GDN_PREFILL_STATIC_SCRATCH_BYTES,
                 GDN_ERR_TOO_LARGE);

@@ -19,7 +19,8 @@ static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 }
 
 bool encode_tmap_2d_bf16(CUtensorMap *map, const void *base, uint64_t cols, uint64_t rows,
-                         uint64_t row_stride_elems, uint32_t box_cols, uint32_t box_rows) {
+                         uint64_t row_stride_elems, uint32_t box_cols, uint32_t box_rows,
+                         bool swizzle128) {
     auto fn = encode_fn();
     if (!fn || rows == 0 || cols == 0) return false;
     cuuint64_t dims[2] = {cols, rows};
@@ -27,7 +28,8 @@ bool encode_tmap_2d_bf16(CUtensorMap *map, const void *base, uint64_t cols, uint
     cuuint32_t box[2] = {box_cols, box_rows};
     cuuint32_t estr[2] = {1, 1};
     CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims,
-                    strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                    strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                    swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
 }

@@ -203,8 +203,8 @@ size_t gdn_prefill_workspace_size(int32_t n_seqs, int64_t n_tokens,
  * allocates nothing.
  *
  * Arguments are those of gdn_prefill_chunked with dk = dv = 128, chunk = 64,
- * dtype = GDN_BF16 fixed (and no workspace); q, k, v must be 16-byte aligned
- * with row strides that are multiples of 8 elements.
+ * dtype = GDN_BF16 fixed (and no workspace); q, k, v and o must be 16-byte
+ * aligned, the q, k, v row strides multiples of 8 elements.
  * Capacity: gdn_prefill_workspace_size(n_seqs, n_tokens, hv, 128, 128, 64,
  * GDN_BF16) <= GDN_PREFILL_STATIC_SCRATCH_BYTES (16 MiB: 496 (chunk, V head)
  * items, i.e. ceil(n_tokens / 64) + n_seqs <= 15 at hv = 32),
