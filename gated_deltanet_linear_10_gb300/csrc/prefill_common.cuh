@@ -143,14 +143,21 @@ __device__ __forceinline__ void g_to_a_p(const uint32_t (&gr)[32], int p, int ch
     const int cb = 32 * chalf;
     const float coef = krow ? beta[i] * rk[i] : scale * rq[i];
     float e = (i > cb + 31) ? __expf(gam[i] - gam[cb + 31]) : 1.f;
+    const int lim = ok ? (krow ? i : i + 1) : 0;      // kept: j < lim
+    float rkc[32], alc[32];
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+        const float4 a4 = *reinterpret_cast<const float4 *>(rk + cb + 4 * q);
+        const float4 b4 = *reinterpret_cast<const float4 *>(alpha + cb + 4 * q);
+        rkc[4 * q] = a4.x; rkc[4 * q + 1] = a4.y; rkc[4 * q + 2] = a4.z; rkc[4 * q + 3] = a4.w;
+        alc[4 * q] = b4.x; alc[4 * q + 1] = b4.y; alc[4 * q + 2] = b4.z; alc[4 * q + 3] = b4.w;
+    }
     float v[32];
 #pragma unroll
     for (int jj = 31; jj >= 0; --jj) {
         const int j = cb + jj;
-        const bool on = j <= i;
-        const bool keep = ok && (krow ? j < i : on);
-        v[jj] = keep ? coef * e * rk[j] * __uint_as_float(gr[jj]) : 0.f;
-        if (on) e *= alpha[j];
+        v[jj] = j < lim ? coef * e * rkc[jj] * __uint_as_float(gr[jj]) : 0.f;
+        if (j <= i) e *= alc[jj];
     }
     if (krow) {
         float *arow = Af + i * kLd + cb;
@@ -257,6 +264,166 @@ __device__ __forceinline__ void ut_solve(const float *Af, float *Tf, float *Wb, 
         acc[0] = z.x; acc[1] = z.y; acc[2] = z.z; acc[3] = z.w;
         half_mac(acc, Af, 48, 32, Tf, 32, col, r, cg);
         half_finish(acc, Tf, wb, 3, col, r, cg);
+    } else {                   // meanwhile rows 0..47: 384 chunks over 192 threads
+        const int u = t - 64;
+        write_t12(u >> 2, 2 * (u & 3));
+        write_t12(u >> 2, 2 * (u & 3) + 1);
+    }
+    named_sync(1, 256);
+    if (t < 128) write_t12(48 + (t >> 3), t & 7);
+}
+
+// ------------------------------------------- UT solve, block products on
+// the warp-level tensor cores (mma.sync m16n8k8, tf32 in, fp32 accumulate).
+// The 16 x 16 blocks are below the 64-row minimum of tcgen05, and each warp
+// only ever needs a 16 x 8 half-block.  Fragment layouts (g = lane / 4,
+// t = lane % 4): A 16 x 8 row-major a0 = A[g][t], a1 = A[g+8][t],
+// a2 = A[g][t+4], a3 = A[g+8][t+4]; B 8 x 8 b0 = B[t][g], b1 = B[t+4][g];
+// C 16 x 8 c0 = C[g][2t], c1 = C[g][2t+1], c2 = C[g+8][2t], c3 = C[g+8][2t+1].
+__device__ __forceinline__ uint32_t tf32_of(float x) {
+    uint32_t r;
+    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
+    return r;
+}
+__device__ __forceinline__ void mma_tf32(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
+                                         uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+        "{%8,%9}, {%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+// acc += X[xr.., xc..] (16 x 16) * Y[yr.., col..col+7] (16 x 8); row stride kLd
+__device__ __forceinline__ void hm_mac(float (&acc)[4], const float *X, int xr, int xc,
+                                       const float *Y, int yr, int col, int lane) {
+    const int g = lane >> 2, t = lane & 3;
+#pragma unroll
+    for (int ks = 0; ks < 16; ks += 8) {
+        const uint32_t a[4] = {tf32_of(X[(xr + g) * kLd + xc + ks + t]),
+                               tf32_of(X[(xr + g + 8) * kLd + xc + ks + t]),
+                               tf32_of(X[(xr + g) * kLd + xc + ks + t + 4]),
+                               tf32_of(X[(xr + g + 8) * kLd + xc + ks + t + 4])};
+        mma_tf32(acc, a, tf32_of(Y[(yr + ks + t) * kLd + col + g]),
+                 tf32_of(Y[(yr + ks + t + 4) * kLd + col + g]));
+    }
+}
+// Tf[block row bi][col..col+7] = -T_ii * W, W = acc (16 x 8) staged in wb
+// (16 x 8 floats, this warp's own)
+__device__ __forceinline__ void hm_finish(const float (&acc)[4], float *Tf, float *wb, int bi,
+                                          int col, int lane) {
+    const int g = lane >> 2, t = lane & 3;
+    *reinterpret_cast<float2 *>(wb + g * 8 + 2 * t) = make_float2(acc[0], acc[1]);
+    *reinterpret_cast<float2 *>(wb + (g + 8) * 8 + 2 * t) = make_float2(acc[2], acc[3]);
+    __syncwarp();
+    float out[4] = {0.f, 0.f, 0.f, 0.f};
+    const float *Tii = Tf + 16 * bi * kLd + 16 * bi;
+#pragma unroll
+    for (int ks = 0; ks < 16; ks += 8) {
+        const uint32_t a[4] = {tf32_of(-Tii[g * kLd + ks + t]), tf32_of(-Tii[(g + 8) * kLd + ks + t]),
+                               tf32_of(-Tii[g * kLd + ks + t + 4]),
+                               tf32_of(-Tii[(g + 8) * kLd + ks + t + 4])};
+        mma_tf32(out, a, tf32_of(wb[(ks + t) * 8 + g]), tf32_of(wb[(ks + t + 4) * 8 + g]));
+    }
+    float *dst = Tf + (16 * bi) * kLd + col;
+    *reinterpret_cast<float2 *>(dst + g * kLd + 2 * t) = make_float2(out[0], out[1]);
+    *reinterpret_cast<float2 *>(dst + (g + 8) * kLd + 2 * t) = make_float2(out[2], out[3]);
+    __syncwarp();
+}
+
+// ut_solve with the off-diagonal levels on mma.sync (same blocking, same
+// outputs, tf32 rounding of the block-product operands).
+template <bool kT2>
+__device__ __forceinline__ void ut_solve_mma(const float *Af, float *Tf, float *Wb, int t, int pw,
+                                             int lane, const float *beta, const float *xs,
+                                             uint8_t *dst) {
+    float *Zs = Wb + 8 * 16 * kWbLd;          // Z30, 16 x 16
+    if (pw < 4) {   // diagonal blocks: forward substitution, exact fp32
+        const int r = lane >> 1, hh = lane & 1;
+        const int bb = pw;
+        const int R = 16 * bb + r;
+        float tv[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) tv[k] = (8 * hh + k == r) ? 1.f : 0.f;
+#pragma unroll
+        for (int m = 0; m < 15; ++m) {
+            const float a = Af[R * kLd + 16 * bb + m];
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+                const float vm = __shfl_sync(0xffffffffu, tv[k], 2 * m + hh);
+                if (r > m) tv[k] = fmaf(-a, vm, tv[k]);
+            }
+        }
+        *reinterpret_cast<float4 *>(Tf + R * kLd + 16 * bb + 8 * hh) = make_float4(tv[0], tv[1], tv[2], tv[3]);
+        *reinterpret_cast<float4 *>(Tf + R * kLd + 16 * bb + 8 * hh + 4) = make_float4(tv[4], tv[5], tv[6], tv[7]);
+    }
+    named_sync(1, 256);
+    const int g = lane >> 2, tq = lane & 3;
+    float *wb = Wb + pw * 16 * kWbLd;
+    float acc[4];
+    if (pw < 6) {              // level 1: T10, T21, T32
+        const int b0 = pw >> 1, half = pw & 1;
+        const int col = 16 * b0 + 8 * half;
+        acc[0] = acc[1] = acc[2] = acc[3] = 0.f;
+        hm_mac(acc, Af, 16 * (b0 + 1), 16 * b0, Tf, 16 * b0, col, lane);
+        hm_finish(acc, Tf, wb, b0 + 1, col, lane);
+    }
+    named_sync(1, 256);
+    if (pw < 6) {              // level 2: T20, T31 and Z30 = A30 T00 + A31 T10
+        const int item = pw >> 1, half = pw & 1;
+        acc[0] = acc[1] = acc[2] = acc[3] = 0.f;
+        if (item == 0) {
+            const int col = 8 * half;
+            hm_mac(acc, Af, 32, 0, Tf, 0, col, lane);
+            hm_mac(acc, Af, 32, 16, Tf, 16, col, lane);
+            hm_finish(acc, Tf, wb, 2, col, lane);
+        } else if (item == 1) {
+            const int col = 16 + 8 * half;
+            hm_mac(acc, Af, 48, 16, Tf, 16, col, lane);
+            hm_mac(acc, Af, 48, 32, Tf, 32, col, lane);
+            hm_finish(acc, Tf, wb, 3, col, lane);
+        } else {
+            const int col = 8 * half;
+            hm_mac(acc, Af, 48, 0, Tf, 0, col, lane);
+            hm_mac(acc, Af, 48, 16, Tf, 16, col, lane);
+            *reinterpret_cast<float2 *>(Zs + g * 16 + col + 2 * tq) = make_float2(acc[0], acc[1]);
+            *reinterpret_cast<float2 *>(Zs + (g + 8) * 16 + col + 2 * tq) = make_float2(acc[2], acc[3]);
+        }
+    }
+    named_sync(1, 256);
+    // block rows 0..2 are final now, block row 3 after level 3
+    auto write_t12 = [&](int i, int ch) {   // 8 columns: float4 loads of T, beta, xs
+        float tv[8], bv[8], xv[8];
+#pragma unroll
+        for (int h4 = 0; h4 < 2; ++h4) {
+            const float4 t4 = *reinterpret_cast<const float4 *>(Tf + i * kLd + ch * 8 + 4 * h4);
+            const float4 b4 = *reinterpret_cast<const float4 *>(beta + ch * 8 + 4 * h4);
+            tv[4 * h4] = t4.x; tv[4 * h4 + 1] = t4.y; tv[4 * h4 + 2] = t4.z; tv[4 * h4 + 3] = t4.w;
+            bv[4 * h4] = b4.x; bv[4 * h4 + 1] = b4.y; bv[4 * h4 + 2] = b4.z; bv[4 * h4 + 3] = b4.w;
+            if (kT2) {
+                const float4 x4 = *reinterpret_cast<const float4 *>(xs + ch * 8 + 4 * h4);
+                xv[4 * h4] = x4.x; xv[4 * h4 + 1] = x4.y; xv[4 * h4 + 2] = x4.z; xv[4 * h4 + 3] = x4.w;
+            }
+        }
+        uint32_t w1[4], w2[4];
+#pragma unroll
+        for (int e = 0; e < 8; e += 2) {
+            const float t0 = ch * 8 + e <= i ? tv[e] * bv[e] : 0.f;      // above the
+            const float t1 = ch * 8 + e + 1 <= i ? tv[e + 1] * bv[e + 1] : 0.f;   // diagonal: 0
+            w1[e / 2] = pack_bf16(t0, t1);
+            if (kT2) w2[e / 2] = pack_bf16(-t0 * xv[e], -t1 * xv[e + 1]);
+        }
+        *reinterpret_cast<uint4 *>(dst + sw128_chunk(i, ch)) = make_uint4(w1[0], w1[1], w1[2], w1[3]);
+        if (kT2)
+            *reinterpret_cast<uint4 *>(dst + kMatBytes + sw128_chunk(i, ch)) =
+                make_uint4(w2[0], w2[1], w2[2], w2[3]);
+    };
+    if (pw < 2) {              // level 3: T30 = -T33 (Z30 + A32 T20)
+        const int col = 8 * pw;
+        const float2 z0 = *reinterpret_cast<const float2 *>(Zs + g * 16 + col + 2 * tq);
+        const float2 z1 = *reinterpret_cast<const float2 *>(Zs + (g + 8) * 16 + col + 2 * tq);
+        acc[0] = z0.x; acc[1] = z0.y; acc[2] = z1.x; acc[3] = z1.y;
+        hm_mac(acc, Af, 48, 32, Tf, 32, col, lane);
+        hm_finish(acc, Tf, wb, 3, col, lane);
     } else {                   // meanwhile rows 0..47: 384 chunks over 192 threads
         const int u = t - 64;
         write_t12(u >> 2, 2 * (u & 3));

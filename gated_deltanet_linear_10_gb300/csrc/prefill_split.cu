@@ -110,9 +110,10 @@ struct PrepBars {
     uint32_t tmem_base;
     int abort;
 };
-// Shared memory.  The raw K|Q tile keeps its K rows (scaled in place to
-// K~ = -xs K for the W MMA); its Q halves become the P and T1 staging once
-// G is in TMEM.  After the solve, Af stages W'^T and Wb the row factors.
+// Shared memory.  The raw K|Q tile keeps its K rows for the W MMA; its Q
+// halves become the P and T1 staging once G is in TMEM.  T2 is written over
+// the dead rows of Af (the last solve level reads only rows 48..63), and
+// after the W MMA Af stages W'^T and Wb the row factors.
 constexpr uint32_t P_OFF_KQ = 0;
 constexpr uint32_t P_OFF_P = P_OFF_KQ + 64 * 128;              // Q rows of k-block 0
 constexpr uint32_t P_OFF_T1 = P_OFF_KQ + kKBlk + 64 * 128;     // Q rows of k-block 1
@@ -123,14 +124,17 @@ constexpr uint32_t kPWbBytes = (8 * 16 * kWbLd + 16 * 16) * 4;
 constexpr uint32_t P_OFF_SCAL = P_OFF_WB + kPWbBytes;
 constexpr uint32_t P_OFF_BARS = P_OFF_SCAL + (sizeof(PrepScal) + 127) / 128 * 128;
 constexpr uint32_t P_SMEM_BYTES = P_OFF_BARS + 128 + 1024;   // + slack to align to 1024
-constexpr uint32_t kPrepTmemCols = 64;                       // G, then W'^T
+constexpr uint32_t kPrepTmemCols = 128;                      // G = [K;Q][K;Q]^T, then W'^T
 static_assert(kItemWBytes <= C * kLd * 4 && sizeof(ItemScal) <= kPWbBytes, "staging");
+static_assert(P_OFF_T1 + kMatBytes == P_OFF_AF && kMatBytes <= 48 * kLd * 4,
+              "T2 lands on Af rows below 48");
 static_assert(sizeof(PrepBars) <= 128, "barrier block");
 static_assert(3 * (P_SMEM_BYTES + 1024) <= 233472, "three prep CTAs per SM");
 
 // One CTA per (chunk, V head) item.  Warp 0: TMEM, TMA of the raw K|Q tile,
-// M1 G = [K;Q] K^T, then MW W'^T = K~^T T1^T; warps 1..8: the prep
-// arithmetic (as in the fused kernel), then bulk stores of the item block.
+// M1 G = [K;Q] [K;Q]^T (its diagonal gives the row norms), then
+// MW W'^T = K^T T2^T; warps 1..8: the prep arithmetic, then bulk stores of
+// the item block.
 __global__ void __launch_bounds__(kPrepKernelThreads, 3)
 prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
             const float *__restrict__ g, const float *__restrict__ beta,
@@ -182,23 +186,23 @@ prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
             uint64_t *last = nullptr;   // the last commit: TMEM is freed once it completes
             if (mbar_wait(&B.kq_full, 0, abort)) {
                 tc_fence_after();
-                const uint32_t id64 = idesc_bf16(128, 64);
+                const uint32_t id128 = idesc_bf16(128, 128);
                 const uint32_t kb0 = smem_u32(kq);
                 for (int s = 0; s < 8; ++s) {
                     const uint32_t off = (s >> 2) * kKBlk + (s & 3) * 32;
                     mma_ss(tbase, sdesc_sw128(kb0 + off, 16, 1024), sdesc_sw128(kb0 + off, 16, 1024),
-                           id64, s > 0);
+                           id128, s > 0);
                 }
                 mma_commit(&B.g_full);
                 last = &B.g_full;
                 if (mbar_wait(&B.w_go, 0, abort)) {
-                    // MW: W'^T[a][i] = sum_j K~[j][a] T1[i][j]  (A = K~^T, MN-major)
+                    // MW: W'^T[a][i] = sum_j K[j][a] T2[i][j]  (A = K^T, MN-major)
                     tc_fence_after();
                     const uint32_t id64amn = idesc_bf16(128, 64, true, false);
-                    const uint32_t t1 = smem_u32(sm + P_OFF_T1);
+                    const uint32_t t2 = smem_u32(sm + P_OFF_AF);
                     for (int s = 0; s < 4; ++s)
                         mma_ss(tbase, sdesc_sw128(kb0 + s * 16 * 128, kKBlk, 1024),
-                               sdesc_sw128(t1 + s * 32, 16, 1024), id64amn, s > 0);
+                               sdesc_sw128(t2 + s * 32, 16, 1024), id64amn, s > 0);
                     mma_commit(&B.w_full);
                     last = &B.w_full;
                 }
@@ -230,14 +234,6 @@ prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
                 b1 = beta[(c0 + 2 * t + 1) * hv + h];
             }
         }
-        mbar_wait(&B.kq_full, 0, abort);
-        {
-            const float r = kq_row_inv_norm(kq, t, l2norm);
-            const int row = t >> 1;
-            if ((t & 1) == 0) {
-                if (row < C) S.rk[row] = r; else S.rq[row - C] = r;
-            }
-        }
         if (t < 32) {   // prefix sum of g, per-token decay alpha = exp(g)
             float x = g0 + g1;
 #pragma unroll
@@ -252,6 +248,31 @@ prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
             S.alpha[2 * t] = __expf(g0);
             S.alpha[2 * t + 1] = __expf(g1);
         }
+        mbar_wait(&B.g_full, 0, abort);
+        tc_fence_after();
+        uint32_t gr[32];
+        tmem_ld32(tmem_addr(tbase, q4 * 32, 32 * chalf), gr);
+        {   // inverse L2 norms from the diagonal of G: row p's own column, p for
+            // a K row, 64 + (p - 64) for a Q row (q . q); p % 32 is the lane
+            // (both conditions are warp-uniform)
+            float dg = 0.f;
+            bool own = p < C && (p >> 5) == chalf;
+            if (own) {
+#pragma unroll
+                for (int jj = 0; jj < 32; ++jj) dg = jj == lane ? __uint_as_float(gr[jj]) : dg;
+            }
+            if (p >= C && ((p - C) >> 5) == chalf) {
+                uint32_t gq[32];
+                tmem_ld32(tmem_addr(tbase, q4 * 32, C + 32 * chalf), gq);
+#pragma unroll
+                for (int jj = 0; jj < 32; ++jj) dg = jj == lane ? __uint_as_float(gq[jj]) : dg;
+                own = true;
+            }
+            if (own) {
+                const float r = l2norm ? rsqrtf(dg + kEps) : 1.f;
+                if (p < C) S.rk[p] = r; else S.rq[p - C] = r;
+            }
+        }
         named_sync(1, kPrepThreads);
         float ksv = 0.f, sqv = 0.f, gl = 0.f;
         if (t < C) {
@@ -263,28 +284,14 @@ prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
             ksv = ok ? __expf(gl - x) * S.rk[t] : 0.f;
             sqv = ok ? scale * ex * S.rq[t] : 0.f;
         }
-        mbar_wait(&B.g_full, 0, abort);
-        tc_fence_after();
-        {
-            uint32_t gr[32];
-            tmem_ld32(tmem_addr(tbase, q4 * 32, 32 * chalf), gr);
-            // the Q rows are dead from here on: P goes to k-block 0's
-            g_to_a_p(gr, p, chalf, n, S.beta, S.gam, S.alpha, S.rk, S.rq, scale, Af, sm + P_OFF_P);
-        }
+        // the Q rows are dead: P goes to k-block 0's
+        g_to_a_p(gr, p, chalf, n, S.beta, S.gam, S.alpha, S.rk, S.rq, scale, Af, sm + P_OFF_P);
         named_sync(1, kPrepThreads);
-        {   // K~_j = -xs_j K_j in place (4 of the 1024 16-byte chunks per thread)
-            const int j = t >> 2, kb = (t >> 1) & 1, ch0 = (t & 1) * 4;
-            const float f = -S.xs[j];
-#pragma unroll
-            for (int ch = ch0; ch < ch0 + 4; ++ch) {
-                uint4 *pk = reinterpret_cast<uint4 *>(kq + kb * kKBlk + sw128_chunk((uint32_t)j, ch));
-                *pk = scale_chunk(*pk, f);
-            }
-        }
-        ut_solve<false>(Af, Tf, Wb, t, pw, lane, S.beta, S.xs, sm + P_OFF_T1);
+        // T1 over k-block 1's Q rows, T2 over Af's dead rows
+        ut_solve_mma<true>(Af, Tf, Wb, t, pw, lane, S.beta, S.xs, sm + P_OFF_T1);
         fence_async_smem();
         tc_fence_before();
-        mbar_arrive(&B.w_go);                  // T1 and K~ are in place: MW may run
+        mbar_arrive(&B.w_go);                  // T2 is in place: MW may run
         // the solve scratch is dead: the row factors go to Wb, W'^T to Af
         ItemScal &I = *reinterpret_cast<ItemScal *>(Wb);
         if (t < C) {
@@ -320,7 +327,7 @@ prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
             bulk_store(item + kItemW, sm + P_OFF_AF, kItemWBytes);
             bulk_store(item + kItemOps, Wb, kItemScalCopy);
             bulk_commit();
-            bulk_wait_all();
+            bulk_wait_read_all();       // the shared memory may go; the writes complete on their own
         }
     }
     tc_fence_before();
@@ -727,7 +734,7 @@ chain_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
             }
             mbar_arrive(&B.c_empty[c % kCStages]);
         }
-        if (lane == 0) bulk_wait_all();              // o tiles written before the exit
+        if (lane == 0) bulk_wait_read_all();         // the staged o tiles have been read
         __syncwarp();
     }
     tc_fence_before();

@@ -110,10 +110,6 @@ __device__ __forceinline__ void bulk_store(void *dst, const void *src, uint32_t 
 __device__ __forceinline__ void bulk_commit() {
     asm volatile("cp.async.bulk.commit_group;" ::: "memory");
 }
-// Waits until every committed bulk store of this thread has completed.
-__device__ __forceinline__ void bulk_wait_all() {
-    asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
-}
 // 2-D tiled store of a box from shared memory (bulk-group completion).  x
 // times the element size must be a multiple of 16 B; never negative.
 __device__ __forceinline__ void tma_store_2d(const CUtensorMap *map, const void *src, int32_t x,
