@@ -99,6 +99,10 @@ def load_peaks():
             "source": "fallback"}
 
 
+SPLIT_SOURCES = ["gated_deltanet_linear_10_gb300/csrc/" + f for f in
+                 ("prefill_split.cu", "prefill_common.cuh", "tc.cuh", "common.cuh")]
+
+
 def profile_traffic(kernel_key: str, source_files):
     """DRAM bytes per launch recorded from an ncu capture in profiles/traffic.txt
     (lines: key bytes sha256-of-sources), or None when the kernel's sources
@@ -469,6 +473,8 @@ def bench_prefill(gdn, workloads, dev, flush, peaks, steps=5):
             "conv_kernel_ms": round(conv, 4),
             "conv_gbs": round(conv_bytes / (conv / 1e3) / 1e9, 1),
             "prefill_tflops": round(tf, 2),
+            "prep_kernel_traffic_bytes": profile_traffic("prep_kernel", SPLIT_SOURCES),
+            "chain_kernel_traffic_bytes": profile_traffic("chain_kernel", SPLIT_SOURCES),
             "prefill_frac_bf16_peak": round(tf / peaks["bf16_tflops"], 4),
             "flops_per_token": prefill_flops_per_token(d.hv, d.dk, d.dv, w.chunk)}
 
