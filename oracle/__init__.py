@@ -58,6 +58,8 @@ def lib():
         L.oracle_conv1d_seq.argtypes = [P, ctypes.c_long, ctypes.c_int, ctypes.c_int,
                                         P, P, P, ctypes.c_int, P, P]
         L.oracle_l2norm.argtypes = [P, ctypes.c_long, ctypes.c_int, ctypes.c_double, P]
+        L.oracle_gated_rmsnorm.argtypes = [P, P, P, ctypes.c_long, ctypes.c_int,
+                                           ctypes.c_double, P]
         L.oracle_gdn_recurrent.argtypes = [P, P, P, P, P, ctypes.c_long, ctypes.c_int,
                                            ctypes.c_int, ctypes.c_double, ctypes.c_int,
                                            ctypes.c_double, P, P, P]
@@ -131,6 +133,20 @@ def l2norm(x, eps=L2NORM_EPS):
     out = np.empty_like(flat)
     lib().oracle_l2norm(_p(flat), flat.shape[0], d, eps, _p(out))
     return out.reshape(x.shape)
+
+
+RMSNORM_EPS = 1e-6
+
+
+def gated_rmsnorm(o, z, weight, eps=RMSNORM_EPS):
+    """y = o / sqrt(mean(o^2) + eps) * weight * SiLU(z) over the last axis."""
+    o, z, w = _f64(o), _f64(z), _f64(weight)
+    d = o.shape[-1]
+    assert z.shape == o.shape and w.shape == (d,)
+    fo, fz = o.reshape(-1, d), z.reshape(-1, d)
+    y = np.empty_like(fo)
+    lib().oracle_gated_rmsnorm(_p(fo), _p(fz), _p(w), fo.shape[0], d, eps, _p(y))
+    return y.reshape(o.shape)
 
 
 def recurrent_chain(q, k, v, g, beta, S0=None, scale=1.0, l2norm_qk=True,

@@ -300,3 +300,23 @@ void oracle_gdn_chunked(const double *q, const double *k, const double *v,
     free(U);
     free(Snew);
 }
+
+/*
+ * Gated RMSNorm of the layer output ("gated RMSNorm", LightLLM blog on the
+ * Qwen3next kernels; the pages name the kernel without a formula).  Reading
+ * taken: per (token, V head) row of dv values,
+ *   y = o / sqrt(mean(o^2) + eps) * w * SiLU(z)
+ * normalising first, then gating.  o, z, y: [n][d]; w: [d].
+ */
+void oracle_gated_rmsnorm(const double *o, const double *z, const double *w,
+                          long n, int d, double eps, double *y)
+{
+    for (long i = 0; i < n; ++i) {
+        double ss = 0.0;
+        for (int j = 0; j < d; ++j)
+            ss += o[i * d + j] * o[i * d + j];
+        double inv = 1.0 / sqrt(ss / d + eps);
+        for (int j = 0; j < d; ++j)
+            y[i * d + j] = o[i * d + j] * inv * w[j] * silu(z[i * d + j]);
+    }
+}
