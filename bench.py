@@ -297,6 +297,7 @@ def run_ours(args):
     if not args.no_extras:
         extras["mtp"] = bench_mtp(gdn, workloads, dev, flush)
         extras["prefill"] = bench_prefill(gdn, workloads, dev, flush, peaks)
+        extras["decode_gated"] = bench_decode_gated(gdn, workloads, dev, flush)
 
     cpu = None
     if rank == 0:
@@ -393,6 +394,57 @@ def bench_mtp(gdn, workloads, dev, flush, steps=50):
             "gpu_launches_per_step": 5}
 
 
+def bench_decode_gated(gdn, workloads, dev, flush, steps=50):
+    """The decode step's recurrence with the gated RMSNorm on its output
+    (gdn_decode_recurrent_gated: at dv = 128 decode, then the norm kernel in
+    place) against the plain decode, and the norm kernel alone."""
+    w = workloads.decode(pool_device=dev)
+    d = w.dims
+    gen = torch.Generator().manual_seed(2024)
+    z = torch.randn(w.q.shape[0], d.hv, d.dv, generator=gen).to(w.q.dtype).to(dev)
+    nw = (torch.rand(d.dv, generator=gen) + 0.5).to(dev)
+    q, k, v = w.q.to(dev), w.k.to(dev), w.v.to(dev)
+    g, beta = gdn.gdn_gating(w.a.to(dev), w.b.to(dev), w.A_log.to(dev), w.dt_bias.to(dev))
+    spool, slots = w.state_pool, w.slots.to(dev)
+    o = torch.empty((q.shape[0], d.hv, d.dv), dtype=q.dtype, device=dev)
+    y = torch.empty_like(o)
+    stream = torch.cuda.current_stream(dev)
+
+    def timed(fn):
+        ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(steps)]
+        for _ in range(3):
+            fn()
+            flush.zero_()
+        torch.cuda.synchronize(dev)
+        torch.cuda._sleep(1_000_000)
+        for i in range(steps):
+            ev[i][0].record(stream)
+            fn()
+            ev[i][1].record(stream)
+            flush.zero_()
+        torch.cuda.synchronize(dev)
+        return sum(e[0].elapsed_time(e[1]) for e in ev) / steps
+
+    def plain():
+        gdn.gdn_decode_recurrent(q, k, v, g, beta, 1, spool, slots, scale=w.scale, o=o)
+
+    def gated():
+        gdn.gdn_decode_recurrent_gated(q, k, v, g, beta, 1, spool, slots, z, nw, 1e-6,
+                                       scale=w.scale, y=y)
+
+    def norm():
+        gdn.gdn_gated_rmsnorm(o, z, nw, 1e-6, y=y)
+
+    t_plain, t_gated, t_norm = timed(plain), timed(gated), timed(norm)
+    nbytes = 3 * o.numel() * o.element_size()       # o and z read, y written
+    del spool, w
+    return {"workload": "decode 256 x 1 token + gated RMSNorm (dv 128) of its output",
+            "gated_decode_ms": round(t_gated, 5), "plain_decode_ms": round(t_plain, 5),
+            "norm_kernel_ms": round(t_norm, 5),
+            "norm_kernel_gbs": round(nbytes / (t_norm / 1e3) / 1e9, 1),
+            "gated_tokens_per_s": round(256 / (t_gated / 1e3), 1)}
+
+
 def prefill_flops_per_token(hv, dk, dv, chunk):
     """Flops of the chunked form per token, full chunk x chunk tiles:
     hv * (6 dk dv + 2 C (3 dk + 2 dv))."""
@@ -450,6 +502,22 @@ def bench_prefill(gdn, workloads, dev, flush, peaks, steps=5):
     torch.cuda.synchronize(dev)
     pre_fused = sum(e[2].elapsed_time(e[3]) for e in ev) / steps
 
+    # the gated RMSNorm of the prefill output (standalone kernel, in place)
+    z = torch.randn(o.shape, generator=torch.Generator().manual_seed(7)).to(o.dtype).to(dev)
+    nw = torch.ones(d.dv, device=dev)
+    for _ in range(2):
+        gdn.gdn_gated_rmsnorm(o, z, nw, 1e-6, y=o)
+        flush.zero_()
+    torch.cuda.synchronize(dev)
+    for i in range(steps):
+        ev[i][0].record(stream)
+        gdn.gdn_gated_rmsnorm(o, z, nw, 1e-6, y=o)
+        ev[i][1].record(stream)
+        flush.zero_()
+    torch.cuda.synchronize(dev)
+    norm_ms = sum(e[0].elapsed_time(e[1]) for e in ev) / steps
+    norm_bytes = 3 * o.numel() * o.element_size()
+
     for _ in range(2):
         step()
         flush.zero_()
@@ -473,6 +541,8 @@ def bench_prefill(gdn, workloads, dev, flush, peaks, steps=5):
             "conv_kernel_ms": round(conv, 4),
             "conv_gbs": round(conv_bytes / (conv / 1e3) / 1e9, 1),
             "prefill_tflops": round(tf, 2),
+            "gated_norm_ms": round(norm_ms, 4),
+            "gated_norm_gbs": round(norm_bytes / (norm_ms / 1e3) / 1e9, 1),
             "prep_kernel_traffic_bytes": profile_traffic("prep_kernel", SPLIT_SOURCES),
             "chain_kernel_traffic_bytes": profile_traffic("chain_kernel", SPLIT_SOURCES),
             "prefill_frac_bf16_peak": round(tf / peaks["bf16_tflops"], 4),

@@ -28,7 +28,8 @@ EXPORTS = (
     "gdn_status_string", "gdn_version", "gdn_last_cuda_error", "gdn_gating",
     "causal_conv1d_fwd", "causal_conv1d_update", "gdn_prefill_chunked",
     "gdn_prefill_workspace_size", "gdn_decode_recurrent", "gdn_state_snapshot",
-    "gdn_get_device_status", "gdn_prefill_chunked_static",
+    "gdn_get_device_status", "gdn_prefill_chunked_static", "gdn_gated_rmsnorm",
+    "gdn_decode_recurrent_gated",
 )
 
 if not os.path.exists(LIB_PATH):
@@ -57,6 +58,10 @@ _SIGS = {
                              _i32, _i32, _f32, _i32, _vp, _i64, _vp, _vp, _vp, _i32, _vp],
     "gdn_state_snapshot": [_vp, _i64, _i64, _vp, _vp, _i32, _vp],
     "gdn_get_device_status": [ctypes.POINTER(ctypes.c_uint32), _i32, _vp],
+    "gdn_gated_rmsnorm": [_vp, _vp, _i64, _vp, _i64, _i32, _i32, _f32, _vp, _i32, _vp],
+    "gdn_decode_recurrent_gated": [_vp, _i64, _vp, _i64, _vp, _i64, _vp, _vp, _i32, _i32, _i32,
+                                   _i32, _i32, _i32, _f32, _i32, _vp, _i64, _vp, _vp, _vp, _i64,
+                                   _vp, _f32, _vp, _i32, _vp],
     "gdn_prefill_chunked_static": [_vp, _i64, _vp, _i64, _vp, _i64, _vp, _vp, _vp, _i32, _i64,
                                    _i32, _i32, _f32, _i32, _vp, _i64, _vp, _vp, _vp, _vp],
 }
@@ -311,6 +316,61 @@ def gdn_decode_recurrent(q, k, v, g, beta, tokens_per_seq, state_pool, state_ind
                                      _ptr(snap_indices), _ptr(o), _dtype_code(q),
                                      _stream(q.device)), "gdn_decode_recurrent")
     return o
+
+
+def gdn_decode_recurrent_gated(q, k, v, g, beta, tokens_per_seq, state_pool, state_indices, z,
+                               norm_weight, norm_eps=1e-6, snap_indices=None, scale=None,
+                               l2norm_qk=True, y=None):
+    """gdn_decode_recurrent with the gated RMSNorm fused into the output:
+    returns y = o / sqrt(mean(o^2) + eps) * norm_weight * SiLU(z), [N*tps, hv, dv].
+    z: [N*tps, hv, dv] (a view with a free row stride), norm_weight [dv] fp32."""
+    _cuda(q, k, v, g, beta, state_pool, state_indices, snap_indices, z, norm_weight)
+    T, hqk, dk = q.shape
+    hv, dv = v.shape[1], v.shape[2]
+    qs = _heads_view(q, hqk, dk, "q")
+    ks = _heads_view(k, hqk, dk, "k")
+    vs = _heads_view(v, hv, dv, "v")
+    zs = _heads_view(z, hv, dv, "z")
+    _need(q.dtype == k.dtype == v.dtype == z.dtype, "q, k, v, z: one dtype")
+    _need(norm_weight.dtype == torch.float32 and norm_weight.is_contiguous()
+          and norm_weight.shape == (dv,), "norm_weight: [dv] fp32")
+    _i32_vec(state_indices, "state_indices")
+    _i32_vec(snap_indices, "snap_indices")
+    N = state_indices.numel()
+    _need(T == N * tokens_per_seq and z.shape[0] == T, "rows != n_seqs * tokens_per_seq")
+    _need(g.shape == (T, hv) and beta.shape == (T, hv) and g.dtype == torch.float32
+          and beta.dtype == torch.float32 and g.is_contiguous() and beta.is_contiguous(), "g, beta")
+    _need(state_pool.dtype == torch.float32 and state_pool.is_contiguous()
+          and state_pool.shape[1:] == (hv, dv, dk), "state_pool: [slots, hv, dv, dk] fp32")
+    if snap_indices is not None:
+        _need(snap_indices.numel() == T, "snap_indices: [n_seqs, tps]")
+    scale = dk ** -0.5 if scale is None else scale
+    y = torch.empty((T, hv, dv), dtype=q.dtype, device=q.device) if y is None else y
+    _need(y.is_contiguous() and y.shape == (T, hv, dv), "y: [T, hv, dv] contiguous")
+    _check(_lib.gdn_decode_recurrent_gated(
+        _ptr(q), qs, _ptr(k), ks, _ptr(v), vs, _ptr(g), _ptr(beta), N, tokens_per_seq, hqk, hv,
+        dk, dv, float(scale), int(l2norm_qk), _ptr(state_pool), state_pool.shape[0],
+        _ptr(state_indices), _ptr(snap_indices), _ptr(z), zs, _ptr(norm_weight),
+        float(norm_eps), _ptr(y), _dtype_code(q), _stream(q.device)), "gdn_decode_recurrent_gated")
+    return y
+
+
+def gdn_gated_rmsnorm(o, z, weight, eps=1e-6, y=None):
+    """y = o / sqrt(mean(o^2) + eps) * weight * SiLU(z) per (token, head) row.
+    o [T, hv, dv] contiguous; z [T, hv, dv] (a view with a free row stride);
+    weight [dv] fp32.  y defaults to a new tensor; pass y=o for in place."""
+    _cuda(o, z, weight)
+    T, hv, dv = o.shape
+    _need(o.is_contiguous(), "o: contiguous")
+    zs = _heads_view(z, hv, dv, "z")
+    _need(z.shape == o.shape and z.dtype == o.dtype, "z: same shape and dtype as o")
+    _need(weight.dtype == torch.float32 and weight.is_contiguous() and weight.shape == (dv,),
+          "weight: [dv] fp32")
+    y = torch.empty_like(o) if y is None else y
+    _need(y.is_contiguous() and y.shape == o.shape and y.dtype == o.dtype, "y: like o")
+    _check(_lib.gdn_gated_rmsnorm(_ptr(o), _ptr(z), zs, _ptr(weight), T, hv, dv, float(eps),
+                                  _ptr(y), _dtype_code(o), _stream(o.device)), "gdn_gated_rmsnorm")
+    return y
 
 
 def gdn_state_snapshot(pool, src, dst):

@@ -11,6 +11,9 @@
 //   u   = beta (v - alpha S k)
 //   S  <- alpha S + u k^T
 //   o   = scale (alpha S_old q + u (k . q))   (= scale S_new q)
+// With GATED (one CTA per state only) the kernel writes
+// y = o / sqrt(mean(o^2) + eps) * w * SiLU(z) ("gated RMSNorm", same pages)
+// instead of o.
 #include "common.cuh"
 
 namespace gdn {
@@ -37,13 +40,14 @@ __device__ __forceinline__ float dot4(float4 a, float4 b) {
 
 // SPLIT CTAs share one (sequence, V head): CTA `part` owns the state rows
 // [part*rows, (part+1)*rows).  Fewer registers per thread, more resident CTAs.
-template <int DK, int SPLIT, typename T>
+template <int DK, int SPLIT, typename T, bool GATED>
 __global__ void __launch_bounds__(kDecThreads)
 decode_kernel(const T *__restrict__ q, int64_t qs, const T *__restrict__ k, int64_t ks,
               const T *__restrict__ v, int64_t vs, const float *__restrict__ g,
               const float *__restrict__ beta, int tps, int hv, int grp, int dv, float scale,
               int l2norm, float *__restrict__ pool, int64_t n_slots,
               const int32_t *__restrict__ idx, const int32_t *__restrict__ snap,
+              const T *__restrict__ z, int64_t zs, const float *__restrict__ nw, float neps,
               T *__restrict__ o) {
     constexpr int LPR = DK / 4;                     // lanes per state row
     constexpr int RPW = 32 / LPR;                   // rows per warp per pass
@@ -141,44 +145,65 @@ decode_kernel(const T *__restrict__ q, int64_t qs, const T *__restrict__ k, int6
         }
     }
     __syncthreads();
-    for (int e = threadIdx.x; e < tps * nr; e += kDecThreads) {
-        const int t = e / nr, r = e - t * nr;
-        Io<T>::store(o + (((int64_t)i * tps + t) * hv + h) * dv + r0 + r, o_s[t][r]);
+    if constexpr (GATED) {
+        static_assert(SPLIT == 1, "the norm needs every row of the state in this CTA");
+        __shared__ float ss_s[kMaxTps];
+        for (int t = warp; t < tps; t += kDecWarps) {
+            float a = 0.f;
+            for (int r = lane; r < nr; r += 32) a = fmaf(o_s[t][r], o_s[t][r], a);
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) a += __shfl_xor_sync(0xffffffffu, a, off);
+            if (lane == 0) ss_s[t] = a;
+        }
+        __syncthreads();
+        for (int e = threadIdx.x; e < tps * nr; e += kDecThreads) {
+            const int t = e / nr, r = e - t * nr;
+            const int64_t row = (int64_t)i * tps + t;
+            const float inv = rsqrtf(ss_s[t] / (float)dv + neps);
+            const float zz = Io<T>::load(z + row * zs + (int64_t)h * dv + r0 + r);
+            Io<T>::store(o + (row * hv + h) * dv + r0 + r, o_s[t][r] * inv * nw[r0 + r] * silu_f(zz));
+        }
+    } else {
+        for (int e = threadIdx.x; e < tps * nr; e += kDecThreads) {
+            const int t = e / nr, r = e - t * nr;
+            Io<T>::store(o + (((int64_t)i * tps + t) * hv + h) * dv + r0 + r, o_s[t][r]);
+        }
     }
 }
 
-template <int DK, typename T>
-static void launch_decode(const void *q, int64_t qs, const void *k, int64_t ks, const void *v,
-                          int64_t vs, const float *g, const float *beta, int n_seqs, int tps,
-                          int hqk, int hv, int dv, float scale, int l2norm, float *pool,
-                          int64_t n_slots, const int32_t *idx, const int32_t *snap, void *o,
-                          cudaStream_t s) {
+template <int DK, typename T, bool GATED>
+static cudaError_t launch_decode(const void *q, int64_t qs, const void *k, int64_t ks,
+                                 const void *v, int64_t vs, const float *g, const float *beta,
+                                 int n_seqs, int tps, int hqk, int hv, int dv, float scale,
+                                 int l2norm, float *pool, int64_t n_slots, const int32_t *idx,
+                                 const int32_t *snap, const void *z, int64_t zs, const float *nw,
+                                 float neps, void *o, cudaStream_t s) {
     const int64_t heads = (int64_t)n_seqs * hv;
     if (dv > 64) {     // two CTAs per state: half the registers, twice the CTAs in flight
-        decode_kernel<DK, 2, T><<<(unsigned)(heads * 2), kDecThreads, 0, s>>>(
+        decode_kernel<DK, 2, T, false><<<(unsigned)(heads * 2), kDecThreads, 0, s>>>(
             (const T *)q, qs, (const T *)k, ks, (const T *)v, vs, g, beta, tps, hv, hv / hqk, dv,
-            scale, l2norm, pool, n_slots, idx, snap, (T *)o);
+            scale, l2norm, pool, n_slots, idx, snap, nullptr, 0, nullptr, 0.f, (T *)o);
     } else {
-        decode_kernel<DK, 1, T><<<(unsigned)heads, kDecThreads, 0, s>>>(
+        decode_kernel<DK, 1, T, GATED><<<(unsigned)heads, kDecThreads, 0, s>>>(
             (const T *)q, qs, (const T *)k, ks, (const T *)v, vs, g, beta, tps, hv, hv / hqk, dv,
-            scale, l2norm, pool, n_slots, idx, snap, (T *)o);
+            scale, l2norm, pool, n_slots, idx, snap, (const T *)z, zs, nw, neps, (T *)o);
     }
+    return cudaGetLastError();
 }
 
 }  // namespace gdn
 
 using namespace gdn;
 
-extern "C" gdn_status gdn_decode_recurrent(const void *q, int64_t q_row_stride, const void *k,
-                                           int64_t k_row_stride, const void *v,
-                                           int64_t v_row_stride, const float *g,
-                                           const float *beta, int32_t n_seqs,
-                                           int32_t tokens_per_seq, int32_t hqk, int32_t hv,
-                                           int32_t dk, int32_t dv, float scale, int32_t l2norm_qk,
-                                           float *state_pool, int64_t n_slots,
-                                           const int32_t *state_indices,
-                                           const int32_t *snap_indices, void *o, int32_t dtype,
-                                           void *stream) {
+static gdn_status decode_entry(const void *q, int64_t q_row_stride, const void *k,
+                               int64_t k_row_stride, const void *v, int64_t v_row_stride,
+                               const float *g, const float *beta, int32_t n_seqs,
+                               int32_t tokens_per_seq, int32_t hqk, int32_t hv, int32_t dk,
+                               int32_t dv, float scale, int32_t l2norm_qk, float *state_pool,
+                               int64_t n_slots, const int32_t *state_indices,
+                               const int32_t *snap_indices, const void *z, int64_t z_row_stride,
+                               const float *norm_weight, float norm_eps, void *o, int32_t dtype,
+                               void *stream) {
     GDN_REQUIRE(dtype == GDN_F32 || dtype == GDN_BF16, GDN_ERR_INVALID_ARG);
     GDN_REQUIRE(n_seqs >= 0 && hqk > 0 && hv > 0 && n_slots >= 0, GDN_ERR_INVALID_ARG);
     GDN_REQUIRE(hv % hqk == 0, GDN_ERR_INVALID_ARG);
@@ -191,6 +216,13 @@ extern "C" gdn_status gdn_decode_recurrent(const void *q, int64_t q_row_stride, 
     GDN_REQUIRE(q_row_stride >= (int64_t)hqk * dk && k_row_stride >= (int64_t)hqk * dk &&
                     v_row_stride >= (int64_t)hv * dv,
                 GDN_ERR_INVALID_ARG);
+    const bool gated = z != nullptr;
+    GDN_REQUIRE(!gated || (norm_weight && norm_eps >= 0.f && z_row_stride >= (int64_t)hv * dv),
+                GDN_ERR_INVALID_ARG);
+    GDN_REQUIRE(!gated || dv <= 64 || dv == 128, GDN_ERR_UNSUPPORTED);   // the norm pass's sizes
+    GDN_REQUIRE(!gated || dv <= 64 ||
+                    (((uintptr_t)z % 16) == 0 && ((uintptr_t)o % 16) == 0 && z_row_stride % 4 == 0),
+                GDN_ERR_INVALID_ARG);                                      // and its alignment
     const int64_t align = dtype == GDN_F32 ? 16 : 8;      // load4 of q/k rows
     const int64_t elem = dtype == GDN_F32 ? 4 : 2;
     GDN_REQUIRE(((uintptr_t)q % align) == 0 && ((uintptr_t)k % align) == 0, GDN_ERR_INVALID_ARG);
@@ -198,10 +230,17 @@ extern "C" gdn_status gdn_decode_recurrent(const void *q, int64_t q_row_stride, 
                 GDN_ERR_INVALID_ARG);
     GDN_REQUIRE(((uintptr_t)state_pool % 16) == 0, GDN_ERR_INVALID_ARG);
     cudaStream_t s = (cudaStream_t)stream;
+    cudaError_t e = cudaSuccess;
 #define GDN_DEC(DK, T)                                                                          \
-    launch_decode<DK, T>(q, q_row_stride, k, k_row_stride, v, v_row_stride, g, beta, n_seqs,    \
-                         tokens_per_seq, hqk, hv, dv, scale, l2norm_qk, state_pool, n_slots,    \
-                         state_indices, snap_indices, o, s)
+    e = gated ? launch_decode<DK, T, true>(q, q_row_stride, k, k_row_stride, v, v_row_stride, g,  \
+                                           beta, n_seqs, tokens_per_seq, hqk, hv, dv, scale,     \
+                                           l2norm_qk, state_pool, n_slots, state_indices,        \
+                                           snap_indices, z, z_row_stride, norm_weight, norm_eps, \
+                                           o, s)                                                 \
+              : launch_decode<DK, T, false>(q, q_row_stride, k, k_row_stride, v, v_row_stride,   \
+                                            g, beta, n_seqs, tokens_per_seq, hqk, hv, dv, scale, \
+                                            l2norm_qk, state_pool, n_slots, state_indices,       \
+                                            snap_indices, nullptr, 0, nullptr, 0.f, o, s)
     if (dtype == GDN_BF16) {
         switch (dk) {
             case 16: GDN_DEC(16, __nv_bfloat16); break;
@@ -218,5 +257,48 @@ extern "C" gdn_status gdn_decode_recurrent(const void *q, int64_t q_row_stride, 
         }
     }
 #undef GDN_DEC
+    if (e != cudaSuccess) {
+        set_last_cuda_error(e);
+        return GDN_ERR_LAUNCH;
+    }
+    if (gated && dv > 64) {
+        // The state's rows are split over two CTAs.  Pairing them as a cluster
+        // to add their halves of sum(o^2) cost more (the pair waits on each
+        // other) than the separate norm pass below.
+        gdn_status st = launch_status();
+        if (st != GDN_OK) return st;
+        return gdn_gated_rmsnorm(o, z, z_row_stride, norm_weight,
+                                 (int64_t)n_seqs * tokens_per_seq, hv, dv, norm_eps, o, dtype,
+                                 stream);
+    }
     return launch_status();
+}
+
+extern "C" gdn_status gdn_decode_recurrent(const void *q, int64_t q_row_stride, const void *k,
+                                           int64_t k_row_stride, const void *v,
+                                           int64_t v_row_stride, const float *g,
+                                           const float *beta, int32_t n_seqs,
+                                           int32_t tokens_per_seq, int32_t hqk, int32_t hv,
+                                           int32_t dk, int32_t dv, float scale, int32_t l2norm_qk,
+                                           float *state_pool, int64_t n_slots,
+                                           const int32_t *state_indices,
+                                           const int32_t *snap_indices, void *o, int32_t dtype,
+                                           void *stream) {
+    return decode_entry(q, q_row_stride, k, k_row_stride, v, v_row_stride, g, beta, n_seqs,
+                        tokens_per_seq, hqk, hv, dk, dv, scale, l2norm_qk, state_pool, n_slots,
+                        state_indices, snap_indices, nullptr, 0, nullptr, 0.f, o, dtype, stream);
+}
+
+extern "C" gdn_status gdn_decode_recurrent_gated(
+    const void *q, int64_t q_row_stride, const void *k, int64_t k_row_stride, const void *v,
+    int64_t v_row_stride, const float *g, const float *beta, int32_t n_seqs,
+    int32_t tokens_per_seq, int32_t hqk, int32_t hv, int32_t dk, int32_t dv, float scale,
+    int32_t l2norm_qk, float *state_pool, int64_t n_slots, const int32_t *state_indices,
+    const int32_t *snap_indices, const void *z, int64_t z_row_stride, const float *norm_weight,
+    float norm_eps, void *y, int32_t dtype, void *stream) {
+    GDN_REQUIRE(z != nullptr, GDN_ERR_INVALID_ARG);
+    return decode_entry(q, q_row_stride, k, k_row_stride, v, v_row_stride, g, beta, n_seqs,
+                        tokens_per_seq, hqk, hv, dk, dv, scale, l2norm_qk, state_pool, n_slots,
+                        state_indices, snap_indices, z, z_row_stride, norm_weight, norm_eps, y,
+                        dtype, stream);
 }

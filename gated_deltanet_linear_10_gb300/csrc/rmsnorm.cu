@@ -1,0 +1,141 @@
+// Gated RMSNorm of the layer output ("gated RMSNorm", LightLLM blog on the
+// Qwen3next kernels; the pages name the kernel without a formula):
+//   y = o / sqrt(mean(o^2) + eps) * w * SiLU(z)
+// per (token, V head) row of dv values, normalising first, then gating.
+//
+// One warp per row, kNormRows rows per warp at a time; lane l holds dv / 32
+// consecutive elements (at least one), the mean square is a warp-shuffle
+// reduction.  HBM-bound: o and z read once, y written once (y may be o).
+// Grid-stride over rows, sized to the SMs.
+#include <algorithm>
+
+#include "common.cuh"
+
+namespace gdn {
+
+constexpr int kNormWarps = 8;
+
+__device__ __forceinline__ void store4(float *p, const float (&r)[4]) {
+    *reinterpret_cast<float4 *>(p) = make_float4(r[0], r[1], r[2], r[3]);
+}
+__device__ __forceinline__ void store4(__nv_bfloat16 *p, const float (&r)[4]) {
+    const __nv_bfloat162 lo = __floats2bfloat162_rn(r[0], r[1]), hi = __floats2bfloat162_rn(r[2], r[3]);
+    uint2 u;
+    u.x = *reinterpret_cast<const uint32_t *>(&lo);
+    u.y = *reinterpret_cast<const uint32_t *>(&hi);
+    *reinterpret_cast<uint2 *>(p) = u;
+}
+
+// Rows per warp and iteration: their loads are all issued before any
+// reduction (two at dv = 256 to stay within 64 registers).
+template <int DV> constexpr int norm_rows() { return DV >= 256 ? 2 : 4; }
+
+template <int DV, typename T>
+__global__ void __launch_bounds__(kNormWarps * 32, 4)   // 32 warps per SM: loads in flight
+gated_rmsnorm_kernel(const T *__restrict__ o, const T *__restrict__ z, int64_t zs,
+                     const float *__restrict__ w, uint32_t n_rows, uint32_t hv, float eps,
+                     T *__restrict__ y) {
+    constexpr int kNormRows = norm_rows<DV>();
+    constexpr int EPL = DV >= 128 ? DV / 32 : 4;     // elements per lane, 4-wide vectors
+    constexpr int LANES = DV / EPL;
+    const int lane = threadIdx.x & 31;
+    const bool on = lane < LANES;
+    const int j0 = lane * EPL;
+    float wv[EPL];
+#pragma unroll
+    for (int e = 0; e < EPL; ++e) wv[e] = on ? w[j0 + e] : 0.f;
+    const uint32_t stride = gridDim.x * kNormWarps * kNormRows;
+    for (uint32_t base = (blockIdx.x * kNormWarps + (threadIdx.x >> 5)) * kNormRows;
+         base < n_rows; base += stride) {
+        float ov[kNormRows][EPL], zv[kNormRows][EPL];
+#pragma unroll
+        for (int u = 0; u < kNormRows; ++u) {
+            const uint32_t row = base + u;
+            const bool ok = on && row < n_rows;
+            const uint32_t t = row / hv, h = row - t * hv;
+            const T *orow = o + (int64_t)row * DV;
+            const T *zrow = z + (int64_t)t * zs + (int64_t)h * DV;
+#pragma unroll
+            for (int e = 0; e < EPL; e += 4) {
+                const float4 a = ok ? load4(orow + j0 + e) : make_float4(0.f, 0.f, 0.f, 0.f);
+                const float4 b = ok ? load4(zrow + j0 + e) : make_float4(0.f, 0.f, 0.f, 0.f);
+                ov[u][e] = a.x; ov[u][e + 1] = a.y; ov[u][e + 2] = a.z; ov[u][e + 3] = a.w;
+                zv[u][e] = b.x; zv[u][e + 1] = b.y; zv[u][e + 2] = b.z; zv[u][e + 3] = b.w;
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < kNormRows; ++u) {
+            const uint32_t row = base + u;
+            float ss = 0.f;
+#pragma unroll
+            for (int e = 0; e < EPL; ++e) ss = fmaf(ov[u][e], ov[u][e], ss);
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
+            const float inv = rsqrtf(ss * (1.0f / DV) + eps);
+            if (on && row < n_rows) {
+                T *yrow = y + (int64_t)row * DV;
+#pragma unroll
+                for (int e = 0; e < EPL; e += 4) {
+                    float r[4];
+#pragma unroll
+                    for (int c = 0; c < 4; ++c)
+                        r[c] = ov[u][e + c] * inv * wv[e + c] * silu_f(zv[u][e + c]);
+                    store4(yrow + j0 + e, r);
+                }
+            }
+        }
+    }
+}
+
+template <int DV, typename T>
+static void launch_norm(const void *o, const void *z, int64_t zs, const float *w, int64_t rows,
+                        int hv, float eps, void *y, cudaStream_t s) {
+    int dev = 0, sms = 148;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    const int64_t per = kNormWarps * norm_rows<DV>();
+    const int64_t need = (rows + per - 1) / per;
+    const unsigned blocks = (unsigned)std::min<int64_t>(need, (int64_t)sms * 8);
+    gated_rmsnorm_kernel<DV, T><<<blocks, kNormWarps * 32, 0, s>>>(
+        (const T *)o, (const T *)z, zs, w, (uint32_t)rows, (uint32_t)hv, eps, (T *)y);
+}
+
+}  // namespace gdn
+
+using namespace gdn;
+
+extern "C" gdn_status gdn_gated_rmsnorm(const void *o, const void *z, int64_t z_row_stride,
+                                        const float *weight, int64_t n_tokens, int32_t hv,
+                                        int32_t dv, float eps, void *y, int32_t dtype,
+                                        void *stream) {
+    GDN_REQUIRE(dtype == GDN_F32 || dtype == GDN_BF16, GDN_ERR_INVALID_ARG);
+    GDN_REQUIRE(n_tokens >= 0 && hv > 0 && eps >= 0.f, GDN_ERR_INVALID_ARG);
+    GDN_REQUIRE(dv == 16 || dv == 32 || dv == 64 || dv == 128 || dv == 256, GDN_ERR_UNSUPPORTED);
+    if (n_tokens == 0) return GDN_OK;
+    GDN_REQUIRE(o && z && weight && y, GDN_ERR_INVALID_ARG);
+    GDN_REQUIRE(z_row_stride >= (int64_t)hv * dv, GDN_ERR_INVALID_ARG);
+    const int64_t elem = dtype == GDN_F32 ? 4 : 2;           // 4-element vector accesses
+    GDN_REQUIRE(((uintptr_t)o % (4 * elem)) == 0 && ((uintptr_t)z % (4 * elem)) == 0 &&
+                    ((uintptr_t)y % (4 * elem)) == 0 && (z_row_stride % 4) == 0,
+                GDN_ERR_INVALID_ARG);
+    const int64_t rows = n_tokens * hv;
+    GDN_REQUIRE(rows < (1ll << 31), GDN_ERR_UNSUPPORTED);
+    cudaStream_t s = (cudaStream_t)stream;
+#define GDN_NORM(DV, T) launch_norm<DV, T>(o, z, z_row_stride, weight, rows, hv, eps, y, s)
+#define GDN_NORM_DV(T)                          \
+    switch (dv) {                               \
+        case 16: GDN_NORM(16, T); break;        \
+        case 32: GDN_NORM(32, T); break;        \
+        case 64: GDN_NORM(64, T); break;        \
+        case 128: GDN_NORM(128, T); break;      \
+        default: GDN_NORM(256, T); break;       \
+    }
+    if (dtype == GDN_BF16) {
+        GDN_NORM_DV(__nv_bfloat16)
+    } else {
+        GDN_NORM_DV(float)
+    }
+#undef GDN_NORM_DV
+#undef GDN_NORM
+    return launch_status();
+}

@@ -262,6 +262,48 @@ gdn_status gdn_decode_recurrent(const void *q, int64_t q_row_stride,
                                 int32_t dtype, void *stream);
 
 /*
+ * Gated RMSNorm of the layer output ("gated RMSNorm", LightLLM blog on the
+ * Qwen3next kernels; the pages name the kernel without a formula).  Reading
+ * taken: per (token, V head) row of dv values
+ *   y = o / sqrt(mean(o^2) + eps) * weight * SiLU(z)     (normalise, then gate)
+ *   o, y: [n_tokens][hv][dv] contiguous, `dtype`; y may be o (in place).
+ *   z: n_tokens rows of [hv][dv], row stride z_row_stride elements (>= hv*dv),
+ *      `dtype`.  weight: [dv] fp32.  eps >= 0.
+ * o, z, y aligned to 4 elements and z_row_stride a multiple of 4 (vector
+ * accesses), else GDN_ERR_INVALID_ARG.
+ * Built: dv in {16, 32, 64, 128, 256}.  All pointers device, caller-owned.
+ */
+gdn_status gdn_gated_rmsnorm(const void *o, const void *z, int64_t z_row_stride,
+                             const float *weight, int64_t n_tokens, int32_t hv,
+                             int32_t dv, float eps, void *y, int32_t dtype,
+                             void *stream);
+
+/*
+ * gdn_decode_recurrent with the gated RMSNorm above fused into its output:
+ * writes y = RMSNorm(o) * norm_weight * SiLU(z) instead of o.  Arguments as
+ * gdn_decode_recurrent, plus z (rows i * tokens_per_seq + t, stride
+ * z_row_stride elements, `dtype`), norm_weight [dv] fp32 and norm_eps.
+ * Rows of sequences with no slot are written as zeros.  With dv <= 64 the
+ * norm runs inside the decode kernel (one CTA holds a whole state); with
+ * dv > 64 the state's rows are split over two CTAs and the call is decode
+ * followed by gdn_gated_rmsnorm in place (two launches, same result).
+ * Built: dv <= 64 or dv = 128.
+ */
+gdn_status gdn_decode_recurrent_gated(const void *q, int64_t q_row_stride,
+                                      const void *k, int64_t k_row_stride,
+                                      const void *v, int64_t v_row_stride,
+                                      const float *g, const float *beta,
+                                      int32_t n_seqs, int32_t tokens_per_seq,
+                                      int32_t hqk, int32_t hv, int32_t dk,
+                                      int32_t dv, float scale, int32_t l2norm_qk,
+                                      float *state_pool, int64_t n_slots,
+                                      const int32_t *state_indices,
+                                      const int32_t *snap_indices, const void *z,
+                                      int64_t z_row_stride,
+                                      const float *norm_weight, float norm_eps,
+                                      void *y, int32_t dtype, void *stream);
+
+/*
  * Whole-slot copy pool[dst[i]] <- pool[src[i]], bit for bit (the buffer copy
  * from source to destination indices of "[model] support Qwen3next", review
  * of the MTP buffer copy).  Used for the recurrent pool (slot_bytes =

@@ -115,3 +115,17 @@ def test_prefill_workspace_size(lib):
     item = (c - a) // 32
     assert c - a == 32 * item and item >= 3 * 64 * 128   # at least T1, T2, P in bf16
     assert a - 20 * 32 * item in (1024, 2048)          # header: n_seqs + 1 offsets, 1 KiB pages
+
+
+def test_gated_rmsnorm_host_checks(lib):
+    """Unsupported head size, misaligned z or stride, negative eps: refused
+    on the host before any launch."""
+    f = lib.gdn_gated_rmsnorm
+    f.argtypes = [V, V, I64, V, I64, I32, I32, F32, V, I32, V]
+    A = 1 << 20                                   # 16-byte aligned fake addresses
+    assert f(A, A, 512, A, 4, 4, 96, 1e-6, A, 1, None) == 2        # dv 96 not built
+    assert f(A, A + 2, 512, A, 4, 4, 128, 1e-6, A, 1, None) == 1    # z not 4-element aligned
+    assert f(A, A, 514, A, 4, 4, 128, 1e-6, A, 1, None) == 1        # stride not a multiple of 4
+    assert f(A, A, 512, A, 4, 4, 128, -1.0, A, 1, None) == 1        # eps < 0
+    assert f(A, A, 256, A, 4, 4, 128, 1e-6, A, 1, None) == 1        # stride < hv * dv
+    assert f(None, None, 512, None, 0, 4, 128, 1e-6, None, 1, None) == 0   # empty: no launch
