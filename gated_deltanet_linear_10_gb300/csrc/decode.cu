@@ -14,7 +14,10 @@
 // With GATED (one CTA per state only) the kernel writes
 // y = o / sqrt(mean(o^2) + eps) * w * SiLU(z) ("gated RMSNorm", same pages)
 // instead of o.
+#include <algorithm>
+
 #include "common.cuh"
+#include "tc.cuh"
 
 namespace gdn {
 
@@ -171,6 +174,154 @@ decode_kernel(const T *__restrict__ q, int64_t qs, const T *__restrict__ k, int6
     }
 }
 
+
+// ------------------------------------------------ streaming decode (T = 1)
+using namespace tc;
+
+// Persistent CTAs loop over (sequence, V head, row half) items of a 1-token
+// decode with dk = dv = 128.  Each item's 64 x 128 fp32 half-state is one
+// contiguous 32 KiB block of the pool: it is bulk-copied into one of two
+// shared-memory stages while the CTA computes the previous item, updated in
+// shared memory, and bulk-stored back, so a load and a store stay in flight
+// through the compute.  The next item's q, k, v, g, beta are loaded into
+// registers one item ahead.  Warp w updates rows 8w .. 8w + 7 of the item.
+constexpr int kStrRows = 64;
+constexpr uint32_t kStrBytes = kStrRows * 128 * 4;
+constexpr int kStrCtasPerSm = 3;
+
+template <typename T>
+struct StrIn {            // one item's inputs, as this thread needs them
+    float4 q4, k4;        // columns 4 lane .. 4 lane + 3
+    float v;              // row 8 warp + lane (lanes 0..7)
+    float g, b;
+};
+
+template <typename T>
+__global__ void __launch_bounds__(kDecThreads, kStrCtasPerSm)
+decode_stream_kernel(const T *__restrict__ q, int64_t qs, const T *__restrict__ k, int64_t ks,
+                     const T *__restrict__ v, int64_t vs, const float *__restrict__ g,
+                     const float *__restrict__ beta, int n_items, int hv, int grp, float scale,
+                     int l2norm, float *__restrict__ pool, int64_t n_slots,
+                     const int32_t *__restrict__ idx, T *__restrict__ o) {
+    extern __shared__ __align__(128) uint8_t smem_raw[];
+    __shared__ uint64_t full[2];
+    __shared__ float o_s[kStrRows];
+    __shared__ int abort_flag;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (threadIdx.x == 0) {
+        mbar_init(&full[0], 1);
+        mbar_init(&full[1], 1);
+        abort_flag = 0;
+        fence_mbar_init();
+    }
+    __syncthreads();
+    volatile int *abort = &abort_flag;
+
+    // item w: part = w % 2 (rows 64 part ..), (i, h) = w / 2
+    auto slot_of = [&](int w, int &i, int &h, int &part) -> int64_t {
+        part = w & 1;
+        const int ih = w >> 1;
+        i = ih / hv;
+        h = ih - i * hv;
+        return idx[i];
+    };
+    auto state_ptr = [&](int64_t slot, int h, int part) {
+        return pool + ((slot * hv + h) * (int64_t)128 + part * kStrRows) * 128;
+    };
+    auto load_in = [&](int i, int h, int part, StrIn<T> &in) {
+        const int hq = h / grp;
+        in.q4 = load4(q + (int64_t)i * qs + (int64_t)hq * 128 + 4 * lane);
+        in.k4 = load4(k + (int64_t)i * ks + (int64_t)hq * 128 + 4 * lane);
+        in.v = lane < 8 ? Io<T>::load(v + (int64_t)i * vs + (int64_t)h * 128 + part * kStrRows + 8 * warp + lane)
+                        : 0.f;
+        in.g = g[(int64_t)i * hv + h];
+        in.b = beta[(int64_t)i * hv + h];
+    };
+    int ph[2] = {0, 0};          // loads issued into each stage (same in every thread)
+
+    int w = blockIdx.x;
+    StrIn<T> cur;
+    if (w < n_items) {
+        int i, h, part;
+        const int64_t slot = slot_of(w, i, h, part);
+        if (slot >= 0 && slot < n_slots) {
+            if (threadIdx.x == 0) {
+                mbar_arrive_expect_tx(&full[0], kStrBytes);
+                bulk_load(smem_raw, state_ptr(slot, h, part), kStrBytes, &full[0]);
+            }
+            ++ph[0];
+        }
+        load_in(i, h, part, cur);
+    }
+    for (int n = 0; w < n_items; w += gridDim.x, ++n) {
+        const int s = n & 1;
+        int i, h, part;
+        const int64_t slot = slot_of(w, i, h, part);
+        const bool live = slot >= 0 && slot < n_slots;
+        if (slot >= n_slots && threadIdx.x == 0) flag_status(GDN_DEVSTAT_BAD_INDEX);
+        // prefetch the next item into the other stage (its previous store has
+        // been read: the wait below), and its inputs into registers
+        const int wn = w + gridDim.x;
+        StrIn<T> nxt = cur;
+        if (wn < n_items) {
+            int in_, hn, pn;
+            const int64_t sn = slot_of(wn, in_, hn, pn);
+            if (sn >= 0 && sn < n_slots) {
+                if (threadIdx.x == 0) {
+                    bulk_wait_read_all();
+                    mbar_arrive_expect_tx(&full[s ^ 1], kStrBytes);
+                    bulk_load(smem_raw + (s ^ 1) * kStrBytes, state_ptr(sn, hn, pn), kStrBytes,
+                              &full[s ^ 1]);
+                }
+                ++ph[s ^ 1];
+            }
+            load_in(in_, hn, pn, nxt);
+        }
+        float *st = reinterpret_cast<float *>(smem_raw + s * kStrBytes);
+        if (live) {
+            mbar_wait(&full[s], (ph[s] - 1) & 1, abort);
+            float4 q4 = cur.q4, k4 = cur.k4;
+            if (l2norm) {
+                const float qn = rsqrtf(row_sum<32>(dot4(q4, q4)) + kL2Eps);
+                const float kn = rsqrtf(row_sum<32>(dot4(k4, k4)) + kL2Eps);
+                q4 = make_float4(q4.x * qn, q4.y * qn, q4.z * qn, q4.w * qn);
+                k4 = make_float4(k4.x * kn, k4.y * kn, k4.z * kn, k4.w * kn);
+            }
+            const float kq = row_sum<32>(dot4(k4, q4));
+            const float alpha = expf(cur.g);
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                float4 *sp = reinterpret_cast<float4 *>(st + (8 * warp + j) * 128) + lane;
+                const float4 sv = *sp;
+                const float sk = row_sum<32>(dot4(sv, k4));
+                const float sq = row_sum<32>(dot4(sv, q4));
+                const float vj = __shfl_sync(0xffffffffu, cur.v, j);
+                const float u = cur.b * (vj - alpha * sk);
+                *sp = make_float4(fmaf(alpha, sv.x, u * k4.x), fmaf(alpha, sv.y, u * k4.y),
+                                  fmaf(alpha, sv.z, u * k4.z), fmaf(alpha, sv.w, u * k4.w));
+                if (lane == 0) o_s[8 * warp + j] = scale * fmaf(alpha, sq, u * kq);
+            }
+            fence_async_smem();
+        } else if (lane == 0) {
+#pragma unroll
+            for (int j = 0; j < 8; ++j) o_s[8 * warp + j] = 0.f;
+        }
+        __syncthreads();
+        if (live && threadIdx.x == 0) {
+            bulk_store(state_ptr(slot, h, part), st, kStrBytes);
+            bulk_commit();
+        }
+        if (threadIdx.x < kStrRows)
+            Io<T>::store(o + ((int64_t)i * hv + h) * 128 + part * kStrRows + threadIdx.x, o_s[threadIdx.x]);
+        __syncthreads();                 // o_s is rewritten by the next item
+        cur = nxt;
+    }
+    if (threadIdx.x == 0) {
+        bulk_wait_read_all();
+        if (abort_flag) flag_status(GDN_DEVSTAT_TIMEOUT);
+    }
+}
+
 template <int DK, typename T, bool GATED>
 static cudaError_t launch_decode(const void *q, int64_t qs, const void *k, int64_t ks,
                                  const void *v, int64_t vs, const float *g, const float *beta,
@@ -179,6 +330,22 @@ static cudaError_t launch_decode(const void *q, int64_t qs, const void *k, int64
                                  const int32_t *snap, const void *z, int64_t zs, const float *nw,
                                  float neps, void *o, cudaStream_t s) {
     const int64_t heads = (int64_t)n_seqs * hv;
+    if (DK == 128 && dv == 128 && tps == 1 && !snap && !GATED &&
+        ((uintptr_t)pool % 16) == 0) {   // the streaming kernel: state blocks through bulk copies
+        int dev = 0, sms = 148;
+        cudaGetDevice(&dev);
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        const int n_items = (int)(heads * 2);
+        const int grid = (int)std::min<int64_t>(n_items, (int64_t)sms * kStrCtasPerSm);
+        cudaError_t e = cudaFuncSetAttribute(decode_stream_kernel<T>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             (int)(2 * kStrBytes));
+        if (e != cudaSuccess) return e;
+        decode_stream_kernel<T><<<grid, kDecThreads, 2 * kStrBytes, s>>>(
+            (const T *)q, qs, (const T *)k, ks, (const T *)v, vs, g, beta, n_items, hv, hv / hqk,
+            scale, l2norm, pool, n_slots, idx, (T *)o);
+        return cudaGetLastError();
+    }
     if (dv > 64) {     // two CTAs per state: half the registers, twice the CTAs in flight
         decode_kernel<DK, 2, T, false><<<(unsigned)(heads * 2), kDecThreads, 0, s>>>(
             (const T *)q, qs, (const T *)k, ks, (const T *)v, vs, g, beta, tps, hv, hv / hqk, dv,
