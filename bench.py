@@ -36,8 +36,9 @@ sys.path.insert(0, ROOT)
 
 METRIC = "GDN decode tokens/s + state HBM GB/s; chunked prefill tokens/s; % roofline"
 UNIT = "tokens/s"
-DECODE_WORKLOAD = ("decode step: 256 sequences x 1 token, causal_conv1d_update (8192 ch, width 4) "
-                   "+ gdn_gating + gdn_decode_recurrent, 16 QK / 32 V heads, head_dim 128, "
+DECODE_WORKLOAD = ("decode step: 256 sequences x 1 token, causal conv update (8192 ch, width 4) "
+                   "+ gating + q/k L2 norm + recurrent decode in one kernel "
+                   "(gdn_decode_step_fused), 16 QK / 32 V heads, head_dim 128, "
                    "bf16 activations, fp32 state pool 1024 slots x 32 x 128 x 128")
 
 
@@ -168,6 +169,18 @@ class ClockSampler:
 
 # ------------------------------------------------------------- our kernels --
 
+def decode_step_bytes(n, hqk, hv, channels, width=4):
+    """Algorithmic bytes of the fused decode step (bf16 activations, dk = dv
+    = 128): the state read + written once, the conv state read + written,
+    x, a, b, o, the conv weights once, A_log / dt_bias, slot ids."""
+    state = 2 * n * hv * 128 * 128 * 4
+    conv_state = 2 * n * (width - 1) * channels * 2
+    x = n * channels * 2
+    ab = 2 * n * hv * 2
+    o = n * hv * 128 * 2
+    return state + conv_state + x + ab + o + channels * width * 2 + 2 * hv * 4 + n * 4
+
+
 def decode_kernel_bytes(n, hqk, hv, dk, dv, io_bytes):
     """Algorithmic bytes of one decode launch (1 token per sequence): the
     state read + written once, q/k per QK head, v, o, g, beta, slot ids."""
@@ -223,7 +236,15 @@ def run_ours(args):
 
     stream = torch.cuda.current_stream(dev)
 
-    def step(ev=None):
+    def step(ev=None):      # the decode step: one fused kernel
+        if ev is not None:
+            ev[0].record(stream)
+        gdn.gdn_decode_step_fused(x, conv_w, cpool, a, b, A_log, dt_bias, d.hqk, spool, slots,
+                                  scale=w.scale, o=o)
+        if ev is not None:
+            ev[1].record(stream)
+
+    def step_unfused(ev=None):   # the same step as three calls
         if ev is not None:
             ev[0].record(stream)
         gdn.causal_conv1d_update(x, 1, conv_w, cpool, slots, y=y)
@@ -257,18 +278,37 @@ def run_ours(args):
     barrier()
     wall = time.perf_counter() - t0
     clocks = sampler.stop()
-    step_ms = [e[0].elapsed_time(e[3]) for e in evs]
-    conv_ms = [e[0].elapsed_time(e[1]) for e in evs]
-    gate_ms = [e[1].elapsed_time(e[2]) for e in evs]
-    dec_ms = [e[2].elapsed_time(e[3]) for e in evs]
+    step_ms = [e[0].elapsed_time(e[1]) for e in evs]
     ms_step = sum(step_ms) / K
     ms_step_max = reduce_max(ms_step, dev)
     value = whole_job(N, ms_step_max / 1e3, world)
-    dec_avg = sum(dec_ms) / K
-    dec_bytes = decode_kernel_bytes(N, d.hqk, d.hv, d.dk, d.dv, 2)
+    dec_avg = ms_step                            # the step is the one kernel
+    dec_bytes = decode_step_bytes(N, d.hqk, d.hv, d.channels)
     achieved = dec_bytes / (dec_avg / 1e3) / 1e9
-    traffic = profile_traffic("decode_kernel", ["gated_deltanet_linear_10_gb300/csrc/decode.cu",
-                                                "gated_deltanet_linear_10_gb300/csrc/common.cuh"])
+    traffic = profile_traffic("decode_step_kernel",
+                              ["gated_deltanet_linear_10_gb300/csrc/" + f for f in
+                               ("decode_step.cu", "common.cuh", "tc.cuh")])
+
+    # ---- the same step as three calls (conv update, gating, decode)
+    Ku = min(K, 200)
+    evu = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(Ku)]
+    for _ in range(3):
+        step_unfused()
+        flush.zero_()
+    torch.cuda.synchronize(dev)
+    torch.cuda._sleep(2_000_000)
+    for i in range(Ku):
+        step_unfused(evu[i])
+        flush.zero_()
+    torch.cuda.synchronize(dev)
+    unf_dec = sum(e[2].elapsed_time(e[3]) for e in evu) / Ku
+    unfused = {"ms_per_step": round(sum(e[0].elapsed_time(e[3]) for e in evu) / Ku, 5),
+               "causal_conv1d_update_ms": round(sum(e[0].elapsed_time(e[1]) for e in evu) / Ku, 5),
+               "gdn_gating_ms": round(sum(e[1].elapsed_time(e[2]) for e in evu) / Ku, 5),
+               "gdn_decode_recurrent_ms": round(unf_dec, 5),
+               "decode_kernel_frac_hbm": round(
+                   decode_kernel_bytes(N, d.hqk, d.hv, d.dk, d.dv, 2) / (unf_dec / 1e3) / 1e9 /
+                   peaks["hbm_gbs"], 4)}
 
     # ---- end to end: host -> device inputs, the three calls, o -> host
     x_h = w.x.pin_memory()
@@ -311,19 +351,18 @@ def run_ours(args):
         "config": {"workload": DECODE_WORKLOAD, "global_batch": N * world, "seq_len": 1,
                    "io_dtype": "bf16", "l2": "flushed between steps (256 MiB write)",
                    "parallelism": f"replicas x{world}"},
-        "roofline": {"bound": "hbm", "kernel": "decode_kernel", "achieved": round(achieved, 1),
+        "roofline": {"bound": "hbm", "kernel": "decode_step_kernel", "achieved": round(achieved, 1),
                      "peak": peaks["hbm_gbs"], "unit": "GB/s",
                      "frac": round(achieved / peaks["hbm_gbs"], 4), "traffic": traffic,
                      "algorithmic_bytes": dec_bytes, "avg_launch_ms": round(dec_avg, 5),
                      "peak_source": peaks["source"]},
-        "kernels_ms": {"causal_conv1d_update": round(sum(conv_ms) / K, 5),
-                       "gdn_gating": round(sum(gate_ms) / K, 5),
-                       "gdn_decode_recurrent": round(dec_avg, 5)},
+        "kernels_ms": {"gdn_decode_step_fused": round(dec_avg, 5)},
         "state_gbs": round(achieved, 1),
+        "step_unfused": unfused,
         "e2e": {"value": round(whole_job(N, e2e_ms / 1e3, world), 1), "unit": UNIT,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "ms_per_step": round(e2e_ms, 5)},
-        "gpu_launches": 3 * K,
+        "gpu_launches": K,
         "clocks": clocks,
         "wall_s_timed": round(wall, 3),
         "cpu_baseline": cpu,

@@ -29,7 +29,7 @@ EXPORTS = (
     "causal_conv1d_fwd", "causal_conv1d_update", "gdn_prefill_chunked",
     "gdn_prefill_workspace_size", "gdn_decode_recurrent", "gdn_state_snapshot",
     "gdn_get_device_status", "gdn_prefill_chunked_static", "gdn_gated_rmsnorm",
-    "gdn_decode_recurrent_gated",
+    "gdn_decode_recurrent_gated", "gdn_decode_step_fused",
 )
 
 if not os.path.exists(LIB_PATH):
@@ -58,6 +58,8 @@ _SIGS = {
                              _i32, _i32, _f32, _i32, _vp, _i64, _vp, _vp, _vp, _i32, _vp],
     "gdn_state_snapshot": [_vp, _i64, _i64, _vp, _vp, _i32, _vp],
     "gdn_get_device_status": [ctypes.POINTER(ctypes.c_uint32), _i32, _vp],
+    "gdn_decode_step_fused": [_vp, _i64, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32,
+                              _f32, _vp, _i64, _vp, _vp, _vp],
     "gdn_gated_rmsnorm": [_vp, _vp, _i64, _vp, _i64, _i32, _i32, _f32, _vp, _i32, _vp],
     "gdn_decode_recurrent_gated": [_vp, _i64, _vp, _i64, _vp, _i64, _vp, _vp, _i32, _i32, _i32,
                                    _i32, _i32, _i32, _f32, _i32, _vp, _i64, _vp, _vp, _vp, _i64,
@@ -353,6 +355,41 @@ def gdn_decode_recurrent_gated(q, k, v, g, beta, tokens_per_seq, state_pool, sta
         _ptr(state_indices), _ptr(snap_indices), _ptr(z), zs, _ptr(norm_weight),
         float(norm_eps), _ptr(y), _dtype_code(q), _stream(q.device)), "gdn_decode_recurrent_gated")
     return y
+
+
+def gdn_decode_step_fused(x, conv_weight, conv_state_pool, a, b, A_log, dt_bias, hqk,
+                          state_pool, state_indices, scale=None, conv_bias=None, o=None):
+    """One decode step in one kernel: conv update + SiLU of the raw q|k|v
+    stream x [N, C], gating from a, b [N, hv], L2 norms and the recurrent
+    update.  Same result as causal_conv1d_update + gdn_gating +
+    gdn_decode_recurrent.  bf16, dk = dv = 128; both pools use state_indices.
+    Returns o [N, hv, 128]."""
+    _cuda(x, conv_weight, conv_state_pool, a, b, A_log, dt_bias, state_pool, state_indices,
+          conv_bias)
+    N, C = x.shape
+    hv = a.shape[1]
+    _need(x.dtype == torch.bfloat16 and x.stride(1) == 1, "x: bf16 rows")
+    _need(C == 2 * hqk * 128 + hv * 128, "x: 2*hqk*128 + hv*128 channels")
+    _need(conv_weight.shape == (C, 4) and conv_weight.is_contiguous()
+          and conv_weight.dtype == torch.bfloat16, "conv_weight: [C, 4] bf16")
+    _need(conv_state_pool.dtype == torch.bfloat16 and conv_state_pool.is_contiguous()
+          and conv_state_pool.shape[1:] == (3, C), "conv_state_pool: [slots, 3, C] bf16")
+    _need(a.shape == (N, hv) and b.shape == (N, hv) and a.is_contiguous() and b.is_contiguous()
+          and a.dtype == b.dtype == torch.bfloat16, "a, b: [N, hv] bf16")
+    _need(state_pool.dtype == torch.float32 and state_pool.is_contiguous()
+          and state_pool.shape[1:] == (hv, 128, 128), "state_pool: [slots, hv, 128, 128] fp32")
+    _need(conv_state_pool.shape[0] == state_pool.shape[0], "pools: same slot count")
+    _i32_vec(state_indices, "state_indices")
+    _need(state_indices.numel() == N, "state_indices: [N]")
+    scale = 128 ** -0.5 if scale is None else scale
+    o = torch.empty((N, hv, 128), dtype=torch.bfloat16, device=x.device) if o is None else o
+    _need(o.is_contiguous() and o.shape == (N, hv, 128), "o: [N, hv, 128] contiguous")
+    _check(_lib.gdn_decode_step_fused(
+        _ptr(x), x.stride(0), _ptr(conv_weight), _ptr(conv_bias), _ptr(conv_state_pool), _ptr(a),
+        _ptr(b), _ptr(A_log), _ptr(dt_bias), N, hqk, hv, float(scale), _ptr(state_pool),
+        state_pool.shape[0], _ptr(state_indices), _ptr(o), _stream(x.device)),
+        "gdn_decode_step_fused")
+    return o
 
 
 def gdn_gated_rmsnorm(o, z, weight, eps=1e-6, y=None):

@@ -29,6 +29,7 @@ gdn_status read_status_decode(uint32_t *out, int clear, cudaStream_t s);
 gdn_status read_status_prefill_simt(uint32_t *out, int clear, cudaStream_t s);
 gdn_status read_status_prefill_tc(uint32_t *out, int clear, cudaStream_t s);
 gdn_status read_status_prefill_split(uint32_t *out, int clear, cudaStream_t s);
+gdn_status read_status_decode_step(uint32_t *out, int clear, cudaStream_t s);
 gdn_status read_status_api(uint32_t *out, int clear, cudaStream_t s);
 
 #define GDN_STATUS_READER(fn, word)                                             \

@@ -304,6 +304,37 @@ gdn_status gdn_decode_recurrent_gated(const void *q, int64_t q_row_stride,
                                       void *y, int32_t dtype, void *stream);
 
 /*
+ * One decode step of the layer in one kernel (fusion of the
+ * "causal 1D convolution", "fused GDN gating" and "fused recurrent GDN"
+ * kernels the Qwen3next pages name): for each sequence i with one new token,
+ *   y   = SiLU(conv_bias + sum_w conv_weight[c][w] * [state; x_i][w])   (width 4)
+ *   q|k|v = split(y), q and k L2-normalised per head (eps 1e-6)
+ *   g = -exp(A_log[h]) softplus(a_ih + dt_bias[h]), beta = sigmoid(b_ih)
+ *   the gated delta rule update of slot state_indices[i], o = scale S q.
+ * Equal to causal_conv1d_update + gdn_gating + gdn_decode_recurrent.
+ *   x: [n_seqs] rows of the raw q|k|v stream, 2*hqk*128 + hv*128 channels,
+ *      row stride x_row_stride elements, bf16.
+ *   conv_weight: [channels][4] bf16 (8-byte aligned); conv_bias: [channels]
+ *      bf16 or NULL; conv_state_pool: [slots][3][channels] bf16, updated in
+ *      place in slot state_indices[i] (the same slot id as the state pool).
+ *   a, b: [n_seqs][hv] bf16; A_log, dt_bias: [hv] fp32.
+ *   state_pool: [n_slots][hv][128][128] fp32 (16-byte aligned).
+ *   o: [n_seqs][hv][128] bf16.
+ * A slot < 0 skips the sequence (o rows zero, neither pool touched); a slot
+ * >= n_slots is skipped the same way and sets GDN_DEVSTAT_BAD_INDEX.
+ * Built: bf16, dk = dv = 128, hv / hqk <= 2, conv width 4, SiLU on.
+ */
+gdn_status gdn_decode_step_fused(const void *x, int64_t x_row_stride,
+                                 const void *conv_weight, const void *conv_bias,
+                                 void *conv_state_pool, const void *a,
+                                 const void *b, const float *A_log,
+                                 const float *dt_bias, int32_t n_seqs,
+                                 int32_t hqk, int32_t hv, float scale,
+                                 float *state_pool, int64_t n_slots,
+                                 const int32_t *state_indices, void *o,
+                                 void *stream);
+
+/*
  * Whole-slot copy pool[dst[i]] <- pool[src[i]], bit for bit (the buffer copy
  * from source to destination indices of "[model] support Qwen3next", review
  * of the MTP buffer copy).  Used for the recurrent pool (slot_bytes =
