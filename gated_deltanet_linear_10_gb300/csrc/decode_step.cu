@@ -10,9 +10,10 @@
 // grp = hv / hqk V heads that read one QK head, as 2 * grp items of 64
 // state rows.  Per group, thread t computes the conv of one q|k channel
 // (t < 256) and of one of the group's v channels, writes both conv states,
-// and the group's q, k are normalised once in shared memory; then the items
-// stream their 32 KiB half-states through two shared-memory stages exactly as
-// the streaming decode kernel does.  Doing the conv of the shared q|k
+// and the group's q, k are normalised once in shared memory (double-buffered:
+// group G + 1's are computed after group G's first item, while its other
+// items stream); the items stream their 32 KiB half-states through two
+// shared-memory stages exactly as the streaming decode kernel does.  Doing the conv of the shared q|k
 // channels in one CTA is what makes the in-place conv state update safe:
 // no other CTA reads those channels.  The next group's raw inputs are loaded
 // into registers one group ahead.
@@ -104,8 +105,11 @@ decode_step_kernel(const __nv_bfloat16 *__restrict__ x, int64_t xs,
                    const int32_t *__restrict__ idx, __nv_bfloat16 *__restrict__ o) {
     extern __shared__ __align__(128) uint8_t smem_raw[];
     __shared__ uint64_t full[2];
-    __shared__ float q_s[128], k_s[128], v_s[128 * kMaxGrp], red_s[8], g_s[kMaxGrp], b_s[kMaxGrp];
-    __shared__ float o_s[kRows];
+    // per-group vectors, double-buffered: group G + 1's are computed while
+    // group G's items stream
+    __shared__ float q_s[2][128], k_s[2][128], v_s[2][128 * kMaxGrp], g_s[2][kMaxGrp],
+        b_s[2][kMaxGrp];
+    __shared__ float red_s[8], o_s[kRows];
     __shared__ int abort_flag;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int grp = hv / hqk;
@@ -120,23 +124,48 @@ decode_step_kernel(const __nv_bfloat16 *__restrict__ x, int64_t xs,
     __syncthreads();
     volatile int *abort = &abort_flag;
 
+    auto live_slot = [&](int64_t slot) { return slot >= 0 && slot < n_slots; };
     auto load_group = [&](int gi, GroupIn &in) {
         const int i = gi / hqk, hq = gi - i * hqk;
         in.slot = idx[i];
-        const bool live = in.slot >= 0 && in.slot < n_slots;
-        const int64_t cs = live ? in.slot : 0;
         const __nv_bfloat16 *xr = x + (int64_t)i * xs;
         const int qk_ch = tid < 128 ? hq * 128 + tid : nq + hq * 128 + (tid - 128);
         const int v_ch = 2 * nq + hq * grp * 128 + tid;          // grp * 128 <= 256 channels
-        if (live) {
-            load_conv(in.qk, xr, cw, cb, cpool, cs, C, qk_ch);
-            if (tid < grp * 128) load_conv(in.vv, xr, cw, cb, cpool, cs, C, v_ch);
+        if (live_slot(in.slot)) {
+            load_conv(in.qk, xr, cw, cb, cpool, in.slot, C, qk_ch);
+            if (tid < grp * 128) load_conv(in.vv, xr, cw, cb, cpool, in.slot, C, v_ch);
         }
         if (tid < grp) {
             const int h = hq * grp + tid;
             in.a = bf(a + (int64_t)i * hv + h);
             in.b = bf(b + (int64_t)i * hv + h);
         }
+    };
+    // conv + SiLU of this thread's q|k and v channels, their conv states, the
+    // gates and the q / k norms of group gi into buffer bb (all threads)
+    auto prologue = [&](int gi, const GroupIn &in, int bb) {
+        if (!live_slot(in.slot)) return;         // uniform over the CTA
+        const int hq = gi % hqk;
+        const float yq = conv_out(in.qk);
+        store_conv_state(in.qk, cpool, in.slot, C,
+                         tid < 128 ? hq * 128 + tid : nq + hq * 128 + (tid - 128));
+        const float ss = wsum<32>(yq * yq);       // q rows: warps 0..3, k rows: 4..7
+        if (lane == 0) red_s[warp] = ss;
+        if (tid < grp * 128) {
+            v_s[bb][tid] = conv_out(in.vv);
+            store_conv_state(in.vv, cpool, in.slot, C, 2 * nq + hq * grp * 128 + tid);
+        }
+        if (tid < grp) {
+            const int h = hq * grp + tid;
+            g_s[bb][tid] = -__expf(A_log[h]) * softplus_f(in.a + dt_bias[h]);
+            b_s[bb][tid] = 1.f / (1.f + __expf(-in.b));
+        }
+        __syncthreads();
+        const float nrm = rsqrtf((tid < 128 ? red_s[0] + red_s[1] + red_s[2] + red_s[3]
+                                            : red_s[4] + red_s[5] + red_s[6] + red_s[7]) +
+                                 kL2Eps);
+        if (tid < 128) q_s[bb][tid] = yq * nrm; else k_s[bb][tid - 128] = yq * nrm;
+        __syncthreads();                          // red_s is reused, the vectors are read
     };
     auto state_ptr = [&](int64_t slot, int h, int part) {
         return pool + ((slot * hv + h) * (int64_t)128 + part * kRows) * 128;
@@ -151,56 +180,34 @@ decode_step_kernel(const __nv_bfloat16 *__restrict__ x, int64_t xs,
     int ph[2] = {0, 0};
     int n = 0;                                  // items processed by this CTA
     int gi = blockIdx.x;
-    GroupIn cur;
+    GroupIn cur, nxt;
     if (gi < n_groups) {
         load_group(gi, cur);
-        if (cur.slot >= 0 && cur.slot < n_slots) {
+        if (live_slot(cur.slot)) {
             if (tid == 0) issue_state(gi, cur.slot, 0, 0);
             ++ph[0];
         }
+        prologue(gi, cur, 0);
     }
-    for (; gi < n_groups; gi += gridDim.x) {
+    for (int it = 0; gi < n_groups; gi += gridDim.x, ++it) {
         const int i = gi / hqk, hq = gi - i * hqk;
-        const bool live = cur.slot >= 0 && cur.slot < n_slots;
+        const int bb = it & 1;
+        const bool live = live_slot(cur.slot);
         if (cur.slot >= n_slots && tid == 0) flag_status(GDN_DEVSTAT_BAD_INDEX);
         const int gn = gi + gridDim.x;
-        GroupIn nxt = cur;
-        if (gn < n_groups) load_group(gn, nxt);   // one group ahead, into registers
-        // ---- conv + SiLU of this thread's q|k and v channels, conv states, gates
-        if (live) {
-            const float yq = conv_out(cur.qk);
-            store_conv_state(cur.qk, cpool, cur.slot, C,
-                             tid < 128 ? hq * 128 + tid : nq + hq * 128 + (tid - 128));
-            float ss = wsum<32>(yq * yq);            // q rows: warps 0..3, k rows: 4..7
-            if (lane == 0) red_s[warp] = ss;
-            if (tid < grp * 128) {
-                v_s[tid] = conv_out(cur.vv);
-                store_conv_state(cur.vv, cpool, cur.slot, C, 2 * nq + hq * grp * 128 + tid);
-            }
-            if (tid < grp) {
-                const int h = hq * grp + tid;
-                g_s[tid] = -__expf(A_log[h]) * softplus_f(cur.a + dt_bias[h]);
-                b_s[tid] = 1.f / (1.f + __expf(-cur.b));
-            }
-            __syncthreads();
-            const float nrm = rsqrtf((tid < 128 ? red_s[0] + red_s[1] + red_s[2] + red_s[3]
-                                                : red_s[4] + red_s[5] + red_s[6] + red_s[7]) +
-                                     kL2Eps);
-            if (tid < 128) q_s[tid] = yq * nrm; else k_s[tid - 128] = yq * nrm;
-        }
-        __syncthreads();
-        const float4 q4 = *reinterpret_cast<const float4 *>(q_s + 4 * lane);
-        const float4 k4 = *reinterpret_cast<const float4 *>(k_s + 4 * lane);
+        if (gn < n_groups) load_group(gn, nxt);   // into registers; used after item 0
+        const float4 q4 = *reinterpret_cast<const float4 *>(q_s[bb] + 4 * lane);
+        const float4 k4 = *reinterpret_cast<const float4 *>(k_s[bb] + 4 * lane);
         const float kq = wsum<32>(dot4(k4, q4));
         for (int kk = 0; kk < 2 * grp; ++kk, ++n) {
             const int s = n & 1;
             const int h = hq * grp + (kk >> 1), part = kk & 1;
-            // prefetch the next item's state (this group's next item, or the
-            // next group's first) into the other stage
-            {   // every thread keeps the same count of loads per stage
+            {   // prefetch the next item's state (this group's next item, or the
+                // next group's first) into the other stage; every thread keeps
+                // the same count of loads per stage
                 const bool in_group = kk + 1 < 2 * grp;
                 const int64_t sn = in_group ? cur.slot : (gn < n_groups ? nxt.slot : -1);
-                if (sn >= 0 && sn < n_slots) {
+                if (live_slot(sn)) {
                     if (tid == 0) {
                         bulk_wait_read_all();    // the stage's last store has read it
                         issue_state(in_group ? gi : gn, sn, in_group ? kk + 1 : 0, s ^ 1);
@@ -211,8 +218,8 @@ decode_step_kernel(const __nv_bfloat16 *__restrict__ x, int64_t xs,
             float *st = reinterpret_cast<float *>(smem_raw + s * kStageBytes);
             if (live) {
                 mbar_wait(&full[s], (ph[s] - 1) & 1, abort);
-                const float alpha = __expf(g_s[kk >> 1]);
-                const float bb = b_s[kk >> 1];
+                const float alpha = __expf(g_s[bb][kk >> 1]);
+                const float beta_ = b_s[bb][kk >> 1];
 #pragma unroll
                 for (int j = 0; j < 8; ++j) {
                     const int r = 8 * warp + j;
@@ -220,7 +227,7 @@ decode_step_kernel(const __nv_bfloat16 *__restrict__ x, int64_t xs,
                     const float4 sv = *sp;
                     const float sk = wsum<32>(dot4(sv, k4));
                     const float sq = wsum<32>(dot4(sv, q4));
-                    const float u = bb * (v_s[(kk >> 1) * 128 + part * kRows + r] - alpha * sk);
+                    const float u = beta_ * (v_s[bb][(kk >> 1) * 128 + part * kRows + r] - alpha * sk);
                     *sp = make_float4(fmaf(alpha, sv.x, u * k4.x), fmaf(alpha, sv.y, u * k4.y),
                                       fmaf(alpha, sv.z, u * k4.z), fmaf(alpha, sv.w, u * k4.w));
                     if (lane == 0) o_s[r] = scale * fmaf(alpha, sq, u * kq);
@@ -238,6 +245,7 @@ decode_step_kernel(const __nv_bfloat16 *__restrict__ x, int64_t xs,
             if (tid < kRows)
                 o[((int64_t)i * hv + h) * 128 + part * kRows + tid] = __float2bfloat16_rn(o_s[tid]);
             __syncthreads();
+            if (kk == 0 && gn < n_groups) prologue(gn, nxt, bb ^ 1);   // overlaps the streaming
         }
         cur = nxt;
     }
