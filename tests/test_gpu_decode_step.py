@@ -3,7 +3,8 @@ and the recurrent update in one kernel) through the C ABI, against the
 oracle's conv update -> gating -> decode chain: o and the updated states
 within the bf16 tolerance, the conv state pool bit for bit, untouched slots
 unchanged, at the full decode size (with a padding row) and at small shapes
-with one and two V heads per QK head and a conv bias."""
+with one and two V heads per QK head and a conv bias, and with many more
+groups than CTAs and padding rows between them."""
 import numpy as np
 import pytest
 import torch
@@ -74,4 +75,23 @@ def test_fused_step_small_with_bias(hqk, hv):
     pool0 = torch.randn(n_slots, hv, 128, 128, generator=g) * 0.02
     idx = torch.tensor([3, 0, -1, 11, 7, 1, 5], dtype=torch.int32)
     _check_step(x, conv_w, conv_b, cpool0, a, b, A_log, dt_bias, pool0, idx, hqk, hv,
+                128 ** -0.5)
+
+
+def test_fused_step_many_groups_with_padding():
+    """600 sequences of one QK / two V heads: each persistent CTA loops over
+    several groups, with a padding row (no slot) every seventh sequence."""
+    g = torch.Generator().manual_seed(4242)
+    hqk, hv, n, n_slots = 1, 2, 600, 700
+    C = 2 * hqk * 128 + hv * 128
+    x = torch.randn(n, C, generator=g).bfloat16()
+    conv_w = (torch.rand(C, 4, generator=g) - 0.5).bfloat16()
+    cpool0 = torch.randn(n_slots, 3, C, generator=g).bfloat16()
+    a = torch.randn(n, hv, generator=g).bfloat16()
+    b = torch.randn(n, hv, generator=g).bfloat16()
+    A_log, dt_bias = workloads.gating_params(g, hv, False)
+    pool0 = torch.randn(n_slots, hv, 128, 128, generator=g) * 0.02
+    idx = torch.randperm(n_slots, generator=g)[:n].to(torch.int32)
+    idx[::7] = -1
+    _check_step(x, conv_w, None, cpool0, a, b, A_log, dt_bias, pool0, idx, hqk, hv,
                 128 ** -0.5)
