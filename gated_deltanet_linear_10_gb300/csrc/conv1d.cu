@@ -5,7 +5,11 @@
 // Each thread owns 16 bytes of channels (8 bf16 or 4 fp32) and walks a run of
 // tokens, keeping the last width-1 inputs in registers, so every input row is
 // read from HBM once (plus width-1 rows at the head of each run).
+#include <algorithm>
+#include <type_traits>
+
 #include "common.cuh"
+#include "tc.cuh"
 
 namespace gdn {
 
@@ -13,31 +17,76 @@ GDN_DECLARE_STATUS_WORD(g_status_conv)
 GDN_STATUS_READER(read_status_conv, g_status_conv)
 
 constexpr int kConvThreads = 128;
-constexpr int kConvTokensPerThread = 8;
+constexpr int kConvTokensPerThread = 8;   // token run of a thread in the forward kernel
 
-template <typename T, int W>
+// SiLU(z) = z / (1 + e^-z) with the fast exponential and the fast division
+// (relative error a few ulp of fp32, far below the bf16 output rounding; for
+// z << 0 the quotient goes to 0).  The forward conv is issue-bound on this
+// arithmetic, so it takes the two-instruction form.
+__device__ __forceinline__ float silu_fast(float z) { return __fdividef(z, 1.0f + __expf(-z)); }
+
+// Four channels of T as one vector access (8 bytes of bf16, 16 of fp32).
+template <typename T> struct Vec4;
+template <> struct Vec4<float> {
+    using Raw = float4;
+    static __device__ __forceinline__ Raw raw(const float *p) { return *reinterpret_cast<const float4 *>(p); }
+    static __device__ __forceinline__ void unpack(const Raw &r, float *out) {
+        out[0] = r.x; out[1] = r.y; out[2] = r.z; out[3] = r.w;
+    }
+    static __device__ __forceinline__ void load(const float *p, float *out) { unpack(raw(p), out); }
+    static __device__ __forceinline__ void store(float *p, const float *in) {
+        *reinterpret_cast<float4 *>(p) = make_float4(in[0], in[1], in[2], in[3]);
+    }
+};
+template <> struct Vec4<__nv_bfloat16> {
+    using Raw = uint2;
+    static __device__ __forceinline__ Raw raw(const __nv_bfloat16 *p) { return *reinterpret_cast<const uint2 *>(p); }
+    static __device__ __forceinline__ void unpack(const Raw &r, float *out) {
+        const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&r.x));
+        const float2 b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&r.y));
+        out[0] = a.x; out[1] = a.y; out[2] = b.x; out[3] = b.y;
+    }
+    static __device__ __forceinline__ void load(const __nv_bfloat16 *p, float *out) { unpack(raw(p), out); }
+    static __device__ __forceinline__ void store(__nv_bfloat16 *p, const float *in) {
+        const __nv_bfloat162 lo = __floats2bfloat162_rn(in[0], in[1]), hi = __floats2bfloat162_rn(in[2], in[3]);
+        uint2 u;
+        u.x = *reinterpret_cast<const uint32_t *>(&lo);
+        u.y = *reinterpret_cast<const uint32_t *>(&hi);
+        *reinterpret_cast<uint2 *>(p) = u;
+    }
+};
+
+// V channels' taps and bias in registers.
+template <typename T, int W, int V = Vec16<T>::N>
 struct ConvTaps {
-    static constexpr int V = Vec16<T>::N;
     float w[W][V];
     float bias[V];
-    // The V x W taps of channels c0 .. c0+V-1 are 16 W contiguous bytes: W
-    // 16-byte loads (weight and bias 16-byte aligned, checked on the host).
+    // The V x W taps of channels c0 .. c0+V-1 are V W contiguous elements,
+    // read as 8-byte pieces (V W sizeof(T) is a multiple of 8 and c0 W
+    // sizeof(T) one of 8 for V >= 4; weight and bias are 16-byte aligned,
+    // checked on the host).
     __device__ __forceinline__ void load(const T *weight, const T *b, int c0) {
-        float e[V * W];
-        const uint4 *src = reinterpret_cast<const uint4 *>(weight + (int64_t)c0 * W);
+        constexpr int kPer8 = 8 / (int)sizeof(T);
+        constexpr int kPieces = V * W / kPer8;
+        static_assert((V * W) % kPer8 == 0, "taps are whole 8-byte pieces");
+        __align__(8) T e[V * W];
+        const uint2 *src = reinterpret_cast<const uint2 *>(weight + (int64_t)c0 * W);
 #pragma unroll
-        for (int u = 0; u < W; ++u) Vec16<T>::unpack(__ldg(src + u), e + u * V);
+        for (int u = 0; u < kPieces; ++u) *reinterpret_cast<uint2 *>(e + u * kPer8) = __ldg(src + u);
 #pragma unroll
         for (int v = 0; v < V; ++v)
 #pragma unroll
-            for (int j = 0; j < W; ++j) w[j][v] = e[v * W + j];
+            for (int j = 0; j < W; ++j) w[j][v] = to_f(e[v * W + j]);
         if (b) {
-            Vec16<T>::load(b + c0, bias);
+#pragma unroll
+            for (int v = 0; v < V; ++v) bias[v] = to_f(b[c0 + v]);
         } else {
 #pragma unroll
             for (int v = 0; v < V; ++v) bias[v] = 0.0f;
         }
     }
+    static __device__ __forceinline__ float to_f(float a) { return a; }
+    static __device__ __forceinline__ float to_f(__nv_bfloat16 a) { return __bfloat162float(a); }
     // out = act(bias + sum_j w[j] * e[t-(W-1)+j]); win holds e[t-(W-1) .. t-1].
     __device__ __forceinline__ void apply(const float (&win)[W - 1][V], const float *cur,
                                           int silu, float *out) const {
@@ -47,7 +96,7 @@ struct ConvTaps {
 #pragma unroll
             for (int j = 0; j < W - 1; ++j) acc = fmaf(w[j][v], win[j][v], acc);
             acc = fmaf(w[W - 1][v], cur[v], acc);
-            out[v] = silu ? silu_f(acc) : acc;
+            out[v] = silu ? silu_fast(acc) : acc;
         }
     }
 };
@@ -75,28 +124,39 @@ __device__ __forceinline__ int64_t history_slot(const int32_t *idx, const uint8_
     return s;
 }
 
-// Prefill: blockIdx.x = token run, blockIdx.y * blockDim.x + tid = channel group.
-template <typename T, int W>
+// Prefill: blockIdx.x = token run of R tokens, blockIdx.y * blockDim.x + tid
+// = group of 4 channels.  A thread keeps 4 channels' taps, its W-1 window
+// and its R input rows in registers (about 70 at R = 8 in bf16), so 8 warps
+// and more share an SM: the kernel is issue-bound on the conv + SiLU
+// arithmetic, not on HBM, when fewer warps hide its latencies.
+template <typename T, int W, int R>
 __global__ void __launch_bounds__(kConvThreads)
 conv_fwd_kernel(const T *__restrict__ x, int64_t x_stride, const T *__restrict__ weight,
                 const T *__restrict__ bias, const int32_t *__restrict__ cu, int n_seqs,
                 int64_t n_tokens, int C, const T *__restrict__ pool, int64_t n_slots,
                 const int32_t *__restrict__ idx, const uint8_t *__restrict__ has_init,
                 int silu, T *__restrict__ y) {
-    constexpr int V = Vec16<T>::N;
+    constexpr int V = 4;
+    using VT = Vec4<T>;
     const int c0 = (blockIdx.y * blockDim.x + threadIdx.x) * V;
     if (c0 >= C) return;
-    const int64_t t0 = (int64_t)blockIdx.x * kConvTokensPerThread;
+    const int64_t t0 = (int64_t)blockIdx.x * R;
     if (t0 >= n_tokens) return;
-    const int64_t t1 = min(t0 + (int64_t)kConvTokensPerThread, n_tokens);
+    const int64_t t1 = min(t0 + (int64_t)R, n_tokens);
 
-    // The token rows and taps do not depend on the sequence lookup: issue
-    // their loads first, so the binary search below overlaps them.
-    uint4 raw[kConvTokensPerThread];
+    // The token rows, the W-1 rows before the run (the window when the run
+    // does not start a sequence) and the taps do not depend on the sequence
+    // lookup: issue their loads first, so the binary search overlaps them.
+    typename VT::Raw raw[R], hraw[W - 1];
 #pragma unroll
-    for (int tt = 0; tt < kConvTokensPerThread; ++tt)
-        if (t0 + tt < t1) raw[tt] = *reinterpret_cast<const uint4 *>(x + (t0 + tt) * x_stride + c0);
-    ConvTaps<T, W> taps;
+    for (int tt = 0; tt < R; ++tt)
+        if (t0 + tt < t1) raw[tt] = VT::raw(x + (t0 + tt) * x_stride + c0);
+#pragma unroll
+    for (int r = 0; r < W - 1; ++r) {
+        const int64_t n = t0 - (W - 1) + r;
+        if (n >= 0) hraw[r] = VT::raw(x + n * x_stride + c0);
+    }
+    ConvTaps<T, W, V> taps;
     taps.load(weight, bias, c0);
 
     // first sequence i with cu[i+1] > t0
@@ -107,8 +167,7 @@ conv_fwd_kernel(const T *__restrict__ x, int64_t x_stride, const T *__restrict__
     }
     int i = lo;
     float win[W - 1][V];
-    // fast path: the whole run lies in one sequence, so every load is issued
-    // before the first use (8 token rows + the history rows in flight)
+    // fast path: the whole run lies in one sequence
     if (i < n_seqs) {
         const int64_t ss = cu[i], se = cu[i + 1];
         if (ss >= 0 && ss <= t0 && t1 <= se && se <= n_tokens) {
@@ -117,27 +176,28 @@ conv_fwd_kernel(const T *__restrict__ x, int64_t x_stride, const T *__restrict__
             for (int r = 0; r < W - 1; ++r) {
                 const int64_t n = t0 - (W - 1) + r;
                 if (n >= ss) {
-                    Vec16<T>::load(x + n * x_stride + c0, win[r]);
+                    VT::unpack(hraw[r], win[r]);
                 } else if (hs >= 0) {
-                    Vec16<T>::load(pool + (hs * (W - 1) + (W - 1) + (n - ss)) * C + c0, win[r]);
+                    VT::load(pool + (hs * (W - 1) + (W - 1) + (n - ss)) * C + c0, win[r]);
                 } else {
 #pragma unroll
                     for (int v = 0; v < V; ++v) win[r][v] = 0.0f;
                 }
             }
 #pragma unroll
-            for (int tt = 0; tt < kConvTokensPerThread; ++tt) {
+            for (int tt = 0; tt < R; ++tt) {
                 if (t0 + tt < t1) {
                     float cur[V], out[V];
-                    Vec16<T>::unpack(raw[tt], cur);
+                    VT::unpack(raw[tt], cur);
                     taps.apply(win, cur, silu, out);
-                    Vec16<T>::store(y + (t0 + tt) * C + c0, out);
+                    VT::store(y + (t0 + tt) * C + c0, out);
                     shift_in<W, V>(win, cur);
                 }
             }
             return;
         }
     }
+    // the run crosses a sequence boundary (or cu_seqlens is malformed)
     int64_t s_end = -1;
     for (int64_t t = t0; t < t1; ++t) {
         if (t >= s_end) {
@@ -157,10 +217,10 @@ conv_fwd_kernel(const T *__restrict__ x, int64_t x_stride, const T *__restrict__
             for (int r = 0; r < W - 1; ++r) {
                 const int64_t n = t - (W - 1) + r;
                 if (n >= s_start) {
-                    Vec16<T>::load(x + n * x_stride + c0, win[r]);
+                    VT::load(x + n * x_stride + c0, win[r]);
                 } else if (hs >= 0) {
                     const int64_t hr = (W - 1) + (n - s_start);   // history row, oldest first
-                    Vec16<T>::load(pool + (hs * (W - 1) + hr) * C + c0, win[r]);
+                    VT::load(pool + (hs * (W - 1) + hr) * C + c0, win[r]);
                 } else {
 #pragma unroll
                     for (int v = 0; v < V; ++v) win[r][v] = 0.0f;
@@ -168,11 +228,178 @@ conv_fwd_kernel(const T *__restrict__ x, int64_t x_stride, const T *__restrict__
             }
         }
         float cur[V], out[V];
-        Vec16<T>::load(x + t * x_stride + c0, cur);
+        VT::load(x + t * x_stride + c0, cur);
         taps.apply(win, cur, silu, out);
-        Vec16<T>::store(y + t * C + c0, out);
+        VT::store(y + t * C + c0, out);
         shift_in<W, V>(win, cur);
     }
+}
+
+// Prefill, TMA-staged (bf16, channels a multiple of 512): a persistent grid
+// of CTAs walks tiles of 32 tokens x 512 channels.  A tile's 32 input rows
+// and the 3 rows before them come into shared memory as two 2-D TMA boxes
+// of 256 channels x 35 rows (zero-filled outside the tensor), through a ring
+// of 2 stages on mbarriers (3 CTAs per SM), so the next tile is in flight
+// while this one is computed, whatever the registers.  256 threads: thread t
+// convolves channels 4 (t % 128) .. +3 over tokens 16 (t / 128) .. +15 of
+// the tile from shared memory (its window is in the staged rows too) and
+// stores y directly.
+// The kernel is bound by the latency of its conv + SiLU chains more than by
+// HBM: a tile that lies inside one sequence with its window staged (nearly
+// all) runs a branch-free loop over its 16 tokens, so the compiler can
+// interleave 64 independent chains per thread.  A CTA's tiles move forward
+// in tokens, so its sequence index only ever advances.
+constexpr int kTileTok = 32;
+constexpr int kTileCh = 512;                        // 128 channel threads x 4 channels
+constexpr int kTileHist = 3;                        // rows before the tile (W - 1 <= 3)
+constexpr int kTileRows = kTileTok + kTileHist;
+constexpr int kBoxCh = 256;                         // TMA box width (<= 256 elements)
+constexpr uint32_t kBoxBytes = kTileRows * kBoxCh * 2;
+constexpr uint32_t kTileBytes = 2 * kBoxBytes;
+constexpr int kTileStages = 2;
+constexpr int kTileCtasPerSm = 3;
+constexpr int kTileParts = 2;                       // token halves of a tile
+constexpr int kPartTok = kTileTok / kTileParts;
+constexpr int kTmaThreads = (kTileCh / 4) * kTileParts;
+
+template <int W>
+__global__ void __launch_bounds__(kTmaThreads, kTileCtasPerSm)
+conv_fwd_tma_kernel(const __grid_constant__ CUtensorMap tm_x, const __nv_bfloat16 *__restrict__ weight,
+                    const __nv_bfloat16 *__restrict__ bias, const int32_t *__restrict__ cu,
+                    int n_seqs, int n_tokens, int C, const __nv_bfloat16 *__restrict__ pool,
+                    int64_t n_slots, const int32_t *__restrict__ idx,
+                    const uint8_t *__restrict__ has_init, int silu, __nv_bfloat16 *__restrict__ y) {
+    using namespace tc;
+    using VT = Vec4<__nv_bfloat16>;
+    constexpr int V = 4;
+    extern __shared__ __align__(128) uint8_t smem_raw[];
+    __shared__ uint64_t full[kTileStages];
+    __shared__ int abort_flag;
+    const int tid = threadIdx.x;
+    const int ct = tid % (kTileCh / V), part = tid / (kTileCh / V);
+    const int n_cb = C / kTileCh;
+    const int n_tiles = ((n_tokens + kTileTok - 1) / kTileTok) * n_cb;
+    if (tid == 0) {
+        for (int st = 0; st < kTileStages; ++st) mbar_init(&full[st], 1);
+        abort_flag = 0;
+        fence_mbar_init();
+        prefetch_tensormap(&tm_x);
+    }
+    __syncthreads();
+    volatile int *abort = &abort_flag;
+    auto issue = [&](int tile, int st) {   // thread 0
+        const int tb = tile / n_cb, cb = tile - tb * n_cb;
+        uint8_t *dst = smem_raw + st * kTileBytes;
+        mbar_arrive_expect_tx(&full[st], kTileBytes);
+        tma_load_2d(dst, &tm_x, &full[st], cb * kTileCh, tb * kTileTok - kTileHist);
+        tma_load_2d(dst + kBoxBytes, &tm_x, &full[st], cb * kTileCh + kBoxCh, tb * kTileTok - kTileHist);
+    };
+    if (tid == 0)
+        for (int j = 0; j < kTileStages - 1; ++j) {
+            const int tile = blockIdx.x + j * gridDim.x;
+            if (tile < n_tiles) issue(tile, j);
+        }
+    // this thread's 4 channels within a staged row (row r = token tb*32 - 3 + r)
+    const int box = ct / (kBoxCh / V), col = ct % (kBoxCh / V);
+    auto row_raw = [&](const uint8_t *stage, int r) {
+        return *reinterpret_cast<const VT::Raw *>(stage + box * kBoxBytes + r * (kBoxCh * 2) + col * 8);
+    };
+    int i = -1;                       // sequence of this thread's current token
+    int64_t ss = 0, se = 0;           // its token range
+    bool bad = false;                 // cu_seqlens does not describe the tokens
+    int cb_taps = -1;
+    ConvTaps<__nv_bfloat16, W, V> taps;
+    for (int j = 0;; ++j) {
+        const int tile = blockIdx.x + j * gridDim.x;
+        if (tile >= n_tiles) break;
+        const int st = j % kTileStages;
+        if (tid == 0) {               // refill the stage the previous tile used
+            const int tn = tile + (kTileStages - 1) * gridDim.x;
+            if (tn < n_tiles) issue(tn, (j + kTileStages - 1) % kTileStages);
+        }
+        const int tb = tile / n_cb, cb = tile - tb * n_cb;
+        const int c0 = cb * kTileCh + ct * V;
+        if (cb != cb_taps) {
+            taps.load(weight, bias, c0);
+            cb_taps = cb;
+        }
+        const int64_t tbase = (int64_t)tb * kTileTok;             // staged row 3
+        const int64_t t0 = tbase + part * kPartTok;                // this thread's tokens
+        const int64_t t1 = min(t0 + (int64_t)kPartTok, (int64_t)n_tokens);
+        const bool any = t0 < t1;
+        // the sequence holding t0 (forward from the last one, else a search)
+        if (any && (i < 0 || t0 < ss)) {
+            int lo = 0, hi = n_seqs;
+            while (lo < hi) {
+                const int mid = (lo + hi) >> 1;
+                if (cu[mid + 1] > t0) hi = mid; else lo = mid + 1;
+            }
+            i = lo;
+            if (i < n_seqs) { ss = cu[i]; se = cu[i + 1]; }
+        }
+        while (any && i < n_seqs && se <= t0) {
+            ++i;
+            if (i < n_seqs) { ss = cu[i]; se = cu[i + 1]; }
+        }
+        if (any && (i >= n_seqs || ss < 0 || ss > t0 || se > n_tokens)) bad = true;
+        const uint8_t *stage = smem_raw + st * kTileBytes;
+        const int r0 = part * kPartTok + kTileHist;                // staged row of t0
+        mbar_wait(&full[st], (j / kTileStages) & 1, abort);
+        if (!bad && t1 - t0 == kPartTok && t0 - ss >= W - 1 && se >= t1) {
+            // inside one sequence with the window staged: no branches
+            float win[W - 1][V];
+#pragma unroll
+            for (int r = 0; r < W - 1; ++r) VT::unpack(row_raw(stage, r0 - (W - 1) + r), win[r]);
+#pragma unroll
+            for (int tt = 0; tt < kPartTok; ++tt) {
+                float cur[V], out[V];
+                VT::unpack(row_raw(stage, r0 + tt), cur);
+                taps.apply(win, cur, silu, out);
+                VT::store(y + (t0 + tt) * C + c0, out);
+                shift_in<W, V>(win, cur);
+            }
+        } else if (!bad && any) {
+            float win[W - 1][V];
+            // history of the sequence from its slot (or zeros) for rows
+            // before its start, else the staged rows
+            auto fill_window = [&](int64_t t) {
+                const int64_t hs = (t - ss < W - 1) ? history_slot(idx, has_init, i, n_slots) : -1;
+#pragma unroll
+                for (int r = 0; r < W - 1; ++r) {
+                    const int64_t n = t - (W - 1) + r;
+                    if (n >= ss) {
+                        VT::unpack(row_raw(stage, (int)(n - tbase) + kTileHist), win[r]);
+                    } else if (hs >= 0) {
+                        VT::load(pool + (hs * (W - 1) + (W - 1) + (n - ss)) * C + c0, win[r]);
+                    } else {
+#pragma unroll
+                        for (int v = 0; v < V; ++v) win[r][v] = 0.0f;
+                    }
+                }
+            };
+            fill_window(t0);
+            for (int tt = 0; tt < kPartTok; ++tt) {
+                const int64_t t = t0 + tt;
+                if (t >= t1) break;
+                if (t == se) {        // the next sequence starts here
+                    do {              // (skipping empty ones)
+                        ++i;
+                        if (i < n_seqs) { ss = cu[i]; se = cu[i + 1]; }
+                    } while (i < n_seqs && se == t && ss == t);
+                    if (i >= n_seqs || ss != t || se < ss || se > n_tokens) { bad = true; break; }
+                    fill_window(t);
+                }
+                float cur[V], out[V];
+                VT::unpack(row_raw(stage, r0 + tt), cur);
+                taps.apply(win, cur, silu, out);
+                VT::store(y + t * C + c0, out);
+                shift_in<W, V>(win, cur);
+            }
+        }
+        __syncthreads();              // the stage is refilled next iteration
+    }
+    if (bad) flag_status(GDN_DEVSTAT_BAD_SEQLEN);
+    if (tid == 0 && abort_flag) flag_status(GDN_DEVSTAT_TIMEOUT);
 }
 
 // Final conv state of every sequence: the last W-1 inputs of history ++ x.
@@ -263,21 +490,53 @@ conv_update_kernel(const T *__restrict__ x, int tps, int C, const T *__restrict_
         for (int r = 0; r < W - 1; ++r) Vec16<T>::store(pool + (slot * (W - 1) + r) * C + c0, win[r]);
 }
 
+// The TMA-staged kernel when the shape allows it (bf16, channels a multiple
+// of 512, token coordinates in int32); false: use the register kernel.
+template <int W>
+static bool launch_fwd_tma(const void *x, int64_t xs, const void *w, const void *b,
+                           const int32_t *cu, int n_seqs, int64_t n_tokens, int C, void *pool,
+                           int64_t n_slots, const int32_t *idx, const uint8_t *has, int silu,
+                           void *y, cudaStream_t s) {
+    if (C % kTileCh != 0 || n_tokens + kTileTok >= (1ll << 31)) return false;
+    CUtensorMap tm;
+    if (!encode_tmap_2d_bf16(&tm, x, (uint64_t)C, (uint64_t)n_tokens, (uint64_t)xs, kBoxCh,
+                             kTileRows, false))
+        return false;
+    const int smem = kTileStages * kTileBytes;
+    if (cudaFuncSetAttribute(conv_fwd_tma_kernel<W>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             smem) != cudaSuccess)
+        return false;
+    int dev = 0, sms = 148;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    const int64_t n_tiles = ((n_tokens + kTileTok - 1) / kTileTok) * (C / kTileCh);
+    const int grid = (int)std::min<int64_t>(n_tiles, (int64_t)sms * kTileCtasPerSm);
+    conv_fwd_tma_kernel<W><<<grid, kTmaThreads, smem, s>>>(
+        tm, (const __nv_bfloat16 *)w, (const __nv_bfloat16 *)b, cu, n_seqs, (int)n_tokens, C,
+        (const __nv_bfloat16 *)pool, n_slots, idx, has, silu, (__nv_bfloat16 *)y);
+    return true;
+}
+
 template <typename T, int W>
 static void launch_fwd(const void *x, int64_t xs, const void *w, const void *b, const int32_t *cu,
                        int n_seqs, int64_t n_tokens, int C, void *pool, int64_t n_slots,
                        const int32_t *idx, const uint8_t *has, int silu, void *y, cudaStream_t s) {
-    constexpr int V = Vec16<T>::N;
-    const int groups = C / V;
     dim3 block(kConvThreads);
-    if (n_tokens > 0) {
+    bool done = n_tokens == 0;
+    if constexpr (std::is_same<T, __nv_bfloat16>::value)
+        if (!done)
+            done = launch_fwd_tma<W>(x, xs, w, b, cu, n_seqs, n_tokens, C, pool, n_slots, idx, has,
+                                     silu, y, s);
+    if (!done) {
         dim3 grid((unsigned)((n_tokens + kConvTokensPerThread - 1) / kConvTokensPerThread),
-                  (unsigned)((groups + kConvThreads - 1) / kConvThreads));
-        conv_fwd_kernel<T, W><<<grid, block, 0, s>>>(
+                  (unsigned)((C / 4 + kConvThreads - 1) / kConvThreads));
+        conv_fwd_kernel<T, W, kConvTokensPerThread><<<grid, block, 0, s>>>(
             (const T *)x, xs, (const T *)w, (const T *)b, cu, n_seqs, n_tokens, C,
             (const T *)pool, n_slots, idx, has, silu, (T *)y);
     }
     if (pool) {
+        constexpr int V = Vec16<T>::N;
+        const int groups = C / V;
         dim3 grid2((unsigned)n_seqs, (unsigned)((groups + kConvThreads - 1) / kConvThreads));
         conv_final_state_kernel<T, W><<<grid2, block, 0, s>>>(
             (const T *)x, xs, cu, n_tokens, C, (T *)pool, n_slots, idx, has);

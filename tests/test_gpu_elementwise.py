@@ -33,8 +33,9 @@ def test_gating(dtype, T, hv):
     np.testing.assert_allclose(to_np(beta), b_ref, rtol=2e-6, atol=1e-30)
 
 
-def _conv_oracle(x, cu, w, pool, idx, has):
-    y, upd = oracle.conv1d_fwd(to_np(x), to_np(cu).astype(np.int64), to_np(w), None,
+def _conv_oracle(x, cu, w, pool, idx, has, bias=None):
+    y, upd = oracle.conv1d_fwd(to_np(x), to_np(cu).astype(np.int64), to_np(w),
+                               None if bias is None else to_np(bias),
                                pool, to_np(idx).astype(np.int64),
                                None if has is None else to_np(has).astype(np.int64))
     return y, upd
@@ -66,6 +67,39 @@ def test_conv_fwd_varlen_ragged(dtype):
         if s in upd:
             ref = torch.from_numpy(upd[s]).to(dtype)
             assert bits_equal(got[s], ref), f"conv state slot {s}"    # states are copies of inputs
+        else:
+            assert bits_equal(got[s], pool[s]), f"untouched slot {s}"
+
+
+@pytest.mark.parametrize("W", [2, 3, 4])
+def test_conv_fwd_tma_ragged(W):
+    """The TMA-staged path (bf16, channels a multiple of 512): 1024 channels,
+    138 tokens in tiles of 32 with sequence starts inside tiles, empty
+    sequences at the start, inside a tile and at a tile edge, sequences of
+    1..3 tokens, slots with / without history, a padding slot, a strided x
+    view, a conv bias and a ragged last tile."""
+    gen = torch.Generator().manual_seed(12 + W)
+    C = 1024
+    lens = [0, 17, 0, 1, 2, 12, 0, 40, 3, 0, 58, 5]
+    cu = torch.tensor(np.concatenate([[0], np.cumsum(lens)]), dtype=torch.int32)
+    T = int(cu[-1])
+    xbig = torch.randn(T, C + 64, generator=gen).to(torch.bfloat16)
+    x = xbig[:, 32:32 + C]                            # row stride C + 64
+    w = workloads.conv_weight(gen, C, W, torch.bfloat16)
+    bias = (torch.randn(C, generator=gen) * 0.1).to(torch.bfloat16)
+    pool = torch.randn(14, W - 1, C, generator=gen).to(torch.bfloat16)
+    idx = torch.tensor([9, 3, 1, -1, 5, 11, 12, 0, 6, 8, 2, 13], dtype=torch.int32)
+    has = torch.tensor([1, 1, 1, 1, 0, 1, 1, 1, 1, 1, 0, 1], dtype=torch.uint8)
+    xd, pd = cuda(xbig)[:, 32:32 + C], cuda(pool)
+    y = gdn().causal_conv1d_fwd(xd, cuda(w), cuda(cu), pd, cuda(idx), cuda(has), bias=cuda(bias))
+    torch.cuda.synchronize()
+    status_clean()
+    y_ref, upd = _conv_oracle(x, cu, w, to_np(pool), idx, has, bias)
+    assert_close(y, y_ref, TOL[torch.bfloat16], "conv y (TMA path)")
+    got = pd.cpu()
+    for s in range(pool.shape[0]):
+        if s in upd:
+            assert bits_equal(got[s], torch.from_numpy(upd[s]).to(torch.bfloat16)), f"slot {s}"
         else:
             assert bits_equal(got[s], pool[s]), f"untouched slot {s}"
 
