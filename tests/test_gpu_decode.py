@@ -136,7 +136,7 @@ def test_mtp_full_size_snapshots_and_accept():
 
 @pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
 @pytest.mark.parametrize("dk,dv,tps", [(16, 16, 1), (16, 24, 3), (32, 32, 2), (64, 128, 16),
-                                       (128, 64, 5), (128, 128, 1)])
+                                       (128, 64, 5), (128, 128, 1), (128, 128, 4), (128, 128, 16)])
 def test_decode_small_shapes(dtype, dk, dv, tps):
     gen = torch.Generator().manual_seed(dk * 1000 + dv * 10 + tps)
     hqk, hv, N, slots = 2, 4, 5, 12
@@ -164,6 +164,40 @@ def test_decode_small_shapes(dtype, dk, dv, tps):
                                    to_np(idx).astype(np.int64),
                                    None if snap is None else to_np(snap).astype(np.int64), scale=0.3)
     assert_close(o, o_ref, TOL[dtype], "o")
+    got = pd.cpu()
+    for s in range(slots):
+        for h in range(hv):
+            if (s, h) in upd:
+                assert_close(got[s, h], upd[(s, h)], TOL[dtype], f"state {s},{h}")
+            else:
+                assert bits_equal(got[s, h], pool[s, h]), f"untouched {s},{h}"
+
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+def test_decode_multitoken_in_place(dtype):
+    """dk = dv = 128, 3 tokens per sequence and no snapshots: the state is
+    updated in its own slot after the last token; a padding row is skipped."""
+    gen = torch.Generator().manual_seed(77)
+    hqk, hv, N, tps, slots = 2, 4, 6, 3, 9
+    T = N * tps
+    q = torch.randn(T, hqk, 128, generator=gen).to(dtype)
+    k = torch.randn(T, hqk, 128, generator=gen).to(dtype)
+    v = torch.randn(T, hv, 128, generator=gen).to(dtype)
+    a = torch.randn(T, hv, generator=gen).to(dtype)
+    b = torch.randn(T, hv, generator=gen).to(dtype)
+    A_log, dt_bias = workloads.gating_params(gen, hv, low_decay=True)
+    pool = torch.randn(slots, hv, 128, 128, generator=gen) * 0.05
+    idx = torch.tensor([8, 2, -1, 0, 5, 3], dtype=torch.int32)
+    pd = cuda(pool)
+    g, beta = gdn().gdn_gating(cuda(a), cuda(b), cuda(A_log), cuda(dt_bias))
+    o = gdn().gdn_decode_recurrent(cuda(q), cuda(k), cuda(v), g, beta, tps, pd, cuda(idx), scale=0.2)
+    torch.cuda.synchronize()
+    status_clean()
+    g_ref, b_ref = oracle_gating(a, b, A_log, dt_bias)
+    o_ref, upd = oracle.gdn_decode(to_np(q), to_np(k), to_np(v), g_ref, b_ref, tps, to_np(pool),
+                                   to_np(idx).astype(np.int64), None, scale=0.2)
+    assert_close(o, o_ref, TOL[dtype], "o")
+    assert torch.all(o[2 * tps:3 * tps] == 0)
     got = pd.cpu()
     for s in range(slots):
         for h in range(hv):
