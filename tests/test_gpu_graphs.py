@@ -1,0 +1,121 @@
+"""The C ABI calls are asynchronous on the caller's stream, with no host
+synchronisation and no allocation, so a serving loop can capture them in a
+CUDA graph: the fused decode step, the two-kernel prefill (with a caller
+workspace) and the TMA-staged conv forward are captured with torch.cuda.graph
+and replayed, and every output and pool must be bit-identical to an eager run
+on copies of the same inputs (the kernels are deterministic)."""
+import pytest
+import torch
+
+import workloads
+from tests.gpu_common import DEV, cuda, gdn, status_clean
+from tests.util import bits_equal
+
+pytestmark = pytest.mark.gpu
+
+
+def _graph(fn):
+    """Warm up on a side stream (as torch.cuda.graph wants), capture, replay."""
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        fn()
+    torch.cuda.current_stream().wait_stream(s)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        fn()
+    return g
+
+
+def test_decode_step_graph_replay():
+    """Two replays of the captured step equal two eager steps."""
+    w = workloads.decode(pool_device=DEV)
+    d = w.dims
+    x, a, b = cuda(w.x), cuda(w.a), cuda(w.b)
+    conv_w, A_log, dt_bias, slots = cuda(w.conv_w), cuda(w.A_log), cuda(w.dt_bias), cuda(w.slots)
+    cpool0, spool0 = cuda(w.conv_pool), w.state_pool
+
+    def run(cpool, spool, o):
+        gdn().gdn_decode_step_fused(x, conv_w, cpool, a, b, A_log, dt_bias, d.hqk, spool, slots,
+                                    scale=w.scale, o=o)
+
+    ce, se = cpool0.clone(), spool0.clone()
+    oe = torch.empty((w.n_seqs, d.hv, d.dv), dtype=x.dtype, device=DEV)
+    run(ce, se, oe)
+    run(ce, se, oe)
+    torch.cuda.synchronize()
+    status_clean()
+
+    cg, sg = cpool0.clone(), spool0.clone()
+    og = torch.empty_like(oe)
+    g = _graph(lambda: run(cg, sg, og))       # warm-up + capture ran the step once
+    cg.copy_(cpool0)
+    sg.copy_(spool0)
+    g.replay()
+    g.replay()
+    torch.cuda.synchronize()
+    status_clean()
+    assert bits_equal(og, oe)
+    assert bits_equal(cg, ce)
+    assert bits_equal(sg, se)
+
+
+def test_prefill_split_graph_replay():
+    """The prep + chain prefill with a caller workspace, captured and replayed."""
+    w = workloads.prefill()
+    d = w.dims
+    x = cuda(w.x)
+    cu, slots = cuda(w.cu_seqlens), cuda(w.slots)       # conv slots
+    y = gdn().causal_conv1d_fwd(x, cuda(w.conv_w), cu, cuda(w.conv_pool), slots,
+                                cuda(w.has_initial_state))
+    g_, beta = gdn().gdn_gating(cuda(w.a), cuda(w.b), cuda(w.A_log), cuda(w.dt_bias))
+    nq = d.hqk * d.dk
+    q = y.narrow(1, 0, nq).unflatten(1, (d.hqk, d.dk))
+    k = y.narrow(1, nq, nq).unflatten(1, (d.hqk, d.dk))
+    v = y.narrow(1, 2 * nq, d.hv * d.dv).unflatten(1, (d.hv, d.dv))
+    n_seqs = cu.numel() - 1
+    ws = torch.empty(gdn().gdn_prefill_workspace_size(n_seqs, x.shape[0], d.hv, d.dk, d.dv, 64),
+                     dtype=torch.uint8, device=DEV)
+    # every sequence carries a random initial state in place (slot i)
+    sl = torch.arange(n_seqs, dtype=torch.int32, device=DEV)
+    gen = torch.Generator(device=DEV).manual_seed(21)
+    pool0 = torch.randn(n_seqs, d.hv, d.dv, d.dk, generator=gen, device=DEV) * 0.02
+
+    def run(pool, o):
+        gdn().gdn_prefill_chunked(q, k, v, g_, beta, cu, pool, sl, sl, w.scale, o=o, workspace=ws)
+
+    pe = pool0.clone()
+    oe = torch.empty((x.shape[0], d.hv, d.dv), dtype=x.dtype, device=DEV)
+    run(pe, oe)
+    torch.cuda.synchronize()
+    status_clean()
+    pg = pool0.clone()
+    og = torch.empty_like(oe)
+    gr = _graph(lambda: run(pg, og))
+    pg.copy_(pool0)
+    og.zero_()
+    gr.replay()
+    torch.cuda.synchronize()
+    status_clean()
+    assert bits_equal(og, oe)
+    assert bits_equal(pg, pe)
+
+
+def test_conv_fwd_graph_replay():
+    w = workloads.prefill()
+    x, cw, cu, slots, has = (cuda(t) for t in (w.x, w.conv_w, w.cu_seqlens, w.slots,
+                                                w.has_initial_state))
+    pool0 = cuda(w.conv_pool)
+    pe = pool0.clone()
+    ye = gdn().causal_conv1d_fwd(x, cw, cu, pe, slots, has)
+    torch.cuda.synchronize()
+    pg = pool0.clone()
+    yg = torch.empty_like(ye)
+    gr = _graph(lambda: gdn().causal_conv1d_fwd(x, cw, cu, pg, slots, has, y=yg))
+    pg.copy_(pool0)
+    yg.zero_()
+    gr.replay()
+    torch.cuda.synchronize()
+    status_clean()
+    assert bits_equal(yg, ye)
+    assert bits_equal(pg, pe)
