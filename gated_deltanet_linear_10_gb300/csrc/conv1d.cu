@@ -2,9 +2,15 @@
 // convolutions", "[model] support Qwen3next", Highlights), for packed
 // variable-length prefill and for decode / MTP updates against a slot pool.
 //
-// Each thread owns 16 bytes of channels (8 bf16 or 4 fp32) and walks a run of
-// tokens, keeping the last width-1 inputs in registers, so every input row is
-// read from HBM once (plus width-1 rows at the head of each run).
+// A thread owns a few channels and walks a run of tokens, keeping the last
+// width-1 inputs in registers, so every input row is read from HBM once (plus
+// width-1 rows at the head of each run):
+//   - prefill, bf16 with channels a multiple of 512: tiles of 32 tokens x 512
+//     channels staged in shared memory by TMA (conv_fwd_tma_kernel);
+//   - prefill, other shapes: 4 channels x 8 tokens per thread, straight from
+//     global memory (conv_fwd_kernel);
+//   - decode / MTP update: 16 bytes of channels per thread over the few new
+//     tokens of a sequence (conv_update_kernel).
 #include <algorithm>
 #include <type_traits>
 
