@@ -344,6 +344,7 @@ def run_ours(args):
         extras["mtp"] = bench_mtp(gdn, workloads, dev, flush)
         extras["prefill"] = bench_prefill(gdn, workloads, dev, flush, peaks)
         extras["decode_gated"] = bench_decode_gated(gdn, workloads, dev, flush)
+        extras["mixed"] = bench_mixed(gdn, workloads, dev, flush)
 
     cpu = None
     if rank == 0:
@@ -504,6 +505,59 @@ def bench_mtp(gdn, workloads, dev, flush, steps=50):
             "decode_kernel_gbs": round(dec_bytes / (dec / 1e3) / 1e9, 1),
             "decode_kernel_frac_hbm": round(dec_bytes / (dec / 1e3) / 1e9 / peak, 4),
             "gpu_launches_per_step": 5}
+
+
+def bench_mixed(gdn, workloads, dev, flush, steps=20):
+    """A serving step's mixed batch (256 decode rows + two 2048-token prompts)
+    through gdn_mixed_batch (decode rows on the streaming decode kernel, in
+    place; prompts on the chunked prefill) and, for comparison, the same
+    batch through one gdn_prefill_chunked call."""
+    w = workloads.mixed(pool_device=dev)
+    d = w.dims
+    q, k, v, a, b = (t.to(dev) for t in (w.q, w.k, w.v, w.a, w.b))
+    cu = w.cu_seqlens.to(dev)
+    nd = w.extra["n_decode"]
+    g, beta = gdn.gdn_gating(a, b, w.A_log.to(dev), w.dt_bias.to(dev))
+    slots = w.slots.to(dev)
+    # decode rows continue their slot in place; prompts start from zero and
+    # end in their slot
+    init = torch.where(w.has_initial_state.to(dev).bool(), slots, torch.full_like(slots, -1))
+    T = q.shape[0]
+    o = torch.empty((T, d.hv, d.dv), dtype=q.dtype, device=dev)
+    ws_mixed = torch.empty(gdn.gdn_prefill_workspace_size(w.n_seqs - nd, T, d.hv, d.dk, d.dv, 64),
+                           dtype=torch.uint8, device=dev)
+    ws_all = torch.empty(gdn.gdn_prefill_workspace_size(w.n_seqs, T, d.hv, d.dk, d.dv, 64),
+                         dtype=torch.uint8, device=dev)
+    def mixed():
+        gdn.gdn_mixed_batch(q, k, v, g, beta, cu, nd, w.state_pool, init, slots, w.scale,
+                            decode_in_place=True, o=o, workspace=ws_mixed)
+
+    def one_call():
+        gdn.gdn_prefill_chunked(q, k, v, g, beta, cu, w.state_pool, init, slots, w.scale, o=o,
+                                workspace=ws_all)
+
+    res = {}
+    for name, fn in (("mixed_batch", mixed), ("prefill_call", one_call)):
+        for _ in range(3):
+            fn()
+            flush.zero_()
+        torch.cuda.synchronize(dev)
+        ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(steps)]
+        for i in range(steps):
+            ev[i][0].record()
+            fn()
+            ev[i][1].record()
+            flush.zero_()
+        torch.cuda.synchronize(dev)
+        res[name] = sum(e[0].elapsed_time(e[1]) for e in ev) / steps
+    assert gdn.gdn_get_device_status(clear=True) == 0
+    return {"workload": f"mixed step: {nd} decode rows (1 token, state in place) + prompts of "
+                        f"{[int(x) for x in w.extra['lengths'][nd:]]} tokens, 16 QK / 32 V heads, "
+                        "head_dim 128, bf16",
+            "tokens_per_s": round(T / (res["mixed_batch"] / 1e3), 1),
+            "mixed_batch_ms": round(res["mixed_batch"], 4),
+            "prefill_call_ms": round(res["prefill_call"], 4),
+            "gpu_launches_per_step": 4}
 
 
 def bench_decode_gated(gdn, workloads, dev, flush, steps=50):

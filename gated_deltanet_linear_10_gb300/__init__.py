@@ -29,7 +29,7 @@ EXPORTS = (
     "causal_conv1d_fwd", "causal_conv1d_update", "gdn_prefill_chunked",
     "gdn_prefill_workspace_size", "gdn_decode_recurrent", "gdn_state_snapshot",
     "gdn_get_device_status", "gdn_prefill_chunked_static", "gdn_gated_rmsnorm",
-    "gdn_decode_recurrent_gated", "gdn_decode_step_fused",
+    "gdn_decode_recurrent_gated", "gdn_decode_step_fused", "gdn_mixed_batch",
 )
 
 if not os.path.exists(LIB_PATH):
@@ -66,6 +66,9 @@ _SIGS = {
                                    _vp, _f32, _vp, _i32, _vp],
     "gdn_prefill_chunked_static": [_vp, _i64, _vp, _i64, _vp, _i64, _vp, _vp, _vp, _i32, _i64,
                                    _i32, _i32, _f32, _i32, _vp, _i64, _vp, _vp, _vp, _vp],
+    "gdn_mixed_batch": [_vp, _i64, _vp, _i64, _vp, _i64, _vp, _vp, _vp, _i32, _i32, _i64, _i32,
+                        _i32, _i32, _i32, _f32, _i32, _i32, _vp, _i64, _vp, _vp, _i32, _vp, _i32,
+                        _vp, ctypes.c_size_t, _vp],
 }
 for _name, _args in _SIGS.items():
     _fn = getattr(_lib, _name)
@@ -249,6 +252,55 @@ def gdn_prefill_chunked(q, k, v, g, beta, cu_seqlens, state_pool, initial_state_
                                     _ptr(initial_state_indices), _ptr(final_state_indices),
                                     _ptr(o), dt, _ptr(workspace), wbytes, _stream(q.device)),
            "gdn_prefill_chunked")
+    return o
+
+
+def gdn_mixed_batch(q, k, v, g, beta, cu_seqlens, n_decode, state_pool, initial_state_indices,
+                    final_state_indices, scale, decode_in_place=True, chunk=64, l2norm_qk=True,
+                    o=None, workspace=None):
+    """A serving step's mixed batch: sequences 0 .. n_decode-1 are one-token
+    decode rows (rows 0 .. n_decode-1) continuing the states in
+    initial_state_indices (in place, or into final_state_indices when
+    decode_in_place is False); the rest go through the chunked prefill with
+    both index arrays.  Shapes as gdn_prefill_chunked; workspace as there,
+    sized for the prefill sequences."""
+    _cuda(q, k, v, g, beta, cu_seqlens, state_pool, initial_state_indices, final_state_indices)
+    T, hqk, dk = q.shape
+    hv, dv = v.shape[1], v.shape[2]
+    qs = _heads_view(q, hqk, dk, "q")
+    ks = _heads_view(k, hqk, dk, "k")
+    vs = _heads_view(v, hv, dv, "v")
+    _need(q.dtype == k.dtype == v.dtype, "q, k, v: one dtype")
+    _need(g.dtype == torch.float32 and beta.dtype == torch.float32 and g.is_contiguous()
+          and beta.is_contiguous() and g.shape == (T, hv) and beta.shape == (T, hv), "g, beta")
+    _need(state_pool.dtype == torch.float32 and state_pool.is_contiguous()
+          and state_pool.shape[1:] == (hv, dv, dk), "state_pool: [slots, hv, dv, dk] fp32")
+    _i32_vec(cu_seqlens, "cu_seqlens")
+    n = cu_seqlens.numel() - 1
+    _need(0 <= n_decode <= n and n_decode <= T, "n_decode: 0 .. n_seqs")
+    for name, t in (("initial_state_indices", initial_state_indices),
+                    ("final_state_indices", final_state_indices)):
+        if t is not None:
+            _i32_vec(t, name)
+            _need(t.numel() == n, f"{name}: [n_seqs]")
+    o = torch.empty((T, hv, dv), dtype=q.dtype, device=q.device) if o is None else o
+    _need(o.is_contiguous() and o.shape == (T, hv, dv), "o: [T, hv, dv] contiguous")
+    dt = _dtype_code(q)
+    if workspace is False:
+        workspace = None
+    elif workspace is None:
+        need = gdn_prefill_workspace_size(n - n_decode, T, hv, dk, dv, chunk, dt) if n > n_decode else 0
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device) if need else None
+    else:
+        _cuda(workspace)
+    wbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(_lib.gdn_mixed_batch(_ptr(q), qs, _ptr(k), ks, _ptr(v), vs, _ptr(g), _ptr(beta),
+                                _ptr(cu_seqlens), n, int(n_decode), T, hqk, hv, dk, dv,
+                                float(scale), int(l2norm_qk), chunk, _ptr(state_pool),
+                                state_pool.shape[0], _ptr(initial_state_indices),
+                                _ptr(final_state_indices), int(bool(decode_in_place)), _ptr(o),
+                                dt, _ptr(workspace), wbytes, _stream(q.device)),
+           "gdn_mixed_batch")
     return o
 
 

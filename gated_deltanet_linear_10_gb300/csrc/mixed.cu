@@ -1,0 +1,44 @@
+// A serving step's mixed batch in one call: decode continuations and prefill
+// (or chunked-prefill continuation) sequences of one packed varlen batch
+// (the mixed batches and chunked prefill of "[model] support Qwen3next",
+// which runs decode and prefill requests of one step through the layer).
+//
+// The first n_decode sequences are one token each, rows 0 .. n_decode-1;
+// they go to the recurrent decode kernels, which stream each state once.
+// The rest go to the chunked prefill on the same stream.  No kernel of its
+// own: the two halves are the library's decode and prefill paths, with the
+// prefill half given the tail of cu_seqlens (its token rows are absolute).
+#include "common.cuh"
+
+extern "C" gdn_status gdn_mixed_batch(
+    const void *q, int64_t q_row_stride, const void *k, int64_t k_row_stride, const void *v,
+    int64_t v_row_stride, const float *g, const float *beta, const int32_t *cu_seqlens,
+    int32_t n_seqs, int32_t n_decode, int64_t n_tokens, int32_t hqk, int32_t hv, int32_t dk,
+    int32_t dv, float scale, int32_t l2norm_qk, int32_t chunk, float *state_pool,
+    int64_t n_slots, const int32_t *initial_state_indices, const int32_t *final_state_indices,
+    int32_t decode_in_place, void *o, int32_t dtype, void *workspace, size_t workspace_bytes,
+    void *stream) {
+    GDN_REQUIRE(n_seqs >= 0 && n_decode >= 0 && n_decode <= n_seqs && n_tokens >= n_decode,
+                GDN_ERR_INVALID_ARG);
+    if (n_decode > 0) {
+        // a decode row continues a state: it needs its initial slot
+        GDN_REQUIRE(initial_state_indices != nullptr, GDN_ERR_INVALID_ARG);
+        // in place: the streaming kernel; otherwise the state after the
+        // token goes to the final slot and the initial one is only read
+        const bool in_place = decode_in_place != 0;
+        GDN_REQUIRE(in_place || final_state_indices != nullptr, GDN_ERR_INVALID_ARG);
+        const gdn_status st = gdn_decode_recurrent(
+            q, q_row_stride, k, k_row_stride, v, v_row_stride, g, beta, n_decode, 1, hqk, hv, dk,
+            dv, scale, l2norm_qk, state_pool, n_slots, initial_state_indices,
+            in_place ? nullptr : final_state_indices, o, dtype, stream);
+        if (st != GDN_OK) return st;
+    }
+    if (n_seqs == n_decode) return GDN_OK;
+    GDN_REQUIRE(cu_seqlens != nullptr, GDN_ERR_INVALID_ARG);
+    return gdn_prefill_chunked(
+        q, q_row_stride, k, k_row_stride, v, v_row_stride, g, beta, cu_seqlens + n_decode,
+        n_seqs - n_decode, n_tokens, hqk, hv, dk, dv, scale, l2norm_qk, chunk, state_pool, n_slots,
+        initial_state_indices ? initial_state_indices + n_decode : nullptr,
+        final_state_indices ? final_state_indices + n_decode : nullptr, o, dtype, workspace,
+        workspace_bytes, stream);
+}

@@ -335,6 +335,41 @@ gdn_status gdn_decode_step_fused(const void *x, int64_t x_row_stride,
                                  void *stream);
 
 /*
+ * A serving step's mixed batch in one call: decode continuations and prefill
+ * sequences packed in one varlen batch (the mixed decode / prefill batches
+ * and chunked prefill of "[model] support Qwen3next").
+ *   Sequences 0 .. n_decode-1 are decode rows: one token each, at rows
+ *   0 .. n_decode-1 (cu_seqlens[i] = i for i <= n_decode).  Each continues
+ *   the state in slot initial_state_indices[i] (< 0: the row is skipped and
+ *   its o is zero; a new sequence, even of one token, belongs to the prefill
+ *   part).  decode_in_place != 0 updates those slots in place (the
+ *   streaming decode kernel; final_state_indices[i] is ignored for decode
+ *   rows); decode_in_place == 0 writes the state after the token to
+ *   final_state_indices[i] (< 0: dropped) and only reads the initial slot.
+ *   Sequences n_decode .. n_seqs-1 run through gdn_prefill_chunked with
+ *   cu_seqlens + n_decode (absolute token rows), the tail of both index
+ *   arrays, and the workspace: size it with
+ *   gdn_prefill_workspace_size(n_seqs - n_decode, n_tokens, ...).
+ * Other arguments, layouts and errors as gdn_prefill_chunked and
+ * gdn_decode_recurrent (the decode rows need dk = dv <= 128 as those do).
+ * Returns the first error of the two halves; on an error of the decode half
+ * the prefill half is not launched.
+ */
+gdn_status gdn_mixed_batch(const void *q, int64_t q_row_stride, const void *k,
+                           int64_t k_row_stride, const void *v,
+                           int64_t v_row_stride, const float *g,
+                           const float *beta, const int32_t *cu_seqlens,
+                           int32_t n_seqs, int32_t n_decode, int64_t n_tokens,
+                           int32_t hqk, int32_t hv, int32_t dk, int32_t dv,
+                           float scale, int32_t l2norm_qk, int32_t chunk,
+                           float *state_pool, int64_t n_slots,
+                           const int32_t *initial_state_indices,
+                           const int32_t *final_state_indices,
+                           int32_t decode_in_place, void *o, int32_t dtype,
+                           void *workspace, size_t workspace_bytes,
+                           void *stream);
+
+/*
  * Whole-slot copy pool[dst[i]] <- pool[src[i]], bit for bit (the buffer copy
  * from source to destination indices of "[model] support Qwen3next", review
  * of the MTP buffer copy).  Used for the recurrent pool (slot_bytes =

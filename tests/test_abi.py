@@ -96,6 +96,31 @@ def test_host_argument_checks(lib):
     assert s(FAKE, 8, 32, FAKE, FAKE, 0, None) == 0
 
 
+def test_mixed_batch_host_checks(lib):
+    """n_decode outside 0 .. n_seqs, decode rows without initial slots, and an
+    unsupported head size in the decode half fail before anything launches."""
+    m = lib.gdn_mixed_batch
+    m.argtypes = [V, I64, V, I64, V, I64, V, V, V, I32, I32, I64, I32, I32, I32, I32, F32, I32,
+                  I32, V, I64, V, V, I32, V, I32, V, ctypes.c_size_t, V]
+    base = [FAKE, 2048, FAKE, 2048, FAKE, 4096, FAKE, FAKE, FAKE, 4, 2, 100, 16, 32, 128, 128,
+            1.0, 1, 64, FAKE, 8, FAKE, FAKE, 1, FAKE, 1, None, 0, None]
+    bad = list(base); bad[10] = 5        # n_decode > n_seqs
+    assert m(*bad) == 1
+    bad = list(base); bad[10] = -1
+    assert m(*bad) == 1
+    bad = list(base); bad[11] = 1        # fewer tokens than decode rows
+    assert m(*bad) == 1
+    bad = list(base); bad[21] = None     # decode rows need their initial slots
+    assert m(*bad) == 1
+    bad = list(base); bad[22] = None; bad[23] = 0   # ... and final slots unless in place
+    assert m(*bad) == 1
+    bad = list(base); bad[14] = 96       # dk 96: the decode half is unsupported
+    bad[15] = 96
+    assert m(*bad) == 2
+    empty = list(base); empty[9] = 0; empty[10] = 0; empty[11] = 0
+    assert m(*empty) == 0                # nothing to do: no launch
+
+
 def test_prefill_workspace_size(lib):
     """Only the bf16 dk = dv = 128, chunk-64 path uses scratch: a small header
     plus one operand block per (chunk bound, V head) item, where the chunk

@@ -226,6 +226,36 @@ def prefill(seed=1003, n_seqs=8, lo=512, hi=8192, lengths=None, n_slots=1024,
         extra={"lengths": lengths})
 
 
+def mixed(seed=1006, n_decode=256, prefill_lens=(2048, 2048), n_slots=1024, dims: Dims = FULL,
+          dtype=torch.bfloat16, pool_device="cpu"):
+    """A serving step's mixed batch: n_decode one-token decode rows first, then
+    prompts of prefill_lens tokens; q/k/v/a/b ~ N(0, 1) drawn directly, state
+    pool ~ N(0, 0.02); every sequence has its own slot (seeded permutation),
+    the decode rows continue their state, the prompts start from zero."""
+    d = dims
+    gen = _gen(seed)
+    lengths = torch.tensor([1] * n_decode + list(prefill_lens), dtype=torch.int64)
+    n = len(lengths)
+    cu = torch.zeros(n + 1, dtype=torch.int32)
+    cu[1:] = torch.cumsum(lengths, 0).to(torch.int32)
+    T = int(cu[-1])
+    slots = torch.randperm(n_slots, generator=gen)[:n].to(torch.int32)
+    q = _normal(gen, (T, d.hqk, d.dk), dtype=dtype)
+    k = _normal(gen, (T, d.hqk, d.dk), dtype=dtype)
+    v = _normal(gen, (T, d.hv, d.dv), dtype=dtype)
+    a = _normal(gen, (T, d.hv), dtype=dtype)
+    b = _normal(gen, (T, d.hv), dtype=dtype)
+    A_log, dt_bias = gating_params(gen, d.hv)
+    has = torch.zeros(n, dtype=torch.uint8)
+    has[:n_decode] = 1
+    pool = pool_normal(n_slots, d, 0.02, seed + 7, pool_device)
+    return Workload(
+        name=f"mixed_D{n_decode}_P{len(prefill_lens)}", dims=d, dtype=dtype, scale=d.dk ** -0.5,
+        cu_seqlens=cu, n_seqs=n, q=q, k=k, v=v, a=a, b=b, A_log=A_log, dt_bias=dt_bias,
+        state_pool=pool, slots=slots, has_initial_state=has,
+        extra={"n_decode": n_decode, "lengths": lengths})
+
+
 def long_context(seed=1004, T=65536, dims: Dims = FULL, dtype=torch.bfloat16, chunk=64,
                  n_slots=2, low_decay=False):
     """One sequence of T tokens with q/k/v/a/b ~ N(0, 1) drawn directly (no
