@@ -362,15 +362,15 @@ static cudaError_t launch_decode(const void *q, int64_t qs, const void *k, int64
 
 using namespace gdn;
 
-static gdn_status decode_entry(const void *q, int64_t q_row_stride, const void *k,
-                               int64_t k_row_stride, const void *v, int64_t v_row_stride,
-                               const float *g, const float *beta, int32_t n_seqs,
-                               int32_t tokens_per_seq, int32_t hqk, int32_t hv, int32_t dk,
-                               int32_t dv, float scale, int32_t l2norm_qk, float *state_pool,
-                               int64_t n_slots, const int32_t *state_indices,
-                               const int32_t *snap_indices, const void *z, int64_t z_row_stride,
-                               const float *norm_weight, float norm_eps, void *o, int32_t dtype,
-                               void *stream) {
+namespace gdn {
+// The host-side checks of the decode entries, launching nothing: GDN_OK when
+// the call would run (for n_seqs == 0: when it would return GDN_OK).
+gdn_status decode_check(const void *q, int64_t q_row_stride, const void *k, int64_t k_row_stride,
+                        const void *v, int64_t v_row_stride, const float *g, const float *beta,
+                        int32_t n_seqs, int32_t tokens_per_seq, int32_t hqk, int32_t hv,
+                        int32_t dk, int32_t dv, const float *state_pool, int64_t n_slots,
+                        const int32_t *state_indices, const void *z, int64_t z_row_stride,
+                        const float *norm_weight, float norm_eps, const void *o, int32_t dtype) {
     GDN_REQUIRE(dtype == GDN_F32 || dtype == GDN_BF16, GDN_ERR_INVALID_ARG);
     GDN_REQUIRE(n_seqs >= 0 && hqk > 0 && hv > 0 && n_slots >= 0, GDN_ERR_INVALID_ARG);
     GDN_REQUIRE(hv % hqk == 0, GDN_ERR_INVALID_ARG);
@@ -396,6 +396,25 @@ static gdn_status decode_entry(const void *q, int64_t q_row_stride, const void *
     GDN_REQUIRE((q_row_stride * elem) % align == 0 && (k_row_stride * elem) % align == 0,
                 GDN_ERR_INVALID_ARG);
     GDN_REQUIRE(((uintptr_t)state_pool % 16) == 0, GDN_ERR_INVALID_ARG);
+    return GDN_OK;
+}
+}  // namespace gdn
+
+static gdn_status decode_entry(const void *q, int64_t q_row_stride, const void *k,
+                               int64_t k_row_stride, const void *v, int64_t v_row_stride,
+                               const float *g, const float *beta, int32_t n_seqs,
+                               int32_t tokens_per_seq, int32_t hqk, int32_t hv, int32_t dk,
+                               int32_t dv, float scale, int32_t l2norm_qk, float *state_pool,
+                               int64_t n_slots, const int32_t *state_indices,
+                               const int32_t *snap_indices, const void *z, int64_t z_row_stride,
+                               const float *norm_weight, float norm_eps, void *o, int32_t dtype,
+                               void *stream) {
+    const gdn_status st = decode_check(q, q_row_stride, k, k_row_stride, v, v_row_stride, g, beta,
+                                       n_seqs, tokens_per_seq, hqk, hv, dk, dv, state_pool,
+                                       n_slots, state_indices, z, z_row_stride, norm_weight,
+                                       norm_eps, o, dtype);
+    if (st != GDN_OK || n_seqs == 0) return st;
+    const bool gated = z != nullptr;
     cudaStream_t s = (cudaStream_t)stream;
     cudaError_t e = cudaSuccess;
 #define GDN_DEC(DK, T)                                                                          \

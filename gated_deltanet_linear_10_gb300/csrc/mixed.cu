@@ -10,6 +10,21 @@
 // prefill half given the tail of cu_seqlens (its token rows are absolute).
 #include "common.cuh"
 
+namespace gdn {
+gdn_status prefill_check(const void *q, int64_t q_row_stride, const void *k, int64_t k_row_stride,
+                         const void *v, int64_t v_row_stride, const float *g, const float *beta,
+                         const int32_t *cu_seqlens, int32_t n_seqs, int64_t n_tokens, int32_t hqk,
+                         int32_t hv, int32_t dk, int32_t dv, int32_t chunk, const float *state_pool,
+                         int64_t n_slots, const int32_t *initial_state_indices,
+                         const int32_t *final_state_indices, const void *o, int32_t dtype);
+gdn_status decode_check(const void *q, int64_t q_row_stride, const void *k, int64_t k_row_stride,
+                        const void *v, int64_t v_row_stride, const float *g, const float *beta,
+                        int32_t n_seqs, int32_t tokens_per_seq, int32_t hqk, int32_t hv,
+                        int32_t dk, int32_t dv, const float *state_pool, int64_t n_slots,
+                        const int32_t *state_indices, const void *z, int64_t z_row_stride,
+                        const float *norm_weight, float norm_eps, const void *o, int32_t dtype);
+}  // namespace gdn
+
 extern "C" gdn_status gdn_mixed_batch(
     const void *q, int64_t q_row_stride, const void *k, int64_t k_row_stride, const void *v,
     int64_t v_row_stride, const float *g, const float *beta, const int32_t *cu_seqlens,
@@ -20,13 +35,28 @@ extern "C" gdn_status gdn_mixed_batch(
     void *stream) {
     GDN_REQUIRE(n_seqs >= 0 && n_decode >= 0 && n_decode <= n_seqs && n_tokens >= n_decode,
                 GDN_ERR_INVALID_ARG);
+    // in place: the streaming kernel; otherwise the state after the token
+    // goes to the final slot and the initial one is only read
+    const bool in_place = decode_in_place != 0;
+    // both halves' host checks before either launches
     if (n_decode > 0) {
         // a decode row continues a state: it needs its initial slot
         GDN_REQUIRE(initial_state_indices != nullptr, GDN_ERR_INVALID_ARG);
-        // in place: the streaming kernel; otherwise the state after the
-        // token goes to the final slot and the initial one is only read
-        const bool in_place = decode_in_place != 0;
         GDN_REQUIRE(in_place || final_state_indices != nullptr, GDN_ERR_INVALID_ARG);
+        const gdn_status st = gdn::decode_check(
+            q, q_row_stride, k, k_row_stride, v, v_row_stride, g, beta, n_decode, 1, hqk, hv, dk,
+            dv, state_pool, n_slots, initial_state_indices, nullptr, 0, nullptr, 0.f, o, dtype);
+        if (st != GDN_OK) return st;
+    }
+    if (n_seqs > n_decode) {
+        GDN_REQUIRE(cu_seqlens != nullptr, GDN_ERR_INVALID_ARG);
+        const gdn_status st = gdn::prefill_check(
+            q, q_row_stride, k, k_row_stride, v, v_row_stride, g, beta, cu_seqlens + n_decode,
+            n_seqs - n_decode, n_tokens, hqk, hv, dk, dv, chunk, state_pool, n_slots,
+            initial_state_indices, final_state_indices, o, dtype);
+        if (st != GDN_OK) return st;
+    }
+    if (n_decode > 0) {
         const gdn_status st = gdn_decode_recurrent(
             q, q_row_stride, k, k_row_stride, v, v_row_stride, g, beta, n_decode, 1, hqk, hv, dk,
             dv, scale, l2norm_qk, state_pool, n_slots, initial_state_indices,
@@ -34,7 +64,6 @@ extern "C" gdn_status gdn_mixed_batch(
         if (st != GDN_OK) return st;
     }
     if (n_seqs == n_decode) return GDN_OK;
-    GDN_REQUIRE(cu_seqlens != nullptr, GDN_ERR_INVALID_ARG);
     return gdn_prefill_chunked(
         q, q_row_stride, k, k_row_stride, v, v_row_stride, g, beta, cu_seqlens + n_decode,
         n_seqs - n_decode, n_tokens, hqk, hv, dk, dv, scale, l2norm_qk, chunk, state_pool, n_slots,

@@ -34,17 +34,15 @@ extern "C" size_t gdn_prefill_workspace_size(int32_t n_seqs, int64_t n_tokens, i
     return prefill_split_workspace(n_seqs, n_tokens, hv);
 }
 
-extern "C" gdn_status gdn_prefill_chunked(const void *q, int64_t q_row_stride, const void *k,
-                                          int64_t k_row_stride, const void *v, int64_t v_row_stride,
-                                          const float *g, const float *beta,
-                                          const int32_t *cu_seqlens, int32_t n_seqs,
-                                          int64_t n_tokens, int32_t hqk, int32_t hv, int32_t dk,
-                                          int32_t dv, float scale, int32_t l2norm_qk,
-                                          int32_t chunk, float *state_pool, int64_t n_slots,
-                                          const int32_t *initial_state_indices,
-                                          const int32_t *final_state_indices, void *o,
-                                          int32_t dtype, void *workspace, size_t workspace_bytes,
-                                          void *stream) {
+namespace gdn {
+// The host-side checks of gdn_prefill_chunked, launching nothing: GDN_OK when
+// the call would run (for n_seqs == 0: when it would return GDN_OK).
+gdn_status prefill_check(const void *q, int64_t q_row_stride, const void *k, int64_t k_row_stride,
+                         const void *v, int64_t v_row_stride, const float *g, const float *beta,
+                         const int32_t *cu_seqlens, int32_t n_seqs, int64_t n_tokens, int32_t hqk,
+                         int32_t hv, int32_t dk, int32_t dv, int32_t chunk, const float *state_pool,
+                         int64_t n_slots, const int32_t *initial_state_indices,
+                         const int32_t *final_state_indices, const void *o, int32_t dtype) {
     GDN_REQUIRE(dtype == GDN_F32 || dtype == GDN_BF16, GDN_ERR_INVALID_ARG);
     GDN_REQUIRE(n_seqs >= 0 && n_tokens >= 0 && hqk > 0 && hv > 0 && n_slots >= 0,
                 GDN_ERR_INVALID_ARG);
@@ -61,6 +59,26 @@ extern "C" gdn_status gdn_prefill_chunked(const void *q, int64_t q_row_stride, c
     GDN_REQUIRE(q_row_stride >= (int64_t)hqk * dk && k_row_stride >= (int64_t)hqk * dk &&
                     v_row_stride >= (int64_t)hv * dv,
                 GDN_ERR_INVALID_ARG);
+    return GDN_OK;
+}
+}  // namespace gdn
+
+extern "C" gdn_status gdn_prefill_chunked(const void *q, int64_t q_row_stride, const void *k,
+                                          int64_t k_row_stride, const void *v, int64_t v_row_stride,
+                                          const float *g, const float *beta,
+                                          const int32_t *cu_seqlens, int32_t n_seqs,
+                                          int64_t n_tokens, int32_t hqk, int32_t hv, int32_t dk,
+                                          int32_t dv, float scale, int32_t l2norm_qk,
+                                          int32_t chunk, float *state_pool, int64_t n_slots,
+                                          const int32_t *initial_state_indices,
+                                          const int32_t *final_state_indices, void *o,
+                                          int32_t dtype, void *workspace, size_t workspace_bytes,
+                                          void *stream) {
+    const gdn_status st = prefill_check(q, q_row_stride, k, k_row_stride, v, v_row_stride, g, beta,
+                                        cu_seqlens, n_seqs, n_tokens, hqk, hv, dk, dv, chunk,
+                                        state_pool, n_slots, initial_state_indices,
+                                        final_state_indices, o, dtype);
+    if (st != GDN_OK || n_seqs == 0) return st;
     cudaStream_t s = (cudaStream_t)stream;
     if (n_tokens > 0 && prefill_tc_supported(dtype, dk, dv, chunk, q, q_row_stride, k,
                                              k_row_stride, v, v_row_stride)) {

@@ -352,8 +352,8 @@ gdn_status gdn_decode_step_fused(const void *x, int64_t x_row_stride,
  *   gdn_prefill_workspace_size(n_seqs - n_decode, n_tokens, ...).
  * Other arguments, layouts and errors as gdn_prefill_chunked and
  * gdn_decode_recurrent (the decode rows need dk = dv <= 128 as those do).
- * Returns the first error of the two halves; on an error of the decode half
- * the prefill half is not launched.
+ * Both halves' host-side checks run before either half launches, so a
+ * failed check launches nothing, as for every entry point.
  */
 gdn_status gdn_mixed_batch(const void *q, int64_t q_row_stride, const void *k,
                            int64_t k_row_stride, const void *v,

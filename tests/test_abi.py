@@ -117,6 +117,10 @@ def test_mixed_batch_host_checks(lib):
     bad = list(base); bad[14] = 96       # dk 96: the decode half is unsupported
     bad[15] = 96
     assert m(*bad) == 2
+    # a valid decode half with a prefill half that fails its checks: neither
+    # launches (a launch here, with no GPU, would return GDN_ERR_LAUNCH)
+    bad = list(base); bad[18] = 48       # chunk 48: the prefill half is unsupported
+    assert m(*bad) == 2
     empty = list(base); empty[9] = 0; empty[10] = 0; empty[11] = 0
     assert m(*empty) == 0                # nothing to do: no launch
 
