@@ -8,6 +8,7 @@
 namespace gdn {
 
 GDN_DECLARE_STATUS_WORD(g_status_api)
+gdn_status read_status_norm(uint32_t *out, int clear, cudaStream_t s);   // rmsnorm.cu
 GDN_STATUS_READER(read_status_api, g_status_api)
 
 static thread_local char t_last_err[256] = "";
@@ -89,6 +90,7 @@ gdn_status gdn_get_device_status(uint32_t *out, int32_t clear, void *stream) {
     if ((st = read_status_prefill_tc(out, clear, s)) != GDN_OK) return st;
     if ((st = read_status_prefill_split(out, clear, s)) != GDN_OK) return st;
     if ((st = read_status_decode_step(out, clear, s)) != GDN_OK) return st;
+    if ((st = read_status_norm(out, clear, s)) != GDN_OK) return st;
     return GDN_OK;
 }
 

@@ -27,7 +27,7 @@ def _norm_inputs(seed, T, hv, dv, dtype, zpad=24):
 @pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
 @pytest.mark.parametrize("dv", [16, 64, 128, 256])
 def test_standalone_gated_rmsnorm(dtype, dv):
-    T, hv = 37, 4
+    T, hv = 37, 4        # 16-byte aligned z rows: the bulk-staged kernel
     o, zbig, w = _norm_inputs(dv, T, hv, dv, dtype)
     z = zbig[:, 8:8 + hv * dv].unflatten(1, (hv, dv))
     y = gdn().gdn_gated_rmsnorm(cuda(o), cuda(zbig)[:, 8:8 + hv * dv].unflatten(1, (hv, dv)), cuda(w))
@@ -37,6 +37,23 @@ def test_standalone_gated_rmsnorm(dtype, dv):
     ref = oracle.gated_rmsnorm(to_np(o), to_np(z), to_np(w))
     assert_close(y, ref, TOL[dtype], "y")
     assert bits_equal(yi, y)                    # in place gives the same bits
+
+
+@pytest.mark.parametrize("dtype,hv,dv,off", [(torch.bfloat16, 4, 128, 4),
+                                             (torch.bfloat16, 4, 16, 4),
+                                             (torch.float32, 32, 256, 8)])
+def test_standalone_gated_rmsnorm_register_path(dtype, hv, dv, off):
+    """Shapes the bulk-staged kernel leaves to the register kernel: a z view
+    8 bytes off a 16-byte boundary (bf16), or tokens larger than half a
+    stage (fp32, 32 heads of 256)."""
+    T = 29
+    o, zbig, w = _norm_inputs(dv + off, T, hv, dv, dtype)
+    z = zbig[:, off:off + hv * dv].unflatten(1, (hv, dv))
+    y = gdn().gdn_gated_rmsnorm(cuda(o), cuda(zbig)[:, off:off + hv * dv].unflatten(1, (hv, dv)),
+                                cuda(w))
+    torch.cuda.synchronize()
+    ref = oracle.gated_rmsnorm(to_np(o), to_np(z), to_np(w))
+    assert_close(y, ref, TOL[dtype], "y")
 
 
 def _decode_case(dtype, n, tps, hqk, hv, d, seed):
