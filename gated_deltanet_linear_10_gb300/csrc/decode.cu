@@ -417,8 +417,11 @@ static gdn_status decode_entry(const void *q, int64_t q_row_stride, const void *
     const bool gated = z != nullptr;
     cudaStream_t s = (cudaStream_t)stream;
     cudaError_t e = cudaSuccess;
+    // dv > 64: the norm is a separate pass, so the recurrence takes the plain
+    // launch (and with it the streaming kernel)
+    const bool fused_norm = gated && dv <= 64;
 #define GDN_DEC(DK, T)                                                                          \
-    e = gated ? launch_decode<DK, T, true>(q, q_row_stride, k, k_row_stride, v, v_row_stride, g,  \
+    e = fused_norm ? launch_decode<DK, T, true>(q, q_row_stride, k, k_row_stride, v, v_row_stride, g,  \
                                            beta, n_seqs, tokens_per_seq, hqk, hv, dv, scale,     \
                                            l2norm_qk, state_pool, n_slots, state_indices,        \
                                            snap_indices, z, z_row_stride, norm_weight, norm_eps, \
