@@ -3,8 +3,9 @@ a hand-worked example (tests/golden), special cases with exact answers
 (beta = 0, retrieval with orthonormal keys, k = 0), a brute-force evaluation
 through explicit (I - beta k k^T) matrix products in reverse order, a norm
 bound, the chunked (WY/UT) form against the token form, the UT transform
-against a library inverse, split-and-carry against one pass, and the slot
-rules of prefill / decode / MTP / snapshot."""
+against a library inverse, split-and-carry against one pass, the affine
+dependence on the initial state, and the slot rules of prefill / decode /
+MTP / snapshot."""
 import math
 
 import numpy as np
@@ -286,3 +287,38 @@ def test_layer_chunked_equals_token_tiny():
     assert np.abs(o1 - o2).max() <= 1e-10 * np.abs(o1).max()
     for key in res[None][2]:
         np.testing.assert_allclose(res[w.chunk][2][key], res[None][2][key], rtol=1e-9, atol=1e-12)
+
+
+# ------------------------------------------------- affine state map (scan) --
+
+@pytest.mark.parametrize("form", ["token", "chunked"])
+def test_state_map_is_affine_in_the_initial_state(form):
+    """The chain is affine in its initial state: with dv = dk the identity is
+    a state, the transition is A = S_end(I) - S_end(0), and for any S0,
+    S_end(S0) = S0 A + S_end(0) and o_t(S0) - o_t(0) = S0 (o_t(I) - o_t(0)).
+    Composing two segments' affine maps equals one pass over both.  These
+    are the identities a chunk-state scan over one long sequence rests on."""
+    rng = np.random.default_rng(71 if form == "token" else 72)
+    d, T, m = 16, 53, 20
+    q, k, v, g, beta = _rand_chain(rng, T, d, d)
+
+    def run(S0, lo=0, hi=T):
+        args = (q[lo:hi], k[lo:hi], v[lo:hi], g[lo:hi], beta[lo:hi])
+        if form == "token":
+            return oracle.recurrent_chain(*args, S0=S0, scale=0.3)
+        return oracle.chunked_chain(*args, chunk=8, S0=S0, scale=0.3)
+
+    o0, B = run(np.zeros((d, d)))
+    oI, MI = run(np.eye(d))
+    A = MI - B
+    S0 = rng.normal(size=(d, d)) * 0.1
+    oS, SS = run(S0)
+    np.testing.assert_allclose(SS, S0 @ A + B, rtol=0, atol=1e-10)
+    np.testing.assert_allclose(oS - o0, (S0 @ (oI - o0).T).T, rtol=0, atol=1e-10)
+    # two segments: [0, m) then [m, T), each as (A_p, B_p), composed
+    _, B1 = run(np.zeros((d, d)), 0, m)
+    _, M1 = run(np.eye(d), 0, m)
+    _, B2 = run(np.zeros((d, d)), m, T)
+    _, M2 = run(np.eye(d), m, T)
+    composed = (S0 @ (M1 - B1) + B1) @ (M2 - B2) + B2
+    np.testing.assert_allclose(composed, SS, rtol=0, atol=1e-10)
