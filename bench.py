@@ -51,7 +51,7 @@ def parse_args(argv=None):
     p.add_argument("--warmup", type=int, default=20)
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--no-extras", action="store_true", help="skip the prefill / MTP extras")
-    p.add_argument("--only", choices=["mtp", "prefill"], default=None,
+    p.add_argument("--only", choices=["mtp", "prefill", "long"], default=None,
                    help="profiling aid: run just this extra (its own JSON line, no decode step)")
     p.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle work")
     return p.parse_args(argv)
@@ -200,6 +200,8 @@ def run_only(args):
     flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
     if args.only == "mtp":
         res = bench_mtp(gdn, workloads, dev, flush, steps=max(1, args.steps))
+    elif args.only == "long":
+        res = bench_long(gdn, workloads, dev, flush, load_peaks(), steps=max(1, args.steps))
     else:
         res = bench_prefill(gdn, workloads, dev, flush, load_peaks(), steps=max(1, args.steps))
     assert gdn.gdn_get_device_status(clear=True) == 0
@@ -345,6 +347,7 @@ def run_ours(args):
         extras["prefill"] = bench_prefill(gdn, workloads, dev, flush, peaks)
         extras["decode_gated"] = bench_decode_gated(gdn, workloads, dev, flush)
         extras["mixed"] = bench_mixed(gdn, workloads, dev, flush)
+        extras["long"] = bench_long(gdn, workloads, dev, flush, peaks)
 
     cpu = None
     if rank == 0:
@@ -467,7 +470,7 @@ def bench_mtp(gdn, workloads, dev, flush, steps=50):
     beta = torch.empty_like(g)
     o = torch.empty((T, d.hv, d.dv), dtype=x.dtype, device=dev)
     stream = torch.cuda.current_stream(dev)
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(steps)]
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(steps)]
 
     def step(e=None):
         if e is not None:
@@ -482,6 +485,8 @@ def bench_mtp(gdn, workloads, dev, flush, steps=50):
             e[2].record(stream)
         gdn.gdn_state_snapshot(spool, acc_src, slots)
         gdn.gdn_state_snapshot(cpool, acc_src, slots)
+        if e is not None:
+            e[3].record(stream)
 
     for _ in range(3):
         step()
@@ -493,10 +498,21 @@ def bench_mtp(gdn, workloads, dev, flush, steps=50):
         flush.zero_()
     torch.cuda.synchronize(dev)
     dec = sum(e[1].elapsed_time(e[2]) for e in ev) / steps
+    whole = sum(e[0].elapsed_time(e[3]) for e in ev) / steps
+    front = sum(e[0].elapsed_time(e[1]) for e in ev) / steps
+    accept = sum(e[2].elapsed_time(e[3]) for e in ev) / steps
     # decode kernel algorithmic bytes: source state read once, 4 snapshots written
     st = w.n_seqs * d.hv * d.dv * d.dk * 4
     io = T * (2 * d.hqk * d.dk + 2 * d.hv * d.dv) * 2 + 2 * T * d.hv * 4
     dec_bytes = st * 5 + io
+    # the whole step: conv update (x read, y written, the slot's conv state
+    # read, 4 conv snapshots written), gating (a, b read, g, beta written),
+    # the decode kernel, and the accept copies of both pools (read + write)
+    conv_state = d.channels * 3 * 2
+    conv_bytes = 2 * T * d.channels * 2 + w.n_seqs * conv_state * 5 + d.channels * 4 * 2
+    gate_bytes = 2 * T * d.hv * 2 + 2 * T * d.hv * 4
+    accept_bytes = 2 * w.n_seqs * (d.hv * d.dv * d.dk * 4 + conv_state)
+    step_bytes = conv_bytes + gate_bytes + dec_bytes + accept_bytes
     peak = load_peaks()["hbm_gbs"]
     del spool, w
     return {"workload": "MTP: 128 sequences x 4 tokens, per-token state + conv snapshots, "
@@ -504,6 +520,13 @@ def bench_mtp(gdn, workloads, dev, flush, steps=50):
             "decode_kernel_ms": round(dec, 5),
             "decode_kernel_gbs": round(dec_bytes / (dec / 1e3) / 1e9, 1),
             "decode_kernel_frac_hbm": round(dec_bytes / (dec / 1e3) / 1e9 / peak, 4),
+            "step_ms": round(whole, 5),
+            "tokens_per_s": round(T / (whole / 1e3), 1),
+            "step_bytes": step_bytes,
+            "step_gbs": round(step_bytes / (whole / 1e3) / 1e9, 1),
+            "step_frac_hbm": round(step_bytes / (whole / 1e3) / 1e9 / peak, 4),
+            "conv_update_gating_ms": round(front, 5),
+            "accept_copies_ms": round(accept, 5),
             "gpu_launches_per_step": 5}
 
 
@@ -715,9 +738,78 @@ def bench_prefill(gdn, workloads, dev, flush, peaks, steps=5):
             "flops_per_token": prefill_flops_per_token(d.hv, d.dk, d.dv, w.chunk)}
 
 
+def bench_long(gdn, workloads, dev, flush, peaks, steps=3):
+    """Long-context prefill: one sequence of 65,536 tokens, 16 QK / 32 V heads,
+    head_dim 128, bf16, nonzero initial state (gating + chunked prefill), and
+    the split at 32,768 with the state carried through a pool slot against
+    the single pass."""
+    w = workloads.long_context(device=dev)
+    d = w.dims
+    T = w.q.shape[0]
+    q, k, v, a, b = w.q, w.k, w.v, w.a, w.b
+    A_log, dt_bias = w.A_log.to(dev), w.dt_bias.to(dev)
+    pool = torch.zeros((4, d.hv, d.dv, d.dk), dtype=torch.float32, device=dev)
+    pool[0] = w.state_pool[0]
+    g = torch.empty((T, d.hv), dtype=torch.float32, device=dev)
+    beta = torch.empty_like(g)
+    o = torch.empty((T, d.hv, d.dv), dtype=q.dtype, device=dev)
+    i32 = lambda *x: torch.tensor(x, dtype=torch.int32, device=dev)
+    cu, s0, s1, s2 = i32(0, T), i32(0), i32(1), i32(2)
+    need = gdn.gdn_prefill_workspace_size(1, T, d.hv, d.dk, d.dv, w.chunk)
+    ws = torch.empty(need, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step(e=None):
+        if e is not None:
+            e[0].record(stream)
+        gdn.gdn_gating(a, b, A_log, dt_bias, g=g, beta=beta)
+        if e is not None:
+            e[1].record(stream)
+        gdn.gdn_prefill_chunked(q, k, v, g, beta, cu, pool, s0, s1, w.scale, o=o, workspace=ws)
+        if e is not None:
+            e[2].record(stream)
+
+    for _ in range(2):
+        step()
+        flush.zero_()
+    torch.cuda.synchronize(dev)
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(steps)]
+    for i in range(steps):
+        step(ev[i])
+        flush.zero_()
+    torch.cuda.synchronize(dev)
+    total = sum(e[0].elapsed_time(e[2]) for e in ev) / steps
+    pre = sum(e[1].elapsed_time(e[2]) for e in ev) / steps
+    # split at T/2: [0, T/2) from slot 0 into slot 2, then [T/2, T) from slot 2
+    half = T // 2
+    cu_h = torch.tensor([0, half], dtype=torch.int32, device=dev)
+    o_split = torch.empty_like(o)
+    gdn.gdn_prefill_chunked(q[:half], k[:half], v[:half], g[:half], beta[:half], cu_h, pool, s0,
+                            s2, w.scale, o=o_split[:half], workspace=ws)
+    gdn.gdn_prefill_chunked(q[half:], k[half:], v[half:], g[half:], beta[half:], cu_h, pool, s2,
+                            s2, w.scale, o=o_split[half:], workspace=ws)
+    torch.cuda.synchronize(dev)
+    assert gdn.gdn_get_device_status(clear=True) == 0
+    rel = lambda x, y: float((x.float() - y.float()).abs().max() / y.float().abs().max())
+    flops = prefill_flops_per_token(d.hv, d.dk, d.dv, w.chunk) * T
+    tf = flops / (pre / 1e3) / 1e12
+    res = {"workload": f"long-context prefill: 1 sequence x {T} tokens, nonzero initial state, "
+                       "gating + chunked prefill (chunk 64), 16 QK / 32 V heads, head_dim 128, bf16",
+           "tokens_per_s": round(T / (total / 1e3), 1),
+           "layer_ms": round(total, 4), "prefill_kernel_ms": round(pre, 4),
+           "prefill_tflops": round(tf, 2),
+           "prefill_frac_bf16_peak": round(tf / peaks["bf16_tflops"], 4),
+           "split_at": half,
+           "split_rel_err_o": rel(o_split, o),
+           "split_rel_err_state": rel(pool[2], pool[1]),
+           "workspace_mib": round(need / 2**20, 1)}
+    del w, q, k, v, o, o_split, ws
+    return res
+
+
 # ------------------------------------------------------------ oracle (CPU) --
 
-def _oracle_decode_step(w, n, sub_pool):
+def _oracle_decode_step(w, n, sub_pool, threads=None):
     """The CPU oracle on the first n sequences of a decode step: conv update,
     gating, recurrent decode (the same three steps the GPU step runs)."""
     import numpy as np
@@ -729,7 +821,7 @@ def _oracle_decode_step(w, n, sub_pool):
                                 w.slots[:n].numpy().astype(np.int64))
     q, k, v = oracle.split_qkv(y, d.hqk, d.hv, d.dk, d.dv)
     g, beta = oracle.gating(w.a[:n], w.b[:n], w.A_log, w.dt_bias)
-    oracle.gdn_decode(q, k, v, g, beta, 1, sub_pool, np.arange(n), scale=w.scale)
+    oracle.gdn_decode(q, k, v, g, beta, 1, sub_pool, np.arange(n), scale=w.scale, threads=threads)
 
 
 def cpu_baseline(w, budget_s, n=None):
@@ -746,9 +838,23 @@ def cpu_baseline(w, budget_s, n=None):
         el = time.perf_counter() - t0
         if el >= budget_s or reps >= 1000:
             break
+    # one thread: the first 16 sequences of the step, repeated for ~1/4 of the budget
+    n1 = min(16, n)
+    sub1 = sub[:n1].clone()
+    t1 = time.perf_counter()
+    reps1 = 0
+    while True:
+        _oracle_decode_step(w, n1, sub1, threads=1)
+        reps1 += 1
+        el1 = time.perf_counter() - t1
+        if el1 >= budget_s / 4 or reps1 >= 1000:
+            break
     return {"value": round(reps * n / el, 2), "unit": UNIT, "cores": cores, "kind": "oracle",
             "sample": f"{reps} x decode step of {n} sequences (conv update + gating + "
-                      f"recurrent decode, fp64 C oracle, {cores} threads), {el:.1f} s"}
+                      f"recurrent decode, fp64 C oracle, {cores} threads), {el:.1f} s",
+            "single_thread": {"value": round(reps1 * n1 / el1, 2), "unit": UNIT, "cores": 1,
+                              "sample": f"{reps1} x the first {n1} sequences of the step, "
+                                        f"1 thread, {el1:.1f} s"}}
 
 
 def run_reference(args):

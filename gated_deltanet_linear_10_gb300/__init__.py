@@ -30,6 +30,7 @@ EXPORTS = (
     "gdn_prefill_workspace_size", "gdn_decode_recurrent", "gdn_state_snapshot",
     "gdn_get_device_status", "gdn_prefill_chunked_static", "gdn_gated_rmsnorm",
     "gdn_decode_recurrent_gated", "gdn_decode_step_fused", "gdn_mixed_batch",
+    "gdn_debug_set_wait_limit",
 )
 
 if not os.path.exists(LIB_PATH):
@@ -66,6 +67,7 @@ _SIGS = {
                                    _vp, _f32, _vp, _i32, _vp],
     "gdn_prefill_chunked_static": [_vp, _i64, _vp, _i64, _vp, _i64, _vp, _vp, _vp, _i32, _i64,
                                    _i32, _i32, _f32, _i32, _vp, _i64, _vp, _vp, _vp, _vp],
+    "gdn_debug_set_wait_limit": [ctypes.c_uint64, _i32, _vp],
     "gdn_mixed_batch": [_vp, _i64, _vp, _i64, _vp, _i64, _vp, _vp, _vp, _i32, _i32, _i64, _i32,
                         _i32, _i32, _i32, _f32, _i32, _i32, _vp, _i64, _vp, _vp, _i32, _vp, _i32,
                         _vp, ctypes.c_size_t, _vp],
@@ -480,3 +482,12 @@ def gdn_get_device_status(clear=True, device=None) -> int:
     _check(_lib.gdn_get_device_status(ctypes.byref(out), int(clear), _stream(device)),
            "gdn_get_device_status")
     return int(out.value)
+
+
+def gdn_debug_set_wait_limit(limit_ns=0, drop_prep_loads=False, device=None):
+    """Test control of the two-kernel prefill's failure path: the limit of its
+    bounded waits (0 = the default, one second) and whether the prep kernel
+    skips its K|Q loads (its waits then run out and the call sets
+    DEVSTAT_TIMEOUT; its results are undefined).  Synchronises the stream."""
+    _check(_lib.gdn_debug_set_wait_limit(int(limit_ns), int(bool(drop_prep_loads)),
+                                         _stream(device)), "gdn_debug_set_wait_limit")

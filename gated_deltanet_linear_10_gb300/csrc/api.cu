@@ -18,6 +18,15 @@ void set_last_cuda_error(cudaError_t e) {
              cudaGetErrorString(e));
 }
 
+int sm_count() {
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+        sms <= 0)
+        return 1;
+    return sms;
+}
+
 gdn_status launch_status() {
     cudaError_t e = cudaGetLastError();
     if (e == cudaSuccess) return GDN_OK;
@@ -91,6 +100,7 @@ gdn_status gdn_get_device_status(uint32_t *out, int32_t clear, void *stream) {
     if ((st = read_status_prefill_split(out, clear, s)) != GDN_OK) return st;
     if ((st = read_status_decode_step(out, clear, s)) != GDN_OK) return st;
     if ((st = read_status_norm(out, clear, s)) != GDN_OK) return st;
+    if ((st = read_status_mixed(out, clear, s)) != GDN_OK) return st;
     return GDN_OK;
 }
 

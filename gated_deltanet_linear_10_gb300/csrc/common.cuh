@@ -21,6 +21,7 @@ namespace gdn {
 // Host helpers implemented in api.cu.
 void set_last_cuda_error(cudaError_t e);
 gdn_status launch_status();  // cudaGetLastError() after a launch -> status
+int sm_count();              // multiprocessors of the current device
 
 // Per-TU readers of the status word (defined next to each word).
 gdn_status read_status_gating(uint32_t *out, int clear, cudaStream_t s);
@@ -31,6 +32,7 @@ gdn_status read_status_prefill_tc(uint32_t *out, int clear, cudaStream_t s);
 gdn_status read_status_prefill_split(uint32_t *out, int clear, cudaStream_t s);
 gdn_status read_status_decode_step(uint32_t *out, int clear, cudaStream_t s);
 gdn_status read_status_api(uint32_t *out, int clear, cudaStream_t s);
+gdn_status read_status_mixed(uint32_t *out, int clear, cudaStream_t s);
 
 #define GDN_STATUS_READER(fn, word)                                             \
     gdn_status fn(uint32_t *out, int clear, cudaStream_t s) {                  \

@@ -41,7 +41,8 @@ extern "C" gdn_status gdn_gating(const void *a, const void *b, const float *A_lo
     const int64_t n = n_tokens * hv;
     const int threads = 256;
     int64_t blocks = (n + threads - 1) / threads;
-    if (blocks > 152 * 16) blocks = 152 * 16;
+    const int64_t max_blocks = (int64_t)sm_count() * 16;   // 16 CTAs of 256 per SM
+    if (blocks > max_blocks) blocks = max_blocks;
     cudaStream_t s = (cudaStream_t)stream;
     if (in_dtype == GDN_F32)
         gating_kernel<float><<<(unsigned)blocks, threads, 0, s>>>(

@@ -11,6 +11,19 @@
 #include "common.cuh"
 
 namespace gdn {
+
+GDN_DECLARE_STATUS_WORD(g_status_mixed)
+GDN_STATUS_READER(read_status_mixed, g_status_mixed)
+
+// The decode rows must be one token each at rows 0 .. n_decode-1:
+// cu_seqlens[i] == i for i <= n_decode.  A batch that breaks this is still
+// run (the decode kernels read rows 0 .. n_decode-1) but is reported.
+__global__ void mixed_check_kernel(const int32_t *__restrict__ cu, int n_decode) {
+    for (int i = blockIdx.x * blockDim.x + threadIdx.x; i <= n_decode;
+         i += gridDim.x * blockDim.x)
+        if (cu[i] != i) flag_status(GDN_DEVSTAT_BAD_SEQLEN);
+}
+
 gdn_status prefill_check(const void *q, int64_t q_row_stride, const void *k, int64_t k_row_stride,
                          const void *v, int64_t v_row_stride, const float *g, const float *beta,
                          const int32_t *cu_seqlens, int32_t n_seqs, int64_t n_tokens, int32_t hqk,
@@ -53,10 +66,17 @@ extern "C" gdn_status gdn_mixed_batch(
         const gdn_status st = gdn::prefill_check(
             q, q_row_stride, k, k_row_stride, v, v_row_stride, g, beta, cu_seqlens + n_decode,
             n_seqs - n_decode, n_tokens, hqk, hv, dk, dv, chunk, state_pool, n_slots,
-            initial_state_indices, final_state_indices, o, dtype);
+            initial_state_indices ? initial_state_indices + n_decode : nullptr,
+            final_state_indices ? final_state_indices + n_decode : nullptr, o, dtype);
         if (st != GDN_OK) return st;
     }
     if (n_decode > 0) {
+        if (cu_seqlens) {
+            gdn::mixed_check_kernel<<<(n_decode + 256) / 256, 256, 0, (cudaStream_t)stream>>>(
+                cu_seqlens, n_decode);
+            const gdn_status st = gdn::launch_status();
+            if (st != GDN_OK) return st;
+        }
         const gdn_status st = gdn_decode_recurrent(
             q, q_row_stride, k, k_row_stride, v, v_row_stride, g, beta, n_decode, 1, hqk, hv, dk,
             dv, scale, l2norm_qk, state_pool, n_slots, initial_state_indices,

@@ -30,6 +30,10 @@ namespace gdn {
 GDN_DECLARE_STATUS_WORD(g_status_prefill_split)
 GDN_STATUS_READER(read_status_prefill_split, g_status_prefill_split)
 
+// Debug control (gdn_debug_set_wait_limit): when set, the prep kernel issues
+// no K|Q tile load, so its waits for that tile run out after the wait limit.
+__device__ int g_prep_drop_loads = 0;
+
 namespace psp {
 using namespace ptc;
 
@@ -178,10 +182,14 @@ prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
 
     if (warp == 0) {
         if (lane == 0) {
-            mbar_arrive_expect_tx(&B.kq_full, kKQBytes);
-            for (int kb = 0; kb < 2; ++kb) {
-                tma_load_2d(kq + kb * kKBlk, &tm_k, &B.kq_full, hq * DH + kb * 64, (int)c0);
-                tma_load_2d(kq + kb * kKBlk + 64 * 128, &tm_q, &B.kq_full, hq * DH + kb * 64, (int)c0);
+            const bool drop = *(volatile int *)&g_prep_drop_loads != 0;
+            if (!drop) {
+                mbar_arrive_expect_tx(&B.kq_full, kKQBytes);
+                for (int kb = 0; kb < 2; ++kb) {
+                    tma_load_2d(kq + kb * kKBlk, &tm_k, &B.kq_full, hq * DH + kb * 64, (int)c0);
+                    tma_load_2d(kq + kb * kKBlk + 64 * 128, &tm_q, &B.kq_full, hq * DH + kb * 64,
+                                (int)c0);
+                }
             }
             uint64_t *last = nullptr;   // the last commit: TMEM is freed once it completes
             if (mbar_wait(&B.kq_full, 0, abort)) {
@@ -206,7 +214,7 @@ prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
                     mma_commit(&B.w_full);
                     last = &B.w_full;
                 }
-            } else {
+            } else if (!drop) {
                 int z = 0;       // never leave with the copy in flight
                 mbar_wait(&B.kq_full, 0, &z);
             }
@@ -504,8 +512,10 @@ chain_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
         // ------------------------------------------------ the two MMA issuers
         // Issuer A (warp 1): M2 over a < 64, M6, O2.
         // Issuer B (warp 10): M2 over a >= 64, O1, and MU(c + 1) once M6 has
-        // left the tensor pipe (issued earlier, it slows M6 down more than it
-        // gains).
+        // left the tensor pipe.  Measured: issued by A right behind M6 (A then
+        // waits for the next item's operands before O2 and its stage
+        // releases), the prefill took 0.448 ms against 0.414; issued by B as
+        // soon as M6 is issued, it made no difference.
         if (lane == 0) {
             const bool isA = warp == 1;
             const uint32_t id64 = idesc_bf16(128, 64);
@@ -620,7 +630,7 @@ chain_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
             const ItemScal &I = scal(c);             // c_full(c) was waited one chunk earlier
             const int64_t c0 = s_start + (int64_t)c * C;
             const bool last = c == nch - 1;
-            const int n = I.n;
+            const int n = (int)min((int64_t)C, s_end - c0);   // rows of this chunk (bounds from cu)
             // ---- E2: U = U1 + U2 (this half) -> U16 = bf16(U), U16k = bf16(U diag(ks))
             mbar_wait(&B.u_full, c & 1, abort);
             tc_fence_after();
@@ -793,3 +803,25 @@ gdn_status prefill_split(const void *q, int64_t qs, const void *k, int64_t ks, c
 }
 
 }  // namespace gdn
+
+using namespace gdn;
+
+// Test control of the failure path of the two-kernel prefill: the wait limit
+// of its kernels and the prep kernel's K|Q loads (see gdn.h).
+extern "C" gdn_status gdn_debug_set_wait_limit(uint64_t limit_ns, int32_t drop_prep_loads,
+                                               void *stream) {
+    const uint64_t lim = limit_ns ? limit_ns : tc::kWaitLimitNs;
+    const int drop = drop_prep_loads != 0;
+    cudaStream_t s = (cudaStream_t)stream;
+    cudaError_t e = cudaMemcpyToSymbolAsync(tc::g_wait_limit_ns, &lim, sizeof(lim), 0,
+                                            cudaMemcpyHostToDevice, s);
+    if (e == cudaSuccess)
+        e = cudaMemcpyToSymbolAsync(g_prep_drop_loads, &drop, sizeof(drop), 0,
+                                    cudaMemcpyHostToDevice, s);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);   // the sources live on this stack
+    if (e != cudaSuccess) {
+        set_last_cuda_error(e);
+        return GDN_ERR_CUDA;
+    }
+    return GDN_OK;
+}

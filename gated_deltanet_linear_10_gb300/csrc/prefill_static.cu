@@ -38,10 +38,11 @@ gdn_status static_scratch(void **out) {
     if (!g_scratch_addr[dev]) {
         void *p = nullptr;
         e = cudaGetSymbolAddress(&p, g_prefill_static_scratch);
-        if (e != cudaSuccess || !p) {
+        if (e != cudaSuccess) {
             set_last_cuda_error(e);
             return GDN_ERR_CUDA;
         }
+        if (!p) return GDN_ERR_LAUNCH;   // no CUDA error to report: the lookup gave no address
         g_scratch_addr[dev] = p;
     }
     *out = g_scratch_addr[dev];

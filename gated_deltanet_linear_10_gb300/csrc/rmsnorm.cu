@@ -1,5 +1,6 @@
-// Gated RMSNorm of the layer output ("gated RMSNorm", LightLLM blog on the
-// Qwen3next kernels; the pages name the kernel without a formula):
+// Gated RMSNorm of the layer output ("gated RMSNorm", "[model] Support
+// Qwen3next", LightLLM issue 1097, Highlights; the page names the kernel
+// without a formula):
 //   y = o / sqrt(mean(o^2) + eps) * w * SiLU(z)
 // per (token, V head) row of dv values, normalising first, then gating.
 //

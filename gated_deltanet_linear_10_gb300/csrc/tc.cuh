@@ -20,6 +20,9 @@ namespace tc {
 
 // A bounded wait gives up after this long and reports a timeout.
 constexpr uint64_t kWaitLimitNs = 1000ull * 1000ull * 1000ull;   // 1 s
+// The limit in force: one copy per translation unit (a debug entry point
+// may shorten it for the two-kernel prefill; kWaitLimitNs otherwise).
+static __device__ uint64_t g_wait_limit_ns = kWaitLimitNs;
 
 __device__ __forceinline__ uint32_t smem_u32(const void *p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -62,15 +65,16 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
     return ok != 0;
 }
 // Waits for the phase with the given parity to complete.  Gives up (returns
-// false) once *abort is set by any thread of the CTA, or after kWaitLimitNs,
-// in which case it sets *abort itself.
+// false) once *abort is set by any thread of the CTA, or after the wait limit
+// (g_wait_limit_ns), in which case it sets *abort itself.
 __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, volatile int *abort) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = globaltimer_ns();
+    const uint64_t limit = *(volatile uint64_t *)&g_wait_limit_ns;
     while (true) {
         if (mbar_try_wait(bar, parity)) return true;
         if (*abort) return false;
-        if (globaltimer_ns() - t0 > kWaitLimitNs) {
+        if (globaltimer_ns() - t0 > limit) {
             *abort = 1;
             return false;
         }

@@ -262,8 +262,9 @@ gdn_status gdn_decode_recurrent(const void *q, int64_t q_row_stride,
                                 int32_t dtype, void *stream);
 
 /*
- * Gated RMSNorm of the layer output ("gated RMSNorm", LightLLM blog on the
- * Qwen3next kernels; the pages name the kernel without a formula).  Reading
+ * Gated RMSNorm of the layer output ("gated RMSNorm", "[model] Support
+ * Qwen3next", LightLLM issue 1097, Highlights; the page names the kernel
+ * without a formula).  Reading
  * taken: per (token, V head) row of dv values
  *   y = o / sqrt(mean(o^2) + eps) * weight * SiLU(z)     (normalise, then gate)
  *   o, y: [n_tokens][hv][dv] contiguous, `dtype`; y may be o (in place).
@@ -353,7 +354,10 @@ gdn_status gdn_decode_step_fused(const void *x, int64_t x_row_stride,
  * Other arguments, layouts and errors as gdn_prefill_chunked and
  * gdn_decode_recurrent (the decode rows need dk = dv <= 128 as those do).
  * Both halves' host-side checks run before either half launches, so a
- * failed check launches nothing, as for every entry point.
+ * failed check launches nothing, as for every entry point.  A batch whose
+ * cu_seqlens[i] != i for some i <= n_decode breaks the decode-row layout:
+ * it still runs (the decode half reads rows 0 .. n_decode-1) and sets
+ * GDN_DEVSTAT_BAD_SEQLEN.
  */
 gdn_status gdn_mixed_batch(const void *q, int64_t q_row_stride, const void *k,
                            int64_t k_row_stride, const void *v,
@@ -383,6 +387,21 @@ gdn_status gdn_mixed_batch(const void *q, int64_t q_row_stride, const void *k,
 gdn_status gdn_state_snapshot(void *pool, int64_t n_slots, int64_t slot_bytes,
                               const int32_t *src, const int32_t *dst,
                               int32_t n, void *stream);
+
+/*
+ * Test control of the failure path (not for production use).  Sets the limit
+ * of every bounded wait inside the two-kernel tensor-core prefill (the prep
+ * and chain kernels of gdn_prefill_chunked with a workspace) to limit_ns
+ * nanoseconds on the current device; 0 restores the default of one second.
+ * With drop_prep_loads != 0 the prep kernel issues none of its K|Q tile
+ * loads, so the waits for them run out after the limit: the kernel then
+ * skips its stores, drains, frees its tensor memory, returns and sets
+ * GDN_DEVSTAT_TIMEOUT, and the results of that call are undefined (every
+ * index stays in bounds; the context stays usable).  Synchronises `stream`.
+ * Restore both (0, 0) before production calls.
+ */
+gdn_status gdn_debug_set_wait_limit(uint64_t limit_ns, int32_t drop_prep_loads,
+                                    void *stream);
 
 /*
  * Reads the device status word (bits GDN_DEVSTAT_*) of the current device

@@ -68,7 +68,8 @@ def lib():
                                          ctypes.c_int, ctypes.c_double, ctypes.c_int,
                                          ctypes.c_double, ctypes.c_int, P, P]
         for f in (L.oracle_gating, L.oracle_conv1d_seq, L.oracle_l2norm,
-                  L.oracle_gdn_recurrent, L.oracle_ut_transform, L.oracle_gdn_chunked):
+                  L.oracle_gated_rmsnorm, L.oracle_gdn_recurrent, L.oracle_ut_transform,
+                  L.oracle_gdn_chunked):
             f.restype = None
         _lib = L
     return _lib

@@ -302,8 +302,9 @@ void oracle_gdn_chunked(const double *q, const double *k, const double *v,
 }
 
 /*
- * Gated RMSNorm of the layer output ("gated RMSNorm", LightLLM blog on the
- * Qwen3next kernels; the pages name the kernel without a formula).  Reading
+ * Gated RMSNorm of the layer output ("gated RMSNorm", "[model] Support
+ * Qwen3next", LightLLM issue 1097, Highlights; the page names the kernel
+ * without a formula).  Reading
  * taken: per (token, V head) row of dv values,
  *   y = o / sqrt(mean(o^2) + eps) * w * SiLU(z)
  * normalising first, then gating.  o, z, y: [n][d]; w: [d].

@@ -2,7 +2,8 @@
 SiLU(z)) through the C ABI against the CPU oracle: the standalone kernel
 over head sizes, dtypes, a strided z and in place, and the decode kernel
 with the norm fused into its output (full decode size, MTP with snapshots,
-the one-CTA and the two-CTA-cluster layouts, a padding row)."""
+the one-CTA layout at dv <= 64 and, at dv = 128, the two-CTA layout
+followed by the norm kernel in place; a padding row)."""
 import numpy as np
 import pytest
 import torch
@@ -74,8 +75,8 @@ def _decode_case(dtype, n, tps, hqk, hv, d, seed):
 @pytest.mark.parametrize("d", [64, 128])
 @pytest.mark.parametrize("tps", [1, 4])
 def test_decode_gated_small(d, tps):
-    """d = 64: one CTA per state; d = 128: two CTAs per state launched as a
-    cluster.  tps = 4 writes per-token snapshots.  Sequence 1 has no slot."""
+    """d = 64: one CTA per state, the norm in its epilogue; d = 128: two
+    CTAs per state, then the norm kernel in place.  tps = 4 writes per-token snapshots.  Sequence 1 has no slot."""
     dtype = torch.bfloat16
     n, hqk, hv = 6, 2, 4
     q, k, v, a, b, A_log, dt_bias, z, w, pool = _decode_case(dtype, n, tps, hqk, hv, d, 31 * d + tps)

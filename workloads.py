@@ -257,19 +257,29 @@ def mixed(seed=1006, n_decode=256, prefill_lens=(2048, 2048), n_slots=1024, dims
 
 
 def long_context(seed=1004, T=65536, dims: Dims = FULL, dtype=torch.bfloat16, chunk=64,
-                 n_slots=2, low_decay=False):
+                 n_slots=2, low_decay=False, device="cpu"):
     """One sequence of T tokens with q/k/v/a/b ~ N(0, 1) drawn directly (no
-    conv), initial state slot 0 ~ N(0, 0.02), final state to slot 1."""
+    conv), initial state slot 0 ~ N(0, 0.02), final state to slot 1.  On a
+    CUDA device the tensors are drawn there, from that device's generator
+    (same seed and distributions, a different stream of numbers from the CPU
+    one): the fast path for timing runs, which compare with no oracle."""
     d = dims
-    gen = _gen(seed)
-    q = _normal(gen, (T, d.hqk, d.dk), dtype=dtype)
-    k = _normal(gen, (T, d.hqk, d.dk), dtype=dtype)
-    v = _normal(gen, (T, d.hv, d.dv), dtype=dtype)
-    a = _normal(gen, (T, d.hv), dtype=dtype)
-    b = _normal(gen, (T, d.hv), dtype=dtype)
-    A_log, dt_bias = gating_params(gen, d.hv, low_decay)
-    pool = torch.zeros((n_slots, d.hv, d.dv, d.dk))
-    pool[0] = _normal(gen, (d.hv, d.dv, d.dk), 0.02)
+    gen = torch.Generator(device=device)
+    gen.manual_seed(seed)
+
+    def normal(shape, std=1.0):
+        return (torch.randn(shape, generator=gen, dtype=torch.float32, device=device)
+                * std).to(dtype)
+
+    q = normal((T, d.hqk, d.dk))
+    k = normal((T, d.hqk, d.dk))
+    v = normal((T, d.hv, d.dv))
+    a = normal((T, d.hv))
+    b = normal((T, d.hv))
+    A_log, dt_bias = gating_params(_gen(seed + 1) if device != "cpu" else gen, d.hv, low_decay)
+    pool = torch.zeros((n_slots, d.hv, d.dv, d.dk), device=device)
+    pool[0] = (torch.randn((d.hv, d.dv, d.dk), generator=gen, dtype=torch.float32,
+                           device=device) * 0.02)
     return Workload(
         name=f"long_T{T}", dims=d, dtype=dtype, chunk=chunk, scale=d.dk ** -0.5,
         cu_seqlens=torch.tensor([0, T], dtype=torch.int32), n_seqs=1, q=q, k=k, v=v,
