@@ -707,6 +707,27 @@ def bench_prefill(gdn, workloads, dev, flush, peaks, steps=5):
     norm_ms = sum(e[0].elapsed_time(e[1]) for e in ev) / steps
     norm_bytes = 3 * o.numel() * o.element_size()
 
+    # the prefill with the gated RMSNorm in the chain kernel's epilogue (y
+    # instead of o), after the layer's conv and gating
+    y_gated = torch.empty_like(o)
+
+    def gated():
+        gdn.gdn_prefill_chunked_gated(qv, kv, vv, g, beta, cu, spool, none, sslots, w.scale, z,
+                                      nw, 1e-6, chunk=w.chunk, y=y_gated, workspace=ws)
+
+    step()
+    for _ in range(2):
+        gated()
+        flush.zero_()
+    torch.cuda.synchronize(dev)
+    for i in range(steps):
+        ev[i][0].record(stream)
+        gated()
+        ev[i][1].record(stream)
+        flush.zero_()
+    torch.cuda.synchronize(dev)
+    gated_ms = sum(e[0].elapsed_time(e[1]) for e in ev) / steps
+
     for _ in range(2):
         step()
         flush.zero_()
@@ -732,6 +753,9 @@ def bench_prefill(gdn, workloads, dev, flush, peaks, steps=5):
             "prefill_tflops": round(tf, 2),
             "gated_norm_ms": round(norm_ms, 4),
             "gated_norm_gbs": round(norm_bytes / (norm_ms / 1e3) / 1e9, 1),
+            "prefill_gated_kernel_ms": round(gated_ms, 4),
+            "gated_layer_ms": round(total - pre + gated_ms, 4),
+            "gated_layer_tokens_per_s": round(T / ((total - pre + gated_ms) / 1e3), 1),
             "prep_kernel_traffic_bytes": profile_traffic("prep_kernel", SPLIT_SOURCES),
             "chain_kernel_traffic_bytes": profile_traffic("chain_kernel", SPLIT_SOURCES),
             "prefill_frac_bf16_peak": round(tf / peaks["bf16_tflops"], 4),
@@ -754,7 +778,7 @@ def bench_long(gdn, workloads, dev, flush, peaks, steps=3):
     beta = torch.empty_like(g)
     o = torch.empty((T, d.hv, d.dv), dtype=q.dtype, device=dev)
     i32 = lambda *x: torch.tensor(x, dtype=torch.int32, device=dev)
-    cu, s0, s1, s2 = i32(0, T), i32(0), i32(1), i32(2)
+    cu, s0, s1, s2, s3 = i32(0, T), i32(0), i32(1), i32(2), i32(3)
     need = gdn.gdn_prefill_workspace_size(1, T, d.hv, d.dk, d.dv, w.chunk)
     ws = torch.empty(need, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
@@ -780,6 +804,22 @@ def bench_long(gdn, workloads, dev, flush, peaks, steps=3):
     torch.cuda.synchronize(dev)
     total = sum(e[0].elapsed_time(e[2]) for e in ev) / steps
     pre = sum(e[1].elapsed_time(e[2]) for e in ev) / steps
+    # the same sequence on the serial chain (a workspace without the scan's part)
+    serial_ws = torch.empty(1024 + ((T + 63) // 64 + 1) * d.hv * 33 * 1024, dtype=torch.uint8,
+                            device=dev)
+    o_serial = torch.empty_like(o)
+    ev_s = [torch.cuda.Event(enable_timing=True) for _ in range(2 * steps)]
+    for i in range(steps + 1):
+        if i:
+            ev_s[2 * i - 2].record(stream)
+        gdn.gdn_prefill_chunked(q, k, v, g, beta, cu, pool, s0, s3, w.scale, o=o_serial,
+                                workspace=serial_ws)
+        if i:
+            ev_s[2 * i - 1].record(stream)
+        flush.zero_()
+    torch.cuda.synchronize(dev)
+    pre_serial = sum(ev_s[2 * i].elapsed_time(ev_s[2 * i + 1]) for i in range(steps)) / steps
+    del serial_ws
     # split at T/2: [0, T/2) from slot 0 into slot 2, then [T/2, T) from slot 2
     half = T // 2
     cu_h = torch.tensor([0, half], dtype=torch.int32, device=dev)
@@ -799,11 +839,15 @@ def bench_long(gdn, workloads, dev, flush, peaks, steps=3):
            "layer_ms": round(total, 4), "prefill_kernel_ms": round(pre, 4),
            "prefill_tflops": round(tf, 2),
            "prefill_frac_bf16_peak": round(tf / peaks["bf16_tflops"], 4),
+           "prefill_path": "chunk-state scan: two segments, 3 x 32 chain CTAs",
+           "serial_prefill_kernel_ms": round(pre_serial, 4),
+           "scan_vs_serial_rel_err_o": rel(o, o_serial),
+           "scan_vs_serial_rel_err_state": rel(pool[1], pool[3]),
            "split_at": half,
            "split_rel_err_o": rel(o_split, o),
            "split_rel_err_state": rel(pool[2], pool[1]),
            "workspace_mib": round(need / 2**20, 1)}
-    del w, q, k, v, o, o_split, ws
+    del w, q, k, v, o, o_split, o_serial, ws
     return res
 
 

@@ -30,7 +30,7 @@ EXPORTS = (
     "gdn_prefill_workspace_size", "gdn_decode_recurrent", "gdn_state_snapshot",
     "gdn_get_device_status", "gdn_prefill_chunked_static", "gdn_gated_rmsnorm",
     "gdn_decode_recurrent_gated", "gdn_decode_step_fused", "gdn_mixed_batch",
-    "gdn_debug_set_wait_limit",
+    "gdn_debug_set_wait_limit", "gdn_prefill_chunked_gated",
 )
 
 if not os.path.exists(LIB_PATH):
@@ -68,6 +68,9 @@ _SIGS = {
     "gdn_prefill_chunked_static": [_vp, _i64, _vp, _i64, _vp, _i64, _vp, _vp, _vp, _i32, _i64,
                                    _i32, _i32, _f32, _i32, _vp, _i64, _vp, _vp, _vp, _vp],
     "gdn_debug_set_wait_limit": [ctypes.c_uint64, _i32, _vp],
+    "gdn_prefill_chunked_gated": [_vp, _i64, _vp, _i64, _vp, _i64, _vp, _vp, _vp, _i32, _i64,
+                                  _i32, _i32, _i32, _i32, _f32, _i32, _i32, _vp, _i64, _vp, _vp,
+                                  _vp, _i64, _vp, _f32, _vp, _i32, _vp, ctypes.c_size_t, _vp],
     "gdn_mixed_batch": [_vp, _i64, _vp, _i64, _vp, _i64, _vp, _vp, _vp, _i32, _i32, _i64, _i32,
                         _i32, _i32, _i32, _f32, _i32, _i32, _vp, _i64, _vp, _vp, _i32, _vp, _i32,
                         _vp, ctypes.c_size_t, _vp],
@@ -255,6 +258,57 @@ def gdn_prefill_chunked(q, k, v, g, beta, cu_seqlens, state_pool, initial_state_
                                     _ptr(o), dt, _ptr(workspace), wbytes, _stream(q.device)),
            "gdn_prefill_chunked")
     return o
+
+
+def gdn_prefill_chunked_gated(q, k, v, g, beta, cu_seqlens, state_pool, initial_state_indices,
+                              final_state_indices, scale, z, norm_weight, norm_eps=1e-6, chunk=64,
+                              l2norm_qk=True, y=None, workspace=None):
+    """gdn_prefill_chunked writing y = RMSNorm(o) * norm_weight * SiLU(z) per
+    (token, V head) row instead of o.  z: [T, hv, dv] (a view with a free row
+    stride); norm_weight [dv] fp32.  Returns y [T, hv, dv].  workspace as for
+    gdn_prefill_chunked."""
+    _cuda(q, k, v, g, beta, cu_seqlens, state_pool, initial_state_indices, final_state_indices,
+          z, norm_weight)
+    T, hqk, dk = q.shape
+    hv, dv = v.shape[1], v.shape[2]
+    qs = _heads_view(q, hqk, dk, "q")
+    ks = _heads_view(k, hqk, dk, "k")
+    vs = _heads_view(v, hv, dv, "v")
+    zs = _heads_view(z, hv, dv, "z")
+    _need(q.dtype == k.dtype == v.dtype == z.dtype, "q, k, v, z: one dtype")
+    _need(z.shape[0] == T, "z: [T, hv, dv]")
+    _need(norm_weight.dtype == torch.float32 and norm_weight.is_contiguous()
+          and norm_weight.shape == (dv,), "norm_weight: [dv] fp32")
+    _need(g.dtype == torch.float32 and beta.dtype == torch.float32 and g.is_contiguous()
+          and beta.is_contiguous() and g.shape == (T, hv) and beta.shape == (T, hv), "g, beta")
+    _need(state_pool.dtype == torch.float32 and state_pool.is_contiguous()
+          and state_pool.shape[1:] == (hv, dv, dk), "state_pool: [slots, hv, dv, dk] fp32")
+    _i32_vec(cu_seqlens, "cu_seqlens")
+    n = cu_seqlens.numel() - 1
+    for name, t in (("initial_state_indices", initial_state_indices),
+                    ("final_state_indices", final_state_indices)):
+        if t is not None:
+            _i32_vec(t, name)
+            _need(t.numel() == n, f"{name}: [n_seqs]")
+    y = torch.empty((T, hv, dv), dtype=q.dtype, device=q.device) if y is None else y
+    _need(y.is_contiguous() and y.shape == (T, hv, dv), "y: [T, hv, dv] contiguous")
+    dt = _dtype_code(q)
+    if workspace is False:
+        workspace = None
+    elif workspace is None:
+        need = gdn_prefill_workspace_size(n, T, hv, dk, dv, chunk, dt)
+        if need:
+            workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    else:
+        _cuda(workspace)
+    wbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(_lib.gdn_prefill_chunked_gated(
+        _ptr(q), qs, _ptr(k), ks, _ptr(v), vs, _ptr(g), _ptr(beta), _ptr(cu_seqlens), n, T, hqk,
+        hv, dk, dv, float(scale), int(l2norm_qk), chunk, _ptr(state_pool), state_pool.shape[0],
+        _ptr(initial_state_indices), _ptr(final_state_indices), _ptr(z), zs, _ptr(norm_weight),
+        float(norm_eps), _ptr(y), dt, _ptr(workspace), wbytes, _stream(q.device)),
+        "gdn_prefill_chunked_gated")
+    return y
 
 
 def gdn_mixed_batch(q, k, v, g, beta, cu_seqlens, n_decode, state_pool, initial_state_indices,

@@ -15,11 +15,23 @@ gdn_status prefill_tc(const void *q, int64_t qs, const void *k, int64_t ks, cons
                       float *pool, int64_t n_slots, const int32_t *ii, const int32_t *fi,
                       void *o, cudaStream_t s);
 size_t prefill_split_workspace(int n_seqs, int64_t n_tokens, int hv);
+bool prefill_scan_sized(int n_seqs, int64_t n_tokens);
+bool prefill_scan_fits(int hv);
+size_t prefill_scan_workspace(int64_t n_tokens, int hv);
+gdn_status prefill_scan(const void *q, int64_t qs, const void *k, int64_t ks, const void *v,
+                        int64_t vs, const float *g, const float *beta, const int32_t *cu,
+                        int64_t n_tokens, int hqk, int hv, float scale, int l2norm, float *pool,
+                        int64_t n_slots, const int32_t *ii, const int32_t *fi, void *o, void *ws,
+                        cudaStream_t s);
 gdn_status prefill_split(const void *q, int64_t qs, const void *k, int64_t ks, const void *v,
                          int64_t vs, const float *g, const float *beta, const int32_t *cu,
                          int n_seqs, int64_t n_tokens, int hqk, int hv, float scale, int l2norm,
                          float *pool, int64_t n_slots, const int32_t *ii, const int32_t *fi,
-                         void *o, void *ws, cudaStream_t s);
+                         void *o, void *ws, cudaStream_t s, const void *z = nullptr,
+                         int64_t zs = 0, const float *norm_w = nullptr, float norm_eps = 0.f);
+gdn_status norm_check(const void *o, const void *z, int64_t z_row_stride, const float *weight,
+                      int64_t n_tokens, int32_t hv, int32_t dv, float eps, const void *y,
+                      int32_t dtype);
 }  // namespace gdn
 
 using namespace gdn;
@@ -31,7 +43,10 @@ extern "C" size_t gdn_prefill_workspace_size(int32_t n_seqs, int64_t n_tokens, i
                                              int32_t dtype) {
     if (n_seqs <= 0 || n_tokens <= 0 || hv <= 0) return 0;
     if (dtype != GDN_BF16 || dk != 128 || dv != 128 || chunk != 64) return 0;
-    return prefill_split_workspace(n_seqs, n_tokens, hv);
+    const size_t split = prefill_split_workspace(n_seqs, n_tokens, hv);
+    if (!prefill_scan_sized(n_seqs, n_tokens)) return split;
+    const size_t scan = prefill_scan_workspace(n_tokens, hv);
+    return scan > split ? scan : split;
 }
 
 namespace gdn {
@@ -82,8 +97,15 @@ extern "C" gdn_status gdn_prefill_chunked(const void *q, int64_t q_row_stride, c
     cudaStream_t s = (cudaStream_t)stream;
     if (n_tokens > 0 && prefill_tc_supported(dtype, dk, dv, chunk, q, q_row_stride, k,
                                              k_row_stride, v, v_row_stride)) {
-        if (workspace && ((uintptr_t)workspace & 15u) == 0 && ((uintptr_t)o & 15u) == 0 &&
-            workspace_bytes >= prefill_split_workspace(n_seqs, n_tokens, hv))
+        const bool ws_ok = workspace && ((uintptr_t)workspace & 15u) == 0 &&
+                           ((uintptr_t)o & 15u) == 0;
+        if (ws_ok && prefill_scan_sized(n_seqs, n_tokens) && prefill_scan_fits(hv) &&
+            workspace_bytes >= prefill_scan_workspace(n_tokens, hv))
+            return prefill_scan(q, q_row_stride, k, k_row_stride, v, v_row_stride, g, beta,
+                                cu_seqlens, n_tokens, hqk, hv, scale, l2norm_qk, state_pool,
+                                n_slots, initial_state_indices, final_state_indices, o,
+                                workspace, s);
+        if (ws_ok && workspace_bytes >= prefill_split_workspace(n_seqs, n_tokens, hv))
             return prefill_split(q, q_row_stride, k, k_row_stride, v, v_row_stride, g, beta,
                                  cu_seqlens, n_seqs, n_tokens, hqk, hv, scale, l2norm_qk,
                                  state_pool, n_slots, initial_state_indices,
@@ -95,4 +117,45 @@ extern "C" gdn_status gdn_prefill_chunked(const void *q, int64_t q_row_stride, c
     return prefill_simt(dtype, dk, chunk, q, q_row_stride, k, k_row_stride, v, v_row_stride, g,
                         beta, cu_seqlens, n_seqs, n_tokens, hqk, hv, scale, l2norm_qk,
                         state_pool, n_slots, initial_state_indices, final_state_indices, o, s);
+}
+
+// The prefill with the gated RMSNorm written instead of o.  On the two-kernel
+// tensor-core path (a workspace, one chain per (sequence, V head)) the norm
+// runs in the chain kernel's output epilogue; every other path is the prefill
+// into y followed by gdn_gated_rmsnorm in place.
+extern "C" gdn_status gdn_prefill_chunked_gated(
+    const void *q, int64_t q_row_stride, const void *k, int64_t k_row_stride, const void *v,
+    int64_t v_row_stride, const float *g, const float *beta, const int32_t *cu_seqlens,
+    int32_t n_seqs, int64_t n_tokens, int32_t hqk, int32_t hv, int32_t dk, int32_t dv,
+    float scale, int32_t l2norm_qk, int32_t chunk, float *state_pool, int64_t n_slots,
+    const int32_t *initial_state_indices, const int32_t *final_state_indices, const void *z,
+    int64_t z_row_stride, const float *norm_weight, float norm_eps, void *y, int32_t dtype,
+    void *workspace, size_t workspace_bytes, void *stream) {
+    gdn_status st = prefill_check(q, q_row_stride, k, k_row_stride, v, v_row_stride, g, beta,
+                                  cu_seqlens, n_seqs, n_tokens, hqk, hv, dk, dv, chunk,
+                                  state_pool, n_slots, initial_state_indices,
+                                  final_state_indices, y, dtype);
+    if (st != GDN_OK || n_seqs == 0) return st;
+    st = norm_check(y, z, z_row_stride, norm_weight, n_tokens, hv, dv, norm_eps, y, dtype);
+    if (st != GDN_OK) return st;
+    cudaStream_t s = (cudaStream_t)stream;
+    const bool ws_ok = workspace && ((uintptr_t)workspace & 15u) == 0 && ((uintptr_t)y & 15u) == 0;
+    const bool scan = prefill_scan_sized(n_seqs, n_tokens) && prefill_scan_fits(hv) &&
+                      workspace_bytes >= prefill_scan_workspace(n_tokens, hv);
+    if (n_tokens > 0 && ws_ok && !scan &&
+        prefill_tc_supported(dtype, dk, dv, chunk, q, q_row_stride, k, k_row_stride, v,
+                             v_row_stride) &&
+        ((uintptr_t)z & 15u) == 0 && (z_row_stride % 8) == 0 &&
+        workspace_bytes >= prefill_split_workspace(n_seqs, n_tokens, hv))
+        return prefill_split(q, q_row_stride, k, k_row_stride, v, v_row_stride, g, beta,
+                             cu_seqlens, n_seqs, n_tokens, hqk, hv, scale, l2norm_qk, state_pool,
+                             n_slots, initial_state_indices, final_state_indices, y, workspace, s,
+                             z, z_row_stride, norm_weight, norm_eps);
+    st = gdn_prefill_chunked(q, q_row_stride, k, k_row_stride, v, v_row_stride, g, beta,
+                             cu_seqlens, n_seqs, n_tokens, hqk, hv, dk, dv, scale, l2norm_qk,
+                             chunk, state_pool, n_slots, initial_state_indices,
+                             final_state_indices, y, dtype, workspace, workspace_bytes, stream);
+    if (st != GDN_OK) return st;
+    return gdn_gated_rmsnorm(y, z, z_row_stride, norm_weight, n_tokens, hv, dv, norm_eps, y,
+                             dtype, stream);
 }

@@ -23,7 +23,10 @@
 //
 // Workspace: [chunk offsets, int32 x (n_seqs + 1), padded to 1 KiB]
 //            [items: (ceil(n_tokens / 64) + n_seqs) x hv blocks of kItemBytes]
+#include <stddef.h>
+
 #include "prefill_common.cuh"
+#include "prefill_scan.cuh"
 
 namespace gdn {
 
@@ -377,46 +380,100 @@ struct ChainBars {
     uint64_t kq_full[kKQStages], kq_empty[kKQStages], v_full[kVStages], v_empty[kVStages],
         d_full[kDStages], d_empty[kDStages], c_full[kCStages], c_empty[kCStages];
     uint64_t mu_full, u_full, u2_full, s_full, o1_full, o2_full, s_next, o_free, done_a, done_b;
+    uint64_t zbar[8];             // per epilogue warp: its z tile of the chunk (gated output)
     uint32_t tmem_base;
     int abort;
     int seq;
 };
-constexpr uint32_t C_OFF_KQ = 0;
-constexpr uint32_t C_OFF_V = C_OFF_KQ + kKQStages * kKQBytes;
-constexpr uint32_t C_OFF_D = C_OFF_V + kVStages * kVBytes;
-constexpr uint32_t C_OFF_C = C_OFF_D + kDStages * kItemOps;
 constexpr uint32_t kOTileBytes = 32 * 32 * 2;               // one warp's o tile [i][b]
-constexpr uint32_t C_OFF_OT = C_OFF_C + kCStages * kCStageBytes;
-constexpr uint32_t C_OFF_BARS = C_OFF_OT + 8 * kOTileBytes;
-constexpr uint32_t C_SMEM_BYTES = C_OFF_BARS + (sizeof(ChainBars) + 127) / 128 * 128 + 1024;
+// gated output: [half][chunk parity][warp][token] sums of squares, then
+// [warp][token] inverse norms
+constexpr uint32_t kRedBytes = 2 * 2 * 4 * 32 * 4 + 8 * 32 * 4;
+// Shared memory of the chain kernel.  The gated variant stages each warp's z
+// tile in a buffer of its own (so the next chunk's z load waits for no o
+// store) and pays for it with a K|Q ring of two stages instead of three.
+template <bool kGated>
+struct ChainSmem {
+    static constexpr int kKQ = kGated ? 2 : kKQStages;     // K|Q ring depth
+    static constexpr uint32_t KQ = 0;
+    static constexpr uint32_t V = KQ + kKQ * kKQBytes;
+    static constexpr uint32_t D = V + kVStages * kVBytes;
+    static constexpr uint32_t Cs = D + kDStages * kItemOps;
+    static constexpr uint32_t OT = Cs + kCStages * kCStageBytes;
+    static constexpr uint32_t ZT = OT + 8 * kOTileBytes;   // gated: z tiles
+    static constexpr uint32_t RED = ZT + (kGated ? 8 * kOTileBytes : 0);
+    static constexpr uint32_t BARS = RED + (kGated ? kRedBytes : 0);
+    static constexpr uint32_t BYTES = BARS + (sizeof(ChainBars) + 127) / 128 * 128 + 1024;
+};
 static_assert(kItemOps % 1024 == 0 && kItemScalCopy <= kCStageBytes, "stage layout");
-static_assert(C_SMEM_BYTES <= 232448, "shared memory budget");
+static_assert(ChainSmem<false>::BYTES <= 232448 && ChainSmem<true>::BYTES <= 232448,
+              "shared memory budget");
 
+// Chains beyond the n_seqs * hv ordinary ones (the chunk-state scan): chain
+// j runs sequence seq0 + j from the identity state with v = 0, so that its
+// final state is the sequence's state transition A (S_end = S_0 A + B) and
+// its outputs Phi the map from S_0 to o (o = o(S_0 = 0) + S_0 Phi); Phi rows
+// are counted from the sequence start.  Its final state goes to pool_out
+// slot final0 + j.
+struct IdentChains {
+    int n;
+    int seq0;
+    int final0;
+};
+
+// The gated output (kGated): y = o / sqrt(mean(o^2) + eps) * w * SiLU(z) per
+// (token, V head) row, written instead of o.
+struct GateArgs {
+    const float *w;    // [128] fp32
+    float eps;
+};
+
+// Reduce-scatter step of 32 per-lane values over the warp: with N values
+// left, lanes whose bit N/2 is set keep the upper half, the others the lower,
+// each adding its partner's copy.  After N = 32, 16, 8, 4, 2 lane l holds the
+// warp's sum of value l.
+template <int N>
+__device__ __forceinline__ void reduce_scatter_step(float (&v)[32], int lane) {
+    constexpr int H = N / 2;
+    const bool up = (lane & H) != 0;
+#pragma unroll
+    for (int j = 0; j < H; ++j) {
+        const float send = up ? v[j] : v[H + j];
+        const float keep = up ? v[H + j] : v[j];
+        v[j] = keep + __shfl_xor_sync(0xffffffffu, send, H);
+    }
+}
+
+template <bool kGated>
 __global__ void __launch_bounds__(kChainKernelThreads, 1)
 chain_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
              const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
-             const int32_t *__restrict__ cu,
+             const __grid_constant__ CUtensorMap tm_phi, const __grid_constant__ CUtensorMap tm_z,
+             GateArgs gate, const int32_t *__restrict__ cu,
              const int32_t *__restrict__ base, int n_seqs, int64_t n_tokens, int hv, int grp,
-             const uint8_t *__restrict__ items, float *__restrict__ pool, int64_t n_slots,
-             const int32_t *__restrict__ init_idx, const int32_t *__restrict__ final_idx,
-             __nv_bfloat16 *__restrict__ o) {
+             const uint8_t *__restrict__ items, const float *__restrict__ pool_in, int64_t n_in,
+             float *__restrict__ pool_out, int64_t n_out, const int32_t *__restrict__ init_idx,
+             const int32_t *__restrict__ final_idx, __nv_bfloat16 *__restrict__ o,
+             __nv_bfloat16 *__restrict__ phi, IdentChains ic) {
+    using L = ChainSmem<kGated>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                               ~uintptr_t(1023));
-    ChainBars &B = *reinterpret_cast<ChainBars *>(sm + C_OFF_BARS);
+    ChainBars &B = *reinterpret_cast<ChainBars *>(sm + L::BARS);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
     const int rank = blockIdx.x / hv;
     const int h = blockIdx.x - rank * hv;
     const int hq = h / grp;
-    const int seq = seq_for_rank(cu, n_seqs, rank, &B.seq);
+    const bool ident = rank >= n_seqs;                // CTA-uniform
+    const int seq = ident ? ic.seq0 + (rank - n_seqs) : seq_for_rank(cu, n_seqs, rank, &B.seq);
     const int64_t s_start = cu[seq], s_end = cu[seq + 1];
-    int64_t islot = init_idx ? init_idx[seq] : -1;
-    int64_t fslot = final_idx ? final_idx[seq] : -1;
-    if (islot >= n_slots || fslot >= n_slots) {
+    int64_t islot = ident ? -1 : (init_idx ? init_idx[seq] : -1);
+    int64_t fslot = ident ? ic.final0 + (rank - n_seqs) : (final_idx ? final_idx[seq] : -1);
+    if (islot >= n_in || fslot >= n_out) {
         if (tid == 0) flag_status(GDN_DEVSTAT_BAD_INDEX);
-        if (islot >= n_slots) islot = -1;
-        if (fslot >= n_slots) fslot = -1;
+        if (islot >= n_in) islot = -1;
+        if (fslot >= n_out) fslot = -1;
     }
     if (s_start < 0 || s_end < s_start || s_end > n_tokens) {
         if (tid == 0) flag_status(GDN_DEVSTAT_BAD_SEQLEN);
@@ -425,13 +482,18 @@ chain_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
     const int nch = (int)((s_end - s_start + C - 1) / C);
     const size_t head_off = (size_t)h * DH * DH;
     const size_t slot_stride = (size_t)hv * DH * DH;
-    if (nch == 0) {   // empty sequence: the initial state (or zero) is the final state
+    if (nch == 0) {   // empty sequence: the initial state (zero, identity) is the final state
         if (fslot >= 0)
             for (int e = tid; e < DH * DH; e += kChainKernelThreads)
-                pool[fslot * slot_stride + head_off + e] =
-                    islot >= 0 ? pool[islot * slot_stride + head_off + e] : 0.f;
+                pool_out[fslot * slot_stride + head_off + e] =
+                    ident ? ((e >> 7) == (e & 127) ? 1.f : 0.f)
+                          : (islot >= 0 ? pool_in[islot * slot_stride + head_off + e] : 0.f);
         return;
     }
+    // the output rows: o at absolute rows, Phi from the sequence start
+    const CUtensorMap *tm_out = ident ? &tm_phi : &tm_o;
+    __nv_bfloat16 *out = ident ? phi : o;
+    const int64_t row0 = ident ? s_start : 0;
     const int64_t item0 = base[seq];
 
     if (warp == 1) {
@@ -439,7 +501,7 @@ chain_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
         tmem_relinquish();
     }
     if (tid == 0) {
-        for (int s = 0; s < kKQStages; ++s) { mbar_init(&B.kq_full[s], 1); mbar_init(&B.kq_empty[s], 1); }
+        for (int s = 0; s < L::kKQ; ++s) { mbar_init(&B.kq_full[s], 1); mbar_init(&B.kq_empty[s], 1); }
         for (int s = 0; s < kVStages; ++s) { mbar_init(&B.v_full[s], 1); mbar_init(&B.v_empty[s], 1); }
         for (int s = 0; s < kDStages; ++s) { mbar_init(&B.d_full[s], 1); mbar_init(&B.d_empty[s], 1); }
         for (int s = 0; s < kCStages; ++s) { mbar_init(&B.c_full[s], 1); mbar_init(&B.c_empty[s], kEpiThreads); }
@@ -453,6 +515,7 @@ chain_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
         mbar_init(&B.o_free, kEpiThreads);
         mbar_init(&B.done_a, 1);
         mbar_init(&B.done_b, 1);
+        for (int w = 0; w < 8; ++w) mbar_init(&B.zbar[w], 1);
         B.abort = 0;
         fence_mbar_init();
     }
@@ -467,38 +530,40 @@ chain_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
         if (lane == 0) {
             prefetch_tensormap(&tm_q);
             prefetch_tensormap(&tm_k);
-            prefetch_tensormap(&tm_v);
-            int kq_n[kKQStages] = {0, 0, 0}, v_n[kVStages] = {0, 0}, d_n[kDStages] = {0, 0},
+            if (!ident) prefetch_tensormap(&tm_v);
+            int kq_n[L::kKQ] = {}, v_n[kVStages] = {0, 0}, d_n[kDStages] = {0, 0},
                 c_n[kCStages] = {0, 0, 0, 0};
             for (int c = 0; c < nch && !*abort; ++c) {
                 const int y = (int)(s_start + (int64_t)c * C);
                 const uint8_t *item = items + ((item0 + c) * hv + h) * kItemBytes;
-                const int sk = c % kKQStages, sv = c % kVStages, sd = c % kDStages, sc = c % kCStages;
-                if (c >= kKQStages) mbar_wait(&B.kq_empty[sk], ((c / kKQStages) - 1) & 1, abort);
-                uint8_t *kq = sm + C_OFF_KQ + sk * kKQBytes;
+                const int sk = c % L::kKQ, sv = c % kVStages, sd = c % kDStages, sc = c % kCStages;
+                if (c >= L::kKQ) mbar_wait(&B.kq_empty[sk], ((c / L::kKQ) - 1) & 1, abort);
+                uint8_t *kq = sm + L::KQ + sk * kKQBytes;
                 mbar_arrive_expect_tx(&B.kq_full[sk], kKQBytes);
                 for (int kb = 0; kb < 2; ++kb) {
                     tma_load_2d(kq + kb * kKBlk, &tm_k, &B.kq_full[sk], hq * DH + kb * 64, y);
                     tma_load_2d(kq + kb * kKBlk + 64 * 128, &tm_q, &B.kq_full[sk], hq * DH + kb * 64, y);
                 }
-                kq_n[sk] = c / kKQStages + 1;
+                kq_n[sk] = c / L::kKQ + 1;
                 if (c >= kCStages) mbar_wait(&B.c_empty[sc], ((c / kCStages) - 1) & 1, abort);
                 mbar_arrive_expect_tx(&B.c_full[sc], kItemScalCopy);
-                bulk_load(sm + C_OFF_C + sc * kCStageBytes, item + kItemOps, kItemScalCopy, &B.c_full[sc]);
+                bulk_load(sm + L::Cs + sc * kCStageBytes, item + kItemOps, kItemScalCopy, &B.c_full[sc]);
                 c_n[sc] = c / kCStages + 1;
                 if (c >= kDStages) mbar_wait(&B.d_empty[sd], ((c / kDStages) - 1) & 1, abort);
                 mbar_arrive_expect_tx(&B.d_full[sd], kItemOps);
-                bulk_load(sm + C_OFF_D + sd * kItemOps, item, kItemOps, &B.d_full[sd]);
+                bulk_load(sm + L::D + sd * kItemOps, item, kItemOps, &B.d_full[sd]);
                 d_n[sd] = c / kDStages + 1;
-                if (c >= kVStages) mbar_wait(&B.v_empty[sv], ((c / kVStages) - 1) & 1, abort);
-                uint8_t *vt = sm + C_OFF_V + sv * kVBytes;
-                mbar_arrive_expect_tx(&B.v_full[sv], kVBytes);
-                for (int kb = 0; kb < 2; ++kb)
-                    tma_load_2d(vt + kb * kVBlk, &tm_v, &B.v_full[sv], h * DH + kb * 64, y);
-                v_n[sv] = c / kVStages + 1;
+                if (!ident) {   // v = 0 in an identity chain: no V tiles, no MU
+                    if (c >= kVStages) mbar_wait(&B.v_empty[sv], ((c / kVStages) - 1) & 1, abort);
+                    uint8_t *vt = sm + L::V + sv * kVBytes;
+                    mbar_arrive_expect_tx(&B.v_full[sv], kVBytes);
+                    for (int kb = 0; kb < 2; ++kb)
+                        tma_load_2d(vt + kb * kVBlk, &tm_v, &B.v_full[sv], h * DH + kb * 64, y);
+                    v_n[sv] = c / kVStages + 1;
+                }
             }
             // never leave with copies in flight: wait for the last load of every stage
-            for (int s = 0; s < kKQStages; ++s)
+            for (int s = 0; s < L::kKQ; ++s)
                 if (kq_n[s]) { int z = 0; mbar_wait(&B.kq_full[s], (kq_n[s] - 1) & 1, &z); }
             for (int s = 0; s < kCStages; ++s)
                 if (c_n[s]) { int z = 0; mbar_wait(&B.c_full[s], (c_n[s] - 1) & 1, &z); }
@@ -529,28 +594,28 @@ chain_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
                 mbar_wait(&B.d_full[sd], (c / kDStages) & 1, abort);
                 mbar_wait(&B.v_full[sv], (c / kVStages) & 1, abort);
                 tc_fence_after();
-                const uint32_t dsm = smem_u32(sm + C_OFF_D + sd * kItemOps);
-                const uint32_t vsm = smem_u32(sm + C_OFF_V + sv * kVBytes);
+                const uint32_t dsm = smem_u32(sm + L::D + sd * kItemOps);
+                const uint32_t vsm = smem_u32(sm + L::V + sv * kVBytes);
                 for (int s = 0; s < 4; ++s)
                     mma_ss(tbase + kColU1, sdesc_sw128(vsm + s * 16 * 128, kVBlk, 1024),
                            sdesc_sw128(dsm + kItemT1 + s * 32, 16, 1024), id64amn, s > 0);
                 mma_commit(&B.v_empty[sv]);
                 mma_commit(&B.mu_full);
             };
-            if (!isA) issue_mu(0);
+            if (!isA && !ident) issue_mu(0);
             for (int c = 0; c < nch; ++c) {
-                const int sk = c % kKQStages, sd = c % kDStages;
-                const uint32_t kqb = smem_u32(sm + C_OFF_KQ + sk * kKQBytes);
-                const uint32_t dsm = smem_u32(sm + C_OFF_D + sd * kItemOps);
-                mbar_wait(&B.kq_full[sk], (c / kKQStages) & 1, abort);
+                const int sk = c % L::kKQ, sd = c % kDStages;
+                const uint32_t kqb = smem_u32(sm + L::KQ + sk * kKQBytes);
+                const uint32_t dsm = smem_u32(sm + L::D + sd * kItemOps);
+                mbar_wait(&B.kq_full[sk], (c / L::kKQ) & 1, abort);
                 mbar_wait(&B.d_full[sd], (c / kDStages) & 1, abort);
-                if (isA) mbar_wait(&B.mu_full, c & 1, abort);   // M2 accumulates onto MU
+                if (isA && !ident) mbar_wait(&B.mu_full, c & 1, abort);   // M2 accumulates onto MU
                 mbar_wait(&B.s_next, c & 1, abort);      // S16 of this chunk
                 tc_fence_after();
                 for (int s = s0; s < s0 + 4; ++s)   // M2: U(1|2) (+)= S16 W'^T over this a half
                     mma_ts(tbase + ucol, tbase + kColS16 + s * 8,
                            sdesc_sw128(dsm + kItemW + s * 16 * 128, 8192, 1024), id64bmn,
-                           isA || s > s0);
+                           (isA && !ident) || s > s0);
                 mma_commit(&B.u_full);
                 if (isA) {
                     mbar_wait(&B.u2_full, c & 1, abort);     // U16, U16k in TMEM
@@ -579,7 +644,7 @@ chain_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
                     }
                     mma_commit(&B.o1_full);
                     mbar_wait(&B.s_full, c & 1, abort);      // M6 done (and E2 has read U1)
-                    if (c + 1 < nch) issue_mu(c + 1);
+                    if (c + 1 < nch && !ident) issue_mu(c + 1);
                 }
             }
             mma_commit(isA ? &B.done_a : &B.done_b);
@@ -596,14 +661,28 @@ chain_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
         const uint32_t lrow = tmem_addr(tbase, q4 * 32, 0);
         const uint32_t s32 = lrow + kColS32 + hf * 64, s16 = lrow + kColS16 + hf * 32;
         auto scal = [&](int c) -> const ItemScal & {
-            return *reinterpret_cast<const ItemScal *>(sm + C_OFF_C + (c % kCStages) * kCStageBytes);
+            return *reinterpret_cast<const ItemScal *>(sm + L::Cs + (c % kCStages) * kCStageBytes);
         };
+        __nv_bfloat16 *ot = reinterpret_cast<__nv_bfloat16 *>(sm + L::OT + (warp - 2) * kOTileBytes);
+        __nv_bfloat16 *zt = reinterpret_cast<__nv_bfloat16 *>(sm + L::ZT + (warp - 2) * kOTileBytes);
+        // gated: this warp's z tile (32 tokens x 32 value rows) of chunk c,
+        // TMA-loaded one chunk ahead
+        auto load_z = [&](int c) {
+            mbar_arrive_expect_tx(&B.zbar[warp - 2], kOTileBytes);
+            tma_load_2d(zt, &tm_z, &B.zbar[warp - 2], h * DH + q4 * 32,
+                        (int)(s_start + (int64_t)c * C + 32 * hf));
+        };
+        float wb = 0.f;
+        if constexpr (kGated) {
+            wb = gate.w[b];
+            if (lane == 0) load_z(0);
+        }
         // E0: this half of the initial state -> bf16 operand copy, and the
         //     fp32 accumulator pre-scaled by the first chunk's total decay
         {
             mbar_wait(&B.c_full[0], 0, abort);
             const float gn = scal(0).gam_n;
-            const float *src = islot >= 0 ? pool + islot * slot_stride + head_off + (size_t)b * DH + hf * 64
+            const float *src = islot >= 0 ? pool_in + islot * slot_stride + head_off + (size_t)b * DH + hf * 64
                                           : nullptr;
             for (int c0 = 0; c0 < 64; c0 += 32) {
                 uint32_t v[32], pk[16];
@@ -612,6 +691,10 @@ chain_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
                     const float4 f = src ? *reinterpret_cast<const float4 *>(src + c0 + j) : make_float4(0.f, 0.f, 0.f, 0.f);
                     v[j] = __float_as_uint(f.x); v[j + 1] = __float_as_uint(f.y);
                     v[j + 2] = __float_as_uint(f.z); v[j + 3] = __float_as_uint(f.w);
+                }
+                if (ident) {   // S_0 = I: row b holds a one in column b
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) v[j] = __float_as_uint(hf * 64 + c0 + j == b ? 1.f : 0.f);
                 }
 #pragma unroll
                 for (int jj = 0; jj < 16; ++jj)
@@ -685,7 +768,7 @@ chain_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
                     tmem_st32(s32 + cc, *reinterpret_cast<uint32_t(*)[32]>(sv + cc));
                 }
             } else if (fslot >= 0) {
-                float *dstp = pool + fslot * slot_stride + head_off + (size_t)b * DH + hf * 64;
+                float *dstp = pool_out + fslot * slot_stride + head_off + (size_t)b * DH + hf * 64;
 #pragma unroll
                 for (int j = 0; j < 64; j += 4)
                     *reinterpret_cast<float4 *>(dstp + j) = make_float4(
@@ -704,47 +787,82 @@ chain_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
                 // o rows 32 hf + i of column b; a full tile leaves through TMA,
                 // a partial last one through plain stores
                 const float4 *sq4 = reinterpret_cast<const float4 *>(I.sq + 32 * hf);
+                float f[32];
+#pragma unroll
+                for (int q = 0; q < 8; ++q) {
+                    const float4 s4 = sq4[q];
+                    f[4 * q] = fmaf(s4.x, __uint_as_float(o1[4 * q]), __uint_as_float(o2[4 * q]));
+                    f[4 * q + 1] = fmaf(s4.y, __uint_as_float(o1[4 * q + 1]), __uint_as_float(o2[4 * q + 1]));
+                    f[4 * q + 2] = fmaf(s4.z, __uint_as_float(o1[4 * q + 2]), __uint_as_float(o2[4 * q + 2]));
+                    f[4 * q + 3] = fmaf(s4.w, __uint_as_float(o1[4 * q + 3]), __uint_as_float(o2[4 * q + 3]));
+                }
+                if constexpr (kGated) {
+                    // sum of o^2 over the 128 value rows of each token: the
+                    // warp's 32 rows by a reduce-scatter (lane l: token l),
+                    // then the warpgroup's four warps through shared memory
+                    float v[32];
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) v[i] = f[i] * f[i];
+                    reduce_scatter_step<32>(v, lane);
+                    reduce_scatter_step<16>(v, lane);
+                    reduce_scatter_step<8>(v, lane);
+                    reduce_scatter_step<4>(v, lane);
+                    reduce_scatter_step<2>(v, lane);
+                    float *red = reinterpret_cast<float *>(sm + L::RED) + (hf * 2 + (c & 1)) * 128;
+                    red[q4 * 32 + lane] = v[0];
+                    named_sync(1 + hf, 128);
+                    const float ss = red[lane] + red[32 + lane] + red[64 + lane] + red[96 + lane];
+                    // each lane's token norm, read back by every lane as 8 float4
+                    float *rs = reinterpret_cast<float *>(sm + L::RED) + 512 + (warp - 2) * 32;
+                    rs[lane] = rsqrtf(ss * (1.0f / DH) + gate.eps);
+                    __syncwarp();
+                    mbar_wait(&B.zbar[warp - 2], c & 1, abort);
+                    // y = o rstd w SiLU(z): the fast exponential and division
+                    // (a few fp32 ulp, below the bf16 rounding of y); the
+                    // epilogue is issue-bound, so the exact reciprocal cost
+                    // a third of the chain's time
+#pragma unroll
+                    for (int q = 0; q < 8; ++q) {
+                        const float4 r4 = reinterpret_cast<const float4 *>(rs)[q];
+                        const float rr[4] = {r4.x, r4.y, r4.z, r4.w};
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const float zz = __bfloat162float(zt[(4 * q + e) * 32 + lane]);
+                            f[4 * q + e] *= rr[e] * wb * __fdividef(zz, 1.0f + __expf(-zz));
+                        }
+                    }
+                    fence_async_smem();      // z reads (generic) before the next z load (async)
+                    __syncwarp();
+                    if (c + 1 < nch && lane == 0 && !*abort) load_z(c + 1);
+                }
                 if (32 * hf + 32 <= n) {
-                    __nv_bfloat16 *ot = reinterpret_cast<__nv_bfloat16 *>(sm + C_OFF_OT + (warp - 2) * kOTileBytes);
                     if (lane == 0) bulk_wait_read_all();     // the last tile has left
                     __syncwarp();
 #pragma unroll
-                    for (int q = 0; q < 8; ++q) {
-                        const float4 f = sq4[q];
-                        const float fs[4] = {f.x, f.y, f.z, f.w};
-#pragma unroll
-                        for (int e = 0; e < 4; ++e) {
-                            const int i = 4 * q + e;
-                            ot[i * 32 + lane] = __float2bfloat16_rn(
-                                fmaf(fs[e], __uint_as_float(o1[i]), __uint_as_float(o2[i])));
-                        }
-                    }
+                    for (int i = 0; i < 32; ++i) ot[i * 32 + lane] = __float2bfloat16_rn(f[i]);
                     fence_async_smem();
                     __syncwarp();
                     if (lane == 0) {
-                        tma_store_2d(&tm_o, ot, h * DH + q4 * 32, (int)(c0 + 32 * hf));
+                        tma_store_2d(tm_out, ot, h * DH + q4 * 32, (int)(c0 - row0 + 32 * hf));
                         bulk_commit();
                     }
                 } else {
                     const int64_t ostride = (int64_t)hv * DH;
-                    __nv_bfloat16 *orow = o + ((c0 + 32 * hf) * hv + h) * (int64_t)DH + b;
+                    __nv_bfloat16 *orow = out + ((c0 - row0 + 32 * hf) * hv + h) * (int64_t)DH + b;
 #pragma unroll
-                    for (int q = 0; q < 8; ++q) {
-                        const float4 f = sq4[q];
-                        const float fs[4] = {f.x, f.y, f.z, f.w};
-#pragma unroll
-                        for (int e = 0; e < 4; ++e) {
-                            const int i = 4 * q + e;
-                            if (32 * hf + i < n)
-                                orow[i * ostride] = __float2bfloat16_rn(
-                                    fmaf(fs[e], __uint_as_float(o1[i]), __uint_as_float(o2[i])));
-                        }
-                    }
+                    for (int i = 0; i < 32; ++i)
+                        if (32 * hf + i < n) orow[i * ostride] = __float2bfloat16_rn(f[i]);
                 }
             }
             mbar_arrive(&B.c_empty[c % kCStages]);
         }
         if (lane == 0) bulk_wait_read_all();         // the staged o tiles have been read
+        if constexpr (kGated) {
+            if (lane == 0) {   // never leave with a z load in flight
+                int z = 0;
+                mbar_wait(&B.zbar[warp - 2], (nch - 1) & 1, &z);
+            }
+        }
         __syncwarp();
     }
     tc_fence_before();
@@ -767,21 +885,28 @@ gdn_status prefill_split(const void *q, int64_t qs, const void *k, int64_t ks, c
                          int64_t vs, const float *g, const float *beta, const int32_t *cu,
                          int n_seqs, int64_t n_tokens, int hqk, int hv, float scale, int l2norm,
                          float *pool, int64_t n_slots, const int32_t *ii, const int32_t *fi,
-                         void *o, void *ws, cudaStream_t s) {
+                         void *o, void *ws, cudaStream_t s, const void *z, int64_t zs,
+                         const float *norm_w, float norm_eps) {
     const int64_t items = psp::chunk_bound(n_tokens, n_seqs) * hv;
     if (items >= (1ll << 31)) return GDN_ERR_UNSUPPORTED;
-    CUtensorMap tq, tk, tv, to;
+    CUtensorMap tq, tk, tv, to, tz;
     const uint64_t rows = (uint64_t)n_tokens;
+    const bool gated = z != nullptr;
     if (!encode_tmap_2d_bf16(&tq, q, (uint64_t)hqk * 128, rows, qs, 64, 64) ||
         !encode_tmap_2d_bf16(&tk, k, (uint64_t)hqk * 128, rows, ks, 64, 64) ||
         !encode_tmap_2d_bf16(&tv, v, (uint64_t)hv * 128, rows, vs, 64, 64) ||
-        !encode_tmap_2d_bf16(&to, o, (uint64_t)hv * 128, rows, (uint64_t)hv * 128, 32, 32, false))
+        !encode_tmap_2d_bf16(&to, o, (uint64_t)hv * 128, rows, (uint64_t)hv * 128, 32, 32, false) ||
+        (gated && !encode_tmap_2d_bf16(&tz, z, (uint64_t)hv * 128, rows, (uint64_t)zs, 32, 32, false)))
         return GDN_ERR_LAUNCH;
     cudaError_t e = cudaFuncSetAttribute(psp::prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)psp::P_SMEM_BYTES);
     if (e == cudaSuccess)
-        e = cudaFuncSetAttribute(psp::chain_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)psp::C_SMEM_BYTES);
+        e = gated ? cudaFuncSetAttribute(psp::chain_kernel<true>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)psp::ChainSmem<true>::BYTES)
+                  : cudaFuncSetAttribute(psp::chain_kernel<false>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)psp::ChainSmem<false>::BYTES);
     if (e != cudaSuccess) {
         set_last_cuda_error(e);
         return GDN_ERR_LAUNCH;
@@ -795,11 +920,110 @@ gdn_status prefill_split(const void *q, int64_t qs, const void *k, int64_t ks, c
         tq, tk, g, beta, cu, base, n_seqs, hv, hv / hqk, scale, l2norm, item_blocks);
     st = launch_status();
     if (st != GDN_OK) return st;
-    psp::chain_kernel<<<(unsigned)((int64_t)n_seqs * hv), psp::kChainKernelThreads,
-                        psp::C_SMEM_BYTES, s>>>(tq, tk, tv, to, cu, base, n_seqs, n_tokens, hv,
-                                                hv / hqk, item_blocks, pool, n_slots, ii, fi,
-                                                (__nv_bfloat16 *)o);
+    const unsigned grid = (unsigned)((int64_t)n_seqs * hv);
+    if (gated)
+        psp::chain_kernel<true><<<grid, psp::kChainKernelThreads, psp::ChainSmem<true>::BYTES, s>>>(
+            tq, tk, tv, to, to, tz, psp::GateArgs{norm_w, norm_eps}, cu, base, n_seqs, n_tokens,
+            hv, hv / hqk, item_blocks, pool, n_slots, pool, n_slots, ii, fi, (__nv_bfloat16 *)o,
+            nullptr, psp::IdentChains{0, 0, 0});
+    else
+        psp::chain_kernel<false><<<grid, psp::kChainKernelThreads, psp::ChainSmem<false>::BYTES, s>>>(
+            tq, tk, tv, to, to, to, psp::GateArgs{nullptr, 0.f}, cu, base, n_seqs, n_tokens, hv,
+            hv / hqk, item_blocks, pool, n_slots, pool, n_slots, ii, fi, (__nv_bfloat16 *)o,
+            nullptr, psp::IdentChains{0, 0, 0});
     return launch_status();
+}
+
+// ------------------------------------------------- chunk-state scan (host) --
+// One sequence of at least kScanMinChunks chunks runs as two segments (see
+// prefill_scan.cu): one prep launch over both, one chain launch of 3 x hv
+// CTAs (segment 0 from the true initial state, segment 1 from zero and from
+// the identity), then the combine and the output correction.
+namespace psp {
+constexpr int64_t kScanMinChunks = 64;
+
+inline size_t align1k(size_t x) { return (x + 1023) / 1024 * 1024; }
+inline int64_t scan_phi_rows(int64_t n_tokens) {   // rows of segment 1 at most
+    const int64_t nch = (n_tokens + C - 1) / C;
+    return (int64_t)C * (nch - (nch + 1) / 2);
+}
+struct ScanLayout {
+    size_t base, idx, items, states, s1b, phi, total;
+};
+inline ScanLayout scan_layout(int64_t n_tokens, int hv) {
+    ScanLayout L;
+    L.base = 0;                        // chunk offsets of the two segments
+    L.idx = 1024;                      // scan::ScanIdx
+    L.items = 2048;
+    L.states = align1k(L.items + (size_t)chunk_bound(n_tokens, 2) * hv * kItemBytes);
+    L.s1b = L.states + (size_t)scan::kScratchSlots * hv * DH * DH * 4;
+    L.phi = L.s1b + (size_t)hv * scan::kS1bBytes;
+    L.total = align1k(L.phi + (size_t)scan_phi_rows(n_tokens) * hv * DH * 2);
+    return L;
+}
+}  // namespace psp
+
+bool prefill_scan_sized(int n_seqs, int64_t n_tokens) {
+    return n_seqs == 1 && (n_tokens + psp::C - 1) / psp::C >= psp::kScanMinChunks;
+}
+// The scan pays only while its 3 x hv chain CTAs run at once, one per SM.
+bool prefill_scan_fits(int hv) { return 3 * hv <= sm_count(); }
+size_t prefill_scan_workspace(int64_t n_tokens, int hv) {
+    return psp::scan_layout(n_tokens, hv).total;
+}
+
+gdn_status prefill_scan(const void *q, int64_t qs, const void *k, int64_t ks, const void *v,
+                        int64_t vs, const float *g, const float *beta, const int32_t *cu,
+                        int64_t n_tokens, int hqk, int hv, float scale, int l2norm, float *pool,
+                        int64_t n_slots, const int32_t *ii, const int32_t *fi, void *o, void *ws,
+                        cudaStream_t s) {
+    const psp::ScanLayout L = psp::scan_layout(n_tokens, hv);
+    const int64_t items = psp::chunk_bound(n_tokens, 2) * hv;
+    if (items >= (1ll << 31)) return GDN_ERR_UNSUPPORTED;
+    uint8_t *w = reinterpret_cast<uint8_t *>(ws);
+    int32_t *base = reinterpret_cast<int32_t *>(w + L.base);
+    scan::ScanIdx *idx = reinterpret_cast<scan::ScanIdx *>(w + L.idx);
+    const int32_t *cu_all = reinterpret_cast<const int32_t *>(w + L.idx + offsetof(scan::ScanIdx, cu_all));
+    const int32_t *seg_init = reinterpret_cast<const int32_t *>(w + L.idx + offsetof(scan::ScanIdx, init));
+    const int32_t *seg_fin = reinterpret_cast<const int32_t *>(w + L.idx + offsetof(scan::ScanIdx, fin));
+    uint8_t *item_blocks = w + L.items;
+    float *states = reinterpret_cast<float *>(w + L.states);
+    void *phi = w + L.phi;
+    const int64_t phi_rows = psp::scan_phi_rows(n_tokens);
+    CUtensorMap tq, tk, tv, to, tphi;
+    const uint64_t rows = (uint64_t)n_tokens;
+    if (!encode_tmap_2d_bf16(&tq, q, (uint64_t)hqk * 128, rows, qs, 64, 64) ||
+        !encode_tmap_2d_bf16(&tk, k, (uint64_t)hqk * 128, rows, ks, 64, 64) ||
+        !encode_tmap_2d_bf16(&tv, v, (uint64_t)hv * 128, rows, vs, 64, 64) ||
+        !encode_tmap_2d_bf16(&to, o, (uint64_t)hv * 128, rows, (uint64_t)hv * 128, 32, 32, false) ||
+        !encode_tmap_2d_bf16(&tphi, phi, (uint64_t)hv * 128, (uint64_t)phi_rows,
+                             (uint64_t)hv * 128, 32, 32, false))
+        return GDN_ERR_LAUNCH;
+    cudaError_t e = cudaFuncSetAttribute(psp::prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)psp::P_SMEM_BYTES);
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(psp::chain_kernel<false>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)psp::ChainSmem<false>::BYTES);
+    if (e != cudaSuccess) {
+        set_last_cuda_error(e);
+        return GDN_ERR_LAUNCH;
+    }
+    gdn_status st = scan_setup(cu, n_tokens, ii, fi, n_slots, idx, s);
+    if (st != GDN_OK) return st;
+    psp::chunk_base_kernel<<<1, 1024, 0, s>>>(cu_all, 2, n_tokens, base);
+    if ((st = launch_status()) != GDN_OK) return st;
+    psp::prep_kernel<<<(unsigned)items, psp::kPrepKernelThreads, psp::P_SMEM_BYTES, s>>>(
+        tq, tk, g, beta, cu_all, base, 2, hv, hv / hqk, scale, l2norm, item_blocks);
+    if ((st = launch_status()) != GDN_OK) return st;
+    psp::chain_kernel<false><<<(unsigned)(3 * hv), psp::kChainKernelThreads,
+                               psp::ChainSmem<false>::BYTES, s>>>(
+        tq, tk, tv, to, tphi, tphi, psp::GateArgs{nullptr, 0.f}, cu_all, base, 2, n_tokens, hv,
+        hv / hqk, item_blocks, pool, n_slots,
+        states, scan::kScratchSlots, seg_init, seg_fin, (__nv_bfloat16 *)o, (__nv_bfloat16 *)phi,
+        psp::IdentChains{1, 1, scan::kSlotA});
+    if ((st = launch_status()) != GDN_OK) return st;
+    return scan_finish(states, hv, idx, pool, w + L.s1b, phi, phi_rows, o, n_tokens, s);
 }
 
 }  // namespace gdn

@@ -13,7 +13,8 @@ gdn_status prefill_split(const void *q, int64_t qs, const void *k, int64_t ks, c
                          int64_t vs, const float *g, const float *beta, const int32_t *cu,
                          int n_seqs, int64_t n_tokens, int hqk, int hv, float scale, int l2norm,
                          float *pool, int64_t n_slots, const int32_t *ii, const int32_t *fi,
-                         void *o, void *ws, cudaStream_t s);
+                         void *o, void *ws, cudaStream_t s, const void *z = nullptr,
+                         int64_t zs = 0, const float *norm_w = nullptr, float norm_eps = 0.f);
 
 // One copy per device (a __device__ variable lives in every device's
 // instance of the module).

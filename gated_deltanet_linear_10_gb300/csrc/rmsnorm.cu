@@ -237,14 +237,10 @@ static void launch_norm(const void *o, const void *z, int64_t zs, const float *w
         (const T *)o, (const T *)z, zs, w, (uint32_t)rows, (uint32_t)hv, eps, (T *)y);
 }
 
-}  // namespace gdn
-
-using namespace gdn;
-
-extern "C" gdn_status gdn_gated_rmsnorm(const void *o, const void *z, int64_t z_row_stride,
-                                        const float *weight, int64_t n_tokens, int32_t hv,
-                                        int32_t dv, float eps, void *y, int32_t dtype,
-                                        void *stream) {
+// The host-side checks of gdn_gated_rmsnorm, launching nothing.
+gdn_status norm_check(const void *o, const void *z, int64_t z_row_stride, const float *weight,
+                      int64_t n_tokens, int32_t hv, int32_t dv, float eps, const void *y,
+                      int32_t dtype) {
     GDN_REQUIRE(dtype == GDN_F32 || dtype == GDN_BF16, GDN_ERR_INVALID_ARG);
     GDN_REQUIRE(n_tokens >= 0 && hv > 0 && eps >= 0.f, GDN_ERR_INVALID_ARG);
     GDN_REQUIRE(dv == 16 || dv == 32 || dv == 64 || dv == 128 || dv == 256, GDN_ERR_UNSUPPORTED);
@@ -255,8 +251,21 @@ extern "C" gdn_status gdn_gated_rmsnorm(const void *o, const void *z, int64_t z_
     GDN_REQUIRE(((uintptr_t)o % (4 * elem)) == 0 && ((uintptr_t)z % (4 * elem)) == 0 &&
                     ((uintptr_t)y % (4 * elem)) == 0 && (z_row_stride % 4) == 0,
                 GDN_ERR_INVALID_ARG);
+    GDN_REQUIRE(n_tokens * hv < (1ll << 31), GDN_ERR_UNSUPPORTED);
+    return GDN_OK;
+}
+
+}  // namespace gdn
+
+using namespace gdn;
+
+extern "C" gdn_status gdn_gated_rmsnorm(const void *o, const void *z, int64_t z_row_stride,
+                                        const float *weight, int64_t n_tokens, int32_t hv,
+                                        int32_t dv, float eps, void *y, int32_t dtype,
+                                        void *stream) {
+    const gdn_status chk = norm_check(o, z, z_row_stride, weight, n_tokens, hv, dv, eps, y, dtype);
+    if (chk != GDN_OK || n_tokens == 0) return chk;
     const int64_t rows = n_tokens * hv;
-    GDN_REQUIRE(rows < (1ll << 31), GDN_ERR_UNSUPPORTED);
     cudaStream_t s = (cudaStream_t)stream;
 #define GDN_NORM(DV, T)                                                                     \
     if (!launch_norm_bulk<DV, T>(o, z, z_row_stride, weight, n_tokens, hv, eps, y, s))     \

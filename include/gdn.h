@@ -186,12 +186,52 @@ gdn_status gdn_prefill_chunked(const void *q, int64_t q_row_stride,
                                int32_t dtype, void *workspace,
                                size_t workspace_bytes, void *stream);
 
-/* Bytes of scratch gdn_prefill_chunked uses for these sizes (0: none):
- * 1 KiB-rounded header of n_seqs + 1 chunk offsets, then
- * (ceil(n_tokens / 64) + n_seqs) * hv blocks of 33 KiB. */
+/* Bytes of scratch gdn_prefill_chunked uses for these sizes (0: none).
+ * The two-kernel path takes a 1 KiB-rounded header of n_seqs + 1 chunk
+ * offsets, then (ceil(n_tokens / 64) + n_seqs) * hv blocks of 33 KiB.  One
+ * sequence of at least 64 chunks (4096 tokens) is given more: room for the
+ * chunk-state scan, which cuts the sequence at a chunk boundary into two
+ * segments whose chains run at the same time -- segment 0 from the initial
+ * state, segment 1 from zero and from the identity (its state transition A
+ * and output map Phi) -- then combines them: final state = S_1 A + B, and
+ * segment 1's outputs += S_1 Phi^T (S_1: the state at the cut).  It halves
+ * the serial chain of a long sequence.  The scan runs when the workspace
+ * holds this size and the device has at least 3 * hv SMs; a workspace of
+ * the two-kernel size above keeps the serial chain. */
 size_t gdn_prefill_workspace_size(int32_t n_seqs, int64_t n_tokens,
                                   int32_t hv, int32_t dk, int32_t dv,
                                   int32_t chunk, int32_t dtype);
+
+/*
+ * gdn_prefill_chunked with the gated RMSNorm of gdn_gated_rmsnorm written
+ * instead of o:  y = o / sqrt(mean(o^2) + norm_eps) * norm_weight * SiLU(z)
+ * per (token, V head) row ("gated RMSNorm", "[model] Support Qwen3next",
+ * LightLLM issue 1097, Highlights).  Arguments as gdn_prefill_chunked, plus
+ * z (n_tokens rows of [hv][dv], row stride z_row_stride elements, `dtype`),
+ * norm_weight [dv] fp32 and norm_eps >= 0; y: [n_tokens][hv][dv] contiguous.
+ * On the two-kernel tensor-core path (bf16, dk = dv = 128, chunk 64, a
+ * workspace, z 16-byte aligned with z_row_stride a multiple of 8) the norm
+ * is computed in the chain kernel's output epilogue from the fp32 o, and o
+ * never reaches memory; otherwise (other shapes, or the chunk-state scan) the
+ * call is the prefill into y followed by gdn_gated_rmsnorm in place.  The
+ * host checks of both (including those of gdn_gated_rmsnorm on y and z) run
+ * before anything launches.
+ */
+gdn_status gdn_prefill_chunked_gated(const void *q, int64_t q_row_stride,
+                                     const void *k, int64_t k_row_stride,
+                                     const void *v, int64_t v_row_stride,
+                                     const float *g, const float *beta,
+                                     const int32_t *cu_seqlens, int32_t n_seqs,
+                                     int64_t n_tokens, int32_t hqk, int32_t hv,
+                                     int32_t dk, int32_t dv, float scale,
+                                     int32_t l2norm_qk, int32_t chunk,
+                                     float *state_pool, int64_t n_slots,
+                                     const int32_t *initial_state_indices,
+                                     const int32_t *final_state_indices,
+                                     const void *z, int64_t z_row_stride,
+                                     const float *norm_weight, float norm_eps,
+                                     void *y, int32_t dtype, void *workspace,
+                                     size_t workspace_bytes, void *stream);
 
 /*
  * The prefill above on its bf16, dk = dv = 128, chunk-64 two-kernel path,

@@ -158,3 +158,27 @@ def test_gated_rmsnorm_host_checks(lib):
     assert f(A, A, 512, A, 4, 4, 128, -1.0, A, 1, None) == 1        # eps < 0
     assert f(A, A, 256, A, 4, 4, 128, 1e-6, A, 1, None) == 1        # stride < hv * dv
     assert f(None, None, 512, None, 0, 4, 128, 1e-6, None, 1, None) == 0   # empty: no launch
+
+
+def test_gated_prefill_host_checks(lib):
+    """The gated prefill runs the prefill's and the norm's host checks before
+    any launch: a bad prefill shape, a missing or misaligned z, a z row stride
+    shorter than a token, a negative eps and a missing weight are refused."""
+    f = lib.gdn_prefill_chunked_gated
+    f.argtypes = [V, I64, V, I64, V, I64, V, V, V, I32, I64, I32, I32, I32, I32, F32, I32, I32,
+                  V, I64, V, V, V, I64, V, F32, V, I32, V, ctypes.c_size_t, V]
+    A = 1 << 20
+    base = [A, 2048, A, 2048, A, 4096, A, A, A, 2, 100, 16, 32, 128, 128, 1.0, 1, 64, A, 8, A, A,
+            A, 4096, A, 1e-6, A, 1, None, 0, None]
+    bad = list(base); bad[17] = 48          # chunk 48: the prefill is not built
+    assert f(*bad) == 2
+    bad = list(base); bad[22] = None        # no z
+    assert f(*bad) == 1
+    bad = list(base); bad[22] = A + 2       # z not 4-element aligned
+    assert f(*bad) == 1
+    bad = list(base); bad[23] = 4000        # z row stride < hv * dv
+    assert f(*bad) == 1
+    bad = list(base); bad[25] = -1.0        # eps < 0
+    assert f(*bad) == 1
+    bad = list(base); bad[24] = None        # no norm weight
+    assert f(*bad) == 1

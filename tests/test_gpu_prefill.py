@@ -259,11 +259,22 @@ def long_low_decay():
     return workloads.long_context(low_decay=True)
 
 
+def serial_workspace(n_seqs, T, hv):
+    """Bytes of the two-kernel path without the chunk-state scan (the header's
+    formula): a 1 KiB header, then (ceil(T / 64) + n_seqs) x hv items of
+    33 KiB.  A workspace of this size makes a one-sequence call take the
+    serial chain."""
+    return 1024 + ((T + 63) // 64 + n_seqs) * hv * 33 * 1024
+
+
 def _long_run(w, pool, init, final, lo, hi, workspace=None):
     q, k, v = cuda(w.q[lo:hi]), cuda(w.k[lo:hi]), cuda(w.v[lo:hi])
     g, beta = gdn().gdn_gating(cuda(w.a[lo:hi]), cuda(w.b[lo:hi]), cuda(w.A_log),
                                cuda(w.dt_bias))
     cu = cuda(torch.tensor([0, hi - lo], dtype=torch.int32))
+    if workspace == "serial":
+        workspace = torch.empty(serial_workspace(1, hi - lo, w.dims.hv), dtype=torch.uint8,
+                                device=DEV)
     return gdn().gdn_prefill_chunked(q, k, v, g, beta, cu, pool,
                                      cuda(torch.tensor([init], dtype=torch.int32)),
                                      cuda(torch.tensor([final], dtype=torch.int32)), w.scale,
@@ -272,21 +283,24 @@ def _long_run(w, pool, init, final, lo, hi, workspace=None):
 
 def test_long_context_low_decay_carry(long_low_decay):
     """The long-memory carry over 1024 chunks: o and the final state of two
-    heads against the oracle's token recurrence, element by element (the
-    single pass on the two-kernel path and on the fused kernel); split at
-    32768 and at 32768 + 17 with the state carried through a pool slot
-    against the single pass on every head, and against the oracle on the two
-    heads."""
+    heads against the oracle's token recurrence, element by element, on the
+    chunk-state scan (the default for one long sequence), the serial chain
+    and the fused kernel; split at 32768 (scan) and at 32768 + 17 (serial)
+    with the state carried through a pool slot against the single pass on
+    every head, and against the oracle on the two heads."""
     w = long_low_decay
     d = w.dims
     T = w.q.shape[0]
-    pool = cuda(torch.cat([w.state_pool, torch.zeros(4, d.hv, d.dv, d.dk)]))  # slots 0 .. 5
+    ws = gdn().gdn_prefill_workspace_size(1, T, d.hv, d.dk, d.dv, 64)
+    assert ws > serial_workspace(1, T, d.hv)          # the default path is the scan
+    pool = cuda(torch.cat([w.state_pool, torch.zeros(5, d.hv, d.dv, d.dk)]))  # slots 0 .. 6
     o = _long_run(w, pool, 0, 1, 0, T)
+    o_serial = _long_run(w, pool, 0, 4, 0, T, workspace="serial")
     o_fused = _long_run(w, pool, 0, 5, 0, T, workspace=False)
     splits = {}
-    for slot, cut in ((2, T // 2), (3, T // 2 + 17)):
-        oa = _long_run(w, pool, 0, slot, 0, cut)
-        ob = _long_run(w, pool, slot, slot, cut, T)
+    for slot, cut, path in ((2, T // 2, None), (3, T // 2 + 17, "serial")):
+        oa = _long_run(w, pool, 0, slot, 0, cut, workspace=path)
+        ob = _long_run(w, pool, slot, slot, cut, T, workspace=path)
         splits[cut] = (torch.cat([oa, ob]), slot)
     torch.cuda.synchronize()
     status_clean()
@@ -298,14 +312,58 @@ def test_long_context_low_decay_carry(long_low_decay):
         to_np(w.cu_seqlens).astype(np.int64), w.state_pool, [0], [1], w.scale,
         chains=[(0, h) for h in picks], threads=len(picks))
     tol = TOL[torch.bfloat16]
-    for h in picks:
-        assert_close(o[:, h], o_ref[:, h], tol, f"long o head {h}")
-        assert_close(pool[1, h], finals[(0, h)], tol, f"long S head {h}")
-        assert_close(o_fused[:, h], o_ref[:, h], tol, f"long o head {h} (fused kernel)")
-        assert_close(pool[5, h], finals[(0, h)], tol, f"long S head {h} (fused kernel)")
+    for name, oo, slot in (("scan", o, 1), ("serial", o_serial, 4), ("fused", o_fused, 5)):
+        for h in picks:
+            assert_close(oo[:, h], o_ref[:, h], tol, f"long o head {h} ({name})")
+            assert_close(pool[slot, h], finals[(0, h)], tol, f"long S head {h} ({name})")
+    assert_close(o, o_serial, tol, "scan vs serial: o")
+    assert_close(pool[1], pool[4], tol, "scan vs serial: final state")
     for cut, (o_split, slot) in splits.items():
         assert_close(o_split, o, tol, f"split at {cut}: o")
         assert_close(pool[slot], pool[1], tol, f"split at {cut}: final state")
         for h in picks:
             assert_close(o_split[:, h], o_ref[:, h], tol, f"split at {cut}: o head {h}")
             assert_close(pool[slot, h], finals[(0, h)], tol, f"split at {cut}: S head {h}")
+
+
+@pytest.mark.parametrize("T,low_decay,init,final", [
+    (64 * 70 + 13, True, 0, 0),       # ragged tail, state carried in place
+    (64 * 64, True, 1, -1),           # the shortest scanned length, no final slot
+    (64 * 201 + 1, False, -1, 2),     # a one-token last chunk, zero initial state
+    (64 * 130 + 40, True, 3, 3),
+])
+def test_chunk_state_scan_small_heads(T, low_decay, init, final):
+    """The chunk-state scan of one sequence (split into two segments, the
+    second run from zero and from the identity, then combined) against the
+    oracle on every head: o and the final state; slots the call must not
+    write stay bit-identical.  2 QK / 4 V heads, bf16, dk = dv = 128."""
+    hqk, hv = 2, 4
+    cu, q, k, v, a, b, A_log, dt_bias, pool = _direct_batch(9000 + T, [T], hqk, hv, 128,
+                                                            torch.bfloat16, low_decay, n_slots=4)
+    assert gdn().gdn_prefill_workspace_size(1, T, hv, 128, 128, 64) > serial_workspace(1, T, hv)
+    ii = torch.tensor([init], dtype=torch.int32)
+    fi = torch.tensor([final], dtype=torch.int32)
+    pd = cuda(pool)
+    g, beta = gdn().gdn_gating(cuda(a), cuda(b), cuda(A_log), cuda(dt_bias))
+    o = gdn().gdn_prefill_chunked(cuda(q), cuda(k), cuda(v), g, beta, cuda(cu), pd, cuda(ii),
+                                  cuda(fi), 0.0884)
+    pd2 = cuda(pool)
+    o2 = gdn().gdn_prefill_chunked(cuda(q), cuda(k), cuda(v), g, beta, cuda(cu), pd2, cuda(ii),
+                                   cuda(fi), 0.0884,
+                                   workspace=torch.empty(serial_workspace(1, T, hv),
+                                                         dtype=torch.uint8, device=DEV))
+    torch.cuda.synchronize()
+    status_clean()
+    g_ref, b_ref = oracle_gating(a, b, A_log, dt_bias)
+    o_ref, upd, _ = oracle.gdn_prefill(to_np(q), to_np(k), to_np(v), g_ref, b_ref, to_np(cu),
+                                       to_np(pool), to_np(ii), to_np(fi), 0.0884)
+    tol = TOL[torch.bfloat16]
+    assert_close(o, o_ref, tol, "o (scan)")
+    assert_close(o2, o_ref, tol, "o (serial)")
+    got = pd.cpu()
+    for s_ in range(pool.shape[0]):
+        for h in range(hv):
+            if (s_, h) in upd:
+                assert_close(got[s_, h], upd[(s_, h)], tol, f"state {s_},{h}")
+            else:
+                assert bits_equal(got[s_, h], pool[s_, h]), f"untouched {s_},{h}"
