@@ -54,6 +54,8 @@ def parse_args(argv=None):
     p.add_argument("--only", choices=["mtp", "prefill", "long"], default=None,
                    help="profiling aid: run just this extra (its own JSON line, no decode step)")
     p.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle work")
+    p.add_argument("--long-tokens", type=int, default=65536,
+                   help="length of the long-context sequence (profiling aid with --only long)")
     return p.parse_args(argv)
 
 
@@ -201,7 +203,8 @@ def run_only(args):
     if args.only == "mtp":
         res = bench_mtp(gdn, workloads, dev, flush, steps=max(1, args.steps))
     elif args.only == "long":
-        res = bench_long(gdn, workloads, dev, flush, load_peaks(), steps=max(1, args.steps))
+        res = bench_long(gdn, workloads, dev, flush, load_peaks(), steps=max(1, args.steps),
+                         T=args.long_tokens)
     else:
         res = bench_prefill(gdn, workloads, dev, flush, load_peaks(), steps=max(1, args.steps))
     assert gdn.gdn_get_device_status(clear=True) == 0
@@ -762,12 +765,12 @@ def bench_prefill(gdn, workloads, dev, flush, peaks, steps=5):
             "flops_per_token": prefill_flops_per_token(d.hv, d.dk, d.dv, w.chunk)}
 
 
-def bench_long(gdn, workloads, dev, flush, peaks, steps=3):
-    """Long-context prefill: one sequence of 65,536 tokens, 16 QK / 32 V heads,
-    head_dim 128, bf16, nonzero initial state (gating + chunked prefill), and
-    the split at 32,768 with the state carried through a pool slot against
-    the single pass."""
-    w = workloads.long_context(device=dev)
+def bench_long(gdn, workloads, dev, flush, peaks, steps=3, T=65536):
+    """Long-context prefill: one sequence of T = 65,536 tokens, 16 QK / 32 V
+    heads, head_dim 128, bf16, nonzero initial state (gating + chunked
+    prefill), and the split at T / 2 with the state carried through a pool
+    slot against the single pass."""
+    w = workloads.long_context(device=dev, T=T)
     d = w.dims
     T = w.q.shape[0]
     q, k, v, a, b = w.q, w.k, w.v, w.a, w.b

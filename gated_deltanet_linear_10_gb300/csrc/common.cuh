@@ -130,6 +130,24 @@ template <> struct Vec16<__nv_bfloat16> {
     }
 };
 
+// Reduce-scatter step over a warp of N per-lane values: lanes whose bit N/2
+// is set keep the upper half of the values, the others the lower half, each
+// adding its partner's (lane ^ N/2) copy of the half it keeps.  Steps N, N/2,
+// ..., 2 leave in lane l the sum, over the lanes that differ from l only in
+// bits below N, of value (l mod N).
+template <int N, int M>
+__device__ __forceinline__ void reduce_scatter_step(float (&v)[M], int lane) {
+    static_assert(N <= M && N >= 2, "step size");
+    constexpr int H = N / 2;
+    const bool up = (lane & H) != 0;
+#pragma unroll
+    for (int j = 0; j < H; ++j) {
+        const float send = up ? v[j] : v[H + j];
+        const float keep = up ? v[H + j] : v[j];
+        v[j] = keep + __shfl_xor_sync(0xffffffffu, send, H);
+    }
+}
+
 // SiLU(z) = z * sigmoid(z), with the fast exponential and a correctly rounded
 // reciprocal (relative error ~1e-6; for z << 0 the reciprocal goes to 0).
 __device__ __forceinline__ float silu_f(float z) { return z * __frcp_rn(1.0f + __expf(-z)); }

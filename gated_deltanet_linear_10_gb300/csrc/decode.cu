@@ -44,7 +44,7 @@ __device__ __forceinline__ float dot4(float4 a, float4 b) {
 // SPLIT CTAs share one (sequence, V head): CTA `part` owns the state rows
 // [part*rows, (part+1)*rows).  Fewer registers per thread, more resident CTAs.
 template <int DK, int SPLIT, typename T, bool GATED>
-__global__ void __launch_bounds__(kDecThreads)
+__global__ void __launch_bounds__(kDecThreads, SPLIT == 2 ? 4 : 1)   // split: 64 registers
 decode_kernel(const T *__restrict__ q, int64_t qs, const T *__restrict__ k, int64_t ks,
               const T *__restrict__ v, int64_t vs, const float *__restrict__ g,
               const float *__restrict__ beta, int tps, int hv, int grp, int dv, float scale,
@@ -60,6 +60,11 @@ decode_kernel(const T *__restrict__ q, int64_t qs, const T *__restrict__ k, int6
 
     __shared__ float o_s[kMaxTps][kMaxRows];
     __shared__ float v_s[kMaxTps][kMaxRows];
+    // every token's q, k (this QK head), exp(g) and beta, staged once with
+    // the state load: no token waits on a global load
+    __shared__ __align__(16) float q_s[kMaxTps][DK];
+    __shared__ __align__(16) float k_s[kMaxTps][DK];
+    __shared__ float a_s[kMaxTps], b_s[kMaxTps];
 
     const int part = blockIdx.x % SPLIT;
     const int ih = blockIdx.x / SPLIT;
@@ -96,12 +101,23 @@ decode_kernel(const T *__restrict__ q, int64_t qs, const T *__restrict__ k, int6
         const int t = e / nr, r = e - t * nr;
         v_s[t][r] = Io<T>::load(v + ((int64_t)i * tps + t) * vs + (int64_t)h * dv + r0 + r);
     }
+    for (int e = threadIdx.x; e < tps * DK; e += kDecThreads) {
+        const int t = e / DK, c = e - t * DK;
+        const int64_t row = (int64_t)i * tps + t;
+        q_s[t][c] = Io<T>::load(q + row * qs + (int64_t)hq * DK + c);
+        k_s[t][c] = Io<T>::load(k + row * ks + (int64_t)hq * DK + c);
+    }
+    if (threadIdx.x < tps) {
+        const int64_t row = (int64_t)i * tps + threadIdx.x;
+        a_s[threadIdx.x] = expf(g[row * hv + h]);
+        b_s[threadIdx.x] = beta[row * hv + h];
+    }
     __syncthreads();
 
     for (int t = 0; t < tps; ++t) {
         const int64_t row = (int64_t)i * tps + t;
-        float4 q4 = load4(q + row * qs + (int64_t)hq * DK + col);
-        float4 k4 = load4(k + row * ks + (int64_t)hq * DK + col);
+        float4 q4 = *reinterpret_cast<const float4 *>(&q_s[t][col]);
+        float4 k4 = *reinterpret_cast<const float4 *>(&k_s[t][col]);
         if (l2norm) {
             const float qn = rsqrtf(row_sum<LPR>(dot4(q4, q4)) + kL2Eps);
             const float kn = rsqrtf(row_sum<LPR>(dot4(k4, k4)) + kL2Eps);
@@ -109,20 +125,54 @@ decode_kernel(const T *__restrict__ q, int64_t qs, const T *__restrict__ k, int6
             k4 = make_float4(k4.x * kn, k4.y * kn, k4.z * kn, k4.w * kn);
         }
         const float kq = row_sum<LPR>(dot4(k4, q4));
-        const float alpha = expf(g[row * hv + h]);
-        const float b = beta[row * hv + h];
+        const float alpha = a_s[t];
+        const float b = b_s[t];
+        if constexpr (LPR == 32 && NP == 8) {
+            // a row per warp and pass: the dot products S k, S q of four of
+            // the warp's rows reduced together (reduce-scatter: lane l ends
+            // with value l mod 8), then read back -- 34 shuffles for the 8
+            // rows instead of 80
 #pragma unroll
-        for (int p = 0; p < NP; ++p) {
-            const int r = p * RPP + warp * RPW + sub;
-            if (p * RPP < nr) {                      // warp-uniform: shuffles stay converged
-                const float4 s = st[p];
-                const float sk = row_sum<LPR>(dot4(s, k4));
-                const float sq = row_sum<LPR>(dot4(s, q4));
-                if (r < nr) {
-                    const float u = b * (v_s[t][r] - alpha * sk);
-                    st[p] = make_float4(fmaf(alpha, s.x, u * k4.x), fmaf(alpha, s.y, u * k4.y),
-                                        fmaf(alpha, s.z, u * k4.z), fmaf(alpha, s.w, u * k4.w));
-                    if ((lane % LPR) == 0) o_s[t][r] = scale * fmaf(alpha, sq, u * kq);
+            for (int p0 = 0; p0 < 8; p0 += 4) {
+                float pv[8];
+#pragma unroll
+                for (int p = 0; p < 4; ++p) {
+                    pv[p] = dot4(st[p0 + p], k4);
+                    pv[4 + p] = dot4(st[p0 + p], q4);
+                }
+                reduce_scatter_step<8>(pv, lane);
+                reduce_scatter_step<4>(pv, lane);
+                reduce_scatter_step<2>(pv, lane);
+                float tot = pv[0] + __shfl_xor_sync(0xffffffffu, pv[0], 8);
+                tot += __shfl_xor_sync(0xffffffffu, tot, 16);
+#pragma unroll
+                for (int p = 0; p < 4; ++p) {
+                    const int r = (p0 + p) * RPP + warp;
+                    const float sk = __shfl_sync(0xffffffffu, tot, p);
+                    const float sq = __shfl_sync(0xffffffffu, tot, 4 + p);
+                    if (r < nr) {
+                        const float4 s = st[p0 + p];
+                        const float u = b * (v_s[t][r] - alpha * sk);
+                        st[p0 + p] = make_float4(fmaf(alpha, s.x, u * k4.x), fmaf(alpha, s.y, u * k4.y),
+                                                 fmaf(alpha, s.z, u * k4.z), fmaf(alpha, s.w, u * k4.w));
+                        if (lane == 0) o_s[t][r] = scale * fmaf(alpha, sq, u * kq);
+                    }
+                }
+            }
+        } else {
+#pragma unroll
+            for (int p = 0; p < NP; ++p) {
+                const int r = p * RPP + warp * RPW + sub;
+                if (p * RPP < nr) {                  // warp-uniform: shuffles stay converged
+                    const float4 s = st[p];
+                    const float sk = row_sum<LPR>(dot4(s, k4));
+                    const float sq = row_sum<LPR>(dot4(s, q4));
+                    if (r < nr) {
+                        const float u = b * (v_s[t][r] - alpha * sk);
+                        st[p] = make_float4(fmaf(alpha, s.x, u * k4.x), fmaf(alpha, s.y, u * k4.y),
+                                            fmaf(alpha, s.z, u * k4.z), fmaf(alpha, s.w, u * k4.w));
+                        if ((lane % LPR) == 0) o_s[t][r] = scale * fmaf(alpha, sq, u * kq);
+                    }
                 }
             }
         }

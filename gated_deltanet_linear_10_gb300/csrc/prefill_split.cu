@@ -428,22 +428,6 @@ struct GateArgs {
     float eps;
 };
 
-// Reduce-scatter step of 32 per-lane values over the warp: with N values
-// left, lanes whose bit N/2 is set keep the upper half, the others the lower,
-// each adding its partner's copy.  After N = 32, 16, 8, 4, 2 lane l holds the
-// warp's sum of value l.
-template <int N>
-__device__ __forceinline__ void reduce_scatter_step(float (&v)[32], int lane) {
-    constexpr int H = N / 2;
-    const bool up = (lane & H) != 0;
-#pragma unroll
-    for (int j = 0; j < H; ++j) {
-        const float send = up ? v[j] : v[H + j];
-        const float keep = up ? v[H + j] : v[j];
-        v[j] = keep + __shfl_xor_sync(0xffffffffu, send, H);
-    }
-}
-
 template <bool kGated>
 __global__ void __launch_bounds__(kChainKernelThreads, 1)
 chain_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
