@@ -59,50 +59,53 @@ __global__ void scan_setup_kernel(const int32_t *__restrict__ cu, int64_t n_toke
     *out = r;
 }
 
-// One CTA of 256 threads per V head: S_final = S_1 A + B in fp32 (thread
-// (ty, tx) owns rows 8 ty .. 8 ty + 7 and columns 8 tx .. 8 tx + 7), and
-// S_1 rounded to bf16 in the 128-byte-swizzled K-major layout of a 128 x 128
-// tcgen05 A operand (two k-blocks of 128 rows x 128 B).
+// Four CTAs of 256 threads per V head, 32 state rows each: S_final = S_1 A +
+// B in fp32 (thread (ty, tx) owns rows 2 ty, 2 ty + 1 of the CTA's rows and
+// columns 8 tx .. 8 tx + 7), and those rows of S_1 rounded to bf16 in the
+// 128-byte-swizzled K-major layout of a 128 x 128 tcgen05 A operand (two
+// k-blocks of 128 rows x 128 B).
 constexpr int kCombThreads = 256;
+constexpr int kCombRows = 32;    // rows of S per CTA
 constexpr int kKt = 16;          // k-tile
 __global__ void __launch_bounds__(kCombThreads)
 scan_combine_kernel(const float *__restrict__ states, int hv, const ScanIdx *__restrict__ idx,
                     float *__restrict__ pool, uint8_t *__restrict__ s1b) {
-    __shared__ float As[128][kKt + 1];
+    __shared__ float As[kCombRows][kKt + 1];
     __shared__ float Bs[kKt][128 + 4];
-    const int h = blockIdx.x, t = threadIdx.x;
+    const int h = blockIdx.x, rb = blockIdx.y * kCombRows, t = threadIdx.x;
     const size_t slot = (size_t)hv * 128 * 128, head = (size_t)h * 128 * 128;
     const float *S1 = states + kSlotS1 * slot + head;
     const float *Bm = states + kSlotB * slot + head;
     const float *Am = states + kSlotA * slot + head;
     const int ty = t >> 4, tx = t & 15;
-    float acc[8][8];
+    const int r0 = rb + 2 * ty;
+    float acc[2][8];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-        const float4 b0 = *reinterpret_cast<const float4 *>(Bm + (8 * ty + i) * 128 + 8 * tx);
-        const float4 b1 = *reinterpret_cast<const float4 *>(Bm + (8 * ty + i) * 128 + 8 * tx + 4);
+    for (int i = 0; i < 2; ++i) {
+        const float4 b0 = *reinterpret_cast<const float4 *>(Bm + (r0 + i) * 128 + 8 * tx);
+        const float4 b1 = *reinterpret_cast<const float4 *>(Bm + (r0 + i) * 128 + 8 * tx + 4);
         acc[i][0] = b0.x; acc[i][1] = b0.y; acc[i][2] = b0.z; acc[i][3] = b0.w;
         acc[i][4] = b1.x; acc[i][5] = b1.y; acc[i][6] = b1.z; acc[i][7] = b1.w;
     }
     for (int k0 = 0; k0 < 128; k0 += kKt) {
-        for (int e = t; e < 128 * kKt; e += kCombThreads) {
+        for (int e = t; e < kCombRows * kKt; e += kCombThreads) {
             const int r = e / kKt, c = e % kKt;
-            As[r][c] = S1[r * 128 + k0 + c];
+            As[r][c] = S1[(rb + r) * 128 + k0 + c];
+        }
+        for (int e = t; e < kKt * 128; e += kCombThreads) {
             const int kr = e / 128, kc = e % 128;
             Bs[kr][kc] = Am[(k0 + kr) * 128 + kc];
         }
         __syncthreads();
 #pragma unroll
         for (int kk = 0; kk < kKt; ++kk) {
-            float a[8], b[8];
+            const float a0 = As[2 * ty][kk], a1 = As[2 * ty + 1][kk];
 #pragma unroll
-            for (int i = 0; i < 8; ++i) a[i] = As[8 * ty + i][kk];
-#pragma unroll
-            for (int j = 0; j < 8; ++j) b[j] = Bs[kk][8 * tx + j];
-#pragma unroll
-            for (int i = 0; i < 8; ++i)
-#pragma unroll
-                for (int j = 0; j < 8; ++j) acc[i][j] = fmaf(a[i], b[j], acc[i][j]);
+            for (int j = 0; j < 8; ++j) {
+                const float b = Bs[kk][8 * tx + j];
+                acc[0][j] = fmaf(a0, b, acc[0][j]);
+                acc[1][j] = fmaf(a1, b, acc[1][j]);
+            }
         }
         __syncthreads();
     }
@@ -110,17 +113,17 @@ scan_combine_kernel(const float *__restrict__ states, int hv, const ScanIdx *__r
     if (fs >= 0) {
         float *dst = pool + (size_t)fs * slot + head;
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            *reinterpret_cast<float4 *>(dst + (8 * ty + i) * 128 + 8 * tx) =
+        for (int i = 0; i < 2; ++i) {
+            *reinterpret_cast<float4 *>(dst + (r0 + i) * 128 + 8 * tx) =
                 make_float4(acc[i][0], acc[i][1], acc[i][2], acc[i][3]);
-            *reinterpret_cast<float4 *>(dst + (8 * ty + i) * 128 + 8 * tx + 4) =
+            *reinterpret_cast<float4 *>(dst + (r0 + i) * 128 + 8 * tx + 4) =
                 make_float4(acc[i][4], acc[i][5], acc[i][6], acc[i][7]);
         }
     }
-    // S_1 -> bf16 operand: 16-byte chunk (8 columns) per step
+    // this CTA's rows of S_1 -> bf16 operand: one 16-byte chunk (8 columns) per step
     uint8_t *out = s1b + (size_t)h * kS1bBytes;
-    for (int e = t; e < 128 * 16; e += kCombThreads) {
-        const int r = e >> 4, ch = e & 15;          // row r, columns 8 ch .. 8 ch + 7
+    for (int e = t; e < kCombRows * 16; e += kCombThreads) {
+        const int r = rb + (e >> 4), ch = e & 15;   // row r, columns 8 ch .. 8 ch + 7
         const float4 x0 = *reinterpret_cast<const float4 *>(S1 + r * 128 + 8 * ch);
         const float4 x1 = *reinterpret_cast<const float4 *>(S1 + r * 128 + 8 * ch + 4);
         const uint4 w = make_uint4(pack_bf16(x0.x, x0.y), pack_bf16(x0.z, x0.w),
@@ -129,15 +132,16 @@ scan_combine_kernel(const float *__restrict__ states, int hv, const ScanIdx *__r
     }
 }
 
-// One CTA of 128 threads per (128-token tile of segment 1, V head):
+// One CTA of 256 threads per (128-token tile of segment 1, V head):
 //   D[b][t] = sum_a S_1[b][a] Phi[t][a]        (tcgen05, M = N = K = 128)
 //   o[t][h][b] += D[b][t]
 // A = S_1 (bf16 operand from scan_combine_kernel, one bulk copy), B = the
 // Phi tile (TMA, 128-byte swizzle); the o tile [t][b] comes in by TMA, is
-// updated in shared memory (thread b owns column b) and leaves by one TMA
-// store.  Warp w reads TMEM lanes 32 w .. 32 w + 31.  Rows of the tile past
-// segment 1 go back unchanged.
-constexpr int kCorrThreads = 128;
+// updated in shared memory and leaves by one TMA store.  Warp w reads TMEM
+// lanes 32 (w % 4) .. + 31 (value rows b) for the tokens of its half, 64 (w / 4)
+// .. + 63; each thread updates column b of those tokens.  Rows of the tile
+// past segment 1 go back unchanged.
+constexpr int kCorrThreads = 256;
 constexpr uint32_t kCorrTmemCols = 128;
 constexpr uint32_t kOTile = 128 * 128 * 2;
 struct CorrBars {
@@ -206,11 +210,12 @@ scan_correct_kernel(const __grid_constant__ CUtensorMap tm_phi,
     tc_fence_after();
     const bool go = __all_sync(0xffffffffu, done && !*abort);   // warp-uniform: tcgen05.ld is .aligned
     if (go) {
-        const int b = warp * 32 + lane;
+        const int q4 = warp & 3, half = warp >> 2;
+        const int b = q4 * 32 + lane;
         const int nrow = (int)min((int64_t)128, r1 - row0);     // rows of segment 1 in the tile
-        for (int j = 0; j < 4; ++j) {
+        for (int j = 2 * half; j < 2 * half + 2; ++j) {
             uint32_t r[32];
-            tmem_ld32(tmem_addr(tbase, warp * 32, 32 * j), r);
+            tmem_ld32(tmem_addr(tbase, q4 * 32, 32 * j), r);
 #pragma unroll
             for (int i = 0; i < 32; ++i) {
                 const int t = 32 * j + i;
@@ -251,7 +256,8 @@ gdn_status scan_setup(const int32_t *cu, int64_t n_tokens, const int32_t *ii, co
 gdn_status scan_finish(const float *states, int hv, const scan::ScanIdx *idx, float *pool,
                        uint8_t *s1b, const void *phi, int64_t phi_rows, void *o, int64_t n_tokens,
                        cudaStream_t s) {
-    scan::scan_combine_kernel<<<hv, scan::kCombThreads, 0, s>>>(states, hv, idx, pool, s1b);
+    scan::scan_combine_kernel<<<dim3((unsigned)hv, 128 / scan::kCombRows), scan::kCombThreads, 0,
+                                 s>>>(states, hv, idx, pool, s1b);
     gdn_status st = launch_status();
     if (st != GDN_OK) return st;
     CUtensorMap tm, tmo;
