@@ -1,9 +1,10 @@
 """The C ABI calls are asynchronous on the caller's stream, with no host
 synchronisation and no allocation, so a serving loop can capture them in a
 CUDA graph: the fused decode step, the two-kernel prefill (with a caller
-workspace) and the TMA-staged conv forward are captured with torch.cuda.graph
-and replayed, and every output and pool must be bit-identical to an eager run
-on copies of the same inputs (the kernels are deterministic)."""
+workspace), the chunk-state scan and the gated prefill, and the TMA-staged
+conv forward are captured with torch.cuda.graph and replayed, and every
+output and pool must be bit-identical to an eager run on copies of the same
+inputs (the kernels are deterministic)."""
 import pytest
 import torch
 
@@ -118,4 +119,53 @@ def test_conv_fwd_graph_replay():
     torch.cuda.synchronize()
     status_clean()
     assert bits_equal(yg, ye)
+    assert bits_equal(pg, pe)
+
+
+def test_scan_and_gated_prefill_graph_replay():
+    """The chunk-state scan of one 8,000-token sequence (setup, prep, the
+    three-role chain launch, combine, correction) and the gated prefill with
+    the norm in the chain's epilogue, captured together and replayed: outputs
+    and pools bit-identical to eager runs."""
+    gen = torch.Generator().manual_seed(404)
+    hqk, hv, T = 2, 4, 8000
+    q = cuda(torch.randn(T, hqk, 128, generator=gen).bfloat16())
+    k = cuda(torch.randn(T, hqk, 128, generator=gen).bfloat16())
+    v = cuda(torch.randn(T, hv, 128, generator=gen).bfloat16())
+    g = cuda(-torch.rand(T, hv, generator=gen) * 0.05)
+    beta = cuda(torch.rand(T, hv, generator=gen))
+    z = cuda(torch.randn(T, hv, 128, generator=gen).bfloat16())
+    nw = cuda(torch.rand(128, generator=gen) + 0.5)
+    pool0 = cuda(torch.randn(4, hv, 128, 128, generator=gen) * 0.05)
+    cu1 = cuda(torch.tensor([0, T], dtype=torch.int32))
+    cu2 = cuda(torch.tensor([0, 3000, T], dtype=torch.int32))
+    i32 = lambda *x: cuda(torch.tensor(x, dtype=torch.int32))
+    s0, s1, s1n, s23 = i32(0), i32(1), i32(1, -1), i32(2, 3)     # made before any capture
+    ws1 = torch.empty(gdn().gdn_prefill_workspace_size(1, T, hv, 128, 128, 64), dtype=torch.uint8,
+                      device=DEV)
+    ws2 = torch.empty(gdn().gdn_prefill_workspace_size(2, T, hv, 128, 128, 64), dtype=torch.uint8,
+                      device=DEV)
+
+    def run(pool, o1, o2):
+        gdn().gdn_prefill_chunked(q, k, v, g, beta, cu1, pool, s0, s1, 0.0884, o=o1,
+                                  workspace=ws1)
+        gdn().gdn_prefill_chunked_gated(q, k, v, g, beta, cu2, pool, s1n, s23, 0.0884, z, nw,
+                                        1e-6, y=o2, workspace=ws2)
+
+    pe = pool0.clone()
+    o1e = torch.empty(T, hv, 128, dtype=torch.bfloat16, device=DEV)
+    o2e = torch.empty_like(o1e)
+    run(pe, o1e, o2e)
+    torch.cuda.synchronize()
+    status_clean()
+
+    pg = pool0.clone()
+    o1g, o2g = torch.empty_like(o1e), torch.empty_like(o1e)
+    gr = _graph(lambda: run(pg, o1g, o2g))
+    pg.copy_(pool0)
+    gr.replay()
+    torch.cuda.synchronize()
+    status_clean()
+    assert bits_equal(o1g, o1e)
+    assert bits_equal(o2g, o2e)
     assert bits_equal(pg, pe)

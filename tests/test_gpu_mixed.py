@@ -103,3 +103,19 @@ def test_mixed_batch_all_decode_and_all_prefill():
     status_clean()
     o_ref, upd, _ = _oracle(cu, q, k, v, a, b, A_log, dt_bias, pool, init, final)
     _check(o, pd, pool, o_ref, upd)
+
+
+def test_mixed_batch_reports_a_broken_decode_row_layout():
+    """Decode rows must be one token each at rows 0 .. n_decode-1; a batch
+    whose cu_seqlens breaks that still runs but sets GDN_DEVSTAT_BAD_SEQLEN."""
+    cu, q, k, v, a, b, A_log, dt_bias, pool, init, perm = _batch()
+    n = len(init)
+    final = perm[n:2 * n].clone()
+    bad = cu.clone()
+    bad[1] = 2                                # decode row 0 claims two tokens
+    g, beta = gdn().gdn_gating(cuda(a), cuda(b), cuda(A_log), cuda(dt_bias))
+    gdn().gdn_mixed_batch(cuda(q), cuda(k), cuda(v), g, beta, cuda(bad), N_DEC, cuda(pool),
+                          cuda(init), cuda(final), 0.125, decode_in_place=False)
+    torch.cuda.synchronize()
+    st = gdn().gdn_get_device_status(clear=True)
+    assert st & gdn().DEVSTAT_BAD_SEQLEN, f"status {st:#x}"
