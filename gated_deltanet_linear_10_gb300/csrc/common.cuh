@@ -148,9 +148,32 @@ __device__ __forceinline__ void reduce_scatter_step(float (&v)[M], int lane) {
     }
 }
 
-// SiLU(z) = z * sigmoid(z), with the fast exponential and a correctly rounded
-// reciprocal (relative error ~1e-6; for z << 0 the reciprocal goes to 0).
-__device__ __forceinline__ float silu_f(float z) { return z * __frcp_rn(1.0f + __expf(-z)); }
+// SiLU(z) = z / (1 + e^-z) with the fast exponential and the fast division:
+// relative error a few fp32 ulp, below the bf16 rounding of the outputs; for
+// z << 0 the denominator overflows and the quotient goes to 0.  (The
+// correctly rounded reciprocal costs several times the instructions, and the
+// kernels that take SiLU per element are issue-bound.)
+__device__ __forceinline__ float silu_f(float z) { return __fdividef(z, 1.0f + __expf(-z)); }
+
+// SiLU for a bf16 result: z sigmoid(z) = h + h tanh(h) with h = z / 2 and the
+// hardware tanh (tanh.approx.f32, one instruction; relative error about
+// 2^-11, a quarter of the bf16 rounding of the result).
+__device__ __forceinline__ float tanh_approx(float x) {
+    float y;
+    asm("tanh.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+__device__ __forceinline__ float silu_bf16out(float z) {
+    const float h = 0.5f * z;
+    return fmaf(h, tanh_approx(h), h);
+}
+// The SiLU a kernel with outputs of type T takes: the fast division for fp32
+// outputs, the tanh form for bf16.
+template <typename T> __device__ __forceinline__ float silu_for(float z);
+template <> __device__ __forceinline__ float silu_for<float>(float z) { return silu_f(z); }
+template <> __device__ __forceinline__ float silu_for<__nv_bfloat16>(float z) {
+    return silu_bf16out(z);
+}
 
 }  // namespace gdn
 

@@ -25,11 +25,9 @@ GDN_STATUS_READER(read_status_conv, g_status_conv)
 constexpr int kConvThreads = 128;
 constexpr int kConvTokensPerThread = 8;   // token run of a thread in the forward kernel
 
-// SiLU(z) = z / (1 + e^-z) with the fast exponential and the fast division
-// (relative error a few ulp of fp32, far below the bf16 output rounding; for
-// z << 0 the quotient goes to 0).  The forward conv is issue-bound on this
-// arithmetic, so it takes the two-instruction form.
-__device__ __forceinline__ float silu_fast(float z) { return __fdividef(z, 1.0f + __expf(-z)); }
+// SiLU: silu_for<T> (common.cuh) -- the fast division for fp32 outputs, the
+// one-instruction tanh form for bf16.  The forward conv is issue-bound on this
+// arithmetic.
 
 // Four channels of T as one vector access (8 bytes of bf16, 16 of fp32).
 template <typename T> struct Vec4;
@@ -102,7 +100,7 @@ struct ConvTaps {
 #pragma unroll
             for (int j = 0; j < W - 1; ++j) acc = fmaf(w[j][v], win[j][v], acc);
             acc = fmaf(w[W - 1][v], cur[v], acc);
-            out[v] = silu ? silu_fast(acc) : acc;
+            out[v] = silu ? silu_for<T>(acc) : acc;
         }
     }
 };

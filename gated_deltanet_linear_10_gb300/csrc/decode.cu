@@ -214,7 +214,7 @@ decode_kernel(const T *__restrict__ q, int64_t qs, const T *__restrict__ k, int6
             const int64_t row = (int64_t)i * tps + t;
             const float inv = rsqrtf(ss_s[t] / (float)dv + neps);
             const float zz = Io<T>::load(z + row * zs + (int64_t)h * dv + r0 + r);
-            Io<T>::store(o + (row * hv + h) * dv + r0 + r, o_s[t][r] * inv * nw[r0 + r] * silu_f(zz));
+            Io<T>::store(o + (row * hv + h) * dv + r0 + r, o_s[t][r] * inv * nw[r0 + r] * silu_for<T>(zz));
         }
     } else {
         for (int e = threadIdx.x; e < tps * nr; e += kDecThreads) {

@@ -66,7 +66,7 @@ __device__ __forceinline__ float conv_out(const ConvIn &c) {
 #pragma unroll
     for (int r = 0; r < kW - 1; ++r) acc = fmaf(c.w[r], c.h[r], acc);
     acc = fmaf(c.w[kW - 1], c.x, acc);
-    return silu_f(acc);
+    return silu_bf16out(acc);
 }
 
 // Shifted history: the last W-1 pre-activation inputs, oldest first.

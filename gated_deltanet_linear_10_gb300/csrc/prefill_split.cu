@@ -801,10 +801,10 @@ chain_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
                     rs[lane] = rsqrtf(ss * (1.0f / DH) + gate.eps);
                     __syncwarp();
                     mbar_wait(&B.zbar[warp - 2], c & 1, abort);
-                    // y = o rstd w SiLU(z): the fast exponential and division
-                    // (a few fp32 ulp, below the bf16 rounding of y); the
-                    // epilogue is issue-bound, so the exact reciprocal cost
-                    // a third of the chain's time
+                    // y = o rstd w SiLU(z), SiLU by the one-instruction tanh
+                    // form (below the bf16 rounding of y): the epilogue is
+                    // issue-bound, and SiLU with an exact reciprocal cost a
+                    // third of the chain's time
 #pragma unroll
                     for (int q = 0; q < 8; ++q) {
                         const float4 r4 = reinterpret_cast<const float4 *>(rs)[q];
@@ -812,7 +812,7 @@ chain_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
 #pragma unroll
                         for (int e = 0; e < 4; ++e) {
                             const float zz = __bfloat162float(zt[(4 * q + e) * 32 + lane]);
-                            f[4 * q + e] *= rr[e] * wb * __fdividef(zz, 1.0f + __expf(-zz));
+                            f[4 * q + e] *= rr[e] * wb * silu_bf16out(zz);
                         }
                     }
                     fence_async_smem();      // z reads (generic) before the next z load (async)

@@ -84,7 +84,7 @@ gated_rmsnorm_kernel(const T *__restrict__ o, const T *__restrict__ z, int64_t z
                     float r[4];
 #pragma unroll
                     for (int c = 0; c < 4; ++c)
-                        r[c] = ov[u][e + c] * inv * wv[e + c] * silu_f(zv[u][e + c]);
+                        r[c] = ov[u][e + c] * inv * wv[e + c] * silu_for<T>(zv[u][e + c]);
                     store4(yrow + j0 + e, r);
                 }
             }
@@ -188,7 +188,7 @@ gated_rmsnorm_bulk_kernel(const T *__restrict__ o, const T *__restrict__ z, int6
                     for (int e = 0; e < EPL; e += 4) {
                         float q[4];
 #pragma unroll
-                        for (int c = 0; c < 4; ++c) q[c] = ov[u][e + c] * inv[u] * wv[e + c] * silu_f(zv[u][e + c]);
+                        for (int c = 0; c < 4; ++c) q[c] = ov[u][e + c] * inv[u] * wv[e + c] * silu_for<T>(zv[u][e + c]);
                         store4(yrow + j0 + e, q);
                     }
                 }
