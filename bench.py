@@ -523,6 +523,10 @@ def bench_mtp(gdn, workloads, dev, flush, steps=50):
             "decode_kernel_ms": round(dec, 5),
             "decode_kernel_gbs": round(dec_bytes / (dec / 1e3) / 1e9, 1),
             "decode_kernel_frac_hbm": round(dec_bytes / (dec / 1e3) / 1e9 / peak, 4),
+            "decode_kernel_algorithmic_bytes": dec_bytes,
+            "decode_kernel_traffic_bytes": profile_traffic(
+                "decode_kernel_mtp", ["gated_deltanet_linear_10_gb300/csrc/" + f for f in
+                                      ("decode.cu", "common.cuh", "tc.cuh")]),
             "step_ms": round(whole, 5),
             "tokens_per_s": round(T / (whole / 1e3), 1),
             "step_bytes": step_bytes,
