@@ -455,8 +455,10 @@ def e2e_pipelined(gdn, w, d, conv_w, A_log, dt_bias, cpool, spool, slots, dev, s
 
 
 def bench_mtp(gdn, workloads, dev, flush, steps=50):
-    """MTP step: conv update (4 tokens, per-token conv snapshots) -> gating ->
-    decode with per-token state snapshots -> accept copy into the source slot."""
+    """MTP step: conv update (4 tokens, per-token conv snapshots), gating and
+    the decode with per-token state snapshots in one kernel
+    (gdn_mtp_step_fused), then the accept copies into the source slots.  The
+    same step through the three separate calls is timed beside it."""
     w = workloads.mtp(pool_device=dev)
     d = w.dims
     x, a, b = w.x.to(dev), w.a.to(dev), w.b.to(dev)
@@ -473,68 +475,93 @@ def bench_mtp(gdn, workloads, dev, flush, steps=50):
     beta = torch.empty_like(g)
     o = torch.empty((T, d.hv, d.dv), dtype=x.dtype, device=dev)
     stream = torch.cuda.current_stream(dev)
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(steps)]
 
-    def step(e=None):
-        if e is not None:
-            e[0].record(stream)
-        gdn.causal_conv1d_update(x, 4, conv_w, cpool, slots, snap_indices=snap, y=y)
-        gdn.gdn_gating(a, b, A_log, dt_bias, g=g, beta=beta)
-        if e is not None:
-            e[1].record(stream)
-        gdn.gdn_decode_recurrent(qv, kv, vv, g, beta, 4, spool, slots, snap_indices=snap,
-                                 scale=w.scale, o=o)
-        if e is not None:
-            e[2].record(stream)
+    def accept():
         gdn.gdn_state_snapshot(spool, acc_src, slots)
         gdn.gdn_state_snapshot(cpool, acc_src, slots)
-        if e is not None:
-            e[3].record(stream)
 
-    for _ in range(3):
-        step()
-        flush.zero_()
-    torch.cuda.synchronize(dev)
-    torch.cuda._sleep(1_000_000)
-    for i in range(steps):
-        step(ev[i])
-        flush.zero_()
-    torch.cuda.synchronize(dev)
-    dec = sum(e[1].elapsed_time(e[2]) for e in ev) / steps
-    whole = sum(e[0].elapsed_time(e[3]) for e in ev) / steps
-    front = sum(e[0].elapsed_time(e[1]) for e in ev) / steps
-    accept = sum(e[2].elapsed_time(e[3]) for e in ev) / steps
-    # decode kernel algorithmic bytes: source state read once, 4 snapshots written
+    def fused(e):
+        gdn.gdn_mtp_step_fused(x, 4, conv_w, cpool, a, b, A_log, dt_bias, d.hqk, spool, slots,
+                               snap, scale=w.scale, o=o)
+        e[1].record(stream)
+        e[2].record(stream)
+        accept()
+
+    def three_calls(e):
+        gdn.causal_conv1d_update(x, 4, conv_w, cpool, slots, snap_indices=snap, y=y)
+        gdn.gdn_gating(a, b, A_log, dt_bias, g=g, beta=beta)
+        e[1].record(stream)
+        gdn.gdn_decode_recurrent(qv, kv, vv, g, beta, 4, spool, slots, snap_indices=snap,
+                                 scale=w.scale, o=o)
+        e[2].record(stream)
+        accept()
+
+    def timed(body):
+        ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(steps)]
+        for i in range(3):
+            body(ev[i])
+            flush.zero_()
+        torch.cuda.synchronize(dev)
+        torch.cuda._sleep(1_000_000)
+        for e in ev:
+            e[0].record(stream)
+            body(e)
+            e[3].record(stream)
+            flush.zero_()
+        torch.cuda.synchronize(dev)
+        mean = lambda u, v: sum(e[u].elapsed_time(e[v]) for e in ev) / steps
+        return mean(0, 3), mean(0, 1), mean(1, 2), mean(2, 3)
+
+    f_whole, f_kernel, _, f_accept = timed(fused)
+    c_whole, c_front, c_dec, c_accept = timed(three_calls)
+
+    # algorithmic bytes.  state: the source read once, 4 snapshots written;
+    # conv state: the same for the slot's 3 x channels bf16 conv state
     st = w.n_seqs * d.hv * d.dv * d.dk * 4
-    io = T * (2 * d.hqk * d.dk + 2 * d.hv * d.dv) * 2 + 2 * T * d.hv * 4
-    dec_bytes = st * 5 + io
-    # the whole step: conv update (x read, y written, the slot's conv state
-    # read, 4 conv snapshots written), gating (a, b read, g, beta written),
-    # the decode kernel, and the accept copies of both pools (read + write)
     conv_state = d.channels * 3 * 2
-    conv_bytes = 2 * T * d.channels * 2 + w.n_seqs * conv_state * 5 + d.channels * 4 * 2
-    gate_bytes = 2 * T * d.hv * 2 + 2 * T * d.hv * 4
+    ab = 2 * T * d.hv * 2
+    o_bytes = T * d.hv * d.dv * 2
+    # the fused kernel: x, conv weights, a, b read; both states; o written
+    fused_bytes = (st * 5 + w.n_seqs * conv_state * 5 + T * d.channels * 2
+                   + d.channels * 4 * 2 + ab + o_bytes)
     accept_bytes = 2 * w.n_seqs * (d.hv * d.dv * d.dk * 4 + conv_state)
-    step_bytes = conv_bytes + gate_bytes + dec_bytes + accept_bytes
+    step_bytes = fused_bytes + accept_bytes
+    # the three calls: conv update (x read, y written, conv states), gating
+    # (a, b read, g, beta written), decode (q, k, v, g, beta read, o written)
+    io = T * (2 * d.hqk * d.dk + d.hv * d.dv) * 2 + o_bytes + 2 * T * d.hv * 4
+    dec_bytes = st * 5 + io
     peak = load_peaks()["hbm_gbs"]
+    gbs = lambda nbytes, ms: nbytes / (ms / 1e3) / 1e9
     del spool, w
     return {"workload": "MTP: 128 sequences x 4 tokens, per-token state + conv snapshots, "
-                        "accept copy", "tokens_per_s_decode_kernel": round(T / (dec / 1e3), 1),
-            "decode_kernel_ms": round(dec, 5),
-            "decode_kernel_gbs": round(dec_bytes / (dec / 1e3) / 1e9, 1),
-            "decode_kernel_frac_hbm": round(dec_bytes / (dec / 1e3) / 1e9 / peak, 4),
-            "decode_kernel_algorithmic_bytes": dec_bytes,
-            "decode_kernel_traffic_bytes": profile_traffic(
-                "decode_kernel_mtp", ["gated_deltanet_linear_10_gb300/csrc/" + f for f in
-                                      ("decode.cu", "common.cuh", "tc.cuh")]),
-            "step_ms": round(whole, 5),
-            "tokens_per_s": round(T / (whole / 1e3), 1),
+                        "accept copy",
+            "step_ms": round(f_whole, 5),
+            "tokens_per_s": round(T / (f_whole / 1e3), 1),
             "step_bytes": step_bytes,
-            "step_gbs": round(step_bytes / (whole / 1e3) / 1e9, 1),
-            "step_frac_hbm": round(step_bytes / (whole / 1e3) / 1e9 / peak, 4),
-            "conv_update_gating_ms": round(front, 5),
-            "accept_copies_ms": round(accept, 5),
-            "gpu_launches_per_step": 5}
+            "step_gbs": round(gbs(step_bytes, f_whole), 1),
+            "step_frac_hbm": round(gbs(step_bytes, f_whole) / peak, 4),
+            "gpu_launches_per_step": 3,
+            "fused_kernel_ms": round(f_kernel, 5),
+            "fused_kernel_algorithmic_bytes": fused_bytes,
+            "fused_kernel_gbs": round(gbs(fused_bytes, f_kernel), 1),
+            "fused_kernel_frac_hbm": round(gbs(fused_bytes, f_kernel) / peak, 4),
+            "fused_kernel_traffic_bytes": profile_traffic(
+                "mtp_step_kernel", ["gated_deltanet_linear_10_gb300/csrc/" + f for f in
+                                    ("mtp_step.cu", "common.cuh")]),
+            "accept_copies_ms": round(f_accept, 5),
+            "three_calls": {
+                "step_ms": round(c_whole, 5),
+                "tokens_per_s": round(T / (c_whole / 1e3), 1),
+                "gpu_launches_per_step": 5,
+                "conv_update_gating_ms": round(c_front, 5),
+                "decode_kernel_ms": round(c_dec, 5),
+                "decode_kernel_gbs": round(gbs(dec_bytes, c_dec), 1),
+                "decode_kernel_frac_hbm": round(gbs(dec_bytes, c_dec) / peak, 4),
+                "decode_kernel_algorithmic_bytes": dec_bytes,
+                "decode_kernel_traffic_bytes": profile_traffic(
+                    "decode_kernel_mtp", ["gated_deltanet_linear_10_gb300/csrc/" + f for f in
+                                          ("decode.cu", "common.cuh", "tc.cuh")]),
+                "accept_copies_ms": round(c_accept, 5)}}
 
 
 def bench_mixed(gdn, workloads, dev, flush, steps=20):

@@ -30,7 +30,7 @@ EXPORTS = (
     "gdn_prefill_workspace_size", "gdn_decode_recurrent", "gdn_state_snapshot",
     "gdn_get_device_status", "gdn_prefill_chunked_static", "gdn_gated_rmsnorm",
     "gdn_decode_recurrent_gated", "gdn_decode_step_fused", "gdn_mixed_batch",
-    "gdn_debug_set_wait_limit", "gdn_prefill_chunked_gated",
+    "gdn_debug_set_wait_limit", "gdn_prefill_chunked_gated", "gdn_mtp_step_fused",
 )
 
 if not os.path.exists(LIB_PATH):
@@ -68,6 +68,8 @@ _SIGS = {
     "gdn_prefill_chunked_static": [_vp, _i64, _vp, _i64, _vp, _i64, _vp, _vp, _vp, _i32, _i64,
                                    _i32, _i32, _f32, _i32, _vp, _i64, _vp, _vp, _vp, _vp],
     "gdn_debug_set_wait_limit": [ctypes.c_uint64, _i32, _vp],
+    "gdn_mtp_step_fused": [_vp, _i64, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32,
+                           _f32, _vp, _i64, _vp, _vp, _vp, _vp],
     "gdn_prefill_chunked_gated": [_vp, _i64, _vp, _i64, _vp, _i64, _vp, _vp, _vp, _i32, _i64,
                                   _i32, _i32, _i32, _i32, _f32, _i32, _i32, _vp, _i64, _vp, _vp,
                                   _vp, _i64, _vp, _f32, _vp, _i32, _vp, ctypes.c_size_t, _vp],
@@ -497,6 +499,45 @@ def gdn_decode_step_fused(x, conv_weight, conv_state_pool, a, b, A_log, dt_bias,
         _ptr(b), _ptr(A_log), _ptr(dt_bias), N, hqk, hv, float(scale), _ptr(state_pool),
         state_pool.shape[0], _ptr(state_indices), _ptr(o), _stream(x.device)),
         "gdn_decode_step_fused")
+    return o
+
+
+def gdn_mtp_step_fused(x, tokens_per_seq, conv_weight, conv_state_pool, a, b, A_log, dt_bias,
+                       hqk, state_pool, state_indices, snap_indices, scale=None, conv_bias=None,
+                       o=None):
+    """One MTP draft step in one kernel: conv update + SiLU of the raw q|k|v
+    stream x [N * tps, C] (row i * tps + t), gating from a, b [N * tps, hv],
+    L2 norms and the recurrent update over the tps tokens, with the conv and
+    recurrent states after token t written to slot snap_indices[i][t] of
+    both pools (the source slots are only read).  Returns o [N * tps, hv, 128]."""
+    _cuda(x, conv_weight, conv_state_pool, a, b, A_log, dt_bias, state_pool, state_indices,
+          snap_indices, conv_bias)
+    T, C = x.shape
+    hv = a.shape[1]
+    _i32_vec(state_indices, "state_indices")
+    _i32_vec(snap_indices, "snap_indices")
+    N = state_indices.numel()
+    _need(T == N * tokens_per_seq, "x rows != n_seqs * tokens_per_seq")
+    _need(snap_indices.numel() == T, "snap_indices: [n_seqs, tps]")
+    _need(x.dtype == torch.bfloat16 and x.stride(1) == 1, "x: bf16 rows")
+    _need(C == 2 * hqk * 128 + hv * 128, "x: 2*hqk*128 + hv*128 channels")
+    _need(conv_weight.shape == (C, 4) and conv_weight.is_contiguous()
+          and conv_weight.dtype == torch.bfloat16, "conv_weight: [C, 4] bf16")
+    _need(conv_state_pool.dtype == torch.bfloat16 and conv_state_pool.is_contiguous()
+          and conv_state_pool.shape[1:] == (3, C), "conv_state_pool: [slots, 3, C] bf16")
+    _need(a.shape == (T, hv) and b.shape == (T, hv) and a.is_contiguous() and b.is_contiguous()
+          and a.dtype == b.dtype == torch.bfloat16, "a, b: [N*tps, hv] bf16")
+    _need(state_pool.dtype == torch.float32 and state_pool.is_contiguous()
+          and state_pool.shape[1:] == (hv, 128, 128), "state_pool: [slots, hv, 128, 128] fp32")
+    _need(conv_state_pool.shape[0] == state_pool.shape[0], "pools: same slot count")
+    scale = 128 ** -0.5 if scale is None else scale
+    o = torch.empty((T, hv, 128), dtype=torch.bfloat16, device=x.device) if o is None else o
+    _need(o.is_contiguous() and o.shape == (T, hv, 128), "o: [N*tps, hv, 128] contiguous")
+    _check(_lib.gdn_mtp_step_fused(
+        _ptr(x), x.stride(0), _ptr(conv_weight), _ptr(conv_bias), _ptr(conv_state_pool), _ptr(a),
+        _ptr(b), _ptr(A_log), _ptr(dt_bias), N, tokens_per_seq, hqk, hv, float(scale),
+        _ptr(state_pool), state_pool.shape[0], _ptr(state_indices), _ptr(snap_indices), _ptr(o),
+        _stream(x.device)), "gdn_mtp_step_fused")
     return o
 
 

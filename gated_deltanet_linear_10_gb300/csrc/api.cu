@@ -102,6 +102,7 @@ gdn_status gdn_get_device_status(uint32_t *out, int32_t clear, void *stream) {
     if ((st = read_status_norm(out, clear, s)) != GDN_OK) return st;
     if ((st = read_status_mixed(out, clear, s)) != GDN_OK) return st;
     if ((st = read_status_prefill_scan(out, clear, s)) != GDN_OK) return st;
+    if ((st = read_status_mtp_step(out, clear, s)) != GDN_OK) return st;
     return GDN_OK;
 }
 

@@ -34,6 +34,7 @@ gdn_status read_status_decode_step(uint32_t *out, int clear, cudaStream_t s);
 gdn_status read_status_api(uint32_t *out, int clear, cudaStream_t s);
 gdn_status read_status_mixed(uint32_t *out, int clear, cudaStream_t s);
 gdn_status read_status_prefill_scan(uint32_t *out, int clear, cudaStream_t s);
+gdn_status read_status_mtp_step(uint32_t *out, int clear, cudaStream_t s);
 
 #define GDN_STATUS_READER(fn, word)                                             \
     gdn_status fn(uint32_t *out, int clear, cudaStream_t s) {                  \

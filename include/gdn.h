@@ -376,6 +376,37 @@ gdn_status gdn_decode_step_fused(const void *x, int64_t x_row_stride,
                                  void *stream);
 
 /*
+ * One MTP draft step of the layer in one kernel: gdn_decode_step_fused for
+ * tokens_per_seq tokens per sequence (row i * tokens_per_seq + t) with the
+ * per-token snapshots MTP accept / rollback needs (the state copying of
+ * linear-attention states during MTP decode, "[model] support Qwen3next",
+ * Highlights).  For each sequence i with a slot:
+ *   the conv update + SiLU of the raw q|k|v stream, the conv state after
+ *     token t written to slot snap_indices[i][t] of the conv pool;
+ *   the gates, the q / k L2 norms;
+ *   the gated delta rule over the tokens, the state after token t written to
+ *     slot snap_indices[i][t] of the state pool (o as gdn_decode_recurrent).
+ * Slot state_indices[i] of both pools is only read.  Equal to
+ * causal_conv1d_update + gdn_gating + gdn_decode_recurrent, each with the
+ * same snapshots.  snap_indices is required ([n_seqs][tokens_per_seq]; an
+ * entry < 0 is skipped, >= n_slots skipped and flagged); snapshot slots
+ * must differ from one another and from every source slot (a shared slot is
+ * a race).  conv_state_pool must be 16-byte aligned.  Arguments as
+ * gdn_decode_step_fused otherwise: x [n_seqs * tokens_per_seq] rows of the
+ * raw stream, a, b [n_seqs * tokens_per_seq][hv] bf16, o
+ * [n_seqs * tokens_per_seq][hv][128] bf16.
+ * Built: bf16, dk = dv = 128, conv width 4, SiLU on, tokens_per_seq in [1, 16].
+ */
+gdn_status gdn_mtp_step_fused(const void *x, int64_t x_row_stride,
+                              const void *conv_weight, const void *conv_bias,
+                              void *conv_state_pool, const void *a, const void *b,
+                              const float *A_log, const float *dt_bias, int32_t n_seqs,
+                              int32_t tokens_per_seq, int32_t hqk, int32_t hv,
+                              float scale, float *state_pool, int64_t n_slots,
+                              const int32_t *state_indices,
+                              const int32_t *snap_indices, void *o, void *stream);
+
+/*
  * A serving step's mixed batch in one call: decode continuations and prefill
  * sequences packed in one varlen batch (the mixed decode / prefill batches
  * and chunked prefill of "[model] support Qwen3next").
