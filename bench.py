@@ -37,8 +37,9 @@ sys.path.insert(0, ROOT)
 METRIC = "GDN decode tokens/s + state HBM GB/s; chunked prefill tokens/s; % roofline"
 UNIT = "tokens/s"
 DECODE_WORKLOAD = ("decode step: 256 sequences x 1 token, causal conv update (8192 ch, width 4) "
-                   "+ gating + q/k L2 norm + recurrent decode in one kernel "
-                   "(gdn_decode_step_fused), 16 QK / 32 V heads, head_dim 128, "
+                   "+ gating + q/k L2 norm + recurrent decode (gdn_decode_step_fused with its "
+                   "workspace: the conv / gates kernel, then the streaming decode behind it by "
+                   "programmatic dependent launch), 16 QK / 32 V heads, head_dim 128, "
                    "bf16 activations, fp32 state pool 1024 slots x 32 x 128 x 128")
 
 
@@ -241,11 +242,14 @@ def run_ours(args):
 
     stream = torch.cuda.current_stream(dev)
 
-    def step(ev=None):      # the decode step: one fused kernel
+    ws = torch.empty(gdn.gdn_decode_step_workspace_size(N, d.hqk, d.hv), dtype=torch.uint8,
+                     device=dev)
+
+    def step(ev=None, workspace=ws):   # the decode step (two launches with the workspace)
         if ev is not None:
             ev[0].record(stream)
         gdn.gdn_decode_step_fused(x, conv_w, cpool, a, b, A_log, dt_bias, d.hqk, spool, slots,
-                                  scale=w.scale, o=o)
+                                  scale=w.scale, o=o, workspace=workspace)
         if ev is not None:
             ev[1].record(stream)
 
@@ -287,12 +291,34 @@ def run_ours(args):
     ms_step = sum(step_ms) / K
     ms_step_max = reduce_max(ms_step, dev)
     value = whole_job(N, ms_step_max / 1e3, world)
-    dec_avg = ms_step                            # the step is the one kernel
+    # the roofline unit is the whole step (both kernels, the fused step's
+    # algorithmic bytes: the y / gates round trip through the workspace is
+    # not counted)
+    dec_avg = ms_step
     dec_bytes = decode_step_bytes(N, d.hqk, d.hv, d.channels)
     achieved = dec_bytes / (dec_avg / 1e3) / 1e9
-    traffic = profile_traffic("decode_step_kernel",
+    traffic = profile_traffic("decode_step_two_kernels",
                               ["gated_deltanet_linear_10_gb300/csrc/" + f for f in
-                               ("decode_step.cu", "common.cuh", "tc.cuh")])
+                               ("decode_step.cu", "decode.cu", "common.cuh", "tc.cuh")])
+
+    # ---- the same step without a workspace: one kernel
+    Ko = min(K, 300)
+    evo = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(Ko)]
+    for _ in range(3):
+        step(workspace=False)
+        flush.zero_()
+    torch.cuda.synchronize(dev)
+    torch.cuda._sleep(2_000_000)
+    for i in range(Ko):
+        step(evo[i], workspace=False)
+        flush.zero_()
+    torch.cuda.synchronize(dev)
+    one_ms = sum(e[0].elapsed_time(e[1]) for e in evo) / Ko
+    one_kernel = {"ms_per_step": round(one_ms, 5),
+                  "frac_hbm": round(dec_bytes / (one_ms / 1e3) / 1e9 / peaks["hbm_gbs"], 4),
+                  "traffic": profile_traffic("decode_step_kernel",
+                                             ["gated_deltanet_linear_10_gb300/csrc/" + f for f in
+                                              ("decode_step.cu", "common.cuh", "tc.cuh")])}
 
     # ---- the same step as three calls (conv update, gating, decode)
     Ku = min(K, 200)
@@ -364,13 +390,16 @@ def run_ours(args):
         "config": {"workload": DECODE_WORKLOAD, "global_batch": N * world, "seq_len": 1,
                    "io_dtype": "bf16", "l2": "flushed between steps (256 MiB write)",
                    "parallelism": f"replicas x{world}"},
-        "roofline": {"bound": "hbm", "kernel": "decode_step_kernel", "achieved": round(achieved, 1),
+        "roofline": {"bound": "hbm",
+                     "kernel": "decode_front_kernel + decode_stream_kernel (one step)",
+                     "achieved": round(achieved, 1),
                      "peak": peaks["hbm_gbs"], "unit": "GB/s",
                      "frac": round(achieved / peaks["hbm_gbs"], 4), "traffic": traffic,
                      "algorithmic_bytes": dec_bytes, "avg_launch_ms": round(dec_avg, 5),
                      "peak_source": peaks["source"]},
         "kernels_ms": {"gdn_decode_step_fused": round(dec_avg, 5)},
         "state_gbs": round(achieved, 1),
+        "step_one_kernel": one_kernel,
         "step_unfused": unfused,
         "e2e": {"value": round(whole_job(N, e2e_ms / 1e3, world), 1), "unit": UNIT,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
@@ -380,7 +409,7 @@ def run_ours(args):
                            "per step)",
                 "serial_ms_per_step": round(e2e_serial_ms, 5),
                 "serial_value": round(whole_job(N, e2e_serial_ms / 1e3, world), 1)},
-        "gpu_launches": K,
+        "gpu_launches": 2 * K,
         "clocks": clocks,
         "wall_s_timed": round(wall, 3),
         "cpu_baseline": cpu,
@@ -410,6 +439,8 @@ def e2e_pipelined(gdn, w, d, conv_w, A_log, dt_bias, cpool, spool, slots, dev, s
     h2d_done = [torch.cuda.Event() for _ in range(2)]
     step_done = [torch.cuda.Event() for _ in range(2)]
     d2h_done = [torch.cuda.Event() for _ in range(2)]
+    ws = torch.empty(gdn.gdn_decode_step_workspace_size(n, d.hqk, d.hv), dtype=torch.uint8,
+                     device=dev)
 
     def h2d(i):                 # on the copy stream, once buffer i % 2 is consumed
         j = i & 1
@@ -435,7 +466,7 @@ def e2e_pipelined(gdn, w, d, conv_w, A_log, dt_bias, cpool, spool, slots, dev, s
             if i >= 2:
                 comp.wait_event(d2h_done[j])    # o buffer j of step i - 2 is read back
             gdn.gdn_decode_step_fused(xs[j], conv_w, cpool, as_[j], bs[j], A_log, dt_bias, d.hqk,
-                                      spool, slots, scale=w.scale, o=os_[j])
+                                      spool, slots, scale=w.scale, o=os_[j], workspace=ws)
             step_done[j].record(comp)
             with torch.cuda.stream(copy):
                 copy.wait_event(step_done[j])

@@ -31,6 +31,7 @@ EXPORTS = (
     "gdn_get_device_status", "gdn_prefill_chunked_static", "gdn_gated_rmsnorm",
     "gdn_decode_recurrent_gated", "gdn_decode_step_fused", "gdn_mixed_batch",
     "gdn_debug_set_wait_limit", "gdn_prefill_chunked_gated", "gdn_mtp_step_fused",
+    "gdn_decode_step_workspace_size",
 )
 
 if not os.path.exists(LIB_PATH):
@@ -60,7 +61,7 @@ _SIGS = {
     "gdn_state_snapshot": [_vp, _i64, _i64, _vp, _vp, _i32, _vp],
     "gdn_get_device_status": [ctypes.POINTER(ctypes.c_uint32), _i32, _vp],
     "gdn_decode_step_fused": [_vp, _i64, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32,
-                              _f32, _vp, _i64, _vp, _vp, _vp],
+                              _f32, _vp, _i64, _vp, _vp, ctypes.c_size_t, _vp, _vp],
     "gdn_gated_rmsnorm": [_vp, _vp, _i64, _vp, _i64, _i32, _i32, _f32, _vp, _i32, _vp],
     "gdn_decode_recurrent_gated": [_vp, _i64, _vp, _i64, _vp, _i64, _vp, _vp, _i32, _i32, _i32,
                                    _i32, _i32, _i32, _f32, _i32, _vp, _i64, _vp, _vp, _vp, _i64,
@@ -83,6 +84,8 @@ for _name, _args in _SIGS.items():
     _fn.restype = ctypes.c_int
 _lib.gdn_prefill_workspace_size.argtypes = [_i32, _i64, _i32, _i32, _i32, _i32, _i32]
 _lib.gdn_prefill_workspace_size.restype = ctypes.c_size_t
+_lib.gdn_decode_step_workspace_size.argtypes = [_i32, _i32, _i32]
+_lib.gdn_decode_step_workspace_size.restype = ctypes.c_size_t
 
 
 class GdnError(RuntimeError):
@@ -467,13 +470,22 @@ def gdn_decode_recurrent_gated(q, k, v, g, beta, tokens_per_seq, state_pool, sta
     return y
 
 
+def gdn_decode_step_workspace_size(n_seqs, hqk, hv) -> int:
+    return int(_lib.gdn_decode_step_workspace_size(n_seqs, hqk, hv))
+
+
 def gdn_decode_step_fused(x, conv_weight, conv_state_pool, a, b, A_log, dt_bias, hqk,
-                          state_pool, state_indices, scale=None, conv_bias=None, o=None):
-    """One decode step in one kernel: conv update + SiLU of the raw q|k|v
-    stream x [N, C], gating from a, b [N, hv], L2 norms and the recurrent
-    update.  Same result as causal_conv1d_update + gdn_gating +
-    gdn_decode_recurrent.  bf16, dk = dv = 128; both pools use state_indices.
-    Returns o [N, hv, 128]."""
+                          state_pool, state_indices, scale=None, conv_bias=None, o=None,
+                          workspace=None):
+    """One decode step: conv update + SiLU of the raw q|k|v stream x [N, C],
+    gating from a, b [N, hv], L2 norms and the recurrent update.  Same result
+    as causal_conv1d_update + gdn_gating + gdn_decode_recurrent.  bf16,
+    dk = dv = 128; both pools use state_indices.  Returns o [N, hv, 128].
+
+    workspace: None allocates the scratch gdn_decode_step_workspace_size asks
+    for (the step then runs as the conv / gates kernel and the streaming
+    decode behind it); a uint8 CUDA tensor is used as given; False passes
+    none, which selects the single fused kernel."""
     _cuda(x, conv_weight, conv_state_pool, a, b, A_log, dt_bias, state_pool, state_indices,
           conv_bias)
     N, C = x.shape
@@ -494,11 +506,20 @@ def gdn_decode_step_fused(x, conv_weight, conv_state_pool, a, b, A_log, dt_bias,
     scale = 128 ** -0.5 if scale is None else scale
     o = torch.empty((N, hv, 128), dtype=torch.bfloat16, device=x.device) if o is None else o
     _need(o.is_contiguous() and o.shape == (N, hv, 128), "o: [N, hv, 128] contiguous")
+    if workspace is False:
+        workspace = None
+    elif workspace is None:
+        need = gdn_decode_step_workspace_size(N, hqk, hv)
+        if need:
+            workspace = torch.empty(need, dtype=torch.uint8, device=x.device)
+    else:
+        _cuda(workspace)
+    wbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     _check(_lib.gdn_decode_step_fused(
         _ptr(x), x.stride(0), _ptr(conv_weight), _ptr(conv_bias), _ptr(conv_state_pool), _ptr(a),
         _ptr(b), _ptr(A_log), _ptr(dt_bias), N, hqk, hv, float(scale), _ptr(state_pool),
-        state_pool.shape[0], _ptr(state_indices), _ptr(o), _stream(x.device)),
-        "gdn_decode_step_fused")
+        state_pool.shape[0], _ptr(state_indices), _ptr(workspace), wbytes, _ptr(o),
+        _stream(x.device)), "gdn_decode_step_fused")
     return o
 
 

@@ -21,6 +21,14 @@ namespace gdn {
 // Host helpers implemented in api.cu.
 void set_last_cuda_error(cudaError_t e);
 gdn_status launch_status();  // cudaGetLastError() after a launch -> status
+// decode.cu: the streaming decode launched behind the kernel producing its
+// inputs (programmatic dependent launch); used by the fused decode step
+cudaError_t launch_decode_stream_after(const __nv_bfloat16 *q, int64_t qs,
+                                       const __nv_bfloat16 *k, int64_t ks,
+                                       const __nv_bfloat16 *v, int64_t vs, const float *g,
+                                       const float *beta, int n_seqs, int hqk, int hv,
+                                       float scale, float *pool, int64_t n_slots,
+                                       const int32_t *idx, __nv_bfloat16 *o, cudaStream_t s);
 int sm_count();              // multiprocessors of the current device
 
 // Per-TU readers of the status word (defined next to each word).
@@ -168,6 +176,16 @@ __device__ __forceinline__ float silu_bf16out(float z) {
     const float h = 0.5f * z;
     return fmaf(h, tanh_approx(h), h);
 }
+// Programmatic dependent launch.  A kernel launched with programmatic stream
+// serialization may start while the kernel before it in the stream is still
+// running; griddep_wait() returns once that kernel has completed and its
+// writes are visible (immediately when there is none), and griddep_launch()
+// lets the next such kernel start before this CTA exits.
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void griddep_launch() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // The SiLU a kernel with outputs of type T takes: the fast division for fp32
 // outputs, the tanh form for bf16.
 template <typename T> __device__ __forceinline__ float silu_for(float z);

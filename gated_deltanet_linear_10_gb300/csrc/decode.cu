@@ -301,6 +301,10 @@ decode_stream_kernel(const T *__restrict__ q, int64_t qs, const T *__restrict__ 
             }
             ++ph[0];
         }
+        // launched behind the kernel that writes q, k, v, g and beta (the
+        // fused decode step's front kernel): the first state is on its way,
+        // the inputs are read only once that kernel has finished
+        griddep_wait();
         load_in(i, h, part, cur);
     }
     for (int n = 0; w < n_items; w += gridDim.x, ++n) {
@@ -406,6 +410,36 @@ static cudaError_t launch_decode(const void *q, int64_t qs, const void *k, int64
             scale, l2norm, pool, n_slots, idx, snap, (const T *)z, zs, nw, neps, (T *)o);
     }
     return cudaGetLastError();
+}
+
+// The streaming decode (bf16, dk = dv = 128, one token, q / k L2-normalised)
+// launched with programmatic stream serialization: its CTAs may start while
+// the kernel before it in the stream (which writes q, k, v, g, beta) is still
+// finishing, and fetch their first state meanwhile.
+cudaError_t launch_decode_stream_after(const __nv_bfloat16 *q, int64_t qs,
+                                       const __nv_bfloat16 *k, int64_t ks,
+                                       const __nv_bfloat16 *v, int64_t vs, const float *g,
+                                       const float *beta, int n_seqs, int hqk, int hv,
+                                       float scale, float *pool, int64_t n_slots,
+                                       const int32_t *idx, __nv_bfloat16 *o, cudaStream_t s) {
+    const int n_items = (int)((int64_t)n_seqs * hv * 2);
+    const int grid = (int)std::min<int64_t>(n_items, (int64_t)sm_count() * kStrCtasPerSm);
+    cudaError_t e = cudaFuncSetAttribute(decode_stream_kernel<__nv_bfloat16>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)(2 * kStrBytes));
+    if (e != cudaSuccess) return e;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)grid);
+    cfg.blockDim = dim3(kDecThreads);
+    cfg.dynamicSmemBytes = 2 * kStrBytes;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, decode_stream_kernel<__nv_bfloat16>, q, qs, k, ks, v, vs, g,
+                              beta, n_items, hv, hv / hqk, scale, 1, pool, n_slots, idx, o);
 }
 
 }  // namespace gdn

@@ -255,10 +255,102 @@ decode_step_kernel(const __nv_bfloat16 *__restrict__ x, int64_t xs,
     }
 }
 
+// ------------------------------------------------- with a workspace --
+// The same step as two kernels: this front kernel (conv update + SiLU of the
+// raw stream into y, the gates into g / beta, all in the workspace), then the
+// streaming decode kernel launched behind it (programmatic dependent launch),
+// which L2-normalises q and k itself.  Every channel is convolved once, so
+// the in-place conv state update needs no grouping, and the decode streams
+// its state blocks in the pool's order.
+constexpr int kFrontThreads = 256;
+constexpr int kFrontVec = 8;                 // channels per thread: one 16-byte vector
+
+__device__ __forceinline__ float bf_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+
+__global__ void __launch_bounds__(kFrontThreads)
+decode_front_kernel(const __nv_bfloat16 *__restrict__ x, int64_t xs,
+                    const __nv_bfloat16 *__restrict__ cw, const __nv_bfloat16 *__restrict__ cb,
+                    __nv_bfloat16 *__restrict__ cpool, const __nv_bfloat16 *__restrict__ a,
+                    const __nv_bfloat16 *__restrict__ b, const float *__restrict__ A_log,
+                    const float *__restrict__ dt_bias, int n_seqs, int hv, int C,
+                    int64_t n_slots, const int32_t *__restrict__ idx,
+                    __nv_bfloat16 *__restrict__ y, float *__restrict__ g_out,
+                    float *__restrict__ b_out) {
+    // the decode kernel behind this one may start placing its CTAs (they
+    // fetch their first state, then wait for this grid to complete)
+    griddep_launch();
+    const int per_seq = C / kFrontVec;
+    const int64_t gt = (int64_t)blockIdx.x * kFrontThreads + threadIdx.x;
+    const int i = (int)(gt / per_seq);
+    const int v8 = (int)(gt - (int64_t)i * per_seq);
+    if (i < n_seqs) {
+        const int64_t slot = idx[i];
+        // everything but the conv state is requested before the slot id is back
+        const int ch = v8 * kFrontVec;
+        const uint4 xv = *reinterpret_cast<const uint4 *>(x + (int64_t)i * xs + ch);
+        const uint4 *wp = reinterpret_cast<const uint4 *>(cw + (int64_t)ch * kW);
+        const uint4 wv[4] = {wp[0], wp[1], wp[2], wp[3]};   // 8 channels x 4 taps
+        uint4 bv = make_uint4(0u, 0u, 0u, 0u);
+        if (cb) bv = *reinterpret_cast<const uint4 *>(cb + ch);
+        if (v8 < hv) {    // the gates of (i, head v8)
+            const int64_t r = (int64_t)i * hv + v8;
+            g_out[r] = -__expf(A_log[v8]) * softplus_f(bf(a + r) + dt_bias[v8]);
+            b_out[r] = 1.f / (1.f + __expf(-bf(b + r)));
+        }
+        if (slot >= 0 && slot < n_slots) {
+            __nv_bfloat16 *cs = cpool + slot * (kW - 1) * C + ch;
+            const uint4 h0 = *reinterpret_cast<const uint4 *>(cs);
+            const uint4 h1 = *reinterpret_cast<const uint4 *>(cs + C);
+            const uint4 h2 = *reinterpret_cast<const uint4 *>(cs + 2 * C);
+            const uint32_t xw[4] = {xv.x, xv.y, xv.z, xv.w}, w0[4] = {h0.x, h0.y, h0.z, h0.w},
+                           w1[4] = {h1.x, h1.y, h1.z, h1.w}, w2[4] = {h2.x, h2.y, h2.z, h2.w},
+                           bw[4] = {bv.x, bv.y, bv.z, bv.w};
+            const uint32_t *tw = reinterpret_cast<const uint32_t *>(wv);   // taps: 2 words per channel
+            uint32_t out[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {          // channels 2e, 2e + 1
+                float r2[2];
+#pragma unroll
+                for (int u = 0; u < 2; ++u) {
+                    const int c = 2 * e + u;
+                    const uint32_t t01 = tw[2 * c], t23 = tw[2 * c + 1];
+                    const float xin = u ? bf_hi(xw[e]) : bf_lo(xw[e]);
+                    const float s0 = u ? bf_hi(w0[e]) : bf_lo(w0[e]);
+                    const float s1 = u ? bf_hi(w1[e]) : bf_lo(w1[e]);
+                    const float s2 = u ? bf_hi(w2[e]) : bf_lo(w2[e]);
+                    float acc = u ? bf_hi(bw[e]) : bf_lo(bw[e]);
+                    acc = fmaf(bf_lo(t01), s0, acc);
+                    acc = fmaf(bf_hi(t01), s1, acc);
+                    acc = fmaf(bf_lo(t23), s2, acc);
+                    acc = fmaf(bf_hi(t23), xin, acc);
+                    r2[u] = silu_bf16out(acc);
+                }
+                out[e] = pack_bf16(r2[0], r2[1]);
+            }
+            *reinterpret_cast<uint4 *>(y + (int64_t)i * C + ch) = make_uint4(out[0], out[1], out[2], out[3]);
+            // the state shifts by one input: the raw bf16 values move as they are
+            *reinterpret_cast<uint4 *>(cs) = h1;
+            *reinterpret_cast<uint4 *>(cs + C) = h2;
+            *reinterpret_cast<uint4 *>(cs + 2 * C) = xv;
+        } else if (slot >= n_slots && v8 == 0) {
+            flag_status(GDN_DEVSTAT_BAD_INDEX);
+        }
+    }
+}
+
+__host__ __device__ inline size_t align256(size_t n) { return (n + 255) / 256 * 256; }
+
 }  // namespace dstep
 }  // namespace gdn
 
 using namespace gdn;
+
+extern "C" size_t gdn_decode_step_workspace_size(int32_t n_seqs, int32_t hqk, int32_t hv) {
+    if (n_seqs <= 0 || hqk <= 0 || hv <= 0) return 0;
+    const size_t C = 2 * (size_t)hqk * 128 + (size_t)hv * 128;
+    return dstep::align256((size_t)n_seqs * C * 2) + 2 * dstep::align256((size_t)n_seqs * hv * 4);
+}
 
 extern "C" gdn_status gdn_decode_step_fused(const void *x, int64_t x_row_stride,
                                             const void *conv_weight, const void *conv_bias,
@@ -266,7 +358,8 @@ extern "C" gdn_status gdn_decode_step_fused(const void *x, int64_t x_row_stride,
                                             const float *A_log, const float *dt_bias,
                                             int32_t n_seqs, int32_t hqk, int32_t hv, float scale,
                                             float *state_pool, int64_t n_slots,
-                                            const int32_t *state_indices, void *o, void *stream) {
+                                            const int32_t *state_indices, void *workspace,
+                                            size_t workspace_bytes, void *o, void *stream) {
     GDN_REQUIRE(n_seqs >= 0 && hqk > 0 && hv > 0 && n_slots >= 0, GDN_ERR_INVALID_ARG);
     GDN_REQUIRE(hv % hqk == 0, GDN_ERR_INVALID_ARG);
     GDN_REQUIRE(hv / hqk <= dstep::kMaxGrp, GDN_ERR_UNSUPPORTED);
@@ -280,11 +373,39 @@ extern "C" gdn_status gdn_decode_step_fused(const void *x, int64_t x_row_stride,
     GDN_REQUIRE(((uintptr_t)conv_weight % 8) == 0 && ((uintptr_t)state_pool % 16) == 0,
                 GDN_ERR_INVALID_ARG);
     cudaStream_t s = (cudaStream_t)stream;
-    int dev = 0, sms = 148;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    const size_t ws_need = gdn_decode_step_workspace_size(n_seqs, hqk, hv);
+    const bool two_kernels =
+        workspace && workspace_bytes >= ws_need && ((uintptr_t)workspace % 256) == 0 &&
+        ((uintptr_t)x % 16) == 0 && (x_row_stride % 8) == 0 &&
+        ((uintptr_t)conv_weight % 16) == 0 && ((uintptr_t)conv_state_pool % 16) == 0 &&
+        (!conv_bias || ((uintptr_t)conv_bias % 16) == 0);
+    if (two_kernels) {
+        uint8_t *ws = (uint8_t *)workspace;
+        __nv_bfloat16 *y = (__nv_bfloat16 *)ws;
+        float *g = (float *)(ws + dstep::align256((size_t)n_seqs * C * 2));
+        float *beta = g + dstep::align256((size_t)n_seqs * hv * 4) / 4;
+        const int64_t threads = (int64_t)n_seqs * (C / dstep::kFrontVec);
+        dstep::decode_front_kernel<<<(unsigned)((threads + dstep::kFrontThreads - 1) /
+                                                dstep::kFrontThreads),
+                                     dstep::kFrontThreads, 0, s>>>(
+            (const __nv_bfloat16 *)x, x_row_stride, (const __nv_bfloat16 *)conv_weight,
+            (const __nv_bfloat16 *)conv_bias, (__nv_bfloat16 *)conv_state_pool,
+            (const __nv_bfloat16 *)a, (const __nv_bfloat16 *)b, A_log, dt_bias, n_seqs, hv, C,
+            n_slots, state_indices, y, g, beta);
+        gdn_status st = launch_status();
+        if (st != GDN_OK) return st;
+        const int nq = hqk * 128;
+        cudaError_t e = launch_decode_stream_after(y, C, y + nq, C, y + 2 * nq, C, g, beta, n_seqs,
+                                                   hqk, hv, scale, state_pool, n_slots,
+                                                   state_indices, (__nv_bfloat16 *)o, s);
+        if (e != cudaSuccess) {
+            set_last_cuda_error(e);
+            return GDN_ERR_LAUNCH;
+        }
+        return GDN_OK;
+    }
     const int n_groups = n_seqs * hqk;
-    const int grid = std::min(n_groups, sms * dstep::kCtasPerSm);
+    const int grid = std::min(n_groups, sm_count() * dstep::kCtasPerSm);
     cudaError_t e = cudaFuncSetAttribute(dstep::decode_step_kernel,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)(2 * dstep::kStageBytes));

@@ -345,9 +345,16 @@ gdn_status gdn_decode_recurrent_gated(const void *q, int64_t q_row_stride,
                                       void *y, int32_t dtype, void *stream);
 
 /*
- * One decode step of the layer in one kernel (fusion of the
- * "causal 1D convolution", "fused GDN gating" and "fused recurrent GDN"
- * kernels the Qwen3next pages name): for each sequence i with one new token,
+ * Bytes of the workspace gdn_decode_step_fused takes: the conv output y
+ * [n_seqs][channels] bf16 and the gates g, beta [n_seqs][hv] fp32, each
+ * rounded up to 256 bytes.  0 for an empty batch.
+ */
+size_t gdn_decode_step_workspace_size(int32_t n_seqs, int32_t hqk, int32_t hv);
+
+/*
+ * One decode step of the layer (fusion of the "causal 1D convolution",
+ * "fused GDN gating" and "fused recurrent GDN" kernels the Qwen3next pages
+ * name): for each sequence i with one new token,
  *   y   = SiLU(conv_bias + sum_w conv_weight[c][w] * [state; x_i][w])   (width 4)
  *   q|k|v = split(y), q and k L2-normalised per head (eps 1e-6)
  *   g = -exp(A_log[h]) softplus(a_ih + dt_bias[h]), beta = sigmoid(b_ih)
@@ -360,6 +367,14 @@ gdn_status gdn_decode_recurrent_gated(const void *q, int64_t q_row_stride,
  *      place in slot state_indices[i] (the same slot id as the state pool).
  *   a, b: [n_seqs][hv] bf16; A_log, dt_bias: [hv] fp32.
  *   state_pool: [n_slots][hv][128][128] fp32 (16-byte aligned).
+ *   workspace: NULL, or device scratch of workspace_bytes >=
+ *      gdn_decode_step_workspace_size(n_seqs, hqk, hv), 256-byte aligned,
+ *      owned by the caller and not shared with a call in flight on another
+ *      stream.  With it (and x, x_row_stride, conv_weight, conv_bias and
+ *      conv_state_pool 16-byte aligned) the step runs as two kernels: the
+ *      conv update and gates into the workspace, then the streaming decode
+ *      launched behind it (programmatic dependent launch).  Without it, or
+ *      when it is too small, one kernel does the whole step.
  *   o: [n_seqs][hv][128] bf16.
  * A slot < 0 skips the sequence (o rows zero, neither pool touched); a slot
  * >= n_slots is skipped the same way and sets GDN_DEVSTAT_BAD_INDEX.
@@ -372,8 +387,8 @@ gdn_status gdn_decode_step_fused(const void *x, int64_t x_row_stride,
                                  const float *dt_bias, int32_t n_seqs,
                                  int32_t hqk, int32_t hv, float scale,
                                  float *state_pool, int64_t n_slots,
-                                 const int32_t *state_indices, void *o,
-                                 void *stream);
+                                 const int32_t *state_indices, void *workspace,
+                                 size_t workspace_bytes, void *o, void *stream);
 
 /*
  * One MTP draft step of the layer in one kernel: gdn_decode_step_fused for

@@ -1,10 +1,12 @@
 """GPU parity of the fused decode step (conv update + SiLU, gating, L2 norms
-and the recurrent update in one kernel) through the C ABI, against the
-oracle's conv update -> gating -> decode chain: o and the updated states
-within the bf16 tolerance, the conv state pool bit for bit, untouched slots
-unchanged, at the full decode size (with a padding row) and at small shapes
-with one and two V heads per QK head and a conv bias, and with many more
-groups than CTAs and padding rows between them."""
+and the recurrent update) through the C ABI, on both of its paths (one
+kernel without a workspace; the conv / gates kernel and the streaming decode
+behind it with one), against the oracle's conv update -> gating -> decode
+chain: o and the updated states within the bf16 tolerance, the conv state
+pool bit for bit, untouched slots unchanged, at the full decode size (with a
+padding row) and at small shapes with one and two V heads per QK head and a
+conv bias, and with many more groups than CTAs and padding rows between
+them."""
 import numpy as np
 import pytest
 import torch
@@ -18,13 +20,18 @@ from tests.test_gpu_decode import _state_err, _sub_pool, _untouched
 pytestmark = pytest.mark.gpu
 
 
-def _check_step(x, conv_w, conv_b, cpool0, a, b, A_log, dt_bias, pool0, idx, hqk, hv, scale):
+PATHS = ["two_kernels", "one_kernel"]
+
+
+def _check_step(x, conv_w, conv_b, cpool0, a, b, A_log, dt_bias, pool0, idx, hqk, hv, scale,
+                path):
     """Run the fused step on copies of the pools and compare with the oracle."""
     cpool = cuda(cpool0)
     pool = cuda(pool0)
     o = gdn().gdn_decode_step_fused(cuda(x), cuda(conv_w), cpool, cuda(a), cuda(b), cuda(A_log),
                                     cuda(dt_bias), hqk, pool, cuda(idx), scale=scale,
-                                    conv_bias=None if conv_b is None else cuda(conv_b))
+                                    conv_bias=None if conv_b is None else cuda(conv_b),
+                                    workspace=None if path == "two_kernels" else False)
     torch.cuda.synchronize()
     status_clean()
     live = [int(s) for s in idx if s >= 0]
@@ -49,7 +56,8 @@ def _check_step(x, conv_w, conv_b, cpool0, a, b, A_log, dt_bias, pool0, idx, hqk
     assert bits_equal(got[others], cpool0[others])
 
 
-def test_fused_step_full_size():
+@pytest.mark.parametrize("path", PATHS)
+def test_fused_step_full_size(path):
     """256 sequences x 1 token, 16 QK / 32 V heads, 8192 conv channels, pools
     of 1024 slots; sequence 5 has no slot."""
     w = workloads.decode()
@@ -57,11 +65,12 @@ def test_fused_step_full_size():
     idx = w.slots.clone()
     idx[5] = -1
     _check_step(w.x, w.conv_w, None, w.conv_pool, w.a, w.b, w.A_log, w.dt_bias,
-                w.state_pool, idx, d.hqk, d.hv, w.scale)
+                w.state_pool, idx, d.hqk, d.hv, w.scale, path)
 
 
+@pytest.mark.parametrize("path", PATHS)
 @pytest.mark.parametrize("hqk,hv", [(2, 4), (4, 4)])
-def test_fused_step_small_with_bias(hqk, hv):
+def test_fused_step_small_with_bias(hqk, hv, path):
     g = torch.Generator().manual_seed(91 + hv * hqk)
     n, n_slots = 7, 12
     C = 2 * hqk * 128 + hv * 128
@@ -75,10 +84,11 @@ def test_fused_step_small_with_bias(hqk, hv):
     pool0 = torch.randn(n_slots, hv, 128, 128, generator=g) * 0.02
     idx = torch.tensor([3, 0, -1, 11, 7, 1, 5], dtype=torch.int32)
     _check_step(x, conv_w, conv_b, cpool0, a, b, A_log, dt_bias, pool0, idx, hqk, hv,
-                128 ** -0.5)
+                128 ** -0.5, path)
 
 
-def test_fused_step_many_groups_with_padding():
+@pytest.mark.parametrize("path", PATHS)
+def test_fused_step_many_groups_with_padding(path):
     """600 sequences of one QK / two V heads: each persistent CTA loops over
     several groups, with a padding row (no slot) every seventh sequence."""
     g = torch.Generator().manual_seed(4242)
@@ -94,4 +104,4 @@ def test_fused_step_many_groups_with_padding():
     idx = torch.randperm(n_slots, generator=g)[:n].to(torch.int32)
     idx[::7] = -1
     _check_step(x, conv_w, None, cpool0, a, b, A_log, dt_bias, pool0, idx, hqk, hv,
-                128 ** -0.5)
+                128 ** -0.5, path)
