@@ -428,18 +428,9 @@ cudaError_t launch_decode_stream_after(const __nv_bfloat16 *q, int64_t qs,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)(2 * kStrBytes));
     if (e != cudaSuccess) return e;
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)grid);
-    cfg.blockDim = dim3(kDecThreads);
-    cfg.dynamicSmemBytes = 2 * kStrBytes;
-    cfg.stream = s;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, decode_stream_kernel<__nv_bfloat16>, q, qs, k, ks, v, vs, g,
-                              beta, n_items, hv, hv / hqk, scale, 1, pool, n_slots, idx, o);
+    return launch_after(decode_stream_kernel<__nv_bfloat16>, dim3((unsigned)grid),
+                        dim3(kDecThreads), 2 * kStrBytes, s, q, qs, k, ks, v, vs, g, beta,
+                        n_items, hv, hv / hqk, scale, 1, pool, n_slots, idx, o);
 }
 
 }  // namespace gdn

@@ -72,6 +72,7 @@ __device__ __forceinline__ int seq_chunks(const int32_t *cu, int s, int64_t n_to
 __global__ void __launch_bounds__(1024) chunk_base_kernel(const int32_t *__restrict__ cu,
                                                           int n_seqs, int64_t n_tokens,
                                                           int32_t *__restrict__ base) {
+    griddep_launch();        // the prep kernel behind it may start placing its CTAs
     __shared__ int warp_tot[32];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int per = (n_seqs + 1023) / 1024;
@@ -154,6 +155,11 @@ prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int it = (int)(blockIdx.x / (unsigned)hv);
     const int h = (int)blockIdx.x - it * hv;
+    // Launched behind the chunk-offset kernel: once every CTA of this grid
+    // has started, the chain kernel may place its CTAs on the SMs that the
+    // last wave leaves idle.  The chunk offsets are read after the wait.
+    griddep_launch();
+    griddep_wait();
     if (it >= base[n_seqs]) return;
     int lo = 0, hi = n_seqs - 1;          // the sequence: last s with base[s] <= it
     while (lo < hi) {
@@ -460,13 +466,17 @@ chain_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
         if (fslot >= n_out) fslot = -1;
     }
     if (s_start < 0 || s_end < s_start || s_end > n_tokens) {
-        if (tid == 0) flag_status(GDN_DEVSTAT_BAD_SEQLEN);
+        if (tid == 0) {
+            flag_status(GDN_DEVSTAT_BAD_SEQLEN);
+            griddep_wait();   // this grid completes after the prep kernel, on every path
+        }
         return;
     }
     const int nch = (int)((s_end - s_start + C - 1) / C);
     const size_t head_off = (size_t)h * DH * DH;
     const size_t slot_stride = (size_t)hv * DH * DH;
     if (nch == 0) {   // empty sequence: the initial state (zero, identity) is the final state
+        if (tid == 0) griddep_wait();
         if (fslot >= 0)
             for (int e = tid; e < DH * DH; e += kChainKernelThreads)
                 pool_out[fslot * slot_stride + head_off + e] =
@@ -529,6 +539,10 @@ chain_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
                     tma_load_2d(kq + kb * kKBlk + 64 * 128, &tm_q, &B.kq_full[sk], hq * DH + kb * 64, y);
                 }
                 kq_n[sk] = c / L::kKQ + 1;
+                // launched behind the prep kernel: the item blocks are read
+                // only once it has completed (K, Q, V and the initial state
+                // come from earlier kernels)
+                if (c == 0) griddep_wait();
                 if (c >= kCStages) mbar_wait(&B.c_empty[sc], ((c / kCStages) - 1) & 1, abort);
                 mbar_arrive_expect_tx(&B.c_full[sc], kItemScalCopy);
                 bulk_load(sm + L::Cs + sc * kCStageBytes, item + kItemOps, kItemScalCopy, &B.c_full[sc]);
@@ -856,6 +870,7 @@ chain_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
         tmem_dealloc(tbase, kTmemCols);
     }
     if (tid == 0 && B.abort) flag_status(GDN_DEVSTAT_TIMEOUT);
+    if (tid == 0) griddep_wait();   // no-op once the producer has waited
 }
 
 }  // namespace psp
@@ -900,22 +915,33 @@ gdn_status prefill_split(const void *q, int64_t qs, const void *k, int64_t ks, c
     psp::chunk_base_kernel<<<1, 1024, 0, s>>>(cu, n_seqs, n_tokens, base);
     gdn_status st = launch_status();
     if (st != GDN_OK) return st;
-    psp::prep_kernel<<<(unsigned)items, psp::kPrepKernelThreads, psp::P_SMEM_BYTES, s>>>(
-        tq, tk, g, beta, cu, base, n_seqs, hv, hv / hqk, scale, l2norm, item_blocks);
-    st = launch_status();
-    if (st != GDN_OK) return st;
-    const unsigned grid = (unsigned)((int64_t)n_seqs * hv);
+    e = launch_after(psp::prep_kernel, dim3((unsigned)items), dim3(psp::kPrepKernelThreads),
+                     psp::P_SMEM_BYTES, s, tq, tk, g, beta, cu, (const int32_t *)base, n_seqs,
+                     hv, hv / hqk, scale, l2norm, item_blocks);
+    if (e != cudaSuccess) {
+        set_last_cuda_error(e);
+        return GDN_ERR_LAUNCH;
+    }
+    const dim3 grid((unsigned)((int64_t)n_seqs * hv));
     if (gated)
-        psp::chain_kernel<true><<<grid, psp::kChainKernelThreads, psp::ChainSmem<true>::BYTES, s>>>(
-            tq, tk, tv, to, to, tz, psp::GateArgs{norm_w, norm_eps}, cu, base, n_seqs, n_tokens,
-            hv, hv / hqk, item_blocks, pool, n_slots, pool, n_slots, ii, fi, (__nv_bfloat16 *)o,
-            nullptr, psp::IdentChains{0, 0, 0});
+        e = launch_after(psp::chain_kernel<true>, grid, dim3(psp::kChainKernelThreads),
+                         psp::ChainSmem<true>::BYTES, s, tq, tk, tv, to, to, tz,
+                         psp::GateArgs{norm_w, norm_eps}, cu, (const int32_t *)base, n_seqs,
+                         n_tokens, hv, hv / hqk, (const uint8_t *)item_blocks,
+                         (const float *)pool, n_slots, pool, n_slots, ii, fi,
+                         (__nv_bfloat16 *)o, (__nv_bfloat16 *)nullptr, psp::IdentChains{0, 0, 0});
     else
-        psp::chain_kernel<false><<<grid, psp::kChainKernelThreads, psp::ChainSmem<false>::BYTES, s>>>(
-            tq, tk, tv, to, to, to, psp::GateArgs{nullptr, 0.f}, cu, base, n_seqs, n_tokens, hv,
-            hv / hqk, item_blocks, pool, n_slots, pool, n_slots, ii, fi, (__nv_bfloat16 *)o,
-            nullptr, psp::IdentChains{0, 0, 0});
-    return launch_status();
+        e = launch_after(psp::chain_kernel<false>, grid, dim3(psp::kChainKernelThreads),
+                         psp::ChainSmem<false>::BYTES, s, tq, tk, tv, to, to, to,
+                         psp::GateArgs{nullptr, 0.f}, cu, (const int32_t *)base, n_seqs,
+                         n_tokens, hv, hv / hqk, (const uint8_t *)item_blocks,
+                         (const float *)pool, n_slots, pool, n_slots, ii, fi,
+                         (__nv_bfloat16 *)o, (__nv_bfloat16 *)nullptr, psp::IdentChains{0, 0, 0});
+    if (e != cudaSuccess) {
+        set_last_cuda_error(e);
+        return GDN_ERR_LAUNCH;
+    }
+    return GDN_OK;
 }
 
 // ------------------------------------------------- chunk-state scan (host) --
@@ -997,16 +1023,21 @@ gdn_status prefill_scan(const void *q, int64_t qs, const void *k, int64_t ks, co
     if (st != GDN_OK) return st;
     psp::chunk_base_kernel<<<1, 1024, 0, s>>>(cu_all, 2, n_tokens, base);
     if ((st = launch_status()) != GDN_OK) return st;
-    psp::prep_kernel<<<(unsigned)items, psp::kPrepKernelThreads, psp::P_SMEM_BYTES, s>>>(
-        tq, tk, g, beta, cu_all, base, 2, hv, hv / hqk, scale, l2norm, item_blocks);
-    if ((st = launch_status()) != GDN_OK) return st;
-    psp::chain_kernel<false><<<(unsigned)(3 * hv), psp::kChainKernelThreads,
-                               psp::ChainSmem<false>::BYTES, s>>>(
-        tq, tk, tv, to, tphi, tphi, psp::GateArgs{nullptr, 0.f}, cu_all, base, 2, n_tokens, hv,
-        hv / hqk, item_blocks, pool, n_slots,
-        states, scan::kScratchSlots, seg_init, seg_fin, (__nv_bfloat16 *)o, (__nv_bfloat16 *)phi,
-        psp::IdentChains{1, 1, scan::kSlotA});
-    if ((st = launch_status()) != GDN_OK) return st;
+    e = launch_after(psp::prep_kernel, dim3((unsigned)items), dim3(psp::kPrepKernelThreads),
+                     psp::P_SMEM_BYTES, s, tq, tk, g, beta, cu_all, (const int32_t *)base, 2, hv,
+                     hv / hqk, scale, l2norm, item_blocks);
+    if (e == cudaSuccess)
+        e = launch_after(psp::chain_kernel<false>, dim3((unsigned)(3 * hv)),
+                         dim3(psp::kChainKernelThreads), psp::ChainSmem<false>::BYTES, s, tq, tk,
+                         tv, to, tphi, tphi, psp::GateArgs{nullptr, 0.f}, cu_all,
+                         (const int32_t *)base, 2, n_tokens, hv, hv / hqk,
+                         (const uint8_t *)item_blocks, (const float *)pool, n_slots, states,
+                         (int64_t)scan::kScratchSlots, seg_init, seg_fin, (__nv_bfloat16 *)o,
+                         (__nv_bfloat16 *)phi, psp::IdentChains{1, 1, scan::kSlotA});
+    if (e != cudaSuccess) {
+        set_last_cuda_error(e);
+        return GDN_ERR_LAUNCH;
+    }
     return scan_finish(states, hv, idx, pool, w + L.s1b, phi, phi_rows, o, n_tokens, s);
 }
 
