@@ -530,7 +530,7 @@ def bench_mtp(gdn, workloads, dev, flush, steps=50):
     def timed(body):
         ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(steps)]
         for i in range(3):
-            body(ev[i])
+            body(ev[i % steps])
             flush.zero_()
         torch.cuda.synchronize(dev)
         torch.cuda._sleep(1_000_000)
