@@ -25,6 +25,8 @@
 //            [items: (ceil(n_tokens / 64) + n_seqs) x hv blocks of kItemBytes]
 #include <stddef.h>
 
+#include <algorithm>
+
 #include "prefill_common.cuh"
 #include "prefill_scan.cuh"
 
@@ -109,6 +111,7 @@ __global__ void __launch_bounds__(1024) chunk_base_kernel(const int32_t *__restr
 constexpr int kPrepWarps = 9;              // warp 0: TMA + MMA + TMEM; warps 1..8: prep
 constexpr int kPrepKernelThreads = kPrepWarps * 32;
 constexpr int kPrepThreads = 256;
+constexpr int kPrepCtasPerSm = 3;
 
 struct PrepScal {
     float beta[C], gam[C], alpha[C], rk[C], rq[C], xs[C];
@@ -137,13 +140,14 @@ static_assert(kItemWBytes <= C * kLd * 4 && sizeof(ItemScal) <= kPWbBytes, "stag
 static_assert(P_OFF_T1 + kMatBytes == P_OFF_AF && kMatBytes <= 48 * kLd * 4,
               "T2 lands on Af rows below 48");
 static_assert(sizeof(PrepBars) <= 128, "barrier block");
-static_assert(3 * (P_SMEM_BYTES + 1024) <= 233472, "three prep CTAs per SM");
+static_assert(kPrepCtasPerSm * (P_SMEM_BYTES + 1024) <= 233472, "three prep CTAs per SM");
 
-// One CTA per (chunk, V head) item.  Warp 0: TMEM, TMA of the raw K|Q tile,
+// A persistent grid (3 CTAs per SM) over the (chunk, V head) items.  Per
+// item, warp 0: TMA of the raw K|Q tile,
 // M1 G = [K;Q] [K;Q]^T (its diagonal gives the row norms), then
 // MW W'^T = K^T T2^T; warps 1..8: the prep arithmetic, then bulk stores of
 // the item block.
-__global__ void __launch_bounds__(kPrepKernelThreads, 3)
+__global__ void __launch_bounds__(kPrepKernelThreads, kPrepCtasPerSm)
 prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
             const float *__restrict__ g, const float *__restrict__ beta,
             const int32_t *__restrict__ cu, const int32_t *__restrict__ base, int n_seqs, int hv,
@@ -153,22 +157,13 @@ prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
                                               ~uintptr_t(1023));
     PrepBars &B = *reinterpret_cast<PrepBars *>(sm + P_OFF_BARS);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int it = (int)(blockIdx.x / (unsigned)hv);
-    const int h = (int)blockIdx.x - it * hv;
     // Launched behind the chunk-offset kernel: once every CTA of this grid
     // has started, the chain kernel may place its CTAs on the SMs that the
-    // last wave leaves idle.  The chunk offsets are read after the wait.
+    // last items leave idle.  The chunk offsets are read after the wait.
     griddep_launch();
     griddep_wait();
-    if (it >= base[n_seqs]) return;
-    int lo = 0, hi = n_seqs - 1;          // the sequence: last s with base[s] <= it
-    while (lo < hi) {
-        const int mid = (lo + hi + 1) >> 1;
-        if (base[mid] <= it) lo = mid; else hi = mid - 1;
-    }
-    const int64_t c0 = cu[lo] + (int64_t)(it - base[lo]) * C;
-    const int n = (int)min((int64_t)C, (int64_t)cu[lo + 1] - c0);
-    const int hq = h / grp;
+    const int n_work = base[n_seqs] * hv;     // (chunk, V head) items
+    if ((int)blockIdx.x >= n_work) return;
     uint8_t *kq = sm + P_OFF_KQ;
 
     if (warp == 0) {
@@ -188,164 +183,184 @@ prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
     tc_fence_after();
     const uint32_t tbase = B.tmem_base;
     volatile int *abort = &B.abort;
+    // persistent: CTA b takes items b, b + grid, ...; the barriers' phase
+    // flips per item, TMEM and the barriers are set up once
+    for (int wk = blockIdx.x, kk = 0; wk < n_work; wk += gridDim.x, ++kk) {
+        const uint32_t ph = kk & 1;
+        const int it = wk / hv;
+        const int h = wk - it * hv;
+        int lo = 0, hi = n_seqs - 1;          // the sequence: last s with base[s] <= it
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (base[mid] <= it) lo = mid; else hi = mid - 1;
+        }
+        const int64_t c0 = cu[lo] + (int64_t)(it - base[lo]) * C;
+        const int n = (int)min((int64_t)C, (int64_t)cu[lo + 1] - c0);
+        const int hq = h / grp;
 
-    if (warp == 0) {
-        if (lane == 0) {
-            const bool drop = *(volatile int *)&g_prep_drop_loads != 0;
-            if (!drop) {
-                mbar_arrive_expect_tx(&B.kq_full, kKQBytes);
-                for (int kb = 0; kb < 2; ++kb) {
-                    tma_load_2d(kq + kb * kKBlk, &tm_k, &B.kq_full, hq * DH + kb * 64, (int)c0);
-                    tma_load_2d(kq + kb * kKBlk + 64 * 128, &tm_q, &B.kq_full, hq * DH + kb * 64,
-                                (int)c0);
+        if (warp == 0) {
+            if (lane == 0) {
+                const bool drop = *(volatile int *)&g_prep_drop_loads != 0;
+                if (!drop) {
+                    mbar_arrive_expect_tx(&B.kq_full, kKQBytes);
+                    for (int kb = 0; kb < 2; ++kb) {
+                        tma_load_2d(kq + kb * kKBlk, &tm_k, &B.kq_full, hq * DH + kb * 64, (int)c0);
+                        tma_load_2d(kq + kb * kKBlk + 64 * 128, &tm_q, &B.kq_full,
+                                    hq * DH + kb * 64, (int)c0);
+                    }
                 }
-            }
-            uint64_t *last = nullptr;   // the last commit: TMEM is freed once it completes
-            if (mbar_wait(&B.kq_full, 0, abort)) {
-                tc_fence_after();
-                const uint32_t id128 = idesc_bf16(128, 128);
-                const uint32_t kb0 = smem_u32(kq);
-                for (int s = 0; s < 8; ++s) {
-                    const uint32_t off = (s >> 2) * kKBlk + (s & 3) * 32;
-                    mma_ss(tbase, sdesc_sw128(kb0 + off, 16, 1024), sdesc_sw128(kb0 + off, 16, 1024),
-                           id128, s > 0);
-                }
-                mma_commit(&B.g_full);
-                last = &B.g_full;
-                if (mbar_wait(&B.w_go, 0, abort)) {
-                    // MW: W'^T[a][i] = sum_j K[j][a] T2[i][j]  (A = K^T, MN-major)
+                uint64_t *last = nullptr;   // the item's last commit: TMEM is reused after it
+                if (mbar_wait(&B.kq_full, ph, abort)) {
                     tc_fence_after();
-                    const uint32_t id64amn = idesc_bf16(128, 64, true, false);
-                    const uint32_t t2 = smem_u32(sm + P_OFF_AF);
-                    for (int s = 0; s < 4; ++s)
-                        mma_ss(tbase, sdesc_sw128(kb0 + s * 16 * 128, kKBlk, 1024),
-                               sdesc_sw128(t2 + s * 32, 16, 1024), id64amn, s > 0);
-                    mma_commit(&B.w_full);
-                    last = &B.w_full;
+                    const uint32_t id128 = idesc_bf16(128, 128);
+                    const uint32_t kb0 = smem_u32(kq);
+                    for (int s = 0; s < 8; ++s) {
+                        const uint32_t off = (s >> 2) * kKBlk + (s & 3) * 32;
+                        mma_ss(tbase, sdesc_sw128(kb0 + off, 16, 1024),
+                               sdesc_sw128(kb0 + off, 16, 1024),
+                               id128, s > 0);
+                    }
+                    mma_commit(&B.g_full);
+                    last = &B.g_full;
+                    if (mbar_wait(&B.w_go, ph, abort)) {
+                        // MW: W'^T[a][i] = sum_j K[j][a] T2[i][j]  (A = K^T, MN-major)
+                        tc_fence_after();
+                        const uint32_t id64amn = idesc_bf16(128, 64, true, false);
+                        const uint32_t t2 = smem_u32(sm + P_OFF_AF);
+                        for (int s = 0; s < 4; ++s)
+                            mma_ss(tbase, sdesc_sw128(kb0 + s * 16 * 128, kKBlk, 1024),
+                                   sdesc_sw128(t2 + s * 32, 16, 1024), id64amn, s > 0);
+                        mma_commit(&B.w_full);
+                        last = &B.w_full;
+                    }
+                } else if (!drop) {
+                    int z = 0;       // never leave with the copy in flight
+                    mbar_wait(&B.kq_full, ph, &z);
                 }
-            } else if (!drop) {
-                int z = 0;       // never leave with the copy in flight
-                mbar_wait(&B.kq_full, 0, &z);
+                if (last) { int z = 0; mbar_wait(last, ph, &z); }
             }
-            if (last) { int z = 0; mbar_wait(last, 0, &z); }
-        }
-        __syncwarp();
-    } else {
-        const int t = tid - 32;                 // 0 .. 255
-        const int pw = warp - 1;                // 0 .. 7
-        const int q4 = warp & 3;                // TMEM lane quadrant
-        const int p = q4 * 32 + lane;           // G row: 0..63 K rows, 64..127 Q rows
-        const int chalf = pw >> 2;              // which 32 TMEM columns this warp reads
-        PrepScal &S = *reinterpret_cast<PrepScal *>(sm + P_OFF_SCAL);
-        float *Af = reinterpret_cast<float *>(sm + P_OFF_AF);
-        float *Tf = reinterpret_cast<float *>(sm + P_OFF_TF);
-        float *Wb = reinterpret_cast<float *>(sm + P_OFF_WB);
-        float g0 = 0.f, g1 = 0.f, b0 = 0.f, b1 = 0.f;
-        if (t < 32) {
-            if (2 * t < n) {
-                g0 = g[(c0 + 2 * t) * hv + h];
-                b0 = beta[(c0 + 2 * t) * hv + h];
+            __syncwarp();
+        } else {
+            const int t = tid - 32;                 // 0 .. 255
+            const int pw = warp - 1;                // 0 .. 7
+            const int q4 = warp & 3;                // TMEM lane quadrant
+            const int p = q4 * 32 + lane;           // G row: 0..63 K rows, 64..127 Q rows
+            const int chalf = pw >> 2;              // which 32 TMEM columns this warp reads
+            PrepScal &S = *reinterpret_cast<PrepScal *>(sm + P_OFF_SCAL);
+            float *Af = reinterpret_cast<float *>(sm + P_OFF_AF);
+            float *Tf = reinterpret_cast<float *>(sm + P_OFF_TF);
+            float *Wb = reinterpret_cast<float *>(sm + P_OFF_WB);
+            float g0 = 0.f, g1 = 0.f, b0 = 0.f, b1 = 0.f;
+            if (t < 32) {
+                if (2 * t < n) {
+                    g0 = g[(c0 + 2 * t) * hv + h];
+                    b0 = beta[(c0 + 2 * t) * hv + h];
+                }
+                if (2 * t + 1 < n) {
+                    g1 = g[(c0 + 2 * t + 1) * hv + h];
+                    b1 = beta[(c0 + 2 * t + 1) * hv + h];
+                }
             }
-            if (2 * t + 1 < n) {
-                g1 = g[(c0 + 2 * t + 1) * hv + h];
-                b1 = beta[(c0 + 2 * t + 1) * hv + h];
-            }
-        }
-        if (t < 32) {   // prefix sum of g, per-token decay alpha = exp(g)
-            float x = g0 + g1;
+            if (t < 32) {   // prefix sum of g, per-token decay alpha = exp(g)
+                float x = g0 + g1;
 #pragma unroll
-            for (int off = 1; off < 32; off <<= 1) {
-                const float y = __shfl_up_sync(0xffffffffu, x, off);
-                if (lane >= off) x += y;
+                for (int off = 1; off < 32; off <<= 1) {
+                    const float y = __shfl_up_sync(0xffffffffu, x, off);
+                    if (lane >= off) x += y;
+                }
+                S.gam[2 * t] = x - g1;
+                S.gam[2 * t + 1] = x;
+                S.beta[2 * t] = b0;
+                S.beta[2 * t + 1] = b1;
+                S.alpha[2 * t] = __expf(g0);
+                S.alpha[2 * t + 1] = __expf(g1);
             }
-            S.gam[2 * t] = x - g1;
-            S.gam[2 * t + 1] = x;
-            S.beta[2 * t] = b0;
-            S.beta[2 * t + 1] = b1;
-            S.alpha[2 * t] = __expf(g0);
-            S.alpha[2 * t + 1] = __expf(g1);
-        }
-        mbar_wait(&B.g_full, 0, abort);
-        tc_fence_after();
-        uint32_t gr[32];
-        tmem_ld32(tmem_addr(tbase, q4 * 32, 32 * chalf), gr);
-        {   // inverse L2 norms from the diagonal of G: row p's own column, p for
-            // a K row, 64 + (p - 64) for a Q row (q . q); p % 32 is the lane
-            // (both conditions are warp-uniform)
-            float dg = 0.f;
-            bool own = p < C && (p >> 5) == chalf;
-            if (own) {
+            mbar_wait(&B.g_full, ph, abort);
+            tc_fence_after();
+            uint32_t gr[32];
+            tmem_ld32(tmem_addr(tbase, q4 * 32, 32 * chalf), gr);
+            {   // inverse L2 norms from the diagonal of G: row p's own column, p for
+                // a K row, 64 + (p - 64) for a Q row (q . q); p % 32 is the lane
+                // (both conditions are warp-uniform)
+                float dg = 0.f;
+                bool own = p < C && (p >> 5) == chalf;
+                if (own) {
 #pragma unroll
-                for (int jj = 0; jj < 32; ++jj) dg = jj == lane ? __uint_as_float(gr[jj]) : dg;
-            }
-            if (p >= C && ((p - C) >> 5) == chalf) {
-                uint32_t gq[32];
-                tmem_ld32(tmem_addr(tbase, q4 * 32, C + 32 * chalf), gq);
+                    for (int jj = 0; jj < 32; ++jj) dg = jj == lane ? __uint_as_float(gr[jj]) : dg;
+                }
+                if (p >= C && ((p - C) >> 5) == chalf) {
+                    uint32_t gq[32];
+                    tmem_ld32(tmem_addr(tbase, q4 * 32, C + 32 * chalf), gq);
 #pragma unroll
-                for (int jj = 0; jj < 32; ++jj) dg = jj == lane ? __uint_as_float(gq[jj]) : dg;
-                own = true;
+                    for (int jj = 0; jj < 32; ++jj) dg = jj == lane ? __uint_as_float(gq[jj]) : dg;
+                    own = true;
+                }
+                if (own) {
+                    const float r = l2norm ? rsqrtf(dg + kEps) : 1.f;
+                    if (p < C) S.rk[p] = r; else S.rq[p - C] = r;
+                }
             }
-            if (own) {
-                const float r = l2norm ? rsqrtf(dg + kEps) : 1.f;
-                if (p < C) S.rk[p] = r; else S.rq[p - C] = r;
+            named_sync(1, kPrepThreads);
+            float ksv = 0.f, sqv = 0.f, gl = 0.f;
+            if (t < C) {
+                gl = S.gam[C - 1];                  // padded rows carry g = 0
+                const float x = S.gam[t];
+                const bool ok = t < n;
+                const float ex = __expf(x);
+                S.xs[t] = ok ? ex * S.rk[t] : 0.f;
+                ksv = ok ? __expf(gl - x) * S.rk[t] : 0.f;
+                sqv = ok ? scale * ex * S.rq[t] : 0.f;
+            }
+            // the Q rows are dead: P goes to k-block 0's
+            g_to_a_p(gr, p, chalf, n, S.beta, S.gam, S.alpha, S.rk, S.rq, scale, Af, sm + P_OFF_P);
+            named_sync(1, kPrepThreads);
+            // T1 over k-block 1's Q rows, T2 over Af's dead rows
+            ut_solve_mma<true>(Af, Tf, Wb, t, pw, lane, S.beta, S.xs, sm + P_OFF_T1);
+            fence_async_smem();
+            tc_fence_before();
+            mbar_arrive(&B.w_go);                  // T2 is in place: MW may run
+            // the solve scratch is dead: the row factors go to Wb, W'^T to Af
+            ItemScal &I = *reinterpret_cast<ItemScal *>(Wb);
+            if (t < C) {
+                I.ks[t] = ksv;
+                I.sq[t] = sqv;
+                if (t == 0) {
+                    I.gam_n = __expf(gl);
+                    I.n = n;
+                }
+            }
+            mbar_wait(&B.w_full, ph, abort);
+            tc_fence_after();
+            {
+                uint32_t wr[32];
+                tmem_ld32(tmem_addr(tbase, q4 * 32, 32 * chalf), wr);
+                uint8_t *wt = sm + P_OFF_AF;
+#pragma unroll
+                for (int cc = 0; cc < 4; ++cc) {
+                    uint32_t w[4];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e)
+                        w[e] = pack_bf16(__uint_as_float(wr[8 * cc + 2 * e]),
+                                         __uint_as_float(wr[8 * cc + 2 * e + 1]));
+                    *reinterpret_cast<uint4 *>(wt + sw128_chunk((uint32_t)p, 4 * chalf + cc)) =
+                        make_uint4(w[0], w[1], w[2], w[3]);
+                }
+            }
+            fence_async_smem();
+            named_sync(1, kPrepThreads);
+            if (t == 0 && !*abort) {
+                uint8_t *item = items + ((size_t)it * hv + h) * kItemBytes;
+                bulk_store(item + kItemT1, sm + P_OFF_T1, kMatBytes);
+                bulk_store(item + kItemP, sm + P_OFF_P, kMatBytes);
+                bulk_store(item + kItemW, sm + P_OFF_AF, kItemWBytes);
+                bulk_store(item + kItemOps, Wb, kItemScalCopy);
+                bulk_commit();
+                bulk_wait_read_all();   // the staging may go; the writes complete on their own
             }
         }
-        named_sync(1, kPrepThreads);
-        float ksv = 0.f, sqv = 0.f, gl = 0.f;
-        if (t < C) {
-            gl = S.gam[C - 1];                  // padded rows carry g = 0
-            const float x = S.gam[t];
-            const bool ok = t < n;
-            const float ex = __expf(x);
-            S.xs[t] = ok ? ex * S.rk[t] : 0.f;
-            ksv = ok ? __expf(gl - x) * S.rk[t] : 0.f;
-            sqv = ok ? scale * ex * S.rq[t] : 0.f;
-        }
-        // the Q rows are dead: P goes to k-block 0's
-        g_to_a_p(gr, p, chalf, n, S.beta, S.gam, S.alpha, S.rk, S.rq, scale, Af, sm + P_OFF_P);
-        named_sync(1, kPrepThreads);
-        // T1 over k-block 1's Q rows, T2 over Af's dead rows
-        ut_solve_mma<true>(Af, Tf, Wb, t, pw, lane, S.beta, S.xs, sm + P_OFF_T1);
-        fence_async_smem();
         tc_fence_before();
-        mbar_arrive(&B.w_go);                  // T2 is in place: MW may run
-        // the solve scratch is dead: the row factors go to Wb, W'^T to Af
-        ItemScal &I = *reinterpret_cast<ItemScal *>(Wb);
-        if (t < C) {
-            I.ks[t] = ksv;
-            I.sq[t] = sqv;
-            if (t == 0) {
-                I.gam_n = __expf(gl);
-                I.n = n;
-            }
-        }
-        mbar_wait(&B.w_full, 0, abort);
+        __syncthreads();                    // shared memory and TMEM are reused by the next item
         tc_fence_after();
-        {
-            uint32_t wr[32];
-            tmem_ld32(tmem_addr(tbase, q4 * 32, 32 * chalf), wr);
-            uint8_t *wt = sm + P_OFF_AF;
-#pragma unroll
-            for (int cc = 0; cc < 4; ++cc) {
-                uint32_t w[4];
-#pragma unroll
-                for (int e = 0; e < 4; ++e)
-                    w[e] = pack_bf16(__uint_as_float(wr[8 * cc + 2 * e]), __uint_as_float(wr[8 * cc + 2 * e + 1]));
-                *reinterpret_cast<uint4 *>(wt + sw128_chunk((uint32_t)p, 4 * chalf + cc)) =
-                    make_uint4(w[0], w[1], w[2], w[3]);
-            }
-        }
-        fence_async_smem();
-        named_sync(1, kPrepThreads);
-        if (t == 0 && !*abort) {
-            uint8_t *item = items + ((size_t)it * hv + h) * kItemBytes;
-            bulk_store(item + kItemT1, sm + P_OFF_T1, kMatBytes);
-            bulk_store(item + kItemP, sm + P_OFF_P, kMatBytes);
-            bulk_store(item + kItemW, sm + P_OFF_AF, kItemWBytes);
-            bulk_store(item + kItemOps, Wb, kItemScalCopy);
-            bulk_commit();
-            bulk_wait_read_all();       // the shared memory may go; the writes complete on their own
-        }
     }
     tc_fence_before();
     __syncthreads();
@@ -354,6 +369,10 @@ prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
         tmem_dealloc(tbase, kPrepTmemCols);
     }
     if (tid == 0 && B.abort) flag_status(GDN_DEVSTAT_TIMEOUT);
+}
+
+inline unsigned prep_grid(int64_t items) {   // the item bound caps it for tiny batches
+    return (unsigned)std::min<int64_t>(items, (int64_t)kPrepCtasPerSm * sm_count());
 }
 
 // ------------------------------------------------------------ chain kernel --
@@ -915,7 +934,7 @@ gdn_status prefill_split(const void *q, int64_t qs, const void *k, int64_t ks, c
     psp::chunk_base_kernel<<<1, 1024, 0, s>>>(cu, n_seqs, n_tokens, base);
     gdn_status st = launch_status();
     if (st != GDN_OK) return st;
-    e = launch_after(psp::prep_kernel, dim3((unsigned)items), dim3(psp::kPrepKernelThreads),
+    e = launch_after(psp::prep_kernel, dim3(psp::prep_grid(items)), dim3(psp::kPrepKernelThreads),
                      psp::P_SMEM_BYTES, s, tq, tk, g, beta, cu, (const int32_t *)base, n_seqs,
                      hv, hv / hqk, scale, l2norm, item_blocks);
     if (e != cudaSuccess) {
@@ -1023,7 +1042,7 @@ gdn_status prefill_scan(const void *q, int64_t qs, const void *k, int64_t ks, co
     if (st != GDN_OK) return st;
     psp::chunk_base_kernel<<<1, 1024, 0, s>>>(cu_all, 2, n_tokens, base);
     if ((st = launch_status()) != GDN_OK) return st;
-    e = launch_after(psp::prep_kernel, dim3((unsigned)items), dim3(psp::kPrepKernelThreads),
+    e = launch_after(psp::prep_kernel, dim3(psp::prep_grid(items)), dim3(psp::kPrepKernelThreads),
                      psp::P_SMEM_BYTES, s, tq, tk, g, beta, cu_all, (const int32_t *)base, 2, hv,
                      hv / hqk, scale, l2norm, item_blocks);
     if (e == cudaSuccess)
