@@ -289,6 +289,7 @@ def run_ours(args):
     clocks = sampler.stop()
     step_ms = [e[0].elapsed_time(e[1]) for e in evs]
     ms_step = sum(step_ms) / K
+    ms_step_median = sorted(step_ms)[K // 2]
     ms_step_max = reduce_max(ms_step, dev)
     value = whole_job(N, ms_step_max / 1e3, world)
     # the roofline unit is the whole step (both kernels, the fused step's
@@ -398,6 +399,7 @@ def run_ours(args):
                      "algorithmic_bytes": dec_bytes, "avg_launch_ms": round(dec_avg, 5),
                      "peak_source": peaks["source"]},
         "kernels_ms": {"gdn_decode_step_fused": round(dec_avg, 5)},
+        "median_ms_per_step": round(ms_step_median, 5),
         "state_gbs": round(achieved, 1),
         "step_one_kernel": one_kernel,
         "step_unfused": unfused,
@@ -699,10 +701,11 @@ def bench_decode_gated(gdn, workloads, dev, flush, steps=50):
             "gated_tokens_per_s": round(256 / (t_gated / 1e3), 1)}
 
 
-def prefill_flops_per_token(hv, dk, dv, chunk):
+def prefill_flops_per_token(hv, dk, dv, chunk, causal=False):
     """Flops of the chunked form per token, full chunk x chunk tiles:
-    hv * (6 dk dv + 2 C (3 dk + 2 dv))."""
-    return hv * (6 * dk * dv + 2 * chunk * (3 * dk + 2 * dv))
+    hv * (6 dk dv + 2 C (3 dk + 2 dv)); with causal, the C x C tiles count
+    half: hv * (6 dk dv + C (3 dk + 2 dv))."""
+    return hv * (6 * dk * dv + (1 if causal else 2) * chunk * (3 * dk + 2 * dv))
 
 
 def bench_prefill(gdn, workloads, dev, flush, peaks, steps=5):
@@ -824,7 +827,11 @@ def bench_prefill(gdn, workloads, dev, flush, peaks, steps=5):
             "prep_kernel_traffic_bytes": profile_traffic("prep_kernel", SPLIT_SOURCES),
             "chain_kernel_traffic_bytes": profile_traffic("chain_kernel", SPLIT_SOURCES),
             "prefill_frac_bf16_peak": round(tf / peaks["bf16_tflops"], 4),
-            "flops_per_token": prefill_flops_per_token(d.hv, d.dk, d.dv, w.chunk)}
+            "flops_per_token": prefill_flops_per_token(d.hv, d.dk, d.dv, w.chunk),
+            # the same at the causal-half count of the C x C tiles (4.46 MFLOP/token)
+            "prefill_tflops_causal": round(
+                prefill_flops_per_token(d.hv, d.dk, d.dv, w.chunk, causal=True) * T
+                / (pre / 1e3) / 1e12, 2)}
 
 
 def bench_long(gdn, workloads, dev, flush, peaks, steps=3, T=65536):
