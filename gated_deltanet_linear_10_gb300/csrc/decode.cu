@@ -256,6 +256,7 @@ decode_stream_kernel(const T *__restrict__ q, int64_t qs, const T *__restrict__ 
     extern __shared__ __align__(128) uint8_t smem_raw[];
     __shared__ uint64_t full[2];
     __shared__ float o_s[kStrRows];
+    griddep_launch();   // a norm kernel behind this one may be set up meanwhile
     __shared__ int abort_flag;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (threadIdx.x == 0) {

@@ -43,6 +43,7 @@ gated_rmsnorm_kernel(const T *__restrict__ o, const T *__restrict__ z, int64_t z
     constexpr int kNormRows = norm_rows<DV>();
     constexpr int EPL = DV >= 128 ? DV / 32 : 4;     // elements per lane, 4-wide vectors
     constexpr int LANES = DV / EPL;
+    griddep_wait();   // launched behind the kernel that writes o: nothing is read before it
     const int lane = threadIdx.x & 31;
     const bool on = lane < LANES;
     const int j0 = lane * EPL;
@@ -121,6 +122,7 @@ gated_rmsnorm_bulk_kernel(const T *__restrict__ o, const T *__restrict__ z, int6
     const uint32_t row_bytes = DV * sizeof(T);
     const uint32_t half = kBulkStageBytes / 2;          // o rows, then z rows
     const int n_tiles = (n_tokens + tok_per_tile - 1) / tok_per_tile;
+    griddep_wait();   // launched behind the kernel that writes o: nothing is read before it
     if (tid == 0) {
         for (int st = 0; st < kBulkStages; ++st) mbar_init(&full[st], 1);
         abort_flag = 0;
@@ -219,9 +221,10 @@ static bool launch_norm_bulk(const void *o, const void *z, int64_t zs, const flo
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     const int64_t n_tiles = (n_tokens + tok_per_tile - 1) / tok_per_tile;
     const int grid = (int)std::min<int64_t>(n_tiles, (int64_t)sms * kBulkCtasPerSm);
-    gated_rmsnorm_bulk_kernel<DV, T><<<grid, kNormWarps * 32, smem, s>>>(
-        (const T *)o, (const T *)z, zs, w, (int)n_tokens, hv, tok_per_tile, eps, (T *)y);
-    return true;
+    // programmatic launch: the grid is set up while the kernel before it ends
+    return launch_after(gated_rmsnorm_bulk_kernel<DV, T>, dim3(grid), dim3(kNormWarps * 32),
+                        (size_t)smem, s, (const T *)o, (const T *)z, zs, w, (int)n_tokens, hv,
+                        tok_per_tile, eps, (T *)y) == cudaSuccess;
 }
 
 template <int DV, typename T>
@@ -233,8 +236,8 @@ static void launch_norm(const void *o, const void *z, int64_t zs, const float *w
     const int64_t per = kNormWarps * norm_rows<DV>();
     const int64_t need = (rows + per - 1) / per;
     const unsigned blocks = (unsigned)std::min<int64_t>(need, (int64_t)sms * 8);
-    gated_rmsnorm_kernel<DV, T><<<blocks, kNormWarps * 32, 0, s>>>(
-        (const T *)o, (const T *)z, zs, w, (uint32_t)rows, (uint32_t)hv, eps, (T *)y);
+    launch_after(gated_rmsnorm_kernel<DV, T>, dim3(blocks), dim3(kNormWarps * 32), 0, s,
+                 (const T *)o, (const T *)z, zs, w, (uint32_t)rows, (uint32_t)hv, eps, (T *)y);
 }
 
 // The host-side checks of gdn_gated_rmsnorm, launching nothing.
