@@ -182,3 +182,47 @@ def test_gated_prefill_host_checks(lib):
     assert f(*bad) == 1
     bad = list(base); bad[24] = None        # no norm weight
     assert f(*bad) == 1
+
+
+def test_fused_step_host_checks(lib):
+    """The fused decode and MTP steps refuse bad shapes and pointers on the
+    host: unsupported V heads per QK head, tokens per sequence outside 1..16,
+    a row stride shorter than a row, missing buffers, a misaligned pool; an
+    empty batch launches nothing.  The decode step's workspace size is y
+    (bf16) plus g and beta (fp32), each rounded up to 256 bytes."""
+    ws = lib.gdn_decode_step_workspace_size
+    ws.argtypes = [I32, I32, I32]
+    ws.restype = ctypes.c_size_t
+    assert ws(256, 16, 32) == 256 * 8192 * 2 + 2 * 256 * 32 * 4
+    assert ws(3, 1, 2) == 3 * 512 * 2 + 2 * 256
+    assert ws(0, 16, 32) == 0
+    d = lib.gdn_decode_step_fused
+    d.argtypes = [V, I64, V, V, V, V, V, V, V, I32, I32, I32, F32, V, I64, V, V, ctypes.c_size_t,
+                  V, V]
+    A = 1 << 20
+    base = [A, 8192, A, None, A, A, A, A, A, 4, 16, 32, 1.0, A, 8, A, None, 0, A, None]
+    bad = list(base); bad[10] = 8           # 4 V heads per QK head
+    assert d(*bad) == 2
+    bad = list(base); bad[1] = 8000         # row stride < channels
+    assert d(*bad) == 1
+    bad = list(base); bad[18] = None        # no o
+    assert d(*bad) == 1
+    bad = list(base); bad[9] = 0            # empty: no launch
+    assert d(*bad) == 0
+    m = lib.gdn_mtp_step_fused
+    m.argtypes = [V, I64, V, V, V, V, V, V, V, I32, I32, I32, I32, F32, V, I64, V, V, V, V]
+    base = [A, 8192, A, None, A, A, A, A, A, 4, 4, 16, 32, 1.0, A, 8, A, A, A, None]
+    bad = list(base); bad[10] = 17          # 17 tokens per sequence
+    assert m(*bad) == 2
+    bad = list(base); bad[10] = 0
+    assert m(*bad) == 2
+    bad = list(base); bad[12] = 24          # hv not a multiple of hqk
+    assert m(*bad) == 1
+    bad = list(base); bad[17] = None        # snapshots are required
+    assert m(*bad) == 1
+    bad = list(base); bad[1] = 4096         # row stride < channels
+    assert m(*bad) == 1
+    bad = list(base); bad[4] = A + 8        # conv state pool not 16-byte aligned
+    assert m(*bad) == 1
+    bad = list(base); bad[9] = 0            # empty: no launch
+    assert m(*bad) == 0

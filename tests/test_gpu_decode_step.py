@@ -28,10 +28,16 @@ def _check_step(x, conv_w, conv_b, cpool0, a, b, A_log, dt_bias, pool0, idx, hqk
     """Run the fused step on copies of the pools and compare with the oracle."""
     cpool = cuda(cpool0)
     pool = cuda(pool0)
-    o = gdn().gdn_decode_step_fused(cuda(x), cuda(conv_w), cpool, cuda(a), cuda(b), cuda(A_log),
+    xd = cuda(x)
+    workspace = None if path == "two_kernels" else False
+    if path == "small_workspace":      # too small: the one-kernel path
+        workspace = torch.empty(256, dtype=torch.uint8, device=DEV)
+    if path == "unaligned_x":          # rows 8 bytes apart from 16: the one-kernel path
+        xd = cuda(torch.nn.functional.pad(x, (0, 4)))[:, :x.shape[1]]
+    o = gdn().gdn_decode_step_fused(xd, cuda(conv_w), cpool, cuda(a), cuda(b), cuda(A_log),
                                     cuda(dt_bias), hqk, pool, cuda(idx), scale=scale,
                                     conv_bias=None if conv_b is None else cuda(conv_b),
-                                    workspace=None if path == "two_kernels" else False)
+                                    workspace=workspace)
     torch.cuda.synchronize()
     status_clean()
     live = [int(s) for s in idx if s >= 0]
@@ -103,5 +109,24 @@ def test_fused_step_many_groups_with_padding(path):
     pool0 = torch.randn(n_slots, hv, 128, 128, generator=g) * 0.02
     idx = torch.randperm(n_slots, generator=g)[:n].to(torch.int32)
     idx[::7] = -1
+    _check_step(x, conv_w, None, cpool0, a, b, A_log, dt_bias, pool0, idx, hqk, hv,
+                128 ** -0.5, path)
+
+
+@pytest.mark.parametrize("path", ["small_workspace", "unaligned_x"])
+def test_fused_step_falls_back_to_one_kernel(path):
+    """A workspace below gdn_decode_step_workspace_size, or x rows the
+    16-byte vectors cannot take, select the one-kernel path: same results."""
+    g = torch.Generator().manual_seed(515)
+    hqk, hv, n, n_slots = 2, 4, 9, 16
+    C = 2 * hqk * 128 + hv * 128
+    x = torch.randn(n, C, generator=g).bfloat16()
+    conv_w = (torch.rand(C, 4, generator=g) - 0.5).bfloat16()
+    cpool0 = torch.randn(n_slots, 3, C, generator=g).bfloat16()
+    a = torch.randn(n, hv, generator=g).bfloat16()
+    b = torch.randn(n, hv, generator=g).bfloat16()
+    A_log, dt_bias = workloads.gating_params(g, hv, False)
+    pool0 = torch.randn(n_slots, hv, 128, 128, generator=g) * 0.02
+    idx = torch.randperm(n_slots, generator=g)[:n].to(torch.int32)
     _check_step(x, conv_w, None, cpool0, a, b, A_log, dt_bias, pool0, idx, hqk, hv,
                 128 ** -0.5, path)
