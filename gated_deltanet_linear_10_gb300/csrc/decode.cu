@@ -79,6 +79,22 @@ decode_kernel(const T *__restrict__ q, int64_t qs, const T *__restrict__ k, int6
     const int sub = lane / LPR;
 
     const int64_t slot = idx[i];
+    // the inputs need no slot id: they are staged while it is on its way
+    for (int e = threadIdx.x; e < tps * nr; e += kDecThreads) {
+        const int t = e / nr, r = e - t * nr;
+        v_s[t][r] = Io<T>::load(v + ((int64_t)i * tps + t) * vs + (int64_t)h * dv + r0 + r);
+    }
+    for (int e = threadIdx.x; e < tps * DK; e += kDecThreads) {
+        const int t = e / DK, c = e - t * DK;
+        const int64_t row = (int64_t)i * tps + t;
+        q_s[t][c] = Io<T>::load(q + row * qs + (int64_t)hq * DK + c);
+        k_s[t][c] = Io<T>::load(k + row * ks + (int64_t)hq * DK + c);
+    }
+    if (threadIdx.x < tps) {
+        const int64_t row = (int64_t)i * tps + threadIdx.x;
+        a_s[threadIdx.x] = expf(g[row * hv + h]);
+        b_s[threadIdx.x] = beta[row * hv + h];
+    }
     const bool live = slot >= 0 && slot < n_slots;
     if (slot >= n_slots && threadIdx.x == 0 && part == 0) flag_status(GDN_DEVSTAT_BAD_INDEX);
     if (!live) {
@@ -96,21 +112,6 @@ decode_kernel(const T *__restrict__ q, int64_t qs, const T *__restrict__ k, int6
         const int r = p * RPP + warp * RPW + sub;
         st[p] = r < nr ? __ldcs(reinterpret_cast<const float4 *>(src + (int64_t)r * DK + col))
                        : make_float4(0.f, 0.f, 0.f, 0.f);
-    }
-    for (int e = threadIdx.x; e < tps * nr; e += kDecThreads) {
-        const int t = e / nr, r = e - t * nr;
-        v_s[t][r] = Io<T>::load(v + ((int64_t)i * tps + t) * vs + (int64_t)h * dv + r0 + r);
-    }
-    for (int e = threadIdx.x; e < tps * DK; e += kDecThreads) {
-        const int t = e / DK, c = e - t * DK;
-        const int64_t row = (int64_t)i * tps + t;
-        q_s[t][c] = Io<T>::load(q + row * qs + (int64_t)hq * DK + c);
-        k_s[t][c] = Io<T>::load(k + row * ks + (int64_t)hq * DK + c);
-    }
-    if (threadIdx.x < tps) {
-        const int64_t row = (int64_t)i * tps + threadIdx.x;
-        a_s[threadIdx.x] = expf(g[row * hv + h]);
-        b_s[threadIdx.x] = beta[row * hv + h];
     }
     __syncthreads();
 
