@@ -455,10 +455,24 @@ conv_update_kernel(const T *__restrict__ x, int tps, int C, const T *__restrict_
                    const int32_t *__restrict__ idx, const int32_t *__restrict__ snap, int silu,
                    T *__restrict__ y) {
     constexpr int V = Vec16<T>::N;
+    constexpr int kAhead = 4;   // tokens whose x rows and snapshot slots are loaded up front
     const int i = blockIdx.x;
     const int c0 = (blockIdx.y * blockDim.x + threadIdx.x) * V;
     if (c0 >= C) return;
     const int64_t slot = idx[i];
+    // what needs no slot id is requested while the slot id is on its way
+    uint4 xr[kAhead];
+    int64_t sn[kAhead];
+#pragma unroll
+    for (int t = 0; t < kAhead; ++t) {
+        if (t < tps) {
+            const int64_t row = (int64_t)i * tps + t;
+            xr[t] = *reinterpret_cast<const uint4 *>(x + row * C + c0);
+            sn[t] = snap ? (int64_t)snap[row] : -1;
+        }
+    }
+    ConvTaps<T, W> taps;
+    taps.load(weight, bias, c0);
     if (slot < 0 || slot >= n_slots) {
         if (slot >= n_slots) flag_status(GDN_DEVSTAT_BAD_INDEX);
         float z[V];
@@ -467,8 +481,6 @@ conv_update_kernel(const T *__restrict__ x, int tps, int C, const T *__restrict_
         for (int t = 0; t < tps; ++t) Vec16<T>::store(y + ((int64_t)i * tps + t) * C + c0, z);
         return;
     }
-    ConvTaps<T, W> taps;
-    taps.load(weight, bias, c0);
     float win[W - 1][V];
 #pragma unroll
     for (int r = 0; r < W - 1; ++r)
@@ -476,12 +488,25 @@ conv_update_kernel(const T *__restrict__ x, int tps, int C, const T *__restrict_
     for (int t = 0; t < tps; ++t) {
         const int64_t row = (int64_t)i * tps + t;
         float cur[V], out[V];
-        Vec16<T>::load(x + row * C + c0, cur);
+        if (t < kAhead) {
+#pragma unroll
+            for (int u = 0; u < kAhead; ++u)
+                if (u == t) Vec16<T>::unpack(xr[u], cur);
+        } else {
+            Vec16<T>::load(x + row * C + c0, cur);
+        }
         taps.apply(win, cur, silu, out);
         Vec16<T>::store(y + row * C + c0, out);
         shift_in<W, V>(win, cur);
         if (snap) {
-            const int64_t d = snap[row];
+            int64_t d = 0;
+            if (t < kAhead) {
+#pragma unroll
+                for (int u = 0; u < kAhead; ++u)
+                    if (u == t) d = sn[u];
+            } else {
+                d = snap[row];
+            }
             if (d >= n_slots) flag_status(GDN_DEVSTAT_BAD_INDEX);
             else if (d >= 0)
 #pragma unroll
