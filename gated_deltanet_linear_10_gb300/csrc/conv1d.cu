@@ -572,18 +572,20 @@ static void launch_fwd(const void *x, int64_t xs, const void *w, const void *b, 
     }
 }
 
-// One bf16 token per sequence, no snapshots (the decode step): one thread
-// per 8 channels of one sequence, with the taps kept as the raw 16-byte
-// vectors they load as and widened where they are used.  Few registers, so
-// many warps in flight: the kernel is latency-bound (a slot id, then the
-// slot's conv state).
+// bf16, up to kUpd1MaxTps tokens per sequence (the decode step, the MTP
+// step): one thread per 8 channels of one sequence, with the taps kept as
+// the raw 16-byte vectors they load as and widened where they are used.  Few
+// registers, so many warps in flight: the kernel is latency-bound (a slot id,
+// then the slot's conv state).  Same arithmetic order as conv_update_kernel.
 constexpr int kUpd1Threads = 256;
-template <int W>
+constexpr int kUpd1MaxTps = 4;
+template <int W, int kMaxT>   // kMaxT: 1 for the decode step (fewer registers), else 4
 __global__ void __launch_bounds__(kUpd1Threads)
-conv_update1_kernel(const __nv_bfloat16 *__restrict__ x, int n_seqs, int C,
+conv_update1_kernel(const __nv_bfloat16 *__restrict__ x, int n_seqs, int tps, int C,
                     const __nv_bfloat16 *__restrict__ weight, const __nv_bfloat16 *__restrict__ bias,
                     __nv_bfloat16 *__restrict__ pool, int64_t n_slots,
-                    const int32_t *__restrict__ idx, int silu, __nv_bfloat16 *__restrict__ y) {
+                    const int32_t *__restrict__ idx, const int32_t *__restrict__ snap, int silu,
+                    __nv_bfloat16 *__restrict__ y) {
     const int per_seq = C / 8;
     const int64_t gt = (int64_t)blockIdx.x * kUpd1Threads + threadIdx.x;
     const int i = (int)(gt / per_seq);
@@ -591,46 +593,75 @@ conv_update1_kernel(const __nv_bfloat16 *__restrict__ x, int n_seqs, int C,
     const int c0 = (int)(gt - (int64_t)i * per_seq) * 8;
     const int64_t slot = idx[i];
     // everything but the conv state is requested before the slot id is back
-    const uint4 xv = *reinterpret_cast<const uint4 *>(x + (int64_t)i * C + c0);
+    uint4 xv[kMaxT];
+    int64_t sn[kMaxT];
+#pragma unroll
+    for (int t = 0; t < kMaxT; ++t) {
+        if (t < tps) {
+            const int64_t row = (int64_t)i * tps + t;
+            xv[t] = *reinterpret_cast<const uint4 *>(x + row * C + c0);
+            sn[t] = snap ? (int64_t)snap[row] : -1;
+        }
+    }
     uint4 wv[W];                                   // taps of the 8 channels: 8 W bf16
     const uint4 *wsrc = reinterpret_cast<const uint4 *>(weight + (int64_t)c0 * W);
 #pragma unroll
     for (int u = 0; u < W; ++u) wv[u] = __ldg(wsrc + u);
     const uint4 bv = bias ? __ldg(reinterpret_cast<const uint4 *>(bias + c0)) : make_uint4(0u, 0u, 0u, 0u);
-    __nv_bfloat16 *yr = y + (int64_t)i * C + c0;
     if (slot < 0 || slot >= n_slots) {
         if (slot >= n_slots && c0 == 0) flag_status(GDN_DEVSTAT_BAD_INDEX);
-        *reinterpret_cast<uint4 *>(yr) = make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+        for (int t = 0; t < kMaxT; ++t)
+            if (t < tps)
+                *reinterpret_cast<uint4 *>(y + ((int64_t)i * tps + t) * C + c0) =
+                    make_uint4(0u, 0u, 0u, 0u);
         return;
     }
     __nv_bfloat16 *cs = pool + slot * (W - 1) * C + c0;
-    uint4 hv[W];                                   // W - 1 history rows, then x
+    uint4 hv[W];                                   // the window: W - 1 earlier inputs, then x_t
 #pragma unroll
     for (int r = 0; r < W - 1; ++r) hv[r] = *reinterpret_cast<const uint4 *>(cs + (int64_t)r * C);
-    hv[W - 1] = xv;
     auto elem = [](const uint4 *v, int e) {        // bf16 element e of a vector array
         const uint32_t w = reinterpret_cast<const uint32_t *>(v)[e >> 1];
         return __uint_as_float((e & 1) ? (w & 0xffff0000u) : (w << 16));
     };
-    uint32_t out[4];
 #pragma unroll
-    for (int p = 0; p < 4; ++p) {
-        float r2[2];
+    for (int t = 0; t < kMaxT; ++t) {
+        if (t >= tps) break;
+        hv[W - 1] = xv[t];
+        uint32_t out[4];
 #pragma unroll
-        for (int u = 0; u < 2; ++u) {
-            const int v = 2 * p + u;
-            float acc = elem(&bv, v);
+        for (int p = 0; p < 4; ++p) {
+            float r2[2];
 #pragma unroll
-            for (int j = 0; j < W; ++j) acc = fmaf(elem(wv, v * W + j), elem(&hv[j], v), acc);
-            r2[u] = silu ? silu_bf16out(acc) : acc;
+            for (int u = 0; u < 2; ++u) {
+                const int v = 2 * p + u;
+                float acc = elem(&bv, v);
+#pragma unroll
+                for (int j = 0; j < W; ++j) acc = fmaf(elem(wv, v * W + j), elem(&hv[j], v), acc);
+                r2[u] = silu ? silu_bf16out(acc) : acc;
+            }
+            __nv_bfloat162 h2 = __floats2bfloat162_rn(r2[0], r2[1]);
+            out[p] = *reinterpret_cast<uint32_t *>(&h2);
         }
-        __nv_bfloat162 h2 = __floats2bfloat162_rn(r2[0], r2[1]);
-        out[p] = *reinterpret_cast<uint32_t *>(&h2);
-    }
-    *reinterpret_cast<uint4 *>(yr) = make_uint4(out[0], out[1], out[2], out[3]);
-    // the state shifts by one input: the raw bf16 values move as they are
+        *reinterpret_cast<uint4 *>(y + ((int64_t)i * tps + t) * C + c0) =
+            make_uint4(out[0], out[1], out[2], out[3]);
+        // the window shifts by one input: the raw bf16 values move as they are
 #pragma unroll
-    for (int r = 0; r < W - 1; ++r) *reinterpret_cast<uint4 *>(cs + (int64_t)r * C) = hv[r + 1];
+        for (int r = 0; r < W - 1; ++r) hv[r] = hv[r + 1];
+        if (snap) {   // the state after token t (the last W - 1 inputs) to slot sn[t]
+            if (sn[t] >= n_slots) {
+                flag_status(GDN_DEVSTAT_BAD_INDEX);
+            } else if (sn[t] >= 0) {
+                __nv_bfloat16 *ds = pool + sn[t] * (W - 1) * C + c0;
+#pragma unroll
+                for (int r = 0; r < W - 1; ++r) *reinterpret_cast<uint4 *>(ds + (int64_t)r * C) = hv[r];
+            }
+        }
+    }
+    if (!snap)
+#pragma unroll
+        for (int r = 0; r < W - 1; ++r) *reinterpret_cast<uint4 *>(cs + (int64_t)r * C) = hv[r];
 }
 
 template <typename T, int W>
@@ -638,13 +669,19 @@ static void launch_update(const void *x, int n_seqs, int tps, int C, const void 
                           void *pool, int64_t n_slots, const int32_t *idx, const int32_t *snap,
                           int silu, void *y, cudaStream_t s) {
     if constexpr (std::is_same<T, __nv_bfloat16>::value) {
-        if (tps == 1 && !snap) {
+        if (tps <= kUpd1MaxTps) {
             const int64_t threads = (int64_t)n_seqs * (C / 8);
-            conv_update1_kernel<W><<<(unsigned)((threads + kUpd1Threads - 1) / kUpd1Threads),
-                                     kUpd1Threads, 0, s>>>(
-                (const __nv_bfloat16 *)x, n_seqs, C, (const __nv_bfloat16 *)w,
-                (const __nv_bfloat16 *)b, (__nv_bfloat16 *)pool, n_slots, idx, silu,
-                (__nv_bfloat16 *)y);
+            const unsigned grid = (unsigned)((threads + kUpd1Threads - 1) / kUpd1Threads);
+            if (tps == 1)
+                conv_update1_kernel<W, 1><<<grid, kUpd1Threads, 0, s>>>(
+                    (const __nv_bfloat16 *)x, n_seqs, tps, C, (const __nv_bfloat16 *)w,
+                    (const __nv_bfloat16 *)b, (__nv_bfloat16 *)pool, n_slots, idx, snap, silu,
+                    (__nv_bfloat16 *)y);
+            else
+                conv_update1_kernel<W, kUpd1MaxTps><<<grid, kUpd1Threads, 0, s>>>(
+                    (const __nv_bfloat16 *)x, n_seqs, tps, C, (const __nv_bfloat16 *)w,
+                    (const __nv_bfloat16 *)b, (__nv_bfloat16 *)pool, n_slots, idx, snap, silu,
+                    (__nv_bfloat16 *)y);
             return;
         }
     }
