@@ -80,32 +80,22 @@ __device__ __forceinline__ void stage_rows(__nv_bfloat16 (*dst)[kCh], const __nv
 }
 
 // Channel c over the tokens: out[t] = SiLU(conv) from the staged history and
-// inputs; with `writer`, the conv state after token t (the last 3 raw inputs,
-// oldest first) goes to slot sn[t] of the conv pool.
+// inputs.
 __device__ __forceinline__ void conv_channel(const __nv_bfloat16 (*hist)[kCh],
                                              const __nv_bfloat16 (*xin)[kCh], int c, uint2 wv,
-                                             float bias, int tps, const int64_t *sn, bool writer,
-                                             __nv_bfloat16 *__restrict__ cpool, int C, int ch,
-                                             float *out, int out_stride) {
+                                             float bias, int tps, float *out, int out_stride) {
     float h0 = __bfloat162float(hist[0][c]);
     float h1 = __bfloat162float(hist[1][c]);
     float h2 = __bfloat162float(hist[2][c]);
     const float2 w01 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&wv.x));
     const float2 w23 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&wv.y));
     for (int t = 0; t < tps; ++t) {
-        const __nv_bfloat16 xb = xin[t][c];
-        const float xt = __bfloat162float(xb);
+        const float xt = __bfloat162float(xin[t][c]);
         float acc = fmaf(w01.x, h0, bias);
         acc = fmaf(w01.y, h1, acc);
         acc = fmaf(w23.x, h2, acc);
         acc = fmaf(w23.y, xt, acc);
         out[t * out_stride] = silu_bf16out(acc);
-        if (writer && sn[t] >= 0) {
-            __nv_bfloat16 *d = cpool + sn[t] * (kW - 1) * C + ch;   // raw inputs t-2, t-1, t
-            d[0] = __float2bfloat16_rn(h1);
-            d[C] = __float2bfloat16_rn(h2);
-            d[2 * C] = xb;
-        }
         h0 = h1;
         h1 = h2;
         h2 = xt;
@@ -191,15 +181,30 @@ mtp_step_kernel(const __nv_bfloat16 *__restrict__ x, int64_t xs, bool x_vec,
     cp_async_wait_all();
     __syncthreads();
 
-    // conv + SiLU of the CTA's channels.  The q|k conv snapshots of QK head hq
-    // are split over the 2 grp CTAs that share it; each CTA writes those of its
-    // own v channels.
-    const int j = (h - hq * grp) * 2 + part;
-    conv_channel(h_s, x_s, tid, wq, bq, tps, sn_s, (tid * 2 * grp) / 256 == j, cpool, C, chq,
-                 tid < 128 ? &q_s[0][tid] : &k_s[0][tid - 128], 128);
-    if (tid < kRows)
-        conv_channel(h_s, x_s, 256 + tid, wv, bv, tps, sn_s, true, cpool, C, chv, &v_s[0][tid],
-                     kRows);
+    // The conv state after token t is window rows t + 1 .. t + 3 of
+    // [history rows 0..2, x rows 0..tps-1], all staged: each snapshot row is a
+    // copy of a staged row, 16 bytes at a time.  The q|k vectors of QK head hq
+    // are split over the 2 grp CTAs that share it; each CTA writes those of
+    // its own v channels.
+    {
+        const int j = (h - hq * grp) * 2 + part;
+        const int n_units = tps * (kW - 1) * kPieces;
+        for (int e = tid; e < n_units; e += kThreads) {
+            const int t = e / ((kW - 1) * kPieces);
+            const int rem = e - t * ((kW - 1) * kPieces);
+            const int r = rem / kPieces, u = rem - r * kPieces;   // row, 16-byte piece
+            const int64_t d = sn_s[t];
+            if (d < 0 || (u < 32 && (u * 2 * grp) / 32 != j)) continue;
+            const int w = t + 1 + r;                              // window row
+            const uint4 val = w < kW - 1 ? *reinterpret_cast<const uint4 *>(&h_s[w][u * 8])
+                                         : *reinterpret_cast<const uint4 *>(&x_s[w - (kW - 1)][u * 8]);
+            *reinterpret_cast<uint4 *>(cpool + (d * (kW - 1) + r) * C +
+                                       stream_ch(u * 8, hq, nq, h, r0)) = val;
+        }
+    }
+    // conv + SiLU of the CTA's channels
+    conv_channel(h_s, x_s, tid, wq, bq, tps, tid < 128 ? &q_s[0][tid] : &k_s[0][tid - 128], 128);
+    if (tid < kRows) conv_channel(h_s, x_s, 256 + tid, wv, bv, tps, &v_s[0][tid], kRows);
     __syncthreads();
 
     for (int t = 0; t < tps; ++t) {
