@@ -41,6 +41,7 @@ gdn_status launch_status() {
 __global__ void snapshot_kernel(uint4 *__restrict__ pool, int64_t n_slots,
                                 int64_t slot_vecs, const int32_t *__restrict__ src,
                                 const int32_t *__restrict__ dst) {
+    griddep_wait();   // launched behind the kernel that writes the slots: nothing is read before it
     const int i = blockIdx.y;
     const int s = src[i], d = dst[i];
     if (s < 0 || d < 0) return;
@@ -120,9 +121,14 @@ gdn_status gdn_state_snapshot(void *pool, int64_t n_slots, int64_t slot_bytes,
     if (bx > 1024) bx = 1024;
     if (bx < 1) bx = 1;
     dim3 grid((unsigned)bx, (unsigned)n);
-    snapshot_kernel<<<grid, threads, 0, (cudaStream_t)stream>>>(
-        (uint4 *)pool, n_slots, vecs, src, dst);
-    return launch_status();
+    // programmatic launch: the grid is set up while the kernel before it ends
+    const cudaError_t e = launch_after(snapshot_kernel, grid, dim3(threads), 0,
+                                       (cudaStream_t)stream, (uint4 *)pool, n_slots, vecs, src, dst);
+    if (e != cudaSuccess) {
+        set_last_cuda_error(e);
+        return GDN_ERR_LAUNCH;
+    }
+    return GDN_OK;
 }
 
 }  // extern "C"

@@ -119,6 +119,7 @@ mtp_step_kernel(const __nv_bfloat16 *__restrict__ x, int64_t xs, bool x_vec,
     __shared__ float a_s[kMaxTps], b_s[kMaxTps];
     __shared__ int64_t sn_s[kMaxTps];
 
+    griddep_launch();   // an accept copy behind this kernel may be set up meanwhile
     const int part = blockIdx.x & 1;
     const int ih = blockIdx.x >> 1;
     const int i = ih / hv;
