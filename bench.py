@@ -600,8 +600,9 @@ def bench_mtp(gdn, workloads, dev, flush, steps=50):
 def bench_mixed(gdn, workloads, dev, flush, steps=20):
     """A serving step's mixed batch (256 decode rows + two 2048-token prompts)
     through gdn_mixed_batch (decode rows on the streaming decode kernel, in
-    place; prompts on the chunked prefill) and, for comparison, the same
-    batch through one gdn_prefill_chunked call."""
+    place, beside the prompts' chunked prefill), the same call with the two
+    halves one after the other, and the same batch through one
+    gdn_prefill_chunked call."""
     w = workloads.mixed(pool_device=dev)
     d = w.dims
     q, k, v, a, b = (t.to(dev) for t in (w.q, w.k, w.v, w.a, w.b))
@@ -614,20 +615,27 @@ def bench_mixed(gdn, workloads, dev, flush, steps=20):
     init = torch.where(w.has_initial_state.to(dev).bool(), slots, torch.full_like(slots, -1))
     T = q.shape[0]
     o = torch.empty((T, d.hv, d.dv), dtype=q.dtype, device=dev)
-    ws_mixed = torch.empty(gdn.gdn_prefill_workspace_size(w.n_seqs - nd, T, d.hv, d.dk, d.dv, 64),
-                           dtype=torch.uint8, device=dev)
+    need = gdn.gdn_prefill_workspace_size(w.n_seqs - nd, T, d.hv, d.dk, d.dv, 64)
+    # + 512 bytes: the decode runs beside the prefill's chains; without them
+    # the two halves run one after the other
+    ws_mixed = torch.empty(need + 512, dtype=torch.uint8, device=dev)
+    ws_serial = torch.empty(need, dtype=torch.uint8, device=dev)
     ws_all = torch.empty(gdn.gdn_prefill_workspace_size(w.n_seqs, T, d.hv, d.dk, d.dv, 64),
                          dtype=torch.uint8, device=dev)
     def mixed():
         gdn.gdn_mixed_batch(q, k, v, g, beta, cu, nd, w.state_pool, init, slots, w.scale,
                             decode_in_place=True, o=o, workspace=ws_mixed)
 
+    def serial():
+        gdn.gdn_mixed_batch(q, k, v, g, beta, cu, nd, w.state_pool, init, slots, w.scale,
+                            decode_in_place=True, o=o, workspace=ws_serial)
+
     def one_call():
         gdn.gdn_prefill_chunked(q, k, v, g, beta, cu, w.state_pool, init, slots, w.scale, o=o,
                                 workspace=ws_all)
 
     res = {}
-    for name, fn in (("mixed_batch", mixed), ("prefill_call", one_call)):
+    for name, fn in (("mixed_batch", mixed), ("serial", serial), ("prefill_call", one_call)):
         for _ in range(3):
             fn()
             flush.zero_()
@@ -646,8 +654,10 @@ def bench_mixed(gdn, workloads, dev, flush, steps=20):
                         "head_dim 128, bf16",
             "tokens_per_s": round(T / (res["mixed_batch"] / 1e3), 1),
             "mixed_batch_ms": round(res["mixed_batch"], 4),
+            "path": "prefill, then the streaming decode beside its chains (work counter)",
+            "halves_one_after_the_other_ms": round(res["serial"], 4),
             "prefill_call_ms": round(res["prefill_call"], 4),
-            "gpu_launches_per_step": 4}
+            "gpu_launches_per_step": 5}
 
 
 def bench_decode_gated(gdn, workloads, dev, flush, steps=50):

@@ -351,7 +351,8 @@ def gdn_mixed_batch(q, k, v, g, beta, cu_seqlens, n_decode, state_pool, initial_
         workspace = None
     elif workspace is None:
         need = gdn_prefill_workspace_size(n - n_decode, T, hv, dk, dv, chunk, dt) if n > n_decode else 0
-        workspace = torch.empty(need, dtype=torch.uint8, device=q.device) if need else None
+        # + 512 bytes: room for the work counter of the decode beside the prefill
+        workspace = torch.empty(need + 512, dtype=torch.uint8, device=q.device) if need else None
     else:
         _cuda(workspace)
     wbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()

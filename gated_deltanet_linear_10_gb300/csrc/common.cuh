@@ -31,6 +31,15 @@ cudaError_t launch_decode_stream_after(const __nv_bfloat16 *q, int64_t qs,
                                        const float *beta, int n_seqs, int hqk, int hv,
                                        float scale, float *pool, int64_t n_slots,
                                        const int32_t *idx, __nv_bfloat16 *o, cudaStream_t s);
+// decode.cu: the streaming decode with counter-assigned items, launched to run
+// beside the kernel before it (the mixed batch's chain kernel)
+cudaError_t launch_decode_stream_beside(const __nv_bfloat16 *q, int64_t qs,
+                                        const __nv_bfloat16 *k, int64_t ks,
+                                        const __nv_bfloat16 *v, int64_t vs, const float *g,
+                                        const float *beta, int n_seqs, int hqk, int hv,
+                                        float scale, int l2norm, float *pool, int64_t n_slots,
+                                        const int32_t *idx, __nv_bfloat16 *o, int *ctr,
+                                        cudaStream_t s);
 int sm_count();              // multiprocessors of the current device
 
 // Per-TU readers of the status word (defined next to each word).

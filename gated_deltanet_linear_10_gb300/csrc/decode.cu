@@ -247,13 +247,18 @@ struct StrIn {            // one item's inputs, as this thread needs them
     float g, b;
 };
 
-template <typename T>
+// kDyn: the items are handed out by a counter (atomicAdd on *ctr, zero at
+// launch) instead of CTA b taking b, b + grid, ...; the kernel then reads
+// nothing its primary grid writes and waits for that grid only at its end.
+// Used when the decode runs beside the chain kernel of a mixed batch, on the
+// SMs the chains leave free.
+template <typename T, bool kDyn = false>
 __global__ void __launch_bounds__(kDecThreads, kStrCtasPerSm)
 decode_stream_kernel(const T *__restrict__ q, int64_t qs, const T *__restrict__ k, int64_t ks,
                      const T *__restrict__ v, int64_t vs, const float *__restrict__ g,
                      const float *__restrict__ beta, int n_items, int hv, int grp, float scale,
                      int l2norm, float *__restrict__ pool, int64_t n_slots,
-                     const int32_t *__restrict__ idx, T *__restrict__ o) {
+                     const int32_t *__restrict__ idx, T *__restrict__ o, int *__restrict__ ctr) {
     extern __shared__ __align__(128) uint8_t smem_raw[];
     __shared__ uint64_t full[2];
     __shared__ float o_s[kStrRows];
@@ -290,8 +295,17 @@ decode_stream_kernel(const T *__restrict__ q, int64_t qs, const T *__restrict__ 
         in.b = beta[(int64_t)i * hv + h];
     };
     int ph[2] = {0, 0};          // loads issued into each stage (same in every thread)
+    __shared__ int w_sh[3];      // kDyn: a ring of item indices, published through barriers
 
     int w = blockIdx.x;
+    if constexpr (kDyn) {
+        if (threadIdx.x == 0) {
+            w_sh[0] = atomicAdd(ctr, 1);
+            w_sh[1] = atomicAdd(ctr, 1);
+        }
+        __syncthreads();
+        w = w_sh[0];
+    }
     StrIn<T> cur;
     if (w < n_items) {
         int i, h, part;
@@ -306,10 +320,10 @@ decode_stream_kernel(const T *__restrict__ q, int64_t qs, const T *__restrict__ 
         // launched behind the kernel that writes q, k, v, g and beta (the
         // fused decode step's front kernel): the first state is on its way,
         // the inputs are read only once that kernel has finished
-        griddep_wait();
+        if constexpr (!kDyn) griddep_wait();
         load_in(i, h, part, cur);
     }
-    for (int n = 0; w < n_items; w += gridDim.x, ++n) {
+    for (int n = 0; w < n_items; ++n) {
         const int s = n & 1;
         int i, h, part;
         const int64_t slot = slot_of(w, i, h, part);
@@ -317,7 +331,11 @@ decode_stream_kernel(const T *__restrict__ q, int64_t qs, const T *__restrict__ 
         if (slot >= n_slots && threadIdx.x == 0) flag_status(GDN_DEVSTAT_BAD_INDEX);
         // prefetch the next item into the other stage (its previous store has
         // been read: the wait below), and its inputs into registers
-        const int wn = w + gridDim.x;
+        const int wn = kDyn ? w_sh[(n + 1) % 3] : w + (int)gridDim.x;
+        // kDyn: the item after it, read by every thread at the top of the
+        // next iteration; its slot was last read two iterations (or the
+        // prologue) ago, with this CTA's barriers in between
+        if (kDyn && threadIdx.x == 0) w_sh[(n + 2) % 3] = atomicAdd(ctr, 1);
         StrIn<T> nxt = cur;
         if (wn < n_items) {
             int in_, hn, pn;
@@ -371,10 +389,12 @@ decode_stream_kernel(const T *__restrict__ q, int64_t qs, const T *__restrict__ 
             Io<T>::store(o + ((int64_t)i * hv + h) * 128 + part * kStrRows + threadIdx.x, o_s[threadIdx.x]);
         __syncthreads();                 // o_s is rewritten by the next item
         cur = nxt;
+        w = wn;
     }
     if (threadIdx.x == 0) {
         bulk_wait_read_all();
         if (abort_flag) flag_status(GDN_DEVSTAT_TIMEOUT);
+        if constexpr (kDyn) griddep_wait();   // this grid completes after its primary
     }
 }
 
@@ -399,7 +419,7 @@ static cudaError_t launch_decode(const void *q, int64_t qs, const void *k, int64
         if (e != cudaSuccess) return e;
         decode_stream_kernel<T><<<grid, kDecThreads, 2 * kStrBytes, s>>>(
             (const T *)q, qs, (const T *)k, ks, (const T *)v, vs, g, beta, n_items, hv, hv / hqk,
-            scale, l2norm, pool, n_slots, idx, (T *)o);
+            scale, l2norm, pool, n_slots, idx, (T *)o, nullptr);
         return cudaGetLastError();
     }
     if (dv > 64) {     // two CTAs per state: half the registers, twice the CTAs in flight
@@ -432,7 +452,29 @@ cudaError_t launch_decode_stream_after(const __nv_bfloat16 *q, int64_t qs,
     if (e != cudaSuccess) return e;
     return launch_after(decode_stream_kernel<__nv_bfloat16>, dim3((unsigned)grid),
                         dim3(kDecThreads), 2 * kStrBytes, s, q, qs, k, ks, v, vs, g, beta,
-                        n_items, hv, hv / hqk, scale, 1, pool, n_slots, idx, o);
+                        n_items, hv, hv / hqk, scale, 1, pool, n_slots, idx, o, (int *)nullptr);
+}
+
+// The streaming decode with its items handed out by *ctr (zero before the
+// launch), launched behind the kernel before it in the stream so that it runs
+// on the SMs that kernel leaves free.  The caller guarantees that the kernel
+// before it writes none of this decode's inputs, outputs or slots.
+cudaError_t launch_decode_stream_beside(const __nv_bfloat16 *q, int64_t qs,
+                                        const __nv_bfloat16 *k, int64_t ks,
+                                        const __nv_bfloat16 *v, int64_t vs, const float *g,
+                                        const float *beta, int n_seqs, int hqk, int hv,
+                                        float scale, int l2norm, float *pool, int64_t n_slots,
+                                        const int32_t *idx, __nv_bfloat16 *o, int *ctr,
+                                        cudaStream_t s) {
+    const int n_items = (int)((int64_t)n_seqs * hv * 2);
+    const int grid = (int)std::min<int64_t>(n_items, (int64_t)sm_count() * kStrCtasPerSm);
+    cudaError_t e = cudaFuncSetAttribute(decode_stream_kernel<__nv_bfloat16, true>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)(2 * kStrBytes));
+    if (e != cudaSuccess) return e;
+    return launch_after(decode_stream_kernel<__nv_bfloat16, true>, dim3((unsigned)grid),
+                        dim3(kDecThreads), 2 * kStrBytes, s, q, qs, k, ks, v, vs, g, beta,
+                        n_items, hv, hv / hqk, scale, l2norm, pool, n_slots, idx, o, ctr);
 }
 
 }  // namespace gdn

@@ -5,9 +5,17 @@
 //
 // The first n_decode sequences are one token each, rows 0 .. n_decode-1;
 // they go to the recurrent decode kernels, which stream each state once.
-// The rest go to the chunked prefill on the same stream.  No kernel of its
-// own: the two halves are the library's decode and prefill paths, with the
-// prefill half given the tail of cu_seqlens (its token rows are absolute).
+// The rest go to the chunked prefill on the same stream, with the prefill
+// half given the tail of cu_seqlens (its token rows are absolute).
+//
+// When the decode rows take the streaming kernel in place and the workspace
+// has room for a work counter past the prefill's part, the prefill runs
+// first and the streaming decode is launched behind its chain kernel
+// (programmatic dependent launch) with its items handed out by the counter:
+// its CTAs start on the SMs the chains leave free (the chains are one per
+// (prompt, V head), often fewer than the SMs) and take over the rest as the
+// chains end.  The halves touch disjoint rows and slots, so the decode needs
+// nothing from the prefill.
 #include "common.cuh"
 
 namespace gdn {
@@ -70,13 +78,47 @@ extern "C" gdn_status gdn_mixed_batch(
             final_state_indices ? final_state_indices + n_decode : nullptr, o, dtype);
         if (st != GDN_OK) return st;
     }
-    if (n_decode > 0) {
-        if (cu_seqlens) {
-            gdn::mixed_check_kernel<<<(n_decode + 256) / 256, 256, 0, (cudaStream_t)stream>>>(
-                cu_seqlens, n_decode);
-            const gdn_status st = gdn::launch_status();
+    cudaStream_t s = (cudaStream_t)stream;
+    if (n_decode > 0 && cu_seqlens) {
+        gdn::mixed_check_kernel<<<(n_decode + 256) / 256, 256, 0, s>>>(cu_seqlens, n_decode);
+        const gdn_status st = gdn::launch_status();
+        if (st != GDN_OK) return st;
+    }
+    // the decode beside the prefill's chains: the streaming kernel's case,
+    // and a work counter past the prefill's part of the workspace
+    if (n_decode > 0 && n_seqs > n_decode && in_place && dtype == GDN_BF16 && dk == 128 &&
+        dv == 128 && ((uintptr_t)state_pool % 16) == 0 && workspace) {
+        const size_t need = gdn_prefill_workspace_size(n_seqs - n_decode, n_tokens, hv, dk, dv,
+                                                       chunk, dtype);
+        const size_t at = (need + 255) / 256 * 256;
+        if (need > 0 && workspace_bytes >= at + 256) {
+            int *ctr = reinterpret_cast<int *>(reinterpret_cast<uint8_t *>(workspace) + at);
+            cudaError_t e = cudaMemsetAsync(ctr, 0, sizeof(int), s);
+            if (e != cudaSuccess) {
+                gdn::set_last_cuda_error(e);
+                return GDN_ERR_CUDA;
+            }
+            const gdn_status st = gdn_prefill_chunked(
+                q, q_row_stride, k, k_row_stride, v, v_row_stride, g, beta,
+                cu_seqlens + n_decode, n_seqs - n_decode, n_tokens, hqk, hv, dk, dv, scale,
+                l2norm_qk, chunk, state_pool, n_slots,
+                initial_state_indices ? initial_state_indices + n_decode : nullptr,
+                final_state_indices ? final_state_indices + n_decode : nullptr, o, dtype,
+                workspace, need, stream);
             if (st != GDN_OK) return st;
+            e = gdn::launch_decode_stream_beside(
+                (const __nv_bfloat16 *)q, q_row_stride, (const __nv_bfloat16 *)k, k_row_stride,
+                (const __nv_bfloat16 *)v, v_row_stride, g, beta, n_decode, hqk, hv, scale,
+                l2norm_qk, state_pool, n_slots, initial_state_indices, (__nv_bfloat16 *)o, ctr,
+                s);
+            if (e != cudaSuccess) {
+                gdn::set_last_cuda_error(e);
+                return GDN_ERR_LAUNCH;
+            }
+            return GDN_OK;
         }
+    }
+    if (n_decode > 0) {
         const gdn_status st = gdn_decode_recurrent(
             q, q_row_stride, k, k_row_stride, v, v_row_stride, g, beta, n_decode, 1, hqk, hv, dk,
             dv, scale, l2norm_qk, state_pool, n_slots, initial_state_indices,

@@ -470,6 +470,9 @@ chain_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
                                               ~uintptr_t(1023));
     ChainBars &B = *reinterpret_cast<ChainBars *>(sm + L::BARS);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    // a kernel launched behind this one (a mixed batch's decode) may start on
+    // the SMs the chains leave free
+    griddep_launch();
 
     const int rank = blockIdx.x / hv;
     const int h = blockIdx.x - rank * hv;

@@ -437,6 +437,12 @@ gdn_status gdn_mtp_step_fused(const void *x, int64_t x_row_stride,
  *   cu_seqlens + n_decode (absolute token rows), the tail of both index
  *   arrays, and the workspace: size it with
  *   gdn_prefill_workspace_size(n_seqs - n_decode, n_tokens, ...).
+ *   With 512 bytes more (and decode rows in place, bf16, dk = dv = 128), the
+ *   decode rows run beside the prefill: the prefill goes first, and the
+ *   streaming decode is launched behind its last kernel to take the SMs its
+ *   chains leave free, with its items handed out by a counter kept in those
+ *   extra bytes.  Decode rows and prompts must then use distinct slots (as
+ *   slots within one call always must).
  * Other arguments, layouts and errors as gdn_prefill_chunked and
  * gdn_decode_recurrent (the decode rows need dk = dv <= 128 as those do).
  * Both halves' host-side checks run before either half launches, so a

@@ -52,16 +52,26 @@ def _check(o, pd, pool, o_ref, upd):
                 assert bits_equal(got[s, h], pool[s, h]), f"untouched {s},{h}"
 
 
-@pytest.mark.parametrize("in_place", [True, False], ids=["in_place", "to_other_slots"])
-def test_mixed_batch(in_place):
+@pytest.mark.parametrize("in_place,path", [(True, "beside"), (True, "serial"), (False, "serial")],
+                         ids=["in_place_beside", "in_place_serial", "to_other_slots"])
+def test_mixed_batch(in_place, path):
+    """In place with the default workspace the decode runs beside the
+    prefill's chains (a work counter past the prefill's part); with a
+    workspace of exactly the prefill's size the halves run one after the
+    other."""
     cu, q, k, v, a, b, A_log, dt_bias, pool, init, perm = _batch()
     n = len(init)
     final = perm[n:2 * n].clone()            # prompts: from their initial slot (or zero)
     final[3] = -1                            # a decode row whose state is dropped
     pd = cuda(pool)
     g, beta = gdn().gdn_gating(cuda(a), cuda(b), cuda(A_log), cuda(dt_bias))
+    ws = None
+    if path == "serial":
+        T = int(cu[-1])
+        ws = torch.empty(gdn().gdn_prefill_workspace_size(n - N_DEC, T, 4, 128, 128, 64),
+                         dtype=torch.uint8, device="cuda")
     o = gdn().gdn_mixed_batch(cuda(q), cuda(k), cuda(v), g, beta, cuda(cu), N_DEC, pd, cuda(init),
-                              cuda(final), 0.125, decode_in_place=in_place)
+                              cuda(final), 0.125, decode_in_place=in_place, workspace=ws)
     torch.cuda.synchronize()
     status_clean()
     ref_final = final.clone()
@@ -119,3 +129,33 @@ def test_mixed_batch_reports_a_broken_decode_row_layout():
     torch.cuda.synchronize()
     st = gdn().gdn_get_device_status(clear=True)
     assert st & gdn().DEVSTAT_BAD_SEQLEN, f"status {st:#x}"
+
+
+def test_mixed_batch_beside_equals_serial_full_size():
+    """The serving-step workload (256 decode rows over 16 QK / 32 V heads,
+    two 2048-token prompts): the decode beside the prefill's chains, its
+    16,384 items handed out by the counter, gives bit for bit the o and the
+    pool of the two halves run one after the other (every item processed
+    once, by the same arithmetic)."""
+    import workloads
+    w = workloads.mixed(pool_device="cuda")
+    d = w.dims
+    q, k, v, a, b = (cuda(t) for t in (w.q, w.k, w.v, w.a, w.b))
+    cu = cuda(w.cu_seqlens)
+    nd = w.extra["n_decode"]
+    g, beta = gdn().gdn_gating(a, b, cuda(w.A_log), cuda(w.dt_bias))
+    slots = cuda(w.slots)
+    init = torch.where(cuda(w.has_initial_state).bool(), slots, torch.full_like(slots, -1))
+    T = q.shape[0]
+    need = gdn().gdn_prefill_workspace_size(w.n_seqs - nd, T, d.hv, d.dk, d.dv, 64)
+    outs = []
+    for ws_bytes in (need + 512, need):
+        pool = w.state_pool.clone()
+        ws = torch.empty(ws_bytes, dtype=torch.uint8, device="cuda")
+        o = gdn().gdn_mixed_batch(q, k, v, g, beta, cu, nd, pool, init, slots, w.scale,
+                                  decode_in_place=True, workspace=ws)
+        torch.cuda.synchronize()
+        status_clean()
+        outs.append((o, pool))
+    assert bits_equal(outs[0][0], outs[1][0]), "o differs between the two paths"
+    assert bits_equal(outs[0][1], outs[1][1]), "pool differs between the two paths"
