@@ -21,6 +21,7 @@ there is) on a bounded sample of the same workload, on rank 0.
 from __future__ import annotations
 
 import argparse
+import gc
 import hashlib
 import json
 import os
@@ -278,6 +279,7 @@ def run_ours(args):
     time.sleep(0.3)
     barrier()
     torch.cuda.synchronize(dev)
+    gc.disable()                                 # no collector pause while the host enqueues
     t0 = time.perf_counter()
     torch.cuda._sleep(2_000_000)                 # head start: the host enqueues ahead of the GPU
     for i in range(K):
@@ -286,6 +288,7 @@ def run_ours(args):
     torch.cuda.synchronize(dev)
     barrier()
     wall = time.perf_counter() - t0
+    gc.enable()
     clocks = sampler.stop()
     step_ms = [e[0].elapsed_time(e[1]) for e in evs]
     ms_step = sum(step_ms) / K
