@@ -1,10 +1,12 @@
 """The C ABI calls are asynchronous on the caller's stream, with no host
 synchronisation and no allocation, so a serving loop can capture them in a
 CUDA graph: the fused decode step, the two-kernel prefill (with a caller
-workspace), the chunk-state scan and the gated prefill, and the TMA-staged
-conv forward are captured with torch.cuda.graph and replayed, and every
-output and pool must be bit-identical to an eager run on copies of the same
-inputs (the kernels are deterministic)."""
+workspace), the chunk-state scan and the gated prefill, the TMA-staged conv
+forward, the mixed batch with its decode beside the prefill, and the fused
+MTP step with its accept copies are captured with torch.cuda.graph and
+replayed (programmatic dependent launches included), and every output and
+pool must be bit-identical to an eager run on copies of the same inputs (the
+kernels are deterministic)."""
 import pytest
 import torch
 
@@ -169,3 +171,57 @@ def test_scan_and_gated_prefill_graph_replay():
     assert bits_equal(o1g, o1e)
     assert bits_equal(o2g, o2e)
     assert bits_equal(pg, pe)
+
+
+def test_mixed_batch_and_mtp_step_graph_replay():
+    """The mixed batch with the decode beside the prefill's chains (a memset
+    of the work counter, the prefill's launches, the streaming decode behind
+    the chain kernel) and the fused MTP step with its two accept copies
+    (launched behind the MTP kernel), captured and replayed: outputs and
+    pools bit-identical to eager runs."""
+    w = workloads.mixed(pool_device=DEV)
+    d = w.dims
+    q, k, v, a, b = (cuda(t) for t in (w.q, w.k, w.v, w.a, w.b))
+    cu = cuda(w.cu_seqlens)
+    nd = w.extra["n_decode"]
+    gg, beta = gdn().gdn_gating(a, b, cuda(w.A_log), cuda(w.dt_bias))
+    slots = cuda(w.slots)
+    init = torch.where(cuda(w.has_initial_state).bool(), slots, torch.full_like(slots, -1))
+    T = q.shape[0]
+    need = gdn().gdn_prefill_workspace_size(w.n_seqs - nd, T, d.hv, d.dk, d.dv, 64)
+    ws = torch.empty(need + 512, dtype=torch.uint8, device=DEV)
+
+    m = workloads.mtp(n_seqs=16, n_slots=128, pool_device=DEV)
+    mx, ma, mb = cuda(m.x), cuda(m.a), cuda(m.b)
+    mw, mA, mdt = cuda(m.conv_w), cuda(m.A_log), cuda(m.dt_bias)
+    msl, msn = cuda(m.slots), cuda(m.snap)
+    acc = cuda(m.snap[torch.arange(m.n_seqs), m.extra["accept"].long()].to(torch.int32))
+
+    def run(pool, o, cpool, spool, mo):
+        gdn().gdn_mixed_batch(q, k, v, gg, beta, cu, nd, pool, init, slots, w.scale,
+                              decode_in_place=True, o=o, workspace=ws)
+        gdn().gdn_mtp_step_fused(mx, 4, mw, cpool, ma, mb, mA, mdt, m.dims.hqk, spool, msl, msn,
+                                 scale=m.scale, o=mo)
+        gdn().gdn_state_snapshot(spool, acc, msl)
+        gdn().gdn_state_snapshot(cpool, acc, msl)
+
+    def fresh():
+        return (w.state_pool.clone(), torch.empty((T, d.hv, d.dv), dtype=q.dtype, device=DEV),
+                cuda(m.conv_pool), m.state_pool.clone(),
+                torch.empty((m.n_seqs * 4, m.dims.hv, m.dims.dv), dtype=mx.dtype, device=DEV))
+
+    eager = fresh()
+    run(*eager)
+    torch.cuda.synchronize()
+    status_clean()
+    graphed = fresh()
+    gr = _graph(lambda: run(*graphed))
+    init_state = fresh()
+    for dst, src in zip(graphed, init_state):
+        dst.copy_(src)
+    gr.replay()
+    torch.cuda.synchronize()
+    status_clean()
+    for name, x_e, x_g in zip(("mixed pool", "mixed o", "conv pool", "state pool", "mtp o"),
+                              eager, graphed):
+        assert bits_equal(x_g, x_e), name
