@@ -809,6 +809,29 @@ def bench_prefill(gdn, workloads, dev, flush, peaks, steps=5):
     torch.cuda.synchronize(dev)
     gated_ms = sum(e[0].elapsed_time(e[1]) for e in ev) / steps
 
+    # the same layer in one call: gdn_prefill_layer (conv, then the prefill
+    # with the gates formed in its prep kernel)
+    lneed = gdn.gdn_prefill_layer_workspace_size(cu.numel() - 1, T, d.hqk, d.hv)
+    lws_raw = torch.empty(lneed + 1024, dtype=torch.uint8, device=dev)
+    loff = (-lws_raw.data_ptr()) % 1024
+    lws = lws_raw[loff:loff + lneed]
+
+    def layer_call():
+        gdn.gdn_prefill_layer(x, conv_w, cpool, slots, has, a, b, A_log, dt_bias, cu, d.hqk, spool,
+                              none, sslots, scale=w.scale, o=o, workspace=lws)
+
+    for _ in range(2):
+        layer_call()
+        flush.zero_()
+    torch.cuda.synchronize(dev)
+    for i in range(steps):
+        ev[i][0].record(stream)
+        layer_call()
+        ev[i][1].record(stream)
+        flush.zero_()
+    torch.cuda.synchronize(dev)
+    layer_call_ms = sum(e[0].elapsed_time(e[1]) for e in ev) / steps
+
     for _ in range(2):
         step()
         flush.zero_()
@@ -825,8 +848,12 @@ def bench_prefill(gdn, workloads, dev, flush, peaks, steps=5):
     conv_bytes = 2 * T * d.channels * 2
     return {"workload": f"prefill: 8 sequences, {T} tokens (lengths U[512, 8192]), conv fwd + "
                         "gating + chunked prefill (chunk 64)",
-            "tokens_per_s": round(T / (total / 1e3), 1),
+            "tokens_per_s": round(T / (min(total, layer_call_ms) / 1e3), 1),
             "layer_ms": round(total, 4), "prefill_kernel_ms": round(pre, 4),
+            "layer_call_ms": round(layer_call_ms, 4),
+            "layer_path": "gdn_prefill_layer (conv, then the prefill with its gates formed in "
+                          "the prep kernel)" if layer_call_ms < total else
+                          "conv fwd + gating + prefill (three calls)",
             "prefill_path": "prep kernel + chain kernel (workspace %.1f MiB)" % (need / 2**20),
             "prefill_fused_kernel_ms": round(pre_fused, 4),
             "conv_kernel_ms": round(conv, 4),

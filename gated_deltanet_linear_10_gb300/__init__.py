@@ -31,7 +31,7 @@ EXPORTS = (
     "gdn_get_device_status", "gdn_prefill_chunked_static", "gdn_gated_rmsnorm",
     "gdn_decode_recurrent_gated", "gdn_decode_step_fused", "gdn_mixed_batch",
     "gdn_debug_set_wait_limit", "gdn_prefill_chunked_gated", "gdn_mtp_step_fused",
-    "gdn_decode_step_workspace_size",
+    "gdn_decode_step_workspace_size", "gdn_prefill_layer", "gdn_prefill_layer_workspace_size",
 )
 
 if not os.path.exists(LIB_PATH):
@@ -69,6 +69,9 @@ _SIGS = {
     "gdn_prefill_chunked_static": [_vp, _i64, _vp, _i64, _vp, _i64, _vp, _vp, _vp, _i32, _i64,
                                    _i32, _i32, _f32, _i32, _vp, _i64, _vp, _vp, _vp, _vp],
     "gdn_debug_set_wait_limit": [ctypes.c_uint64, _i32, _vp],
+    "gdn_prefill_layer": [_vp, _i64, _vp, _vp, _vp, _i64, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32,
+                          _i64, _i32, _i32, _f32, _vp, _i64, _vp, _vp, _vp, _vp,
+                          ctypes.c_size_t, _vp],
     "gdn_mtp_step_fused": [_vp, _i64, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32,
                            _f32, _vp, _i64, _vp, _vp, _vp, _vp],
     "gdn_prefill_chunked_gated": [_vp, _i64, _vp, _i64, _vp, _i64, _vp, _vp, _vp, _i32, _i64,
@@ -86,6 +89,8 @@ _lib.gdn_prefill_workspace_size.argtypes = [_i32, _i64, _i32, _i32, _i32, _i32, 
 _lib.gdn_prefill_workspace_size.restype = ctypes.c_size_t
 _lib.gdn_decode_step_workspace_size.argtypes = [_i32, _i32, _i32]
 _lib.gdn_decode_step_workspace_size.restype = ctypes.c_size_t
+_lib.gdn_prefill_layer_workspace_size.argtypes = [_i32, _i64, _i32, _i32]
+_lib.gdn_prefill_layer_workspace_size.restype = ctypes.c_size_t
 
 
 class GdnError(RuntimeError):
@@ -521,6 +526,66 @@ def gdn_decode_step_fused(x, conv_weight, conv_state_pool, a, b, A_log, dt_bias,
         _ptr(b), _ptr(A_log), _ptr(dt_bias), N, hqk, hv, float(scale), _ptr(state_pool),
         state_pool.shape[0], _ptr(state_indices), _ptr(workspace), wbytes, _ptr(o),
         _stream(x.device)), "gdn_decode_step_fused")
+    return o
+
+
+def gdn_prefill_layer_workspace_size(n_seqs, n_tokens, hqk, hv) -> int:
+    return int(_lib.gdn_prefill_layer_workspace_size(n_seqs, n_tokens, hqk, hv))
+
+
+def gdn_prefill_layer(x, conv_weight, conv_state_pool, conv_state_indices, has_initial_state, a, b,
+                      A_log, dt_bias, cu_seqlens, hqk, state_pool, initial_state_indices,
+                      final_state_indices, scale=None, conv_bias=None, o=None, workspace=None):
+    """The prefill side of the layer in one call: the causal conv + SiLU of the
+    raw q|k|v stream x [T, C] (conv states as causal_conv1d_fwd), then the
+    chunked prefill on its q, k, v with the gates formed from the raw a, b
+    [T, hv] inside the prefill.  bf16, dk = dv = 128, chunk 64.  Returns o
+    [T, hv, 128].  workspace: None allocates gdn_prefill_layer_workspace_size
+    bytes; a uint8 CUDA tensor is used as given."""
+    _cuda(x, conv_weight, conv_state_pool, conv_state_indices, a, b, A_log, dt_bias, cu_seqlens,
+          state_pool, initial_state_indices, final_state_indices, conv_bias, has_initial_state)
+    T, C = x.shape
+    hv = a.shape[1]
+    _need(x.dtype == torch.bfloat16 and x.stride(1) == 1, "x: bf16 rows")
+    _need(C == 2 * hqk * 128 + hv * 128, "x: 2*hqk*128 + hv*128 channels")
+    _need(conv_weight.shape == (C, 4) and conv_weight.is_contiguous()
+          and conv_weight.dtype == torch.bfloat16, "conv_weight: [C, 4] bf16")
+    _need(conv_state_pool.dtype == torch.bfloat16 and conv_state_pool.is_contiguous()
+          and conv_state_pool.shape[1:] == (3, C), "conv_state_pool: [slots, 3, C] bf16")
+    _need(a.shape == (T, hv) and b.shape == (T, hv) and a.is_contiguous() and b.is_contiguous()
+          and a.dtype == b.dtype == torch.bfloat16, "a, b: [T, hv] bf16")
+    _need(state_pool.dtype == torch.float32 and state_pool.is_contiguous()
+          and state_pool.shape[1:] == (hv, 128, 128), "state_pool: [slots, hv, 128, 128] fp32")
+    _i32_vec(cu_seqlens, "cu_seqlens")
+    n = cu_seqlens.numel() - 1
+    for name, t in (("conv_state_indices", conv_state_indices),
+                    ("initial_state_indices", initial_state_indices),
+                    ("final_state_indices", final_state_indices)):
+        if t is not None:
+            _i32_vec(t, name)
+            _need(t.numel() == n, f"{name}: [n_seqs]")
+    if has_initial_state is not None:
+        _need(has_initial_state.dtype == torch.uint8 and has_initial_state.numel() == n,
+              "has_initial_state: [n_seqs] uint8")
+    scale = 128 ** -0.5 if scale is None else scale
+    o = torch.empty((T, hv, 128), dtype=torch.bfloat16, device=x.device) if o is None else o
+    _need(o.is_contiguous() and o.shape == (T, hv, 128), "o: [T, hv, 128] contiguous")
+    if workspace is None:
+        need = gdn_prefill_layer_workspace_size(n, T, hqk, hv)
+        workspace = torch.empty(need + 1024, dtype=torch.uint8, device=x.device) if need else None
+        if workspace is not None:   # 1 KiB alignment
+            off = (-workspace.data_ptr()) % 1024
+            workspace = workspace[off:off + need]
+    else:
+        _cuda(workspace)
+    wbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(_lib.gdn_prefill_layer(
+        _ptr(x), x.stride(0), _ptr(conv_weight), _ptr(conv_bias), _ptr(conv_state_pool),
+        conv_state_pool.shape[0], _ptr(conv_state_indices), _ptr(has_initial_state), _ptr(a),
+        _ptr(b), _ptr(A_log), _ptr(dt_bias), _ptr(cu_seqlens), n, T, hqk, hv, float(scale),
+        _ptr(state_pool), state_pool.shape[0], _ptr(initial_state_indices),
+        _ptr(final_state_indices), _ptr(o), _ptr(workspace), wbytes, _stream(x.device)),
+        "gdn_prefill_layer")
     return o
 
 

@@ -22,13 +22,22 @@ gdn_status prefill_scan(const void *q, int64_t qs, const void *k, int64_t ks, co
                         int64_t vs, const float *g, const float *beta, const int32_t *cu,
                         int64_t n_tokens, int hqk, int hv, float scale, int l2norm, float *pool,
                         int64_t n_slots, const int32_t *ii, const int32_t *fi, void *o, void *ws,
-                        cudaStream_t s);
+                        cudaStream_t s, const void *ga = nullptr, const void *gb = nullptr,
+                        const float *A_log = nullptr, const float *dt_bias = nullptr);
 gdn_status prefill_split(const void *q, int64_t qs, const void *k, int64_t ks, const void *v,
                          int64_t vs, const float *g, const float *beta, const int32_t *cu,
                          int n_seqs, int64_t n_tokens, int hqk, int hv, float scale, int l2norm,
                          float *pool, int64_t n_slots, const int32_t *ii, const int32_t *fi,
                          void *o, void *ws, cudaStream_t s, const void *z = nullptr,
-                         int64_t zs = 0, const float *norm_w = nullptr, float norm_eps = 0.f);
+                         int64_t zs = 0, const float *norm_w = nullptr, float norm_eps = 0.f,
+                         const void *ga = nullptr, const void *gb = nullptr,
+                         const float *A_log = nullptr, const float *dt_bias = nullptr);
+gdn_status prefill_check(const void *q, int64_t q_row_stride, const void *k, int64_t k_row_stride,
+                         const void *v, int64_t v_row_stride, const float *g, const float *beta,
+                         const int32_t *cu_seqlens, int32_t n_seqs, int64_t n_tokens, int32_t hqk,
+                         int32_t hv, int32_t dk, int32_t dv, int32_t chunk, const float *state_pool,
+                         int64_t n_slots, const int32_t *initial_state_indices,
+                         const int32_t *final_state_indices, const void *o, int32_t dtype);
 gdn_status norm_check(const void *o, const void *z, int64_t z_row_stride, const float *weight,
                       int64_t n_tokens, int32_t hv, int32_t dv, float eps, const void *y,
                       int32_t dtype);
@@ -158,4 +167,61 @@ extern "C" gdn_status gdn_prefill_chunked_gated(
     if (st != GDN_OK) return st;
     return gdn_gated_rmsnorm(y, z, z_row_stride, norm_weight, n_tokens, hv, dv, norm_eps, y,
                              dtype, stream);
+}
+
+// The prefill layer in one call: the conv of the raw q|k|v stream into the
+// workspace, then the chunked prefill on its q, k, v views with the gates
+// formed in the prep kernel from the raw a, b (no gating launch, no g / beta
+// round trip).  Built for the tensor-core path: bf16, dk = dv = 128, chunk 64,
+// conv width 4.
+extern "C" size_t gdn_prefill_layer_workspace_size(int32_t n_seqs, int64_t n_tokens, int32_t hqk,
+                                                   int32_t hv) {
+    if (n_seqs <= 0 || n_tokens <= 0 || hqk <= 0 || hv <= 0) return 0;
+    const size_t C = 2 * (size_t)hqk * 128 + (size_t)hv * 128;
+    const size_t y = ((size_t)n_tokens * C * 2 + 1023) / 1024 * 1024;
+    return y + gdn_prefill_workspace_size(n_seqs, n_tokens, hv, 128, 128, 64, GDN_BF16);
+}
+
+extern "C" gdn_status gdn_prefill_layer(
+    const void *x, int64_t x_row_stride, const void *conv_weight, const void *conv_bias,
+    void *conv_state_pool, int64_t n_conv_slots, const int32_t *conv_state_indices,
+    const uint8_t *has_initial_state, const void *a, const void *b, const float *A_log,
+    const float *dt_bias, const int32_t *cu_seqlens, int32_t n_seqs, int64_t n_tokens,
+    int32_t hqk, int32_t hv, float scale, float *state_pool, int64_t n_slots,
+    const int32_t *initial_state_indices, const int32_t *final_state_indices, void *o,
+    void *workspace, size_t workspace_bytes, void *stream) {
+    GDN_REQUIRE(n_seqs >= 0 && n_tokens >= 0 && hqk > 0 && hv > 0, GDN_ERR_INVALID_ARG);
+    GDN_REQUIRE(hv % hqk == 0, GDN_ERR_INVALID_ARG);
+    if (n_seqs == 0) return n_tokens == 0 ? GDN_OK : GDN_ERR_INVALID_ARG;
+    GDN_REQUIRE(a && b && A_log && dt_bias && x, GDN_ERR_INVALID_ARG);
+    const int64_t C = 2 * (int64_t)hqk * 128 + (int64_t)hv * 128;
+    const int64_t nq = (int64_t)hqk * 128;
+    // the prefill's checks on the views of y (g, beta: stand-ins, never read)
+    gdn_status st = prefill_check(x, C, x, C, x, C, A_log, dt_bias, cu_seqlens, n_seqs, n_tokens,
+                                  hqk, hv, 128, 128, 64, state_pool, n_slots,
+                                  initial_state_indices, final_state_indices, o, GDN_BF16);
+    if (st != GDN_OK) return st;
+    if (n_tokens == 0) return GDN_OK;
+    const size_t need = gdn_prefill_layer_workspace_size(n_seqs, n_tokens, hqk, hv);
+    GDN_REQUIRE(workspace && workspace_bytes >= need && ((uintptr_t)workspace % 1024) == 0,
+                GDN_ERR_INVALID_ARG);
+    GDN_REQUIRE(((uintptr_t)o % 16) == 0, GDN_ERR_INVALID_ARG);
+    const size_t y_bytes = ((size_t)n_tokens * C * 2 + 1023) / 1024 * 1024;
+    __nv_bfloat16 *y = (__nv_bfloat16 *)workspace;
+    void *pws = (uint8_t *)workspace + y_bytes;
+    const size_t pws_bytes = workspace_bytes - y_bytes;
+    st = causal_conv1d_fwd(x, x_row_stride, conv_weight, conv_bias, cu_seqlens, n_seqs, n_tokens,
+                           (int32_t)C, 4, conv_state_pool, n_conv_slots, conv_state_indices,
+                           has_initial_state, 1, y, GDN_BF16, stream);
+    if (st != GDN_OK) return st;
+    cudaStream_t s = (cudaStream_t)stream;
+    if (prefill_scan_sized(n_seqs, n_tokens) && prefill_scan_fits(hv) &&
+        pws_bytes >= prefill_scan_workspace(n_tokens, hv))
+        return prefill_scan(y, C, y + nq, C, y + 2 * nq, C, nullptr, nullptr, cu_seqlens, n_tokens,
+                            hqk, hv, scale, 1, state_pool, n_slots, initial_state_indices,
+                            final_state_indices, o, pws, s, a, b, A_log, dt_bias);
+    return prefill_split(y, C, y + nq, C, y + 2 * nq, C, nullptr, nullptr, cu_seqlens, n_seqs,
+                         n_tokens, hqk, hv, scale, 1, state_pool, n_slots, initial_state_indices,
+                         final_state_indices, o, pws, s, nullptr, 0, nullptr, 0.f, a, b, A_log,
+                         dt_bias);
 }

@@ -108,6 +108,27 @@ __global__ void __launch_bounds__(1024) chunk_base_kernel(const int32_t *__restr
 }
 
 // ------------------------------------------------------------ prep kernel --
+// The gate inputs of the prep kernel: g and beta, or (with a) the raw
+// a, b [n_tokens][hv] bf16 and A_log, dt_bias [hv], from which the kernel
+// forms g = -exp(A_log) softplus(a + dt_bias) and beta = sigmoid(b) itself
+// (the same expressions as the gating kernel, so the same values).
+struct RawGates {
+    const __nv_bfloat16 *a, *b;
+    const float *A_log, *dt_bias;
+};
+__device__ __forceinline__ void gate_of(const float *g, const float *beta, const RawGates &rg,
+                                        int64_t row, int hv, int h, float &gv, float &bv) {
+    const int64_t i = row * hv + h;
+    if (rg.a) {
+        const float x = __bfloat162float(rg.a[i]) + rg.dt_bias[h];
+        gv = -expf(rg.A_log[h]) * (x > 20.0f ? x : log1pf(expf(x)));
+        bv = 1.0f / (1.0f + expf(-__bfloat162float(rg.b[i])));
+    } else {
+        gv = g[i];
+        bv = beta[i];
+    }
+}
+
 constexpr int kPrepWarps = 9;              // warp 0: TMA + MMA + TMEM; warps 1..8: prep
 constexpr int kPrepKernelThreads = kPrepWarps * 32;
 constexpr int kPrepThreads = 256;
@@ -149,7 +170,7 @@ static_assert(kPrepCtasPerSm * (P_SMEM_BYTES + 1024) <= 233472, "three prep CTAs
 // the item block.
 __global__ void __launch_bounds__(kPrepKernelThreads, kPrepCtasPerSm)
 prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-            const float *__restrict__ g, const float *__restrict__ beta,
+            const float *__restrict__ g, const float *__restrict__ beta, RawGates rg,
             const int32_t *__restrict__ cu, const int32_t *__restrict__ base, int n_seqs, int hv,
             int grp, float scale, int l2norm, uint8_t *__restrict__ items) {
     extern __shared__ uint8_t smem_raw[];
@@ -252,14 +273,8 @@ prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
             float *Wb = reinterpret_cast<float *>(sm + P_OFF_WB);
             float g0 = 0.f, g1 = 0.f, b0 = 0.f, b1 = 0.f;
             if (t < 32) {
-                if (2 * t < n) {
-                    g0 = g[(c0 + 2 * t) * hv + h];
-                    b0 = beta[(c0 + 2 * t) * hv + h];
-                }
-                if (2 * t + 1 < n) {
-                    g1 = g[(c0 + 2 * t + 1) * hv + h];
-                    b1 = beta[(c0 + 2 * t + 1) * hv + h];
-                }
+                if (2 * t < n) gate_of(g, beta, rg, c0 + 2 * t, hv, h, g0, b0);
+                if (2 * t + 1 < n) gate_of(g, beta, rg, c0 + 2 * t + 1, hv, h, g1, b1);
             }
             if (t < 32) {   // prefix sum of g, per-token decay alpha = exp(g)
                 float x = g0 + g1;
@@ -907,7 +922,9 @@ gdn_status prefill_split(const void *q, int64_t qs, const void *k, int64_t ks, c
                          int n_seqs, int64_t n_tokens, int hqk, int hv, float scale, int l2norm,
                          float *pool, int64_t n_slots, const int32_t *ii, const int32_t *fi,
                          void *o, void *ws, cudaStream_t s, const void *z, int64_t zs,
-                         const float *norm_w, float norm_eps) {
+                         const float *norm_w, float norm_eps, const void *ga, const void *gb,
+                         const float *A_log, const float *dt_bias) {
+    const psp::RawGates rg{(const __nv_bfloat16 *)ga, (const __nv_bfloat16 *)gb, A_log, dt_bias};
     const int64_t items = psp::chunk_bound(n_tokens, n_seqs) * hv;
     if (items >= (1ll << 31)) return GDN_ERR_UNSUPPORTED;
     CUtensorMap tq, tk, tv, to, tz;
@@ -938,7 +955,7 @@ gdn_status prefill_split(const void *q, int64_t qs, const void *k, int64_t ks, c
     gdn_status st = launch_status();
     if (st != GDN_OK) return st;
     e = launch_after(psp::prep_kernel, dim3(psp::prep_grid(items)), dim3(psp::kPrepKernelThreads),
-                     psp::P_SMEM_BYTES, s, tq, tk, g, beta, cu, (const int32_t *)base, n_seqs,
+                     psp::P_SMEM_BYTES, s, tq, tk, g, beta, rg, cu, (const int32_t *)base, n_seqs,
                      hv, hv / hqk, scale, l2norm, item_blocks);
     if (e != cudaSuccess) {
         set_last_cuda_error(e);
@@ -1008,7 +1025,9 @@ gdn_status prefill_scan(const void *q, int64_t qs, const void *k, int64_t ks, co
                         int64_t vs, const float *g, const float *beta, const int32_t *cu,
                         int64_t n_tokens, int hqk, int hv, float scale, int l2norm, float *pool,
                         int64_t n_slots, const int32_t *ii, const int32_t *fi, void *o, void *ws,
-                        cudaStream_t s) {
+                        cudaStream_t s, const void *ga, const void *gb, const float *A_log,
+                        const float *dt_bias) {
+    const psp::RawGates rg{(const __nv_bfloat16 *)ga, (const __nv_bfloat16 *)gb, A_log, dt_bias};
     const psp::ScanLayout L = psp::scan_layout(n_tokens, hv);
     const int64_t items = psp::chunk_bound(n_tokens, 2) * hv;
     if (items >= (1ll << 31)) return GDN_ERR_UNSUPPORTED;
@@ -1046,7 +1065,7 @@ gdn_status prefill_scan(const void *q, int64_t qs, const void *k, int64_t ks, co
     psp::chunk_base_kernel<<<1, 1024, 0, s>>>(cu_all, 2, n_tokens, base);
     if ((st = launch_status()) != GDN_OK) return st;
     e = launch_after(psp::prep_kernel, dim3(psp::prep_grid(items)), dim3(psp::kPrepKernelThreads),
-                     psp::P_SMEM_BYTES, s, tq, tk, g, beta, cu_all, (const int32_t *)base, 2, hv,
+                     psp::P_SMEM_BYTES, s, tq, tk, g, beta, rg, cu_all, (const int32_t *)base, 2, hv,
                      hv / hqk, scale, l2norm, item_blocks);
     if (e == cudaSuccess)
         e = launch_after(psp::chain_kernel<false>, dim3((unsigned)(3 * hv)),

@@ -14,7 +14,9 @@ gdn_status prefill_split(const void *q, int64_t qs, const void *k, int64_t ks, c
                          int n_seqs, int64_t n_tokens, int hqk, int hv, float scale, int l2norm,
                          float *pool, int64_t n_slots, const int32_t *ii, const int32_t *fi,
                          void *o, void *ws, cudaStream_t s, const void *z = nullptr,
-                         int64_t zs = 0, const float *norm_w = nullptr, float norm_eps = 0.f);
+                         int64_t zs = 0, const float *norm_w = nullptr, float norm_eps = 0.f,
+                         const void *ga = nullptr, const void *gb = nullptr,
+                         const float *A_log = nullptr, const float *dt_bias = nullptr);
 
 // One copy per device (a __device__ variable lives in every device's
 // instance of the module).

@@ -234,7 +234,54 @@ gdn_status gdn_prefill_chunked_gated(const void *q, int64_t q_row_stride,
                                      size_t workspace_bytes, void *stream);
 
 /*
- * The prefill above on its bf16, dk = dv = 128, chunk-64 two-kernel path,
+ * Bytes of the workspace gdn_prefill_layer takes: the conv output y
+ * [n_tokens][2*hqk*128 + hv*128] bf16 (rounded up to 1 KiB), then
+ * gdn_prefill_workspace_size(n_seqs, n_tokens, hv, 128, 128, 64, GDN_BF16).
+ * 0 for an empty batch.
+ */
+size_t gdn_prefill_layer_workspace_size(int32_t n_seqs, int64_t n_tokens,
+                                        int32_t hqk, int32_t hv);
+
+/*
+ * The prefill side of the layer in one call (the "causal 1D convolution",
+ * "fused GDN gating" and chunked GDN kernels of the Qwen3next pages, over a
+ * packed varlen batch):
+ *   y = causal_conv1d_fwd(x) (width 4, SiLU; the conv states of
+ *       conv_state_indices read for sequences with has_initial_state and the
+ *       final ones written, as causal_conv1d_fwd), into the workspace;
+ *   the chunked prefill of gdn_prefill_chunked on the q | k | v views of y,
+ *       q and k L2-normalised, with g = -exp(A_log) softplus(a + dt_bias) and
+ *       beta = sigmoid(b) formed by its prep kernel from the raw a, b (the
+ *       same values gdn_gating writes; no gating launch).
+ *   x: [n_tokens] rows of 2*hqk*128 + hv*128 channels, row stride
+ *      x_row_stride elements (a multiple of 8), bf16, 16-byte aligned.
+ *   conv_weight [channels][4], conv_bias [channels] or NULL, conv_state_pool
+ *      [n_conv_slots][3][channels]: bf16, as causal_conv1d_fwd.
+ *   a, b: [n_tokens][hv] bf16; A_log, dt_bias: [hv] fp32.
+ *   state_pool, the index arrays, o [n_tokens][hv][128] bf16 (16-byte
+ *      aligned): as gdn_prefill_chunked.
+ *   workspace: at least gdn_prefill_layer_workspace_size bytes, 1 KiB
+ *      aligned, owned by the caller.
+ * Built: bf16, dk = dv = 128, chunk 64, conv width 4.  Every host check runs
+ * before the first launch.
+ */
+gdn_status gdn_prefill_layer(const void *x, int64_t x_row_stride,
+                             const void *conv_weight, const void *conv_bias,
+                             void *conv_state_pool, int64_t n_conv_slots,
+                             const int32_t *conv_state_indices,
+                             const uint8_t *has_initial_state, const void *a,
+                             const void *b, const float *A_log,
+                             const float *dt_bias, const int32_t *cu_seqlens,
+                             int32_t n_seqs, int64_t n_tokens, int32_t hqk,
+                             int32_t hv, float scale, float *state_pool,
+                             int64_t n_slots,
+                             const int32_t *initial_state_indices,
+                             const int32_t *final_state_indices, void *o,
+                             void *workspace, size_t workspace_bytes,
+                             void *stream);
+
+/*
+ * gdn_prefill_chunked on its bf16, dk = dv = 128, chunk-64 two-kernel path,
  * with the scratch in a fixed device array built into the library instead of
  * a caller workspace.  The pages describe no such variant: it exists for
  * callers that cannot allocate device memory per call -- a C or C++ runtime

@@ -226,3 +226,38 @@ def test_fused_step_host_checks(lib):
     assert m(*bad) == 1
     bad = list(base); bad[9] = 0            # empty: no launch
     assert m(*bad) == 0
+
+
+def test_prefill_layer_host_checks(lib):
+    """The one-call prefill layer refuses, before any launch: hv not a
+    multiple of hqk, missing raw gates, a workspace below its size or not
+    1 KiB aligned, an unaligned o; an empty batch launches nothing.  Its
+    workspace size is y (bf16, rounded up to 1 KiB) plus the prefill's."""
+    ws = lib.gdn_prefill_layer_workspace_size
+    ws.argtypes = [I32, I64, I32, I32]
+    ws.restype = ctypes.c_size_t
+    pws = lib.gdn_prefill_workspace_size
+    pws.argtypes = [I32, I64, I32, I32, I32, I32, I32]
+    pws.restype = ctypes.c_size_t
+    assert ws(8, 20668, 16, 32) == (20668 * 8192 * 2 + 1023) // 1024 * 1024 + \
+        pws(8, 20668, 32, 128, 128, 64, 1)
+    assert ws(0, 100, 16, 32) == 0
+    f = lib.gdn_prefill_layer
+    f.argtypes = [V, I64, V, V, V, I64, V, V, V, V, V, V, V, I32, I64, I32, I32, F32, V, I64, V, V,
+                  V, V, ctypes.c_size_t, V]
+    A = 1 << 20
+    need = ws(2, 100, 2, 4)
+    base = [A, 1024, A, None, A, 8, A, None, A, A, A, A, A, 2, 100, 2, 4, 1.0, A, 8, A, A, A, A,
+            need, None]
+    bad = list(base); bad[16] = 5           # hv not a multiple of hqk
+    assert f(*bad) == 1
+    bad = list(base); bad[8] = None         # no raw a
+    assert f(*bad) == 1
+    bad = list(base); bad[24] = need - 1    # workspace too small
+    assert f(*bad) == 1
+    bad = list(base); bad[23] = A + 512     # workspace not 1 KiB aligned
+    assert f(*bad) == 1
+    bad = list(base); bad[22] = A + 8       # o not 16-byte aligned
+    assert f(*bad) == 1
+    bad = list(base); bad[13] = 0; bad[14] = 0   # empty: no launch
+    assert f(*bad) == 0

@@ -1,0 +1,104 @@
+"""GPU parity of the prefill layer in one call (gdn_prefill_layer: the conv of
+the raw q|k|v stream, then the chunked prefill with the gates formed in its
+prep kernel from the raw a, b) through the C ABI: against the oracle's layer
+(conv -> split -> gating -> gated delta rule) on ragged batches with carried
+conv and recurrent states, o and states within the bf16 tolerance and the
+conv states bit for bit; and bit for bit against the three calls it replaces
+(causal_conv1d_fwd, gdn_gating, gdn_prefill_chunked) on the 8-sequence
+serving batch and on one long sequence (the chunk-state scan)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads
+from tests.gpu_common import DEV, cuda, gdn, status_clean
+from tests.util import TOL, assert_close, bits_equal, to_np
+
+pytestmark = pytest.mark.gpu
+
+
+def _three_calls(w, cpool, spool, slots, init, final):
+    d = w.dims
+    y = gdn().causal_conv1d_fwd(cuda(w.x), cuda(w.conv_w), cuda(w.cu_seqlens), cpool, slots,
+                                cuda(w.has_initial_state))
+    nq = d.hqk * 128
+    g, beta = gdn().gdn_gating(cuda(w.a), cuda(w.b), cuda(w.A_log), cuda(w.dt_bias))
+    return gdn().gdn_prefill_chunked(y[:, :nq].unflatten(1, (d.hqk, 128)),
+                                     y[:, nq:2 * nq].unflatten(1, (d.hqk, 128)),
+                                     y[:, 2 * nq:].unflatten(1, (d.hv, 128)), g, beta,
+                                     cuda(w.cu_seqlens), spool, init, final, w.scale)
+
+
+def _layer(w, cpool, spool, slots, init, final):
+    return gdn().gdn_prefill_layer(cuda(w.x), cuda(w.conv_w), cpool, slots,
+                                   cuda(w.has_initial_state), cuda(w.a), cuda(w.b),
+                                   cuda(w.A_log), cuda(w.dt_bias), cuda(w.cu_seqlens),
+                                   w.dims.hqk, spool, init, final, scale=w.scale)
+
+
+@pytest.mark.parametrize("lengths", [[70, 1, 130, 64], [5, 300]])
+def test_prefill_layer_vs_oracle(lengths):
+    """2 QK / 4 V heads at head_dim 128, ragged lengths (a one-token
+    sequence, a chunk-aligned one), every sequence continuing a carried conv
+    state and recurrent state from its slot."""
+    d = workloads.Dims(hqk=2, hv=4)
+    w = workloads.prefill(lengths=lengths, n_slots=len(lengths) + 2, dims=d, low_decay=True)
+    w.has_initial_state[:] = 1
+    gen = torch.Generator().manual_seed(17)
+    pool = torch.randn(len(lengths) + 2, d.hv, 128, 128, generator=gen) * 0.05
+    slots = cuda(w.slots)
+    cpool, spool = cuda(w.conv_pool), cuda(pool)
+    o = _layer(w, cpool, spool, slots, slots, slots)
+    torch.cuda.synchronize()
+    status_clean()
+    o_ref, conv_upd, upd, _, _, _ = oracle.layer_prefill(
+        w.x, w.cu_seqlens, w.conv_w, None, w.conv_pool, w.A_log, w.dt_bias, w.a, w.b, pool,
+        w.slots, w.has_initial_state, d.hqk, d.hv, 128, 128, w.scale)
+    assert_close(o, o_ref, TOL[torch.bfloat16], "layer o")
+    got = spool.cpu()
+    for (s, h), st in upd.items():
+        assert_close(got[s, h], st, TOL[torch.bfloat16], f"state {s},{h}")
+    gotc = cpool.cpu()
+    for s, st in conv_upd.items():
+        assert bits_equal(gotc[s], torch.from_numpy(st).to(torch.bfloat16)), f"conv slot {s}"
+
+
+def test_prefill_layer_equals_three_calls_serving_batch():
+    """The 8-sequence batch (lengths U{512..8192}): o, the recurrent pool and
+    the conv pool bit for bit equal to conv fwd + gating + prefill (the
+    prep kernel forms g and beta with the gating kernel's expressions)."""
+    w = workloads.prefill()
+    d = w.dims
+    slots = cuda((w.slots % 64).to(torch.int32))
+    none = torch.full_like(slots, -1)
+    outs = []
+    for fn in (_three_calls, _layer):
+        cpool = cuda(w.conv_pool)
+        spool = torch.zeros((64, d.hv, 128, 128), device=DEV)
+        o = fn(w, cpool, spool, slots, none, slots)
+        torch.cuda.synchronize()
+        status_clean()
+        outs.append((o, spool, cpool))
+    for name, a, b in zip(("o", "state pool", "conv pool"), outs[0], outs[1]):
+        assert bits_equal(a, b), name
+
+
+def test_prefill_layer_equals_three_calls_long_sequence():
+    """One 8,000-token sequence (the chunk-state scan, its prep kernel fed the
+    raw gates) with a carried state: bit for bit equal to the three calls."""
+    d = workloads.Dims(hqk=2, hv=4)
+    w = workloads.prefill(lengths=[8000], n_slots=2, dims=d, low_decay=True)
+    w.has_initial_state[:] = 1
+    gen = torch.Generator().manual_seed(23)
+    pool = cuda(torch.randn(2, d.hv, 128, 128, generator=gen) * 0.05)
+    slots = cuda(w.slots)
+    outs = []
+    for fn in (_three_calls, _layer):
+        cpool, spool = cuda(w.conv_pool), pool.clone()
+        o = fn(w, cpool, spool, slots, slots, slots)
+        torch.cuda.synchronize()
+        status_clean()
+        outs.append((o, spool, cpool))
+    for name, a, b in zip(("o", "state pool", "conv pool"), outs[0], outs[1]):
+        assert bits_equal(a, b), name
