@@ -32,6 +32,7 @@ EXPORTS = (
     "gdn_decode_recurrent_gated", "gdn_decode_step_fused", "gdn_mixed_batch",
     "gdn_debug_set_wait_limit", "gdn_prefill_chunked_gated", "gdn_mtp_step_fused",
     "gdn_decode_step_workspace_size", "gdn_prefill_layer", "gdn_prefill_layer_workspace_size",
+    "gdn_prefill_layer_gated",
 )
 
 if not os.path.exists(LIB_PATH):
@@ -72,6 +73,9 @@ _SIGS = {
     "gdn_prefill_layer": [_vp, _i64, _vp, _vp, _vp, _i64, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32,
                           _i64, _i32, _i32, _f32, _vp, _i64, _vp, _vp, _vp, _vp,
                           ctypes.c_size_t, _vp],
+    "gdn_prefill_layer_gated": [_vp, _i64, _vp, _vp, _vp, _i64, _vp, _vp, _vp, _vp, _vp, _vp, _vp,
+                                _i32, _i64, _i32, _i32, _f32, _vp, _i64, _vp, _vp, _vp, _i64, _vp,
+                                _f32, _vp, _vp, ctypes.c_size_t, _vp],
     "gdn_mtp_step_fused": [_vp, _i64, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32,
                            _f32, _vp, _i64, _vp, _vp, _vp, _vp],
     "gdn_prefill_chunked_gated": [_vp, _i64, _vp, _i64, _vp, _i64, _vp, _vp, _vp, _i32, _i64,
@@ -533,15 +537,11 @@ def gdn_prefill_layer_workspace_size(n_seqs, n_tokens, hqk, hv) -> int:
     return int(_lib.gdn_prefill_layer_workspace_size(n_seqs, n_tokens, hqk, hv))
 
 
-def gdn_prefill_layer(x, conv_weight, conv_state_pool, conv_state_indices, has_initial_state, a, b,
-                      A_log, dt_bias, cu_seqlens, hqk, state_pool, initial_state_indices,
-                      final_state_indices, scale=None, conv_bias=None, o=None, workspace=None):
-    """The prefill side of the layer in one call: the causal conv + SiLU of the
-    raw q|k|v stream x [T, C] (conv states as causal_conv1d_fwd), then the
-    chunked prefill on its q, k, v with the gates formed from the raw a, b
-    [T, hv] inside the prefill.  bf16, dk = dv = 128, chunk 64.  Returns o
-    [T, hv, 128].  workspace: None allocates gdn_prefill_layer_workspace_size
-    bytes; a uint8 CUDA tensor is used as given."""
+def _layer_args(x, conv_weight, conv_state_pool, conv_state_indices, has_initial_state, a, b,
+                A_log, dt_bias, cu_seqlens, hqk, state_pool, initial_state_indices,
+                final_state_indices, conv_bias, out, workspace):
+    """Checks and marshalling shared by the two layer calls: the leading
+    arguments up to the index arrays, the output tensor and the workspace."""
     _cuda(x, conv_weight, conv_state_pool, conv_state_indices, a, b, A_log, dt_bias, cu_seqlens,
           state_pool, initial_state_indices, final_state_indices, conv_bias, has_initial_state)
     T, C = x.shape
@@ -567,9 +567,8 @@ def gdn_prefill_layer(x, conv_weight, conv_state_pool, conv_state_indices, has_i
     if has_initial_state is not None:
         _need(has_initial_state.dtype == torch.uint8 and has_initial_state.numel() == n,
               "has_initial_state: [n_seqs] uint8")
-    scale = 128 ** -0.5 if scale is None else scale
-    o = torch.empty((T, hv, 128), dtype=torch.bfloat16, device=x.device) if o is None else o
-    _need(o.is_contiguous() and o.shape == (T, hv, 128), "o: [T, hv, 128] contiguous")
+    out = torch.empty((T, hv, 128), dtype=torch.bfloat16, device=x.device) if out is None else out
+    _need(out.is_contiguous() and out.shape == (T, hv, 128), "output: [T, hv, 128] contiguous")
     if workspace is None:
         need = gdn_prefill_layer_workspace_size(n, T, hqk, hv)
         workspace = torch.empty(need + 1024, dtype=torch.uint8, device=x.device) if need else None
@@ -579,14 +578,54 @@ def gdn_prefill_layer(x, conv_weight, conv_state_pool, conv_state_indices, has_i
     else:
         _cuda(workspace)
     wbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
-    _check(_lib.gdn_prefill_layer(
-        _ptr(x), x.stride(0), _ptr(conv_weight), _ptr(conv_bias), _ptr(conv_state_pool),
-        conv_state_pool.shape[0], _ptr(conv_state_indices), _ptr(has_initial_state), _ptr(a),
-        _ptr(b), _ptr(A_log), _ptr(dt_bias), _ptr(cu_seqlens), n, T, hqk, hv, float(scale),
-        _ptr(state_pool), state_pool.shape[0], _ptr(initial_state_indices),
-        _ptr(final_state_indices), _ptr(o), _ptr(workspace), wbytes, _stream(x.device)),
-        "gdn_prefill_layer")
+    lead = (_ptr(x), x.stride(0), _ptr(conv_weight), _ptr(conv_bias), _ptr(conv_state_pool),
+            conv_state_pool.shape[0], _ptr(conv_state_indices), _ptr(has_initial_state), _ptr(a),
+            _ptr(b), _ptr(A_log), _ptr(dt_bias), _ptr(cu_seqlens), n, T, hqk, hv)
+    tail = (_ptr(state_pool), state_pool.shape[0], _ptr(initial_state_indices),
+            _ptr(final_state_indices))
+    return lead, tail, out, (_ptr(workspace), wbytes, _stream(x.device))
+
+
+def gdn_prefill_layer(x, conv_weight, conv_state_pool, conv_state_indices, has_initial_state, a, b,
+                      A_log, dt_bias, cu_seqlens, hqk, state_pool, initial_state_indices,
+                      final_state_indices, scale=None, conv_bias=None, o=None, workspace=None):
+    """The prefill side of the layer in one call: the causal conv + SiLU of the
+    raw q|k|v stream x [T, C] (conv states as causal_conv1d_fwd), then the
+    chunked prefill on its q, k, v with the gates formed from the raw a, b
+    [T, hv] inside the prefill.  bf16, dk = dv = 128, chunk 64.  Returns o
+    [T, hv, 128].  workspace: None allocates gdn_prefill_layer_workspace_size
+    bytes; a uint8 CUDA tensor is used as given."""
+    lead, tail, o, ws = _layer_args(x, conv_weight, conv_state_pool, conv_state_indices,
+                                    has_initial_state, a, b, A_log, dt_bias, cu_seqlens, hqk,
+                                    state_pool, initial_state_indices, final_state_indices,
+                                    conv_bias, o, workspace)
+    scale = 128 ** -0.5 if scale is None else scale
+    _check(_lib.gdn_prefill_layer(*lead, float(scale), *tail, _ptr(o), *ws), "gdn_prefill_layer")
     return o
+
+
+def gdn_prefill_layer_gated(x, conv_weight, conv_state_pool, conv_state_indices, has_initial_state,
+                            a, b, A_log, dt_bias, cu_seqlens, hqk, state_pool,
+                            initial_state_indices, final_state_indices, z, norm_weight,
+                            norm_eps=1e-6, scale=None, conv_bias=None, y=None, workspace=None):
+    """gdn_prefill_layer writing the gated RMSNorm y = o / rms(o) * w *
+    SiLU(z) per (token, V head) row instead of o; z [T, hv, 128] or
+    [T, hv*128] bf16 (row stride free), norm_weight [128] fp32.  Returns y
+    [T, hv, 128]."""
+    _cuda(z, norm_weight)
+    zs = _heads_view(z, a.shape[1], 128, "z")
+    _need(z.dtype == torch.bfloat16 and z.shape[0] == x.shape[0], "z: [T, hv, 128] bf16")
+    _need(norm_weight.dtype == torch.float32 and norm_weight.is_contiguous()
+          and norm_weight.numel() == 128, "norm_weight: [128] fp32")
+    lead, tail, y, ws = _layer_args(x, conv_weight, conv_state_pool, conv_state_indices,
+                                    has_initial_state, a, b, A_log, dt_bias, cu_seqlens, hqk,
+                                    state_pool, initial_state_indices, final_state_indices,
+                                    conv_bias, y, workspace)
+    scale = 128 ** -0.5 if scale is None else scale
+    _check(_lib.gdn_prefill_layer_gated(*lead, float(scale), *tail, _ptr(z), zs,
+                                        _ptr(norm_weight), float(norm_eps), _ptr(y), *ws),
+           "gdn_prefill_layer_gated")
+    return y
 
 
 def gdn_mtp_step_fused(x, tokens_per_seq, conv_weight, conv_state_pool, a, b, A_log, dt_bias,

@@ -182,14 +182,20 @@ extern "C" size_t gdn_prefill_layer_workspace_size(int32_t n_seqs, int64_t n_tok
     return y + gdn_prefill_workspace_size(n_seqs, n_tokens, hv, 128, 128, 64, GDN_BF16);
 }
 
-extern "C" gdn_status gdn_prefill_layer(
-    const void *x, int64_t x_row_stride, const void *conv_weight, const void *conv_bias,
-    void *conv_state_pool, int64_t n_conv_slots, const int32_t *conv_state_indices,
-    const uint8_t *has_initial_state, const void *a, const void *b, const float *A_log,
-    const float *dt_bias, const int32_t *cu_seqlens, int32_t n_seqs, int64_t n_tokens,
-    int32_t hqk, int32_t hv, float scale, float *state_pool, int64_t n_slots,
-    const int32_t *initial_state_indices, const int32_t *final_state_indices, void *o,
-    void *workspace, size_t workspace_bytes, void *stream) {
+namespace {
+// The layer's prefill in one call; with z, the gated RMSNorm output y is
+// written instead of o (in the chain kernel's epilogue on the two-kernel
+// path, by the norm kernel in place after the chunk-state scan).
+gdn_status prefill_layer(const void *x, int64_t x_row_stride, const void *conv_weight,
+                         const void *conv_bias, void *conv_state_pool, int64_t n_conv_slots,
+                         const int32_t *conv_state_indices, const uint8_t *has_initial_state,
+                         const void *a, const void *b, const float *A_log, const float *dt_bias,
+                         const int32_t *cu_seqlens, int32_t n_seqs, int64_t n_tokens, int32_t hqk,
+                         int32_t hv, float scale, float *state_pool, int64_t n_slots,
+                         const int32_t *initial_state_indices, const int32_t *final_state_indices,
+                         const void *z, int64_t z_row_stride, const float *norm_weight,
+                         float norm_eps, void *out, void *workspace, size_t workspace_bytes,
+                         void *stream) {
     GDN_REQUIRE(n_seqs >= 0 && n_tokens >= 0 && hqk > 0 && hv > 0, GDN_ERR_INVALID_ARG);
     GDN_REQUIRE(hv % hqk == 0, GDN_ERR_INVALID_ARG);
     if (n_seqs == 0) return n_tokens == 0 ? GDN_OK : GDN_ERR_INVALID_ARG;
@@ -199,13 +205,18 @@ extern "C" gdn_status gdn_prefill_layer(
     // the prefill's checks on the views of y (g, beta: stand-ins, never read)
     gdn_status st = prefill_check(x, C, x, C, x, C, A_log, dt_bias, cu_seqlens, n_seqs, n_tokens,
                                   hqk, hv, 128, 128, 64, state_pool, n_slots,
-                                  initial_state_indices, final_state_indices, o, GDN_BF16);
+                                  initial_state_indices, final_state_indices, out, GDN_BF16);
     if (st != GDN_OK) return st;
+    if (z) {
+        st = norm_check(out, z, z_row_stride, norm_weight, n_tokens, hv, 128, norm_eps, out,
+                        GDN_BF16);
+        if (st != GDN_OK) return st;
+    }
     if (n_tokens == 0) return GDN_OK;
     const size_t need = gdn_prefill_layer_workspace_size(n_seqs, n_tokens, hqk, hv);
     GDN_REQUIRE(workspace && workspace_bytes >= need && ((uintptr_t)workspace % 1024) == 0,
                 GDN_ERR_INVALID_ARG);
-    GDN_REQUIRE(((uintptr_t)o % 16) == 0, GDN_ERR_INVALID_ARG);
+    GDN_REQUIRE(((uintptr_t)out % 16) == 0, GDN_ERR_INVALID_ARG);
     const size_t y_bytes = ((size_t)n_tokens * C * 2 + 1023) / 1024 * 1024;
     __nv_bfloat16 *y = (__nv_bfloat16 *)workspace;
     void *pws = (uint8_t *)workspace + y_bytes;
@@ -216,12 +227,54 @@ extern "C" gdn_status gdn_prefill_layer(
     if (st != GDN_OK) return st;
     cudaStream_t s = (cudaStream_t)stream;
     if (prefill_scan_sized(n_seqs, n_tokens) && prefill_scan_fits(hv) &&
-        pws_bytes >= prefill_scan_workspace(n_tokens, hv))
-        return prefill_scan(y, C, y + nq, C, y + 2 * nq, C, nullptr, nullptr, cu_seqlens, n_tokens,
-                            hqk, hv, scale, 1, state_pool, n_slots, initial_state_indices,
-                            final_state_indices, o, pws, s, a, b, A_log, dt_bias);
-    return prefill_split(y, C, y + nq, C, y + 2 * nq, C, nullptr, nullptr, cu_seqlens, n_seqs,
-                         n_tokens, hqk, hv, scale, 1, state_pool, n_slots, initial_state_indices,
-                         final_state_indices, o, pws, s, nullptr, 0, nullptr, 0.f, a, b, A_log,
-                         dt_bias);
+        pws_bytes >= prefill_scan_workspace(n_tokens, hv)) {
+        st = prefill_scan(y, C, y + nq, C, y + 2 * nq, C, nullptr, nullptr, cu_seqlens, n_tokens,
+                          hqk, hv, scale, 1, state_pool, n_slots, initial_state_indices,
+                          final_state_indices, out, pws, s, a, b, A_log, dt_bias);
+        if (st != GDN_OK || !z) return st;
+        return gdn_gated_rmsnorm(out, z, z_row_stride, norm_weight, n_tokens, hv, 128, norm_eps,
+                                 out, GDN_BF16, stream);
+    }
+    // the chain kernel's gated epilogue loads z by TMA: 16-byte rows
+    const bool z_tma = z && ((uintptr_t)z % 16) == 0 && (z_row_stride % 8) == 0;
+    st = prefill_split(y, C, y + nq, C, y + 2 * nq, C, nullptr, nullptr, cu_seqlens, n_seqs,
+                       n_tokens, hqk, hv, scale, 1, state_pool, n_slots, initial_state_indices,
+                       final_state_indices, out, pws, s, z_tma ? z : nullptr, z_row_stride,
+                       norm_weight, norm_eps, a, b, A_log, dt_bias);
+    if (st != GDN_OK || !z || z_tma) return st;
+    return gdn_gated_rmsnorm(out, z, z_row_stride, norm_weight, n_tokens, hv, 128, norm_eps, out,
+                             GDN_BF16, stream);
+}
+}  // namespace
+
+extern "C" gdn_status gdn_prefill_layer(
+    const void *x, int64_t x_row_stride, const void *conv_weight, const void *conv_bias,
+    void *conv_state_pool, int64_t n_conv_slots, const int32_t *conv_state_indices,
+    const uint8_t *has_initial_state, const void *a, const void *b, const float *A_log,
+    const float *dt_bias, const int32_t *cu_seqlens, int32_t n_seqs, int64_t n_tokens,
+    int32_t hqk, int32_t hv, float scale, float *state_pool, int64_t n_slots,
+    const int32_t *initial_state_indices, const int32_t *final_state_indices, void *o,
+    void *workspace, size_t workspace_bytes, void *stream) {
+    return prefill_layer(x, x_row_stride, conv_weight, conv_bias, conv_state_pool, n_conv_slots,
+                         conv_state_indices, has_initial_state, a, b, A_log, dt_bias, cu_seqlens,
+                         n_seqs, n_tokens, hqk, hv, scale, state_pool, n_slots,
+                         initial_state_indices, final_state_indices, nullptr, 0, nullptr, 0.f, o,
+                         workspace, workspace_bytes, stream);
+}
+
+extern "C" gdn_status gdn_prefill_layer_gated(
+    const void *x, int64_t x_row_stride, const void *conv_weight, const void *conv_bias,
+    void *conv_state_pool, int64_t n_conv_slots, const int32_t *conv_state_indices,
+    const uint8_t *has_initial_state, const void *a, const void *b, const float *A_log,
+    const float *dt_bias, const int32_t *cu_seqlens, int32_t n_seqs, int64_t n_tokens,
+    int32_t hqk, int32_t hv, float scale, float *state_pool, int64_t n_slots,
+    const int32_t *initial_state_indices, const int32_t *final_state_indices, const void *z,
+    int64_t z_row_stride, const float *norm_weight, float norm_eps, void *y, void *workspace,
+    size_t workspace_bytes, void *stream) {
+    GDN_REQUIRE(z || n_tokens == 0, GDN_ERR_INVALID_ARG);
+    return prefill_layer(x, x_row_stride, conv_weight, conv_bias, conv_state_pool, n_conv_slots,
+                         conv_state_indices, has_initial_state, a, b, A_log, dt_bias, cu_seqlens,
+                         n_seqs, n_tokens, hqk, hv, scale, state_pool, n_slots,
+                         initial_state_indices, final_state_indices, z, z_row_stride, norm_weight,
+                         norm_eps, y, workspace, workspace_bytes, stream);
 }

@@ -281,6 +281,42 @@ gdn_status gdn_prefill_layer(const void *x, int64_t x_row_stride,
                              void *stream);
 
 /*
+ * gdn_prefill_layer writing the layer's gated output instead of o ("gated
+ * RMSNorm", Highlights of "[model] Support Qwen3next"):
+ *   y = o / sqrt(mean over each (token, V head) row of o^2 + norm_eps)
+ *       * norm_weight * SiLU(z),
+ * the values gdn_gated_rmsnorm gives on gdn_prefill_layer's o.  On the
+ * two-kernel path the norm runs in the prefill chain kernel's output
+ * epilogue (o never reaches memory); after the chunk-state scan, or with a z
+ * that a TMA tile cannot read (not 16-byte aligned, or a row stride not a
+ * multiple of 8), the norm kernel runs on y in place.
+ *   z: [n_tokens][hv][128] bf16, row stride z_row_stride elements (>= hv*128,
+ *      a multiple of 4), 8-byte aligned; norm_weight: [128] fp32;
+ *      norm_eps >= 0.
+ *   y: [n_tokens][hv][128] bf16, 16-byte aligned.
+ * Every other argument, the workspace and the errors: as gdn_prefill_layer;
+ * z == NULL with n_tokens > 0 is GDN_ERR_INVALID_ARG.
+ */
+gdn_status gdn_prefill_layer_gated(const void *x, int64_t x_row_stride,
+                                   const void *conv_weight,
+                                   const void *conv_bias, void *conv_state_pool,
+                                   int64_t n_conv_slots,
+                                   const int32_t *conv_state_indices,
+                                   const uint8_t *has_initial_state,
+                                   const void *a, const void *b,
+                                   const float *A_log, const float *dt_bias,
+                                   const int32_t *cu_seqlens, int32_t n_seqs,
+                                   int64_t n_tokens, int32_t hqk, int32_t hv,
+                                   float scale, float *state_pool,
+                                   int64_t n_slots,
+                                   const int32_t *initial_state_indices,
+                                   const int32_t *final_state_indices,
+                                   const void *z, int64_t z_row_stride,
+                                   const float *norm_weight, float norm_eps,
+                                   void *y, void *workspace,
+                                   size_t workspace_bytes, void *stream);
+
+/*
  * gdn_prefill_chunked on its bf16, dk = dv = 128, chunk-64 two-kernel path,
  * with the scratch in a fixed device array built into the library instead of
  * a caller workspace.  The pages describe no such variant: it exists for

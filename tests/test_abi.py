@@ -261,3 +261,37 @@ def test_prefill_layer_host_checks(lib):
     assert f(*bad) == 1
     bad = list(base); bad[13] = 0; bad[14] = 0   # empty: no launch
     assert f(*bad) == 0
+
+
+def test_prefill_layer_gated_host_checks(lib):
+    """The gated layer call refuses, before any launch, what the plain one
+    refuses, and also: no z, a z row stride below hv * 128 or not a multiple
+    of 4, no norm weight, a negative eps; an empty batch launches nothing."""
+    ws = lib.gdn_prefill_layer_workspace_size
+    ws.argtypes = [I32, I64, I32, I32]
+    ws.restype = ctypes.c_size_t
+    f = lib.gdn_prefill_layer_gated
+    f.argtypes = [V, I64, V, V, V, I64, V, V, V, V, V, V, V, I32, I64, I32, I32, F32, V, I64, V, V,
+                  V, I64, V, F32, V, V, ctypes.c_size_t, V]
+    A = 1 << 20
+    need = ws(2, 100, 2, 4)
+    base = [A, 1024, A, None, A, 8, A, None, A, A, A, A, A, 2, 100, 2, 4, 1.0, A, 8, A, A,
+            A, 4 * 128, A, 1e-6, A, A, need, None]
+    bad = list(base); bad[16] = 5           # hv not a multiple of hqk
+    assert f(*bad) == 1
+    bad = list(base); bad[22] = None        # no z
+    assert f(*bad) == 1
+    bad = list(base); bad[23] = 4 * 128 - 4  # z rows shorter than hv * 128
+    assert f(*bad) == 1
+    bad = list(base); bad[23] = 4 * 128 + 2  # z row stride not a multiple of 4
+    assert f(*bad) == 1
+    bad = list(base); bad[24] = None        # no norm weight
+    assert f(*bad) == 1
+    bad = list(base); bad[25] = -1.0        # negative eps
+    assert f(*bad) == 1
+    bad = list(base); bad[28] = need - 1    # workspace too small
+    assert f(*bad) == 1
+    bad = list(base); bad[26] = A + 8       # y not 16-byte aligned
+    assert f(*bad) == 1
+    bad = list(base); bad[13] = 0; bad[14] = 0   # empty: no launch
+    assert f(*bad) == 0
