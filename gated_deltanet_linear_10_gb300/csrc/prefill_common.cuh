@@ -176,6 +176,38 @@ __device__ __forceinline__ void g_to_a_p(const uint32_t (&gr)[32], int p, int ch
     }
 }
 
+// The four diagonal 16 x 16 blocks of T = (I + A)^-1 by forward
+// substitution, exact fp32, on warps 0 and 1 of the 256 prep threads: lane c
+// of half-warp hw solves column c of block 2 pw + hw,
+//   T[r][c] = delta_rc - sum_{m < r} A[r][m] T[m][c]   (m ascending),
+// reading the rows of A as broadcasts.  (One lane per row half, with the
+// finished rows passed on by shuffles, took 8 shuffles per step on 4 warps.)
+__device__ __forceinline__ void ut_diag_blocks(const float *Af, float *Tf, int pw, int lane) {
+    if (pw >= 2) return;
+    const int bb = 2 * pw + (lane >> 4), c = lane & 15;
+    const float *Ab = Af + (16 * bb) * kLd + 16 * bb;
+    float x[16];
+#pragma unroll
+    for (int r = 0; r < 16; ++r) {
+        float acc = r == c ? 1.f : 0.f;
+#pragma unroll
+        for (int m4 = 0; m4 < r; m4 += 4) {
+            const float4 f = *reinterpret_cast<const float4 *>(Ab + r * kLd + m4);
+            const float ar[4] = {f.x, f.y, f.z, f.w};
+#pragma unroll
+            for (int u = 0; u < 4; ++u)
+                if (m4 + u < r) acc = fmaf(-ar[u], x[m4 + u], acc);
+        }
+        x[r] = acc;
+        // a compiler barrier: each row's loads stay next to their use
+        // (hoisting all of them spills registers at the prep kernel's 72)
+        asm volatile("" ::: "memory");
+    }
+    float *Tb = Tf + (16 * bb) * kLd + 16 * bb + c;
+#pragma unroll
+    for (int r = 0; r < 16; ++r) Tb[r * kLd] = x[r];
+}
+
 // T = (I + A)^-1 for the strictly lower triangular A in Af (fp32, row stride
 // kLd), then T1 = T diag(beta) and (kT2) T2 = -T diag(beta xs) as bf16
 // K-major operands at dst and dst + kMatBytes (xs = Gam r_k, zero on padded
@@ -189,25 +221,7 @@ __device__ __forceinline__ void ut_solve(const float *Af, float *Tf, float *Wb, 
                                          int lane, const float *beta, const float *xs,
                                          uint8_t *dst) {
     float *Zs = Wb + 8 * 16 * kWbLd;
-    if (pw < 4) {
-        const int r = lane >> 1, hh = lane & 1;
-        const int bb = pw;
-        const int R = 16 * bb + r;
-        float tv[8];
-#pragma unroll
-        for (int k = 0; k < 8; ++k) tv[k] = (8 * hh + k == r) ? 1.f : 0.f;
-#pragma unroll
-        for (int m = 0; m < 15; ++m) {
-            const float a = Af[R * kLd + 16 * bb + m];
-#pragma unroll
-            for (int k = 0; k < 8; ++k) {
-                const float vm = __shfl_sync(0xffffffffu, tv[k], 2 * m + hh);
-                if (r > m) tv[k] = fmaf(-a, vm, tv[k]);
-            }
-        }
-        *reinterpret_cast<float4 *>(Tf + R * kLd + 16 * bb + 8 * hh) = make_float4(tv[0], tv[1], tv[2], tv[3]);
-        *reinterpret_cast<float4 *>(Tf + R * kLd + 16 * bb + 8 * hh + 4) = make_float4(tv[4], tv[5], tv[6], tv[7]);
-    }
+    ut_diag_blocks(Af, Tf, pw, lane);
     named_sync(1, 256);
     const int r = lane >> 1, cg = lane & 1;
     float *wb = Wb + pw * 16 * kWbLd;
@@ -337,25 +351,7 @@ __device__ __forceinline__ void ut_solve_mma(const float *Af, float *Tf, float *
                                              int lane, const float *beta, const float *xs,
                                              uint8_t *dst) {
     float *Zs = Wb + 8 * 16 * kWbLd;          // Z30, 16 x 16
-    if (pw < 4) {   // diagonal blocks: forward substitution, exact fp32
-        const int r = lane >> 1, hh = lane & 1;
-        const int bb = pw;
-        const int R = 16 * bb + r;
-        float tv[8];
-#pragma unroll
-        for (int k = 0; k < 8; ++k) tv[k] = (8 * hh + k == r) ? 1.f : 0.f;
-#pragma unroll
-        for (int m = 0; m < 15; ++m) {
-            const float a = Af[R * kLd + 16 * bb + m];
-#pragma unroll
-            for (int k = 0; k < 8; ++k) {
-                const float vm = __shfl_sync(0xffffffffu, tv[k], 2 * m + hh);
-                if (r > m) tv[k] = fmaf(-a, vm, tv[k]);
-            }
-        }
-        *reinterpret_cast<float4 *>(Tf + R * kLd + 16 * bb + 8 * hh) = make_float4(tv[0], tv[1], tv[2], tv[3]);
-        *reinterpret_cast<float4 *>(Tf + R * kLd + 16 * bb + 8 * hh + 4) = make_float4(tv[4], tv[5], tv[6], tv[7]);
-    }
+    ut_diag_blocks(Af, Tf, pw, lane);
     named_sync(1, 256);
     const int g = lane >> 2, tq = lane & 3;
     float *wb = Wb + pw * 16 * kWbLd;
