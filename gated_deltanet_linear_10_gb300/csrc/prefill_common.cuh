@@ -344,49 +344,58 @@ __device__ __forceinline__ void hm_finish(const float (&acc)[4], float *Tf, floa
     __syncwarp();
 }
 
-// ut_solve with the off-diagonal levels on mma.sync (same blocking, same
-// outputs, tf32 rounding of the block-product operands).
+// acc += (neg ? -X : X) (16 x 16, row stride ldx) * Y (16 x 8, row stride ldy),
+// tf32 operands, X and Y pointing at the blocks' first elements.
+__device__ __forceinline__ void hm_mac_at(float (&acc)[4], const float *X, int ldx, const float *Y,
+                                          int ldy, int lane, bool neg) {
+    const int g = lane >> 2, t = lane & 3;
+    const float sg = neg ? -1.f : 1.f;
+#pragma unroll
+    for (int ks = 0; ks < 16; ks += 8) {
+        const uint32_t a[4] = {tf32_of(sg * X[g * ldx + ks + t]),
+                               tf32_of(sg * X[(g + 8) * ldx + ks + t]),
+                               tf32_of(sg * X[g * ldx + ks + t + 4]),
+                               tf32_of(sg * X[(g + 8) * ldx + ks + t + 4])};
+        mma_tf32(acc, a, tf32_of(Y[(ks + t) * ldy + g]), tf32_of(Y[(ks + t + 4) * ldy + g]));
+    }
+}
+
+// ut_solve with the off-diagonal blocks on mma.sync (tf32 in, fp32
+// accumulate), by the 2 x 2 block inverse at the 32-row level: with
+// T_hi = (I + A_hi)^-1 over block rows 0, 1 and T_lo over rows 2, 3,
+//   T10 = -T11 (A10 T00),  T32 = -T33 (A32 T22),
+//   X = A_ll T_hi:  X20 = A20 T00 + A21 T10, X21 = A21 T11,
+//                   X30 = A30 T00 + A31 T10, X31 = A31 T11,
+//   [T20 T21; T30 T31] = -T_lo X:  T2j = -T22 X2j,  T3j = -(T32 X2j + T33 X3j).
+// Three dependent stages of at most two 16 x 16 products (the level-by-level
+// form needs seven): stage 1 T10, T32 (warps 0..3) and the parts of X that
+// need no T10 (warps 4..7, kept in registers); stage 2 X20, X30 (warps
+// 4..7), X into Wb, and the T1 / T2 rows 0..31 (warps 0..3); stage 3 the
+// lower-left quarter (one 16 x 8 half-block per warp).  Block row 2's and
+// 3's products of T20 and T21 are the level form's: -T22 times the same X.
 template <bool kT2>
 __device__ __forceinline__ void ut_solve_mma(const float *Af, float *Tf, float *Wb, int t, int pw,
                                              int lane, const float *beta, const float *xs,
                                              uint8_t *dst) {
-    float *Zs = Wb + 8 * 16 * kWbLd;          // Z30, 16 x 16
+    constexpr int kXLd = 36;                  // X: 32 x 32 fp32 in Wb
+    static_assert(32 * kXLd <= 8 * 16 * kWbLd + 16 * 16, "X fits in the solve scratch");
+    float *Xs = Wb;
     ut_diag_blocks(Af, Tf, pw, lane);
     named_sync(1, 256);
     const int g = lane >> 2, tq = lane & 3;
-    float *wb = Wb + pw * 16 * kWbLd;
-    float acc[4];
-    if (pw < 6) {              // level 1: T10, T21, T32
-        const int b0 = pw >> 1, half = pw & 1;
-        const int col = 16 * b0 + 8 * half;
-        acc[0] = acc[1] = acc[2] = acc[3] = 0.f;
-        hm_mac(acc, Af, 16 * (b0 + 1), 16 * b0, Tf, 16 * b0, col, lane);
-        hm_finish(acc, Tf, wb, b0 + 1, col, lane);
+    float acc[4] = {0.f, 0.f, 0.f, 0.f}, acc2[4] = {0.f, 0.f, 0.f, 0.f};
+    const int h = pw & 1;                     // which 8 columns of a 16-column block
+    if (pw < 4) {              // stage 1: T10 (warps 0, 1), T32 (warps 2, 3)
+        const int bi = pw < 2 ? 1 : 3;        // block row; block column bi - 1
+        const int col = 16 * (bi - 1) + 8 * h;
+        hm_mac(acc, Af, 16 * bi, 16 * (bi - 1), Tf, 16 * (bi - 1), col, lane);
+        hm_finish(acc, Tf, Wb + pw * 16 * kWbLd, bi, col, lane);
+    } else {                   // X_r0 partial = A_r0 T00 and X_r1 = A_r1 T11 (r = 2 or 3)
+        const int r = pw < 6 ? 2 : 3;
+        hm_mac(acc, Af, 16 * r, 0, Tf, 0, 8 * h, lane);
+        hm_mac(acc2, Af, 16 * r, 16, Tf, 16, 16 + 8 * h, lane);
     }
     named_sync(1, 256);
-    if (pw < 6) {              // level 2: T20, T31 and Z30 = A30 T00 + A31 T10
-        const int item = pw >> 1, half = pw & 1;
-        acc[0] = acc[1] = acc[2] = acc[3] = 0.f;
-        if (item == 0) {
-            const int col = 8 * half;
-            hm_mac(acc, Af, 32, 0, Tf, 0, col, lane);
-            hm_mac(acc, Af, 32, 16, Tf, 16, col, lane);
-            hm_finish(acc, Tf, wb, 2, col, lane);
-        } else if (item == 1) {
-            const int col = 16 + 8 * half;
-            hm_mac(acc, Af, 48, 16, Tf, 16, col, lane);
-            hm_mac(acc, Af, 48, 32, Tf, 32, col, lane);
-            hm_finish(acc, Tf, wb, 3, col, lane);
-        } else {
-            const int col = 8 * half;
-            hm_mac(acc, Af, 48, 0, Tf, 0, col, lane);
-            hm_mac(acc, Af, 48, 16, Tf, 16, col, lane);
-            *reinterpret_cast<float2 *>(Zs + g * 16 + col + 2 * tq) = make_float2(acc[0], acc[1]);
-            *reinterpret_cast<float2 *>(Zs + (g + 8) * 16 + col + 2 * tq) = make_float2(acc[2], acc[3]);
-        }
-    }
-    named_sync(1, 256);
-    // block rows 0..2 are final now, block row 3 after level 3
     auto write_t12 = [&](int i, int ch) {   // 8 columns: float4 loads of T, beta, xs
         float tv[8], bv[8], xv[8];
 #pragma unroll
@@ -413,20 +422,36 @@ __device__ __forceinline__ void ut_solve_mma(const float *Af, float *Tf, float *
             *reinterpret_cast<uint4 *>(dst + kMatBytes + sw128_chunk(i, ch)) =
                 make_uint4(w2[0], w2[1], w2[2], w2[3]);
     };
-    if (pw < 2) {              // level 3: T30 = -T33 (Z30 + A32 T20)
-        const int col = 8 * pw;
-        const float2 z0 = *reinterpret_cast<const float2 *>(Zs + g * 16 + col + 2 * tq);
-        const float2 z1 = *reinterpret_cast<const float2 *>(Zs + (g + 8) * 16 + col + 2 * tq);
-        acc[0] = z0.x; acc[1] = z0.y; acc[2] = z1.x; acc[3] = z1.y;
-        hm_mac(acc, Af, 48, 32, Tf, 32, col, lane);
-        hm_finish(acc, Tf, wb, 3, col, lane);
-    } else {                   // meanwhile rows 0..47: 384 chunks over 192 threads
-        const int u = t - 64;
-        write_t12(u >> 2, 2 * (u & 3));
-        write_t12(u >> 2, 2 * (u & 3) + 1);
+    if (pw >= 4) {             // stage 2: X_r0 += A_r1 T10, then X into Wb
+        const int r = pw < 6 ? 2 : 3;
+        hm_mac(acc, Af, 16 * r, 16, Tf, 16, 8 * h, lane);
+        float *x0 = Xs + (16 * (r - 2)) * kXLd + 8 * h;        // X_r0, this half
+        float *x1 = x0 + 16;                                    // X_r1
+        *reinterpret_cast<float2 *>(x0 + g * kXLd + 2 * tq) = make_float2(acc[0], acc[1]);
+        *reinterpret_cast<float2 *>(x0 + (g + 8) * kXLd + 2 * tq) = make_float2(acc[2], acc[3]);
+        *reinterpret_cast<float2 *>(x1 + g * kXLd + 2 * tq) = make_float2(acc2[0], acc2[1]);
+        *reinterpret_cast<float2 *>(x1 + (g + 8) * kXLd + 2 * tq) = make_float2(acc2[2], acc2[3]);
+    } else {                   // meanwhile T1 / T2 rows 0..31 (block rows 0, 1 are final)
+        write_t12(t >> 2, 2 * (t & 3));
+        write_t12(t >> 2, 2 * (t & 3) + 1);
     }
     named_sync(1, 256);
-    if (t < 128) write_t12(48 + (t >> 3), t & 7);
+    {                          // stage 3: warp pw -> block (2 + pw / 4, (pw / 2) % 2), half h
+        const int r = 2 + (pw >> 2), cb = (pw >> 1) & 1;
+        float o[4] = {0.f, 0.f, 0.f, 0.f};
+        const float *xr = Xs + cb * 16 + 8 * h;                // X_2cb, this half
+        if (r == 2) {          // T2cb = -T22 X2cb
+            hm_mac_at(o, Tf + 32 * kLd + 32, kLd, xr, kXLd, lane, true);
+        } else {               // T3cb = -(T32 X2cb + T33 X3cb)
+            hm_mac_at(o, Tf + 48 * kLd + 32, kLd, xr, kXLd, lane, true);
+            hm_mac_at(o, Tf + 48 * kLd + 48, kLd, xr + 16 * kXLd, kXLd, lane, true);
+        }
+        float *dstT = Tf + (16 * r) * kLd + 16 * cb + 8 * h;
+        *reinterpret_cast<float2 *>(dstT + g * kLd + 2 * tq) = make_float2(o[0], o[1]);
+        *reinterpret_cast<float2 *>(dstT + (g + 8) * kLd + 2 * tq) = make_float2(o[2], o[3]);
+    }
+    named_sync(1, 256);
+    write_t12(32 + (t >> 3), t & 7);
 }
 
 }  // namespace ptc

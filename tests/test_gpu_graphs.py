@@ -2,8 +2,9 @@
 synchronisation and no allocation, so a serving loop can capture them in a
 CUDA graph: the fused decode step, the two-kernel prefill (with a caller
 workspace), the chunk-state scan and the gated prefill, the TMA-staged conv
-forward, the mixed batch with its decode beside the prefill, and the fused
-MTP step with its accept copies are captured with torch.cuda.graph and
+forward, the one-call prefill layer (plain and gated), the mixed batch with
+its decode beside the prefill, and the fused MTP step with its accept copies
+are captured with torch.cuda.graph and
 replayed (programmatic dependent launches included), and every output and
 pool must be bit-identical to an eager run on copies of the same inputs (the
 kernels are deterministic)."""
@@ -171,6 +172,56 @@ def test_scan_and_gated_prefill_graph_replay():
     assert bits_equal(o1g, o1e)
     assert bits_equal(o2g, o2e)
     assert bits_equal(pg, pe)
+
+
+def test_prefill_layer_graph_replay():
+    """gdn_prefill_layer then gdn_prefill_layer_gated on a ragged 4-sequence
+    batch (conv into the workspace, chunk offsets, the prep kernel forming
+    the gates, the chain kernel with and without the gated epilogue; the
+    second call continues the states the first wrote), captured together and
+    replayed: o, y, the conv pool and the recurrent pool bit-identical to
+    eager runs."""
+    d = workloads.Dims(hqk=2, hv=4)
+    w = workloads.prefill(lengths=[300, 77, 1, 640], n_slots=6, dims=d, low_decay=True)
+    T = w.x.shape[0]
+    gen = torch.Generator().manual_seed(405)
+    pool0 = cuda(torch.randn(6, d.hv, 128, 128, generator=gen) * 0.05)
+    z = cuda(torch.randn(T, d.hv, 128, generator=gen).bfloat16())
+    nw = cuda(torch.rand(128, generator=gen) + 0.5)
+    x, cw, cu = cuda(w.x), cuda(w.conv_w), cuda(w.cu_seqlens)
+    a, b, A_log, dt_bias = cuda(w.a), cuda(w.b), cuda(w.A_log), cuda(w.dt_bias)
+    slots, has = cuda(w.slots), cuda(w.has_initial_state)
+    none = torch.full_like(slots, -1)
+    need = gdn().gdn_prefill_layer_workspace_size(4, T, d.hqk, d.hv)
+    raw = torch.empty(need + 1024, dtype=torch.uint8, device=DEV)
+    off = (-raw.data_ptr()) % 1024
+    ws = raw[off:off + need]
+
+    def run(cpool, pool, o, y):
+        gdn().gdn_prefill_layer(x, cw, cpool, slots, has, a, b, A_log, dt_bias, cu, d.hqk, pool,
+                                none, slots, scale=w.scale, o=o, workspace=ws)
+        gdn().gdn_prefill_layer_gated(x, cw, cpool, slots, has, a, b, A_log, dt_bias, cu, d.hqk,
+                                      pool, slots, slots, z, nw, 1e-6, scale=w.scale, y=y,
+                                      workspace=ws)
+
+    cpe, pe = cuda(w.conv_pool), pool0.clone()
+    oe = torch.empty(T, d.hv, 128, dtype=torch.bfloat16, device=DEV)
+    ye = torch.empty_like(oe)
+    run(cpe, pe, oe, ye)
+    torch.cuda.synchronize()
+    status_clean()
+
+    cpg, pg = cuda(w.conv_pool), pool0.clone()
+    og, yg = torch.empty_like(oe), torch.empty_like(oe)
+    gr = _graph(lambda: run(cpg, pg, og, yg))
+    cpg.copy_(cuda(w.conv_pool))
+    pg.copy_(pool0)
+    gr.replay()
+    torch.cuda.synchronize()
+    status_clean()
+    for name, got, ref in (("o", og, oe), ("y", yg, ye), ("conv pool", cpg, cpe),
+                           ("state pool", pg, pe)):
+        assert bits_equal(got, ref), name
 
 
 def test_mixed_batch_and_mtp_step_graph_replay():

@@ -42,19 +42,22 @@ def _layer(w, cpool, spool, slots, init, final):
                                    w.dims.hqk, spool, init, final, scale=w.scale)
 
 
-@pytest.mark.parametrize("lengths", [[70, 1, 130, 64], [5, 300]])
-def test_prefill_layer_vs_oracle(lengths):
+@pytest.mark.parametrize("lengths,has", [([70, 1, 130, 64], [1, 1, 1, 1]), ([5, 300], [1, 1]),
+                                         ([70, 0, 1, 130, 2], [1, 1, 0, 1, 0])])
+def test_prefill_layer_vs_oracle(lengths, has):
     """2 QK / 4 V heads at head_dim 128, ragged lengths (a one-token
-    sequence, a chunk-aligned one), every sequence continuing a carried conv
-    state and recurrent state from its slot."""
+    sequence, a chunk-aligned one, an empty one), sequences continuing a
+    carried conv state and recurrent state from their slot and others (no
+    initial state) starting from zero in both."""
     d = workloads.Dims(hqk=2, hv=4)
     w = workloads.prefill(lengths=lengths, n_slots=len(lengths) + 2, dims=d, low_decay=True)
-    w.has_initial_state[:] = 1
+    w.has_initial_state[:] = torch.tensor(has, dtype=w.has_initial_state.dtype)
     gen = torch.Generator().manual_seed(17)
     pool = torch.randn(len(lengths) + 2, d.hv, 128, 128, generator=gen) * 0.05
     slots = cuda(w.slots)
+    init = cuda(torch.where(w.has_initial_state.bool(), w.slots, torch.full_like(w.slots, -1)))
     cpool, spool = cuda(w.conv_pool), cuda(pool)
-    o = _layer(w, cpool, spool, slots, slots, slots)
+    o = _layer(w, cpool, spool, slots, init, slots)
     torch.cuda.synchronize()
     status_clean()
     o_ref, conv_upd, upd, _, _, _ = oracle.layer_prefill(
