@@ -12,8 +12,8 @@
 //      Each item's T1 | P | W^T | row factors block is written to the
 //      workspace in exactly the shared-memory layout the MMAs read.
 //   2. chain_kernel: per (sequence, V head) only the state chain,
-//        MU  U  = T1 V                  (issued a chunk ahead: no state needed)
-//        M2  U += S W'^T                W' = -W, so U = T1 V - W S^T
+//        M2  U  = S W'^T                W' = -W
+//        MU  U += T1 V                  so U = T1 V - W S^T
 //        O   O  = S Q'^T                Q' = scale Gam r_q Q
 //        E2  U -> bf16;  M6  S += U K'';  M5  O += U P^T
 //        E3  S -> bf16 copy for the next chunk, S pre-scaled by its decay
@@ -393,8 +393,8 @@ inline unsigned prep_grid(int64_t items) {   // the item bound caps it for tiny 
 // ------------------------------------------------------------ chain kernel --
 // One CTA per (sequence, V head).  Per chunk c (S pre-scaled by the chunk's
 // decay, S16 its bf16 copy; K, Q, V raw tiles; T1, P, W' from the item):
-//   MU  U1  = T1 V                    (a chunk ahead: needs no state)
-//   M2  U1 += S16[:, a < 64] W'^T,  U2 = S16[:, a >= 64] W'^T    (W' = T2 K)
+//   M2  U1  = S16[:, a < 64] W'^T,  U2 = S16[:, a >= 64] W'^T    (W' = T2 K)
+//   MU  U2 += T1 V                    (behind U2's half of M2, same issuer)
 //   E2  U = U1 + U2;  U16 = bf16(U), U16k = bf16(U diag(ks))     (ks: K'' rows)
 //   M6  S += U16k K                   (= U K'')
 //   O   O1 = S16 Q^T,  O2 = U16 P^T,  o = diag(sq) O1 + O2       (sq: Q' rows)
@@ -404,7 +404,9 @@ inline unsigned prep_grid(int64_t items) {   // the item bound caps it for tiny 
 // split by K over two issuing threads (warps 1 and 10) into separate
 // accumulators that E2 adds.  The critical path is
 //   s_next -> M2 -> E2 -> M6 -> E3a -> s_next;
-// O1, O2, MU(c + 1) and the o stores fill the gaps.  Warp 0: TMA / bulk
+// O1, O2 and the o stores fill the gaps.  (MU used to run a chunk ahead into
+// U1, with M2 accumulating onto it: the next M2 then waited for MU, whose
+// operands arrive late; behind M2 it adds ~2 % less time.)  Warp 0: TMA / bulk
 // producer; warps 2..9: the epilogues as two warpgroups that each take half
 // of the TMEM columns of S, U and O, and store o a 32 x 32 tile per warp
 // through shared memory with TMA.
@@ -419,7 +421,7 @@ constexpr uint32_t kCStageBytes = 1024;
 struct ChainBars {
     uint64_t kq_full[kKQStages], kq_empty[kKQStages], v_full[kVStages], v_empty[kVStages],
         d_full[kDStages], d_empty[kDStages], c_full[kCStages], c_empty[kCStages];
-    uint64_t mu_full, u_full, u2_full, s_full, o1_full, o2_full, s_next, o_free, done_a, done_b;
+    uint64_t u_full, u2_full, s_full, o1_full, o2_full, s_next, o_free, done_a, done_b;
     uint64_t zbar[8];             // per epilogue warp: its z tile of the chunk (gated output)
     uint32_t tmem_base;
     int abort;
@@ -536,7 +538,6 @@ chain_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
         for (int s = 0; s < kVStages; ++s) { mbar_init(&B.v_full[s], 1); mbar_init(&B.v_empty[s], 1); }
         for (int s = 0; s < kDStages; ++s) { mbar_init(&B.d_full[s], 1); mbar_init(&B.d_empty[s], 1); }
         for (int s = 0; s < kCStages; ++s) { mbar_init(&B.c_full[s], 1); mbar_init(&B.c_empty[s], kEpiThreads); }
-        mbar_init(&B.mu_full, 1);
         mbar_init(&B.u_full, 2);                       // one commit from each issuer
         mbar_init(&B.u2_full, kEpiThreads);
         mbar_init(&B.s_full, 1);
@@ -610,12 +611,9 @@ chain_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
         __syncwarp();
     } else if (warp == 1 || warp == 10) {
         // ------------------------------------------------ the two MMA issuers
-        // Issuer A (warp 1): M2 over a < 64, M6, O2.
-        // Issuer B (warp 10): M2 over a >= 64, O1, and MU(c + 1) once M6 has
-        // left the tensor pipe.  Measured: issued by A right behind M6 (A then
-        // waits for the next item's operands before O2 and its stage
-        // releases), the prefill took 0.448 ms against 0.414; issued by B as
-        // soon as M6 is issued, it made no difference.
+        // Issuer A (warp 1): M2 over a < 64 into U1, M6, O2.
+        // Issuer B (warp 10): M2 over a >= 64 into U2, MU onto U2 right behind
+        // it (one issuer, so the order on the accumulator is fixed), O1.
         if (lane == 0) {
             const bool isA = warp == 1;
             const uint32_t id64 = idesc_bf16(128, 64);
@@ -624,33 +622,31 @@ chain_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
             const uint32_t id128bmn = idesc_bf16(128, 128, false, true);
             const int s0 = isA ? 0 : 4;                  // this issuer's k-steps over a
             const uint32_t ucol = isA ? kColU1 : kColU2;
-            auto issue_mu = [&](int c) {   // MU: U1 = T1 V  (A = V^T, MN-major)
+            auto issue_mu = [&](int c) {   // MU: U2 += T1 V  (A = V^T, MN-major)
                 const int sd = c % kDStages, sv = c % kVStages;
                 mbar_wait(&B.d_full[sd], (c / kDStages) & 1, abort);
                 mbar_wait(&B.v_full[sv], (c / kVStages) & 1, abort);
                 tc_fence_after();
                 const uint32_t dsm = smem_u32(sm + L::D + sd * kItemOps);
                 const uint32_t vsm = smem_u32(sm + L::V + sv * kVBytes);
-                for (int s = 0; s < 4; ++s)
-                    mma_ss(tbase + kColU1, sdesc_sw128(vsm + s * 16 * 128, kVBlk, 1024),
-                           sdesc_sw128(dsm + kItemT1 + s * 32, 16, 1024), id64amn, s > 0);
+                for (int s = 0; s < 4; ++s)   // onto this chunk's U2 (M2 over a >= 64)
+                    mma_ss(tbase + kColU2, sdesc_sw128(vsm + s * 16 * 128, kVBlk, 1024),
+                           sdesc_sw128(dsm + kItemT1 + s * 32, 16, 1024), id64amn, 1);
                 mma_commit(&B.v_empty[sv]);
-                mma_commit(&B.mu_full);
             };
-            if (!isA && !ident) issue_mu(0);
             for (int c = 0; c < nch; ++c) {
                 const int sk = c % L::kKQ, sd = c % kDStages;
                 const uint32_t kqb = smem_u32(sm + L::KQ + sk * kKQBytes);
                 const uint32_t dsm = smem_u32(sm + L::D + sd * kItemOps);
                 mbar_wait(&B.kq_full[sk], (c / L::kKQ) & 1, abort);
                 mbar_wait(&B.d_full[sd], (c / kDStages) & 1, abort);
-                if (isA && !ident) mbar_wait(&B.mu_full, c & 1, abort);   // M2 accumulates onto MU
                 mbar_wait(&B.s_next, c & 1, abort);      // S16 of this chunk
                 tc_fence_after();
                 for (int s = s0; s < s0 + 4; ++s)   // M2: U(1|2) (+)= S16 W'^T over this a half
                     mma_ts(tbase + ucol, tbase + kColS16 + s * 8,
                            sdesc_sw128(dsm + kItemW + s * 16 * 128, 8192, 1024), id64bmn,
-                           (isA && !ident) || s > s0);
+                           s > s0);
+                if (!isA && !ident) issue_mu(c);         // U2 += T1 V, behind its M2 half
                 mma_commit(&B.u_full);
                 if (isA) {
                     mbar_wait(&B.u2_full, c & 1, abort);     // U16, U16k in TMEM
@@ -678,8 +674,6 @@ chain_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
                                id64, s > 0);
                     }
                     mma_commit(&B.o1_full);
-                    mbar_wait(&B.s_full, c & 1, abort);      // M6 done (and E2 has read U1)
-                    if (c + 1 < nch && !ident) issue_mu(c + 1);
                 }
             }
             mma_commit(isA ? &B.done_a : &B.done_b);
