@@ -367,12 +367,13 @@ __device__ __forceinline__ void hm_mac_at(float (&acc)[4], const float *X, int l
 //   X = A_ll T_hi:  X20 = A20 T00 + A21 T10, X21 = A21 T11,
 //                   X30 = A30 T00 + A31 T10, X31 = A31 T11,
 //   [T20 T21; T30 T31] = -T_lo X:  T2j = -T22 X2j,  T3j = -(T32 X2j + T33 X3j).
-// Three dependent stages of at most two 16 x 16 products (the level-by-level
-// form needs seven): stage 1 T10, T32 (warps 0..3) and the parts of X that
-// need no T10 (warps 4..7, kept in registers); stage 2 X20, X30 (warps
-// 4..7), X into Wb, and the T1 / T2 rows 0..31 (warps 0..3); stage 3 the
-// lower-left quarter (one 16 x 8 half-block per warp).  Block row 2's and
-// 3's products of T20 and T21 are the level form's: -T22 times the same X.
+// Three dependent stages of at most two 16 x 16 products each, where the
+// block-row-by-block-row form chains six products from T10 to T30: stage 1
+// T10, T32 (warps 0..3) and the parts of X that need no T10 (warps 4..7, kept
+// in registers); stage 2 X20, X30 (warps 4..7), X into Wb, and the T1 / T2
+// rows 0..31 (warps 0..3); stage 3 the lower-left quarter (one 16 x 8
+// half-block per warp).  T20 and T21 come out as in the row form (-T22 times
+// the same sums); T30 and T31 are associated differently.
 template <bool kT2>
 __device__ __forceinline__ void ut_solve_mma(const float *Af, float *Tf, float *Wb, int t, int pw,
                                              int lane, const float *beta, const float *xs,
