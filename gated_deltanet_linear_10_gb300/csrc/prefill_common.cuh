@@ -42,6 +42,32 @@ __device__ inline int seq_for_rank(const int32_t *cu, int n_seqs, int rank, int 
     return *slot < 0 ? rank : *slot;
 }
 
+// Packed fp32 pairs (sm_100 and later): one instruction rounds each lane as
+// its scalar counterpart does, so results equal the scalar code's.
+__device__ __forceinline__ uint64_t f2_make(float a, float b) {
+    uint64_t d;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(d) : "f"(a), "f"(b));
+    return d;
+}
+__device__ __forceinline__ void f2_split(uint64_t d, float &a, float &b) {
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(d));
+}
+__device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+__device__ __forceinline__ uint64_t f2_mul(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+__device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
+    uint64_t d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+
 // Blocked UT solve helpers.  The 64 x 64 matrices are 4 x 4 blocks of 16.
 // A warp computes half a block (16 rows x 8 columns): lane (r = lane/2,
 // cg = lane%2) owns row r, columns col + 4cg .. col + 4cg + 3.

@@ -749,18 +749,17 @@ chain_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
             {
                 uint32_t u1[32], u2[32], uu[16], uk[16];
                 tmem_ld32x2(lrow + kColU1 + 32 * hf, lrow + kColU2 + 32 * hf, u1, u2);
-                const float4 *ks4 = reinterpret_cast<const float4 *>(I.ks + 32 * hf);
+                const uint64_t *ks2 = reinterpret_cast<const uint64_t *>(I.ks + 32 * hf);
 #pragma unroll
-                for (int q = 0; q < 8; ++q) {
-                    const float4 f = ks4[q];
-                    const float x0 = __uint_as_float(u1[4 * q]) + __uint_as_float(u2[4 * q]);
-                    const float x1 = __uint_as_float(u1[4 * q + 1]) + __uint_as_float(u2[4 * q + 1]);
-                    const float x2 = __uint_as_float(u1[4 * q + 2]) + __uint_as_float(u2[4 * q + 2]);
-                    const float x3 = __uint_as_float(u1[4 * q + 3]) + __uint_as_float(u2[4 * q + 3]);
-                    uu[2 * q] = pack_bf16(x0, x1);
-                    uu[2 * q + 1] = pack_bf16(x2, x3);
-                    uk[2 * q] = pack_bf16(x0 * f.x, x1 * f.y);
-                    uk[2 * q + 1] = pack_bf16(x2 * f.z, x3 * f.w);
+                for (int q = 0; q < 16; ++q) {   // pairs of columns, packed fp32
+                    const uint64_t x = f2_add(f2_make(__uint_as_float(u1[2 * q]), __uint_as_float(u1[2 * q + 1])),
+                                              f2_make(__uint_as_float(u2[2 * q]), __uint_as_float(u2[2 * q + 1])));
+                    const uint64_t xk = f2_mul(x, ks2[q]);
+                    float x0, x1, k0, k1;
+                    f2_split(x, x0, x1);
+                    f2_split(xk, k0, k1);
+                    uu[q] = pack_bf16(x0, x1);
+                    uk[q] = pack_bf16(k0, k1);
                 }
                 tmem_st16(lrow + kColU16k + 16 * hf, uk);
                 tmem_st16(lrow + kColU16 + 16 * hf, uu);
@@ -790,10 +789,17 @@ chain_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
                 mbar_arrive(&B.s_next);
                 mbar_wait(&B.c_full[(c + 1) % kCStages], ((c + 1) / kCStages) & 1, abort);
                 const float gnext = scal(c + 1).gam_n;
+                const uint64_t g2 = f2_make(gnext, gnext);
 #pragma unroll
                 for (int cc = 0; cc < 64; cc += 32) {
 #pragma unroll
-                    for (int j = 0; j < 32; ++j) sv[cc + j] = __float_as_uint(__uint_as_float(sv[cc + j]) * gnext);
+                    for (int j = 0; j < 32; j += 2) {
+                        float a0, a1;
+                        f2_split(f2_mul(f2_make(__uint_as_float(sv[cc + j]), __uint_as_float(sv[cc + j + 1])), g2),
+                                 a0, a1);
+                        sv[cc + j] = __float_as_uint(a0);
+                        sv[cc + j + 1] = __float_as_uint(a1);
+                    }
                     tmem_st32(s32 + cc, *reinterpret_cast<uint32_t(*)[32]>(sv + cc));
                 }
             } else if (fslot >= 0) {
@@ -815,23 +821,24 @@ chain_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
             {
                 // o rows 32 hf + i of column b; a full tile leaves through TMA,
                 // a partial last one through plain stores
-                const float4 *sq4 = reinterpret_cast<const float4 *>(I.sq + 32 * hf);
+                const uint64_t *sq2 = reinterpret_cast<const uint64_t *>(I.sq + 32 * hf);
                 float f[32];
 #pragma unroll
-                for (int q = 0; q < 8; ++q) {
-                    const float4 s4 = sq4[q];
-                    f[4 * q] = fmaf(s4.x, __uint_as_float(o1[4 * q]), __uint_as_float(o2[4 * q]));
-                    f[4 * q + 1] = fmaf(s4.y, __uint_as_float(o1[4 * q + 1]), __uint_as_float(o2[4 * q + 1]));
-                    f[4 * q + 2] = fmaf(s4.z, __uint_as_float(o1[4 * q + 2]), __uint_as_float(o2[4 * q + 2]));
-                    f[4 * q + 3] = fmaf(s4.w, __uint_as_float(o1[4 * q + 3]), __uint_as_float(o2[4 * q + 3]));
-                }
+                for (int q = 0; q < 16; ++q)   // pairs of tokens, packed fp32
+                    f2_split(f2_fma(sq2[q],
+                                    f2_make(__uint_as_float(o1[2 * q]), __uint_as_float(o1[2 * q + 1])),
+                                    f2_make(__uint_as_float(o2[2 * q]), __uint_as_float(o2[2 * q + 1]))),
+                             f[2 * q], f[2 * q + 1]);
                 if constexpr (kGated) {
                     // sum of o^2 over the 128 value rows of each token: the
                     // warp's 32 rows by a reduce-scatter (lane l: token l),
                     // then the warpgroup's four warps through shared memory
                     float v[32];
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) v[i] = f[i] * f[i];
+                    for (int i = 0; i < 32; i += 2) {
+                        const uint64_t fi = f2_make(f[i], f[i + 1]);
+                        f2_split(f2_mul(fi, fi), v[i], v[i + 1]);
+                    }
                     reduce_scatter_step<32>(v, lane);
                     reduce_scatter_step<16>(v, lane);
                     reduce_scatter_step<8>(v, lane);
@@ -850,15 +857,18 @@ chain_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
                     // form (below the bf16 rounding of y): the epilogue is
                     // issue-bound, and SiLU with an exact reciprocal cost a
                     // third of the chain's time
+                    const uint64_t wb2 = f2_make(wb, wb), half2 = f2_make(0.5f, 0.5f);
 #pragma unroll
-                    for (int q = 0; q < 8; ++q) {
-                        const float4 r4 = reinterpret_cast<const float4 *>(rs)[q];
-                        const float rr[4] = {r4.x, r4.y, r4.z, r4.w};
-#pragma unroll
-                        for (int e = 0; e < 4; ++e) {
-                            const float zz = __bfloat162float(zt[(4 * q + e) * 32 + lane]);
-                            f[4 * q + e] *= rr[e] * wb * silu_bf16out(zz);
-                        }
+                    for (int q = 0; q < 16; ++q) {   // pairs of tokens, packed fp32
+                        const uint64_t rr2 = reinterpret_cast<const uint64_t *>(rs)[q];
+                        const uint64_t h2 = f2_mul(f2_make(__bfloat162float(zt[(2 * q) * 32 + lane]),
+                                                           __bfloat162float(zt[(2 * q + 1) * 32 + lane])),
+                                                   half2);      // SiLU(z) = h + h tanh(h), h = z / 2
+                        float h0, h1;
+                        f2_split(h2, h0, h1);
+                        const uint64_t sz = f2_fma(h2, f2_make(tanh_approx(h0), tanh_approx(h1)), h2);
+                        f2_split(f2_mul(f2_make(f[2 * q], f[2 * q + 1]), f2_mul(f2_mul(rr2, wb2), sz)),
+                                 f[2 * q], f[2 * q + 1]);
                     }
                     fence_async_smem();      // z reads (generic) before the next z load (async)
                     __syncwarp();
