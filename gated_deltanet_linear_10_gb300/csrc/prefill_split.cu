@@ -204,10 +204,14 @@ prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
     tc_fence_after();
     const uint32_t tbase = B.tmem_base;
     volatile int *abort = &B.abort;
-    // persistent: CTA b takes items b, b + grid, ...; the barriers' phase
-    // flips per item, TMEM and the barriers are set up once
-    for (int wk = blockIdx.x, kk = 0; wk < n_work; wk += gridDim.x, ++kk) {
+    // persistent: CTA b takes the items n_work - 1 - b, n_work - 1 - b - grid,
+    // ... (in reverse, so that the first chunks, which the chains read first,
+    // are written last and can still be in L2 when the chains start: 0.3788
+    // -> 0.3772 ms on the 8-sequence batch); the barriers' phase flips per
+    // item, TMEM and the barriers are set up once
+    for (int wk0 = blockIdx.x, kk = 0; wk0 < n_work; wk0 += gridDim.x, ++kk) {
         const uint32_t ph = kk & 1;
+        const int wk = n_work - 1 - wk0;
         const int it = wk / hv;
         const int h = wk - it * hv;
         int lo = 0, hi = n_seqs - 1;          // the sequence: last s with base[s] <= it
